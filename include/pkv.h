@@ -1,0 +1,202 @@
+/*
+ * pkv.h -- C ABI of the paged-KV attention library (libpkv.so, sm_103a).
+ *
+ * Attention over a paged KV cache: K/V of every request live in fixed-size
+ * physical blocks of 16 or 32 tokens, and a per-request block table maps the
+ * request's logical block i to a physical block, so that scattered blocks are
+ * read as one contiguous sequence ("PagedAttention과 RadixAttention으로 LLM KV
+ * 캐시 최적화", section 02).  Requests may share physical prefix blocks
+ * (same page, section 03: RadixAttention reuses the longest cached prefix and
+ * computes only the suffix).
+ *
+ * Memory layouts (all row-major, all device memory unless stated):
+ *   k_cache, v_cache  [num_blocks][num_kv_heads][block_size][head_dim]
+ *                     elements of cache_dtype (fp8: one byte per code)
+ *   q, out            [tokens][num_q_heads][head_dim]   act dtype (f16 / bf16)
+ *   k_new, v_new      [tokens][num_kv_heads][head_dim]  act dtype
+ *   block_tables      int32 [batch][max_blocks_per_seq]
+ *   seq_lens          int32 [batch]
+ *   slot_mapping      int64 [tokens]; slot = physical_block * block_size + offset,
+ *                     a negative slot means "do not write this token"
+ *   GQA: query head h reads kv head h / (num_q_heads / num_kv_heads).
+ *
+ * Ownership: the caller owns and allocates every buffer, including the
+ * workspace.  The library allocates no device memory and keeps no state
+ * besides a per-device cache of the SM count.
+ *
+ * Execution: every call only validates its arguments on the host and enqueues
+ * kernels on `stream`; it returns before the GPU work finishes.  Buffers must
+ * stay alive until the stream reaches that point.
+ *
+ * Errors: argument errors are detected on the host and returned before any
+ * launch (PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE).  A
+ * failed launch returns PKV_ERR_CUDA.  Data errors found on the device (a
+ * block id or slot outside the pool, a sequence longer than its block table)
+ * never fault: the offending element is skipped or read as zero, and the
+ * first such event is recorded in a device error word read by
+ * pkv_get_device_error().
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1,   /* null pointer, negative size, Hq % Hkv != 0, ... */
+  PKV_ERR_UNSUPPORTED = 2,   /* valid but not built: head_dim, block_size, dtype combo */
+  PKV_ERR_WORKSPACE = 3,     /* workspace missing or smaller than *_workspace_bytes() */
+  PKV_ERR_CUDA = 4           /* a CUDA runtime/driver call or a launch failed */
+} pkv_status;
+
+typedef enum { PKV_F16 = 0, PKV_BF16 = 1, PKV_FP8_E4M3 = 2 } pkv_dtype;
+
+/* Device error word values (pkv_get_device_error). */
+#define PKV_DEVERR_NONE 0
+#define PKV_DEVERR_BAD_BLOCK 1     /* block table entry outside [0, num_blocks) */
+#define PKV_DEVERR_BAD_SLOT 2      /* slot_mapping entry outside the pool */
+#define PKV_DEVERR_BAD_LENGTH 3    /* seq_len / prefix+suffix beyond the table or hint */
+#define PKV_DEVERR_TIMEOUT 4       /* a bounded wait on an asynchronous copy ran out */
+
+/* Description of one layer's KV pool.
+ *   head_dim in {64, 128}; block_size in {16, 32};
+ *   cache_dtype: PKV_F16, PKV_BF16 or PKV_FP8_E4M3;
+ *   k_scale / v_scale: per-tensor dequantisation scales of an fp8 cache
+ *   (value = code * scale; append stores e4m3(x / scale)).  Ignored (must be
+ *   finite and > 0) for 16-bit caches.  The pages name the fp8_e4m3 format
+ *   only ("KV Cache 완전 정리 — PagedAttention vs RadixAttention, SGLang이
+ *   빠른 이유", section "FP8 KV 캐시"); one fp32 scale per tensor is this
+ *   library's convention. */
+typedef struct {
+  int32_t num_blocks;
+  int32_t block_size;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  pkv_dtype cache_dtype;
+  float k_scale;
+  float v_scale;
+} pkv_cache_desc;
+
+/* ---------------------------------------------------------------------------
+ * pkv_kv_append -- write the K/V rows of new tokens into their cache slots.
+ *
+ * "KV Cache에 대해 알아보자 (Feat. Attention)", §3: at every decode step the
+ * new token's K and V are added to the cache.  Token t, kv head g is stored at
+ * block slot_mapping[t] / block_size, offset slot_mapping[t] % block_size.
+ *   16-bit cache: act dtype must equal the cache dtype; the bits are copied.
+ *   fp8 cache:    code = e4m3(fp32(x) / k_scale) (resp. v_scale), rounded to
+ *                 nearest-even, saturated to +-448.
+ * k_new / v_new: [num_tokens][num_kv_heads][head_dim] act dtype, device.
+ * slot_mapping:  int64 [num_tokens], device.  Negative = skip.  A slot whose
+ *                block lies outside the pool is skipped and reported in the
+ *                device error word.
+ * num_tokens == 0 is a no-op.  Several tokens writing the same slot: one of
+ * them wins (unspecified which).
+ * ------------------------------------------------------------------------- */
+pkv_status pkv_kv_append(const pkv_cache_desc* desc, void* k_cache, void* v_cache,
+                         const void* k_new, const void* v_new, pkv_dtype act_dtype,
+                         const int64_t* slot_mapping, int32_t num_tokens,
+                         cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * pkv_paged_decode_attn -- one query token per request attends over all of the
+ * request's cached tokens, read through its block table.
+ *
+ * Definition: out[b,h] = softmax_t(sm_scale * q[b,h] . K[b,t,g]) V[b,t,g] for
+ * t < seq_lens[b], g = h / (Hq/Hkv) ("KV Cache에 대해 알아보자 (Feat.
+ * Attention)", §1 formula, §3 decode step; the block-table read of
+ * "PagedAttention과 RadixAttention으로 LLM KV 캐시 최적화", section 02).
+ * seq_lens count the current token: its K/V must already be in the cache
+ * (pkv_kv_append first).
+ *
+ * The work is split over the sequence (split-KV): each split runs an online
+ * softmax over its pages and a second pass merges the splits with their
+ * log-sum-exp, which reproduces the one-pass softmax exactly up to rounding.
+ *
+ * q, out:        [batch][num_q_heads][head_dim] act dtype (f16 or bf16).
+ *                16-bit cache: act dtype == cache dtype.  fp8 cache: either.
+ * block_tables:  int32 [batch][max_blocks_per_seq].  Entries past a request's
+ *                last block are never read.
+ * seq_lens:      int32 [batch], each in [0, min(max_seq_len,
+ *                max_blocks_per_seq*block_size)].  seq_len 0 gives out = 0,
+ *                lse = -inf.
+ * sm_scale:      softmax scale (1/sqrt(head_dim) for the textbook formula).
+ * max_seq_len:   host-side upper bound of seq_lens; sizes the split plan.
+ * num_splits:    0 = choose automatically; > 0 forces at most that many splits
+ *                (1 = single pass, no merge).
+ * lse_out:       nullable float [batch][num_q_heads], natural-log LSE.
+ * workspace:     device scratch of pkv_decode_workspace_bytes() bytes (may be
+ *                NULL when that is 0).  Concurrent calls need separate
+ *                workspaces.
+ * Supported: head_dim 64/128, block_size 16/32, num_q_heads/num_kv_heads <= 8.
+ * ------------------------------------------------------------------------- */
+size_t pkv_decode_workspace_bytes(const pkv_cache_desc* desc, int32_t batch,
+                                  int32_t num_q_heads, int32_t max_seq_len,
+                                  int32_t num_splits);
+
+pkv_status pkv_paged_decode_attn(const pkv_cache_desc* desc, const void* k_cache,
+                                 const void* v_cache, const void* q, void* out,
+                                 pkv_dtype act_dtype, const int32_t* block_tables,
+                                 int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                 int32_t batch, int32_t num_q_heads, float sm_scale,
+                                 int32_t max_seq_len, int32_t num_splits, float* lse_out,
+                                 void* workspace, size_t workspace_bytes,
+                                 cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * pkv_paged_extend_attn -- suffix prefill over a cached prefix.
+ *
+ * "PagedAttention과 RadixAttention으로 LLM KV 캐시 최적화", section 03: when
+ * the longest cached prefix of a request has P tokens, only the remaining
+ * suffix is computed (2,000-token request with 1,900 cached -> 100 prefilled).
+ * Request b owns query rows q_indptr[b] .. q_indptr[b+1]-1; its row i sits at
+ * position P_b + i (P_b = prefix_lens[b]) and attends to keys 0 .. P_b + i:
+ * every cached prefix token plus the suffix causally.  The suffix's own K/V
+ * must already be in the cache at positions P_b .. P_b+S_b-1 (pkv_kv_append
+ * first), so every key is read through the block table.
+ *
+ * q, out:        [q_indptr[batch]][num_q_heads][head_dim] act dtype.
+ * q_indptr:      int32 [batch+1], device, non-decreasing, q_indptr[0] = 0.
+ * prefix_lens:   int32 [batch], device.
+ * max_suffix_len / max_total_len: host-side upper bounds of S_b and P_b+S_b.
+ * total_q_rows:  q_indptr[batch] (host value; sizes the grid).
+ * lse_out:       nullable float [q_indptr[batch]][num_q_heads], natural log.
+ * workspace:     pkv_extend_workspace_bytes() bytes (currently 0).
+ * Supported: head_dim 128, block_size 16/32, num_q_heads/num_kv_heads in
+ * {1, 2, 4, 8}, 16-bit caches and fp8.
+ * ------------------------------------------------------------------------- */
+size_t pkv_extend_workspace_bytes(const pkv_cache_desc* desc, int32_t batch,
+                                  int32_t num_q_heads, int32_t total_q_rows,
+                                  int32_t max_total_len);
+
+pkv_status pkv_paged_extend_attn(const pkv_cache_desc* desc, const void* k_cache,
+                                 const void* v_cache, const void* q, void* out,
+                                 pkv_dtype act_dtype, const int32_t* q_indptr,
+                                 const int32_t* prefix_lens, const int32_t* block_tables,
+                                 int32_t max_blocks_per_seq, int32_t batch,
+                                 int32_t num_q_heads, float sm_scale, int32_t total_q_rows,
+                                 int32_t max_suffix_len, int32_t max_total_len,
+                                 float* lse_out, void* workspace, size_t workspace_bytes,
+                                 cudaStream_t stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* pkv_status_string(pkv_status status);
+
+/* Read (and optionally clear) the device error word of the current device.
+ * Synchronises `stream`.  Returns PKV_OK and writes the word to *word. */
+pkv_status pkv_get_device_error(int32_t* word, int32_t clear, cudaStream_t stream);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int32_t pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */
