@@ -1,0 +1,199 @@
+"""Paged-KV attention for GB300 (sm_103a): a thin ctypes binding of libpkv.so.
+
+Every call here only marshals arguments (PyTorch tensors -> device pointers,
+the current CUDA stream) and forwards them to the C ABI declared in
+``include/pkv.h``; all work runs in the library's CUDA kernels.  There is no
+CPU fallback: if libpkv.so is missing or fails to load, every call raises.
+
+The three calls (names as in pkv.h without the ``pkv_`` prefix):
+  * kv_append          -- scatter new K/V rows into their cache slots;
+  * paged_decode_attn  -- one query token per request over its paged K/V
+                          (GQA, split-KV, online softmax, LSE merge);
+  * paged_extend_attn  -- suffix prefill over cached prefix blocks + causal
+                          suffix.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = ["F16", "BF16", "FP8_E4M3", "PkvError", "CacheDesc", "lib_path", "load",
+           "kv_append", "paged_decode_attn", "paged_extend_attn", "decode_workspace_bytes",
+           "extend_workspace_bytes", "get_device_error", "status_string", "version"]
+
+F16, BF16, FP8_E4M3 = 0, 1, 2
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libpkv.so")
+_lib = None
+_lock = threading.Lock()
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+class CacheDesc(ctypes.Structure):
+    """Mirror of pkv_cache_desc."""
+    _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("cache_dtype", ctypes.c_int), ("k_scale", ctypes.c_float),
+                ("v_scale", ctypes.c_float)]
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load libpkv.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"{_LIB_PATH} is not built; run paged_kv_cache_285_gb300.build.build()")
+        lib = ctypes.CDLL(_LIB_PATH)
+        P, I32, SZ, F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_float
+        D = ctypes.POINTER(CacheDesc)
+        lib.pkv_kv_append.argtypes = [D, P, P, P, P, ctypes.c_int, P, I32, P]
+        lib.pkv_kv_append.restype = ctypes.c_int
+        lib.pkv_decode_workspace_bytes.argtypes = [D, I32, I32, I32, I32]
+        lib.pkv_decode_workspace_bytes.restype = SZ
+        lib.pkv_paged_decode_attn.argtypes = [D, P, P, P, P, ctypes.c_int, P, I32, P, I32, I32, F,
+                                              I32, I32, P, P, SZ, P]
+        lib.pkv_paged_decode_attn.restype = ctypes.c_int
+        lib.pkv_extend_workspace_bytes.argtypes = [D, I32, I32, I32, I32]
+        lib.pkv_extend_workspace_bytes.restype = SZ
+        lib.pkv_paged_extend_attn.argtypes = [D, P, P, P, P, ctypes.c_int, P, P, P, I32, I32, I32,
+                                              F, I32, I32, I32, P, P, SZ, P]
+        lib.pkv_paged_extend_attn.restype = ctypes.c_int
+        lib.pkv_status_string.argtypes = [ctypes.c_int]
+        lib.pkv_status_string.restype = ctypes.c_char_p
+        lib.pkv_get_device_error.argtypes = [ctypes.POINTER(I32), I32, P]
+        lib.pkv_get_device_error.restype = ctypes.c_int
+        lib.pkv_version.argtypes = []
+        lib.pkv_version.restype = I32
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load().pkv_status_string(int(status)).decode()
+
+
+def version() -> int:
+    return int(load().pkv_version())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float16:
+        return F16
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.uint8 or t.dtype == getattr(torch, "float8_e4m3fn", None):
+        return FP8_E4M3
+    raise TypeError(f"unsupported tensor dtype {t.dtype}")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libpkv takes device tensors")
+    if not t.is_contiguous():
+        raise ValueError("libpkv takes contiguous tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _desc(k_cache: torch.Tensor, k_scale: float, v_scale: float) -> CacheDesc:
+    if k_cache.dim() != 4:
+        raise ValueError("cache must be [num_blocks, num_kv_heads, block_size, head_dim]")
+    nb, hkv, bs, d = k_cache.shape
+    return CacheDesc(nb, bs, hkv, d, _dtype_code(k_cache), float(k_scale), float(v_scale))
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise PkvError(status, what)
+
+
+def kv_append(k_cache, v_cache, k_new, v_new, slot_mapping, k_scale=1.0, v_scale=1.0,
+              stream=None):
+    """pkv_kv_append: k_new/v_new [T, Hkv, D] act dtype, slot_mapping int64 [T]."""
+    lib = load()
+    desc = _desc(k_cache, k_scale, v_scale)
+    st = lib.pkv_kv_append(ctypes.byref(desc), _ptr(k_cache), _ptr(v_cache), _ptr(k_new),
+                           _ptr(v_new), _dtype_code(k_new), _ptr(slot_mapping),
+                           int(slot_mapping.shape[0]), _stream(stream))
+    _check(st, "pkv_kv_append")
+
+
+def decode_workspace_bytes(k_cache, batch, num_q_heads, max_seq_len, num_splits=0,
+                           k_scale=1.0, v_scale=1.0) -> int:
+    lib = load()
+    desc = _desc(k_cache, k_scale, v_scale)
+    return int(lib.pkv_decode_workspace_bytes(ctypes.byref(desc), batch, num_q_heads,
+                                              max_seq_len, num_splits))
+
+
+def paged_decode_attn(k_cache, v_cache, q, out, block_tables, seq_lens, sm_scale, max_seq_len,
+                      k_scale=1.0, v_scale=1.0, num_splits=0, lse_out=None, workspace=None,
+                      stream=None):
+    """pkv_paged_decode_attn: q/out [B, Hq, D]; block_tables int32 [B, W]; seq_lens int32 [B].
+    ``workspace`` is a uint8 device tensor of at least decode_workspace_bytes() bytes."""
+    lib = load()
+    desc = _desc(k_cache, k_scale, v_scale)
+    b, hq, _ = q.shape
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib.pkv_paged_decode_attn(ctypes.byref(desc), _ptr(k_cache), _ptr(v_cache), _ptr(q),
+                                   _ptr(out), _dtype_code(q), _ptr(block_tables),
+                                   int(block_tables.shape[1]), _ptr(seq_lens), b, hq,
+                                   float(sm_scale), int(max_seq_len), int(num_splits),
+                                   _ptr(lse_out), _ptr(workspace), ws_bytes, _stream(stream))
+    _check(st, "pkv_paged_decode_attn")
+
+
+def extend_workspace_bytes(k_cache, batch, num_q_heads, total_q_rows, max_total_len,
+                           k_scale=1.0, v_scale=1.0) -> int:
+    lib = load()
+    desc = _desc(k_cache, k_scale, v_scale)
+    return int(lib.pkv_extend_workspace_bytes(ctypes.byref(desc), batch, num_q_heads,
+                                              total_q_rows, max_total_len))
+
+
+def paged_extend_attn(k_cache, v_cache, q, out, q_indptr, prefix_lens, block_tables, sm_scale,
+                      max_suffix_len, max_total_len, k_scale=1.0, v_scale=1.0, lse_out=None,
+                      workspace=None, stream=None):
+    """pkv_paged_extend_attn: q/out [sum S, Hq, D]; q_indptr int32 [B+1]; prefix_lens int32 [B]."""
+    lib = load()
+    desc = _desc(k_cache, k_scale, v_scale)
+    rows, hq, _ = q.shape
+    batch = int(prefix_lens.shape[0])
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib.pkv_paged_extend_attn(ctypes.byref(desc), _ptr(k_cache), _ptr(v_cache), _ptr(q),
+                                   _ptr(out), _dtype_code(q), _ptr(q_indptr), _ptr(prefix_lens),
+                                   _ptr(block_tables), int(block_tables.shape[1]), batch, hq,
+                                   float(sm_scale), rows, int(max_suffix_len),
+                                   int(max_total_len), _ptr(lse_out), _ptr(workspace), ws_bytes,
+                                   _stream(stream))
+    _check(st, "pkv_paged_extend_attn")
+
+
+def get_device_error(clear=True, stream=None) -> int:
+    """Read (and by default clear) the library's device error word (synchronises)."""
+    lib = load()
+    w = ctypes.c_int32(0)
+    _check(lib.pkv_get_device_error(ctypes.byref(w), int(bool(clear)), _stream(stream)),
+           "pkv_get_device_error")
+    return int(w.value)

@@ -1,0 +1,344 @@
+// C ABI of libpkv.so: argument validation, split planning, TMA descriptors and
+// launches.  Every check runs on the host before anything is enqueued.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <mutex>
+
+#include "../../include/pkv.h"
+#include "internal.h"
+
+using namespace pkv;
+
+// Device error word: first data error seen by any kernel (see pkv.h).
+__device__ int32_t g_pkv_error_word = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  std::once_flag once;
+  int sm_count = 0;
+  int32_t* err = nullptr;
+  cudaError_t init_error = cudaSuccess;
+};
+DeviceState g_dev[kMaxDevices];
+
+DeviceState* device_state(cudaError_t* e) {
+  int dev = 0;
+  *e = cudaGetDevice(&dev);
+  if (*e != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= kMaxDevices) {
+    *e = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  DeviceState* s = &g_dev[dev];
+  std::call_once(s->once, [s, dev]() {
+    cudaError_t r = cudaDeviceGetAttribute(&s->sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (r == cudaSuccess) r = cudaGetSymbolAddress(reinterpret_cast<void**>(&s->err), g_pkv_error_word);
+    s->init_error = r;
+  });
+  *e = s->init_error;
+  return s->init_error == cudaSuccess ? s : nullptr;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, []() {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+int elem_bytes(pkv_dtype d) { return d == PKV_FP8_E4M3 ? 1 : 2; }
+
+bool valid_dtype(pkv_dtype d) { return d == PKV_F16 || d == PKV_BF16 || d == PKV_FP8_E4M3; }
+
+pkv_status check_desc(const pkv_cache_desc* d) {
+  if (!d) return PKV_ERR_INVALID_ARG;
+  if (d->num_blocks <= 0 || d->num_kv_heads <= 0 || d->head_dim <= 0 || d->block_size <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (!valid_dtype(d->cache_dtype)) return PKV_ERR_INVALID_ARG;
+  if (!(d->head_dim == 64 || d->head_dim == 128)) return PKV_ERR_UNSUPPORTED;
+  if (!(d->block_size == 16 || d->block_size == 32)) return PKV_ERR_UNSUPPORTED;
+  if (d->cache_dtype == PKV_FP8_E4M3) {
+    if (!(std::isfinite(d->k_scale) && d->k_scale > 0.f && std::isfinite(d->v_scale) &&
+          d->v_scale > 0.f))
+      return PKV_ERR_INVALID_ARG;
+  }
+  if ((int64_t)d->num_blocks * d->num_kv_heads > (int64_t)INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  return PKV_OK;
+}
+
+pkv_status check_act(const pkv_cache_desc* d, pkv_dtype act) {
+  if (act != PKV_F16 && act != PKV_BF16) return PKV_ERR_INVALID_ARG;
+  if (d->cache_dtype != PKV_FP8_E4M3 && d->cache_dtype != act) return PKV_ERR_UNSUPPORTED;
+  return PKV_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// One 16-token tile of one kv head per TMA box row group:
+// dims {head_dim, block_size, num_blocks*Hkv}, box {min(128B row) , 16, 1}.
+pkv_status make_page_map(CUtensorMap* m, const void* base, const pkv_cache_desc* d) {
+  auto enc = encode_fn();
+  if (!enc) return PKV_ERR_CUDA;
+  const int elem = elem_bytes(d->cache_dtype);
+  const int rowb = d->head_dim * elem;
+  const int chunkb = rowb < 128 ? rowb : 128;
+  cuuint64_t dims[3] = {(cuuint64_t)d->head_dim, (cuuint64_t)d->block_size,
+                        (cuuint64_t)d->num_blocks * (cuuint64_t)d->num_kv_heads};
+  cuuint64_t strides[2] = {(cuuint64_t)rowb, (cuuint64_t)rowb * (cuuint64_t)d->block_size};
+  cuuint32_t box[3] = {(cuuint32_t)(chunkb / elem), (cuuint32_t)kSubTokens, 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUtensorMapDataType dt =
+      elem == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+  const CUtensorMapSwizzle sw =
+      chunkb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  CUresult r = enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
+}
+
+int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+
+struct DecodePlan {
+  int chunk = 0;
+  int splits = 0;
+  size_t ws_bytes = 0;
+  size_t ws_lse_offset = 0;
+};
+
+// Split plan: the sequence is cut into runs of `chunk` tokens (a multiple of
+// 16).  Automatic: aim for about six waves of two CTAs per SM over the worst
+// case batch*Hkv*max_seq_len, runs between 128 and 4096 tokens.
+DecodePlan plan_decode(const pkv_cache_desc* d, int batch, int hq, int max_seq_len,
+                       int forced, int sm_count) {
+  DecodePlan pl;
+  const int max_sub = max_seq_len > 0 ? ceil_div(max_seq_len, kSubTokens) : 1;
+  int chunk_sub;
+  if (forced > 0) {
+    chunk_sub = ceil_div(max_sub, forced);
+  } else {
+    const int64_t work = (int64_t)max_sub * batch * d->num_kv_heads;
+    const int64_t target = 6LL * 2LL * (sm_count > 0 ? sm_count : 148);
+    chunk_sub = ceil_div(work, target);
+    if (chunk_sub < 8) chunk_sub = 8;
+    if (chunk_sub > 256) chunk_sub = 256;
+  }
+  if (chunk_sub < 1) chunk_sub = 1;
+  pl.chunk = chunk_sub * kSubTokens;
+  pl.splits = ceil_div(max_sub, chunk_sub);
+  if (pl.splits < 1) pl.splits = 1;
+  if (pl.splits > 1) {
+    const size_t o_bytes = (size_t)batch * hq * pl.splits * d->head_dim * sizeof(float);
+    pl.ws_lse_offset = (o_bytes + 255) & ~(size_t)255;
+    pl.ws_bytes = pl.ws_lse_offset + (size_t)batch * hq * pl.splits * sizeof(float);
+  }
+  return pl;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pkv_status_string(pkv_status s) {
+  switch (s) {
+    case PKV_OK: return "PKV_OK";
+    case PKV_ERR_INVALID_ARG: return "PKV_ERR_INVALID_ARG";
+    case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED";
+    case PKV_ERR_WORKSPACE: return "PKV_ERR_WORKSPACE";
+    case PKV_ERR_CUDA: return "PKV_ERR_CUDA";
+    default: return "PKV_ERR_UNKNOWN";
+  }
+}
+
+int32_t pkv_version(void) { return 10000; }
+
+pkv_status pkv_get_device_error(int32_t* word, int32_t clear, cudaStream_t stream) {
+  if (!word) return PKV_ERR_INVALID_ARG;
+  cudaError_t e;
+  DeviceState* ds = device_state(&e);
+  if (!ds) return PKV_ERR_CUDA;
+  int32_t host = 0;
+  if (cudaMemcpyAsync(&host, ds->err, sizeof(int32_t), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  if (clear && cudaMemsetAsync(ds->err, 0, sizeof(int32_t), stream) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return PKV_ERR_CUDA;
+  *word = host;
+  return PKV_OK;
+}
+
+pkv_status pkv_kv_append(const pkv_cache_desc* desc, void* k_cache, void* v_cache,
+                         const void* k_new, const void* v_new, pkv_dtype act_dtype,
+                         const int64_t* slot_mapping, int32_t num_tokens, cudaStream_t stream) {
+  pkv_status st = check_desc(desc);
+  if (st != PKV_OK) return st;
+  if ((st = check_act(desc, act_dtype)) != PKV_OK) return st;
+  if (num_tokens < 0) return PKV_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k_cache || !v_cache || !k_new || !v_new || !slot_mapping) return PKV_ERR_INVALID_ARG;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) ||
+      !aligned(v_cache, 16) || !aligned(slot_mapping, 8))
+    return PKV_ERR_INVALID_ARG;
+  cudaError_t e;
+  DeviceState* ds = device_state(&e);
+  if (!ds) return PKV_ERR_CUDA;
+  AppendParams p;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.slots = slot_mapping;
+  p.err = ds->err;
+  p.num_tokens = num_tokens;
+  p.num_kv_heads = desc->num_kv_heads;
+  p.head_dim = desc->head_dim;
+  p.block_size = desc->block_size;
+  p.num_blocks = desc->num_blocks;
+  p.k_scale = desc->k_scale;
+  p.v_scale = desc->v_scale;
+  e = launch_append(p, (int)desc->cache_dtype, (int)act_dtype, stream);
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+size_t pkv_decode_workspace_bytes(const pkv_cache_desc* desc, int32_t batch, int32_t num_q_heads,
+                                  int32_t max_seq_len, int32_t num_splits) {
+  if (check_desc(desc) != PKV_OK || batch <= 0 || num_q_heads <= 0 || max_seq_len < 0 ||
+      num_splits < 0)
+    return 0;
+  cudaError_t e;
+  DeviceState* ds = device_state(&e);
+  const int sms = ds ? ds->sm_count : 0;
+  return plan_decode(desc, batch, num_q_heads, max_seq_len, num_splits, sms).ws_bytes;
+}
+
+pkv_status pkv_paged_decode_attn(const pkv_cache_desc* desc, const void* k_cache,
+                                 const void* v_cache, const void* q, void* out,
+                                 pkv_dtype act_dtype, const int32_t* block_tables,
+                                 int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                 int32_t batch, int32_t num_q_heads, float sm_scale,
+                                 int32_t max_seq_len, int32_t num_splits, float* lse_out,
+                                 void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  pkv_status st = check_desc(desc);
+  if (st != PKV_OK) return st;
+  if ((st = check_act(desc, act_dtype)) != PKV_OK) return st;
+  if (batch < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || max_seq_len < 0 ||
+      num_splits < 0 || !std::isfinite(sm_scale))
+    return PKV_ERR_INVALID_ARG;
+  if (num_q_heads % desc->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+  const int group = num_q_heads / desc->num_kv_heads;
+  if (group > 8) return PKV_ERR_UNSUPPORTED;
+  if (batch == 0) return PKV_OK;
+  if (batch > 65535 || desc->num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
+  if (!k_cache || !v_cache || !q || !out || !block_tables || !seq_lens)
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 4) || !aligned(out, 2))
+    return PKV_ERR_INVALID_ARG;
+  cudaError_t e;
+  DeviceState* ds = device_state(&e);
+  if (!ds) return PKV_ERR_CUDA;
+  const DecodePlan pl = plan_decode(desc, batch, num_q_heads, max_seq_len, num_splits, ds->sm_count);
+  if (pl.ws_bytes > 0 && (!workspace || workspace_bytes < pl.ws_bytes || !aligned(workspace, 256)))
+    return PKV_ERR_WORKSPACE;
+  if (pl.splits > 65535) return PKV_ERR_UNSUPPORTED;
+  CUtensorMap kmap, vmap;
+  if ((st = make_page_map(&kmap, k_cache, desc)) != PKV_OK) return st;
+  if ((st = make_page_map(&vmap, v_cache, desc)) != PKV_OK) return st;
+  DecodeParams p;
+  p.block_tables = block_tables;
+  p.seq_lens = seq_lens;
+  p.q = q;
+  p.out = out;
+  p.lse_out = lse_out;
+  p.ws_o = pl.ws_bytes ? reinterpret_cast<float*>(workspace) : nullptr;
+  p.ws_lse = pl.ws_bytes ? reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(workspace) + pl.ws_lse_offset)
+                         : nullptr;
+  p.err = ds->err;
+  p.max_blocks = max_blocks_per_seq;
+  p.num_blocks = desc->num_blocks;
+  p.batch = batch;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = desc->num_kv_heads;
+  p.group = group;
+  p.bs_shift = desc->block_size == 16 ? 4 : 5;
+  p.chunk = pl.chunk;
+  p.num_splits = pl.splits;
+  const double kscale = desc->cache_dtype == PKV_FP8_E4M3 ? (double)desc->k_scale : 1.0;
+  p.scale_log2 = (float)((double)sm_scale * kscale * 1.4426950408889634);
+  p.out_scale = desc->cache_dtype == PKV_FP8_E4M3 ? desc->v_scale : 1.0f;
+  e = launch_decode(kmap, vmap, p, desc->head_dim, (int)desc->cache_dtype, (int)act_dtype, stream);
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+size_t pkv_extend_workspace_bytes(const pkv_cache_desc* desc, int32_t batch, int32_t num_q_heads,
+                                  int32_t total_q_rows, int32_t max_total_len) {
+  (void)desc; (void)batch; (void)num_q_heads; (void)total_q_rows; (void)max_total_len;
+  return 0;
+}
+
+pkv_status pkv_paged_extend_attn(const pkv_cache_desc* desc, const void* k_cache,
+                                 const void* v_cache, const void* q, void* out,
+                                 pkv_dtype act_dtype, const int32_t* q_indptr,
+                                 const int32_t* prefix_lens, const int32_t* block_tables,
+                                 int32_t max_blocks_per_seq, int32_t batch, int32_t num_q_heads,
+                                 float sm_scale, int32_t total_q_rows, int32_t max_suffix_len,
+                                 int32_t max_total_len, float* lse_out, void* workspace,
+                                 size_t workspace_bytes, cudaStream_t stream) {
+  (void)workspace; (void)workspace_bytes;
+  pkv_status st = check_desc(desc);
+  if (st != PKV_OK) return st;
+  if ((st = check_act(desc, act_dtype)) != PKV_OK) return st;
+  if (batch < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || total_q_rows < 0 ||
+      max_suffix_len < 0 || max_total_len < 0 || !std::isfinite(sm_scale))
+    return PKV_ERR_INVALID_ARG;
+  if (num_q_heads % desc->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+  const int group = num_q_heads / desc->num_kv_heads;
+  if (!extend_supported(desc->head_dim, (int)desc->cache_dtype, (int)act_dtype, group))
+    return PKV_ERR_UNSUPPORTED;
+  if (batch == 0 || total_q_rows == 0 || max_suffix_len == 0) return PKV_OK;
+  if (!k_cache || !v_cache || !q || !out || !block_tables || !q_indptr || !prefix_lens)
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 16) || !aligned(out, 16))
+    return PKV_ERR_INVALID_ARG;
+  cudaError_t e;
+  DeviceState* ds = device_state(&e);
+  if (!ds) return PKV_ERR_CUDA;
+  CUtensorMap kmap, vmap;
+  if ((st = make_page_map(&kmap, k_cache, desc)) != PKV_OK) return st;
+  if ((st = make_page_map(&vmap, v_cache, desc)) != PKV_OK) return st;
+  ExtendParams p;
+  p.q_indptr = q_indptr;
+  p.prefix_lens = prefix_lens;
+  p.block_tables = block_tables;
+  p.q = q;
+  p.out = out;
+  p.lse_out = lse_out;
+  p.err = ds->err;
+  p.max_blocks = max_blocks_per_seq;
+  p.num_blocks = desc->num_blocks;
+  p.batch = batch;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = desc->num_kv_heads;
+  p.group = group;
+  p.bs_shift = desc->block_size == 16 ? 4 : 5;
+  p.total_rows = total_q_rows;
+  p.tiles_per_head = ceil_div((int64_t)max_suffix_len * group, 128);
+  const double kscale = desc->cache_dtype == PKV_FP8_E4M3 ? (double)desc->k_scale : 1.0;
+  p.scale_log2 = (float)((double)sm_scale * kscale * 1.4426950408889634);
+  p.out_scale = desc->cache_dtype == PKV_FP8_E4M3 ? desc->v_scale : 1.0f;
+  e = launch_extend(kmap, vmap, p, desc->head_dim, (int)desc->cache_dtype, (int)act_dtype, stream);
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // extern "C"

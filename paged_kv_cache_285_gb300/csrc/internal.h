@@ -1,0 +1,86 @@
+// Internal launch interfaces shared by the C-ABI layer (api.cu) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pkv {
+
+enum : int { DT_F16 = 0, DT_BF16 = 1, DT_E4M3 = 2 };
+
+constexpr int kSubTokens = 16;  // tokens per staged K/V tile (one MMA row block)
+
+struct DecodeParams {
+  const int32_t* block_tables;
+  const int32_t* seq_lens;
+  const void* q;
+  void* out;
+  float* lse_out;     // nullable, natural log
+  float* ws_o;        // [B][Hq][S][D] fp32 partials (S > 1)
+  float* ws_lse;      // [B][Hq][S] base-2 LSE partials
+  int32_t* err;       // device error word
+  int max_blocks;     // block table row length
+  int num_blocks;
+  int batch;
+  int num_q_heads;
+  int num_kv_heads;
+  int group;          // Hq / Hkv (<= 8)
+  int bs_shift;       // log2(block_size)
+  int chunk;          // tokens per split, multiple of 16
+  int num_splits;     // S of the plan
+  float scale_log2;   // sm_scale * log2(e) (* k_scale for fp8)
+  float out_scale;    // v_scale for fp8, else 1
+};
+
+struct AppendParams {
+  void* k_cache;
+  void* v_cache;
+  const void* k_new;
+  const void* v_new;
+  const int64_t* slots;
+  int32_t* err;
+  int64_t num_tokens;
+  int num_kv_heads;
+  int head_dim;
+  int block_size;
+  int num_blocks;
+  float k_scale;
+  float v_scale;
+};
+
+struct ExtendParams {
+  const int32_t* q_indptr;
+  const int32_t* prefix_lens;
+  const int32_t* block_tables;
+  const void* q;
+  void* out;
+  float* lse_out;
+  int32_t* err;
+  int max_blocks;
+  int num_blocks;
+  int batch;
+  int num_q_heads;
+  int num_kv_heads;
+  int group;
+  int bs_shift;
+  int total_rows;
+  int tiles_per_head;   // ceil(max_suffix_len * group / 128)
+  float scale_log2;
+  float out_scale;
+};
+
+// Each returns a cudaError_t from the launch.
+cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap,
+                          const DecodeParams& p, int head_dim, int cache_dt, int act_dt,
+                          cudaStream_t stream);
+size_t decode_smem_bytes(int head_dim, int cache_dt);
+cudaError_t launch_append(const AppendParams& p, int cache_dt, int act_dt, cudaStream_t stream);
+cudaError_t launch_extend(const CUtensorMap& kmap, const CUtensorMap& vmap,
+                          const ExtendParams& p, int head_dim, int cache_dt, int act_dt,
+                          cudaStream_t stream);
+bool extend_supported(int head_dim, int cache_dt, int act_dt, int group);
+
+}  // namespace pkv

@@ -1,0 +1,95 @@
+// KV append: scatter the K/V rows of new tokens into their cache slots.
+//
+// "KV Cache에 대해 알아보자 (Feat. Attention)", §3: at each decode step the
+// new token's K and V are added to the cache; with paging the destination is
+// the token's slot (physical block, offset) -- "PagedAttention과
+// RadixAttention으로 LLM KV 캐시 최적화", section 02.
+//
+// One thread moves 16 bytes of one (token, kv head) row for K and for V, so a
+// warp covers two 256-byte rows with fully coalesced 16-byte loads and stores.
+// 16-bit caches copy the bits; fp8 caches store e4m3(fp32(x) / scale) with a
+// correctly rounded fp32 division and a saturating round-to-nearest-even
+// convert (cvt.rn.satfinite).  Slots whose block lies outside the pool are
+// skipped and reported in the error word; negative slots are skipped silently.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace pkv {
+
+namespace {
+
+template <int AT>
+__device__ __forceinline__ float act_to_f32(uint16_t bits) {
+  if constexpr (AT == DT_BF16) return __uint_as_float((uint32_t)bits << 16);
+  else return __half2float(__ushort_as_half(bits));
+}
+
+template <int CT, int AT>
+__global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
+  const int vpr = p.head_dim / 8;  // 16-byte input vectors per row
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t total = p.num_tokens * p.num_kv_heads * vpr;
+  if (idx >= total) return;
+  const int v = (int)(idx % vpr);
+  const int64_t row = idx / vpr;
+  const int g = (int)(row % p.num_kv_heads);
+  const int64_t t = row / p.num_kv_heads;
+  const int64_t slot = p.slots[t];
+  if (slot < 0) return;
+  const int64_t blk = slot / p.block_size, off = slot % p.block_size;
+  if (blk >= p.num_blocks) {
+    if (v == 0 && p.err) atomicCAS(p.err, 0, 2);
+    return;
+  }
+  const int64_t src = (t * p.num_kv_heads + g) * p.head_dim + v * 8;
+  const int64_t dst = ((blk * p.num_kv_heads + g) * p.block_size + off) * p.head_dim + v * 8;
+  const uint4 kx = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.k_new) + src));
+  const uint4 vx = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.v_new) + src));
+  if constexpr (CT != DT_E4M3) {
+    *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.k_cache) + dst) = kx;
+    *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.v_cache) + dst) = vx;
+  } else {
+    const uint32_t kw[4] = {kx.x, kx.y, kx.z, kx.w};
+    const uint32_t vw[4] = {vx.x, vx.y, vx.z, vx.w};
+    uint32_t ko[2], vo[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t kb = 0, vb = 0;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const uint32_t wk = kw[2 * h + q], wv = vw[2 * h + q];
+        const float k0 = __fdiv_rn(act_to_f32<AT>((uint16_t)(wk & 0xFFFFu)), p.k_scale);
+        const float k1 = __fdiv_rn(act_to_f32<AT>((uint16_t)(wk >> 16)), p.k_scale);
+        const float v0 = __fdiv_rn(act_to_f32<AT>((uint16_t)(wv & 0xFFFFu)), p.v_scale);
+        const float v1 = __fdiv_rn(act_to_f32<AT>((uint16_t)(wv >> 16)), p.v_scale);
+        kb |= f32x2_to_e4m3x2(k0, k1) << (16 * q);
+        vb |= f32x2_to_e4m3x2(v0, v1) << (16 * q);
+      }
+      ko[h] = kb;
+      vo[h] = vb;
+    }
+    *reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(p.k_cache) + dst) = make_uint2(ko[0], ko[1]);
+    *reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(p.v_cache) + dst) = make_uint2(vo[0], vo[1]);
+  }
+}
+
+template <int CT, int AT>
+cudaError_t launch_append_t(const AppendParams& p, cudaStream_t stream) {
+  const int64_t total = p.num_tokens * p.num_kv_heads * (p.head_dim / 8);
+  if (total == 0) return cudaSuccess;
+  const unsigned blocks = (unsigned)((total + 255) / 256);
+  append_kernel<CT, AT><<<blocks, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_append(const AppendParams& p, int cache_dt, int act_dt, cudaStream_t stream) {
+  if (cache_dt == DT_F16 && act_dt == DT_F16) return launch_append_t<DT_F16, DT_F16>(p, stream);
+  if (cache_dt == DT_BF16 && act_dt == DT_BF16) return launch_append_t<DT_BF16, DT_BF16>(p, stream);
+  if (cache_dt == DT_E4M3 && act_dt == DT_F16) return launch_append_t<DT_E4M3, DT_F16>(p, stream);
+  if (cache_dt == DT_E4M3 && act_dt == DT_BF16) return launch_append_t<DT_E4M3, DT_BF16>(p, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pkv

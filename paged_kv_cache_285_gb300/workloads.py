@@ -138,9 +138,12 @@ def _alloc_tables(caps, bs, pool_blocks, perm_gen, shared_blocks=0, max_blocks=N
 
 def _slots(tables, positions, bs):
     pos = positions.to(torch.int64)
-    blk = tables.to(torch.int64).gather(1, (pos // bs).clamp(min=0)[:, None])[:, 0]
+    width = tables.shape[1]
+    lb = pos // bs
+    inside = (pos >= 0) & (lb < width)
+    blk = tables.to(torch.int64).gather(1, lb.clamp(0, width - 1)[:, None])[:, 0]
     slot = blk * bs + pos % bs
-    return torch.where((blk >= 0) & (pos >= 0), slot, torch.full_like(slot, -1))
+    return torch.where(inside & (blk >= 0), slot, torch.full_like(slot, -1))
 
 
 def _replicate_prefix_tail(case_k, case_v, tables, prefix, bs):

@@ -2,12 +2,12 @@
 the output comparison rule.
 
 Comparison rule (the tolerance the attention results are held to):
-  * 16-bit outputs: max-abs <= 2e-3 and relative L2 <= 1e-3 between the GPU
-    output and the fp64 oracle output rounded once (round-to-nearest-even) to
-    the output dtype.  Rounding the oracle first is needed because rounding a
-    correctly computed result to bfloat16 alone already gives a relative L2
-    near 1.6e-3; besides, the unrounded oracle must lie within 2e-3 plus half
-    an output ulp of every GPU element.
+  * 16-bit outputs: every element lies within 2e-3 plus half an output ulp
+    of the fp64 oracle (rounding a bf16 value in [1, 2) alone can move it by
+    3.9e-3, so the 2e-3 bound applies to the error beyond the output's own
+    rounding), and the relative L2 error against the fp64 oracle rounded once
+    (round-to-nearest-even) to the output dtype is <= 1e-3 (against the
+    unrounded oracle, bf16 rounding alone gives ~1.6e-3).
   * fp8 caches: max-abs <= 3e-2 against the oracle run on the same codes.
 """
 from __future__ import annotations
@@ -68,15 +68,16 @@ def assert_attention_close(gpu, ref, act_dtype, fp8=False, what=""):
         err = np.max(np.abs(gpu - ref))
         assert err <= 3e-2, f"{what}: fp8 max-abs {err:.3e} > 3e-2"
         return
+    # max-abs: the error beyond the output's own rounding (half an ulp of the act
+    # dtype at the exact value) stays within 2e-3
+    excess = np.abs(gpu - ref) - half_ulp(ref, act_dtype)
+    worst = float(np.max(excess))
+    assert worst <= 2e-3, f"{what}: max-abs beyond output rounding {worst:.3e} > 2e-3"
+    # relative L2 against the oracle rounded once to the output dtype
     ref_r = round_to(ref, act_dtype)
-    err = np.max(np.abs(gpu - ref_r))
     den = np.linalg.norm(ref_r)
     rel = np.linalg.norm(gpu - ref_r) / den if den > 0 else np.linalg.norm(gpu - ref_r)
-    assert err <= 2e-3, f"{what}: max-abs {err:.3e} > 2e-3 (vs rounded oracle)"
     assert rel <= 1e-3, f"{what}: rel-L2 {rel:.3e} > 1e-3 (vs rounded oracle)"
-    bound = 2e-3 + half_ulp(ref, act_dtype)
-    worst = np.max(np.abs(gpu - ref) - bound)
-    assert worst <= 0, f"{what}: element beyond 2e-3 + half ulp of the unrounded oracle"
 
 
 def to_f64(t: torch.Tensor):

@@ -1,0 +1,112 @@
+"""The C ABI without a GPU: libpkv.so builds, loads, exports every symbol that
+include/pkv.h declares, and rejects bad arguments on the host before it
+touches CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_cache_285_gb300 as pkv
+from paged_kv_cache_285_gb300 import build as pkv_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pkv_build.build()
+    return pkv.load()
+
+
+def declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn), encoding="utf-8").read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_symbols()
+    assert {"pkv_kv_append", "pkv_paged_decode_attn", "pkv_paged_extend_attn"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"libpkv.so does not export {n}"
+
+
+def test_status_strings_and_version(lib):
+    assert pkv.status_string(0) == "PKV_OK"
+    assert pkv.status_string(3) == "PKV_ERR_WORKSPACE"
+    assert pkv.status_string(99) == "PKV_ERR_UNKNOWN"
+    assert pkv.version() == 10000
+
+
+def _desc(**kw):
+    d = dict(num_blocks=8, block_size=16, num_kv_heads=2, head_dim=128, cache_dtype=1,
+             k_scale=1.0, v_scale=1.0)
+    d.update(kw)
+    return pkv.CacheDesc(**d)
+
+
+FAKE = ctypes.c_void_p(0x10000)  # never dereferenced: every call below fails validation first
+
+
+def _decode(lib, desc, hq=4, act=1, batch=2, splits=0, scale=0.1, ws=None, ws_bytes=0):
+    return lib.pkv_paged_decode_attn(ctypes.byref(desc), FAKE, FAKE, FAKE, FAKE, act, FAKE, 4,
+                                     FAKE, batch, hq, scale, 64, splits, None, ws, ws_bytes, None)
+
+
+def test_decode_argument_errors(lib):
+    assert _decode(lib, _desc(), hq=3) == 1                 # Hq % Hkv != 0
+    assert _decode(lib, _desc(head_dim=96)) == 2            # unsupported head_dim
+    assert _decode(lib, _desc(block_size=8)) == 2           # unsupported block size
+    assert _decode(lib, _desc(num_blocks=0)) == 1
+    assert _decode(lib, _desc(), act=0) == 2                # bf16 cache with f16 queries
+    assert _decode(lib, _desc(), act=2) == 1                # fp8 is not an act dtype
+    assert _decode(lib, _desc(), hq=2 * 9) == 2             # GQA group of 9 > 8
+    assert _decode(lib, _desc(cache_dtype=2, k_scale=0.0)) == 1   # fp8 needs scales > 0
+    assert _decode(lib, _desc(), scale=float("nan")) == 1
+    assert _decode(lib, _desc(), batch=-1) == 1
+    assert _decode(lib, _desc(), batch=0) == 0              # empty batch: nothing to do
+    assert lib.pkv_paged_decode_attn(None, FAKE, FAKE, FAKE, FAKE, 1, FAKE, 4, FAKE, 2, 4, 0.1,
+                                     64, 0, None, None, 0, None) == 1
+
+
+def test_append_argument_errors(lib):
+    d = _desc()
+    call = lambda desc, act=1, n=4, slots=FAKE: lib.pkv_kv_append(
+        ctypes.byref(desc), FAKE, FAKE, FAKE, FAKE, act, slots, n, None)
+    assert call(d, n=-1) == 1
+    assert call(d, n=0) == 0
+    assert call(d, act=0) == 2
+    assert call(d, slots=None) == 1
+    assert call(_desc(head_dim=80)) == 2
+
+
+def test_extend_argument_errors(lib):
+    d = _desc()
+    r = lib.pkv_paged_extend_attn(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, 1, FAKE, FAKE, FAKE, 4,
+                                  1, 3, 0.1, 10, 10, 100, None, None, 0, None)
+    assert r == 1                                            # Hq % Hkv != 0
+
+
+def test_decode_workspace_plan(lib):
+    # forced 4 splits over max_seq_len 1000: 63 tiles of 16 -> 16 tiles (256 tokens) per
+    # split -> 4 splits; partials 2*8*4*128 floats (256-byte aligned) + 2*8*4 LSE floats
+    d = _desc()
+    assert pkv.decode_workspace_bytes(torch_free_cache(d), 2, 8, 1000, num_splits=4) == \
+        2 * 8 * 4 * 128 * 4 + 2 * 8 * 4 * 4
+    assert pkv.decode_workspace_bytes(torch_free_cache(d), 2, 8, 1000, num_splits=1) == 0
+
+
+class torch_free_cache:
+    """Stand-in with the shape/dtype the binding reads (no device memory)."""
+    def __init__(self, d):
+        import torch
+        self.shape = (d.num_blocks, d.num_kv_heads, d.block_size, d.head_dim)
+        self.dtype = torch.bfloat16
+
+    def dim(self):
+        return 4

@@ -1,0 +1,82 @@
+"""GPU parity of pkv_kv_append against the oracle: bit-exact over the whole
+cache pool (so a stray write anywhere shows up), for 16-bit copies and the fp8
+store, plus skipped / out-of-pool slots."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_285_gb300 as pkv
+from paged_kv_cache_285_gb300 import workloads as W
+from tests.pkv_testlib import BF16, E4M3, F16
+
+pytestmark = pytest.mark.gpu
+S = W.to_numpy_storage
+
+
+def _check_append(k_cache, v_cache, cdt, ks, vs, new_k, new_v, adt, slots):
+    k0, v0 = S(k_cache), S(v_cache)
+    pkv.kv_append(k_cache, v_cache, new_k, new_v, slots, k_scale=ks, v_scale=vs)
+    torch.cuda.synchronize()
+    kr, vr, st = oracle.kv_append(k0, v0, cdt, ks, vs, S(new_k), S(new_v), adt, slots.cpu().numpy())
+    np.testing.assert_array_equal(S(k_cache), kr)
+    np.testing.assert_array_equal(S(v_cache), vr)
+    return st
+
+
+def test_tiny_append_next_position():
+    # one token per request at position seq_len; the 16-token request needs its new block
+    case = W.tiny_decode(device="cuda")
+    assert _check_append(case.k_cache, case.v_cache, F16, 1, 1, case.new_k, case.new_v, F16,
+                         case.slot_next) == 0
+    assert pkv.get_device_error() == 0
+
+
+@pytest.mark.parametrize("cdt,adt", [(BF16, BF16), (F16, F16), (E4M3, BF16), (E4M3, F16)])
+def test_bulk_suffix_append(cdt, adt):
+    # 32 requests x 100 suffix tokens after a shared 1,900-token prefix
+    case = W.extend_case([1900] * 32, [100] * 32, 32, 8, 128, 16, cdt, adt, seed=50,
+                         device="cuda", shared_prefix=1900)
+    assert _check_append(case.k_cache, case.v_cache, cdt, case.k_scale, case.v_scale, case.suffix_k,
+                         case.suffix_v, adt, case.suffix_slots) == 0
+
+
+@pytest.mark.parametrize("adt", [BF16, F16])
+def test_fp8_store_edge_values(adt):
+    # saturation, ties between codes, subnormals and signed zero through the real kernel
+    d, hkv = 64, 1
+    k = torch.zeros((4, hkv, 16, d), dtype=torch.uint8, device="cuda")
+    v = torch.zeros_like(k)
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    finite = codes.view(torch.float8_e4m3fn).float()
+    finite = finite[torch.isfinite(finite)].unique()
+    mids = (finite[1:] + finite[:-1]) / 2
+    extra = torch.tensor([0.0, -0.0, 500.0, -1e4, 1e30, float("inf"), float("-inf"), 448.0,
+                          464.0, -464.0, 2.0 ** -10, 3 * 2.0 ** -10])
+    vals = torch.cat([finite, mids, extra])
+    tdt = torch.bfloat16 if adt == BF16 else torch.float16
+    vals = vals[: (vals.numel() // d) * d]
+    rows = vals.numel() // d
+    x = vals.reshape(rows, hkv, d).to(tdt)
+    slots = torch.arange(rows, dtype=torch.int64) * 3 % 64
+    _check_append(k, v, E4M3, 0.5, 1.0, x.cuda(), (-x).cuda(), adt, slots.cuda())
+
+
+def test_skip_negative_and_out_of_pool():
+    case = W.decode_case([20, 30, 5], 8, 2, 128, 16, BF16, BF16, seed=51, device="cuda")
+    nb = case.k_cache.shape[0]
+    slots = torch.tensor([-1, nb * 16 + 3, 17], dtype=torch.int64, device="cuda")
+    assert pkv.get_device_error() == 0
+    st = _check_append(case.k_cache, case.v_cache, BF16, 1, 1, case.new_k, case.new_v, BF16, slots)
+    assert st == 1
+    assert pkv.get_device_error() == 2  # PKV_DEVERR_BAD_SLOT, then cleared
+    assert pkv.get_device_error() == 0
+
+
+def test_zero_tokens_is_noop():
+    case = W.decode_case([20], 8, 2, 128, 16, BF16, BF16, seed=52, device="cuda")
+    before = S(case.k_cache)
+    pkv.kv_append(case.k_cache, case.v_cache, case.new_k[:0], case.new_v[:0],
+                  case.slot_last[:0])
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(S(case.k_cache), before)
