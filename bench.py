@@ -1,0 +1,481 @@
+"""Benchmark of the paged-KV attention hot path on one GB300 (or N replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl pkv|reference]
+
+One step of the default workload (a Llama-3-8B-shaped decode layer: 64
+requests, seq_lens uniform in [512, 4096], 32 q / 8 kv heads, d128, bf16,
+16-token blocks randomly permuted over the pool) is the whole decode hot path:
+kv_append of every request's current token into its slot, then
+paged_decode_attn (split-KV + LSE merge) over every cached token.  The same
+line reports the suffix-prefill hot path (paged_extend_attn over a shared
+1,900-token cached prefix, 256 requests x 100 suffix tokens) in its own
+object.
+
+Printed (rank 0, one JSON line): value = algorithmic HBM bytes of the step /
+device time (GB/s), decode tokens/s, the roofline of the dominant call
+(paged_decode_attn) against the measured copy bandwidth, the fp64 CPU oracle
+as a baseline, an end-to-end number through host buffers and the SM clocks
+sampled while timing.  `--impl reference` times the fp64 CPU oracle itself
+on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "paged decode attn HBM GB/s (% of GB300 peak) & tokens/s; extend TFLOP/s"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ---------------------------------------------------------------------------------
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0)), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def src_hash(*rel):
+    h = hashlib.sha256()
+    for r in rel:
+        with open(os.path.join(ROOT, r), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(name, sources):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source is unchanged."""
+    path = os.path.join(ROOT, "profiles", name)
+    try:
+        kv = {}
+        with open(path, encoding="utf-8") as f:
+            for line in f:
+                if line.startswith("- ") and ":" in line:
+                    k, v = line[2:].split(":", 1)
+                    kv[k.strip()] = v.strip().strip("`")
+        if kv.get("source_sha256_16") != src_hash(*sources):
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed loop runs."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.samples = []
+        if self.proc is None:
+            return False
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append(parts)
+        return False
+
+    def summary(self):
+        if not getattr(self, "samples", None):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = sorted(float(s[0]) for s in self.samples if s[0].replace(".", "").isdigit())
+        mx = max((float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()), default=None)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for s in self.samples:
+            for n, v in zip(names, s[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(self.samples)}
+
+
+# ---------------------------------------------------------------------------------
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Largest value over all ranks (the slowest rank sets the job's time)."""
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------------
+def decode_step_bytes(case):
+    """Algorithmic HBM bytes of one step: append of B tokens + decode over sum(seq_lens)."""
+    from paged_kv_cache_285_gb300 import workloads as W
+    b = case.q.shape[0]
+    hq, hkv, d = case.num_q_heads, case.num_kv_heads, case.head_dim
+    ce = W.ELEM_BYTES[case.cache_dtype]
+    ae = 2
+    ntok = int(case.seq_lens.sum())
+    nblk = int(sum(math.ceil(int(n) / case.block_size) for n in case.seq_lens.tolist()))
+    append = b * hkv * d * (ae + ce) * 2 + 8 * b
+    decode = ntok * hkv * d * ce * 2 + 2 * b * hq * d * ae + 4 * nblk + 4 * b
+    return append, decode
+
+
+def run_decode_bench(args, world, rank, local):
+    import paged_kv_cache_285_gb300 as pkv
+    from paged_kv_cache_285_gb300 import workloads as W
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pkv.load()
+    makers = {"llama3_8b_layer": (W.llama3_8b_decode, 4096),
+              "fp8_70b_layer": (W.fp8_70b_decode, 4096),
+              "shared_prefix_decode": (W.shared_prefix_decode, 1256),
+              "tiny": (lambda device: W.tiny_decode(device=device), 60)}
+    mk, max_len = makers[args.workload]
+    case = mk(device="cuda")
+    b = case.q.shape[0]
+    out = torch.empty_like(case.q)
+    ws_bytes = pkv.decode_workspace_bytes(case.k_cache, b, case.num_q_heads, max_len, 0,
+                                          case.k_scale, case.v_scale)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def append():
+        pkv.kv_append(case.k_cache, case.v_cache, case.new_k, case.new_v, case.slot_last,
+                      k_scale=case.k_scale, v_scale=case.v_scale)
+
+    def decode():
+        pkv.paged_decode_attn(case.k_cache, case.v_cache, case.q, out, case.block_tables,
+                              case.seq_lens, case.sm_scale, max_len, k_scale=case.k_scale,
+                              v_scale=case.v_scale, workspace=ws)
+
+    for _ in range(args.warmup):
+        append()
+        decode()
+    torch.cuda.synchronize()
+    # The step's launches are captured once into CUDA graphs and replayed, so the
+    # device time is not stretched by host-side enqueue cost (Python + ctypes).
+    g_step, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(g_step, stream=cap):
+            append()
+            decode()
+        with torch.cuda.graph(g_dec, stream=cap):
+            decode()
+    stream.wait_stream(cap)
+    for _ in range(args.warmup):
+        g_step.replay()
+        g_dec.replay()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_wall = time.perf_counter()
+        for i in range(K):
+            flush.zero_()                       # evict the pool from L2 between steps
+            ev[i][0].record(stream)
+            g_step.replay()
+            ev[i][1].record(stream)
+            flush.zero_()
+            ev[i][2].record(stream)
+            g_dec.replay()                      # the decode call alone, for its roofline
+            ev[i][3].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    barrier(world)
+    step_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    dec_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    ms_step = sum(step_ms) / K
+    ms_dec = sum(dec_ms) / K
+    ms_step_max = max_over_ranks(ms_step, world)
+
+    app_b, dec_b = decode_step_bytes(case)
+    step_bytes = app_b + dec_b
+    hbm, bf16, bf16_sus, peak_src = peaks()
+    value = world * step_bytes / (ms_step_max * 1e-3) / 1e9
+    dec_gbs = dec_b / (ms_dec * 1e-3) / 1e9
+    splits_plan = ws_bytes > 0
+    launches_per_step = 1 + 1 + (1 if splits_plan else 0)
+
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step_max, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": W.DTYPE_NAME[case.cache_dtype],
+        "data": "synthetic (seeded N(0,1) K/V/q, random block permutation)",
+        "config": {"workload": args.workload, "batch": b, "num_q_heads": case.num_q_heads,
+                   "num_kv_heads": case.num_kv_heads, "head_dim": case.head_dim,
+                   "block_size": case.block_size, "cache_dtype": W.DTYPE_NAME[case.cache_dtype],
+                   "act_dtype": W.DTYPE_NAME[case.act_dtype],
+                   "cached_tokens": int(case.seq_lens.sum()),
+                   "step": "kv_append(1 token/request) + paged_decode_attn, one CUDA graph",
+                   "l2": "256 MiB buffer written between timed steps (outside the events)",
+                   "parallelism": f"replicas x{world}"},
+        "pct_of_peak": round(100.0 * value / world / hbm, 1),
+        "tokens_per_s": round(world * b / (ms_step_max * 1e-3), 1),
+        "gpu_launches": 2 * launches_per_step * K - K,
+    }
+    traffic = profiled_traffic("decode_kernel_llama3_8b_layer.md",
+                               ["paged_kv_cache_285_gb300/csrc/decode.cu",
+                                "paged_kv_cache_285_gb300/csrc/ptx.cuh"]) \
+        if args.workload == "llama3_8b_layer" else None
+    res["roofline"] = {"kernel": "paged_decode_attn (decode_kernel + merge_kernel)",
+                       "bound": "hbm", "achieved": round(dec_gbs, 1), "peak": hbm,
+                       "unit": "GB/s", "frac": round(dec_gbs / hbm, 4),
+                       "peak_source": f"{peak_src} (hbm_gbs)",
+                       "algorithmic_bytes_per_launch": dec_b,
+                       "traffic": traffic}
+    res["clocks"] = clk.summary()
+    res["wall_s_timed"] = round(t_wall, 3)
+
+    # end to end through the C ABI with host buffers: per step the inputs of the
+    # step (q, the new token's K/V, its slot, seq_lens, block tables) go host->device
+    # from pinned memory and the output comes back device->host
+    res["e2e"] = e2e_decode(case, pkv, max_len, ws, out, stream, K, world)
+    if args.extend and rank == 0 and world == 1:
+        res["extend"] = run_extend_bench(args, dev, bf16, bf16_sus, peak_src)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline_decode(case, budget_s=args.cpu_seconds)
+    return res
+
+
+def e2e_decode(case, pkv, max_len, ws, out, stream, K, world):
+    host = {}
+    names = ["q", "new_k", "new_v", "slot_last", "seq_lens", "block_tables"]
+    for n in names:
+        t = getattr(case, n)
+        host[n] = t.to("cpu").pin_memory()
+    dev_t = {n: torch.empty_like(getattr(case, n)) for n in names}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+    d2h = out_h.numel() * out_h.element_size()
+
+    def step():
+        for n in names:
+            dev_t[n].copy_(host[n], non_blocking=True)
+        pkv.kv_append(case.k_cache, case.v_cache, dev_t["new_k"], dev_t["new_v"],
+                      dev_t["slot_last"], k_scale=case.k_scale, v_scale=case.v_scale)
+        pkv.paged_decode_attn(case.k_cache, case.v_cache, dev_t["q"], out,
+                              dev_t["block_tables"], dev_t["seq_lens"], case.sm_scale, max_len,
+                              k_scale=case.k_scale, v_scale=case.v_scale, workspace=ws)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=out.device)
+    tot = 0.0
+    for _ in range(K):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        e1.synchronize()
+        tot += e0.elapsed_time(e1)
+    ms = max_over_ranks(tot / K, world)
+    app_b, dec_b = decode_step_bytes(case)
+    return {"value": round(world * (app_b + dec_b) / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "ms_per_step": round(ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def run_extend_bench(args, dev, bf16, bf16_sus, peak_src):
+    """paged_extend_attn on 256 requests x 100 suffix tokens over a shared 1,900-token
+    prefix (useful causal flops only), with the suffix's kv_append in the step."""
+    import paged_kv_cache_285_gb300 as pkv
+    from paged_kv_cache_285_gb300 import workloads as W
+    try:
+        case = W.shared_prefix_extend(device="cuda")
+    except Exception as e:  # pragma: no cover
+        return {"error": str(e)}
+    rows = case.q.shape[0]
+    out = torch.empty_like(case.q)
+    P, Sfx = 1900, 100
+    B = case.prefix_lens.shape[0]
+
+    def append():
+        pkv.kv_append(case.k_cache, case.v_cache, case.suffix_k, case.suffix_v, case.suffix_slots)
+
+    def extend():
+        pkv.paged_extend_attn(case.k_cache, case.v_cache, case.q, out, case.q_indptr,
+                              case.prefix_lens, case.block_tables, case.sm_scale, Sfx, P + Sfx)
+
+    try:
+        extend()
+    except pkv.PkvError as e:
+        return {"status": "not built", "error": str(e)}
+    for _ in range(3):
+        append()
+        extend()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    n = max(5, min(50, args.steps))
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    t_ext = t_step = 0.0
+    for _ in range(n):
+        flush.zero_()
+        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        e0.record(stream)
+        append()
+        e1.record(stream)
+        extend()
+        e2.record(stream)
+        e2.synchronize()
+        t_ext += e1.elapsed_time(e2)
+        t_step += e0.elapsed_time(e2)
+    t_ext /= n
+    t_step /= n
+    hq, d = case.num_q_heads, case.head_dim
+    keys = sum(P + i + 1 for i in range(Sfx))
+    flops = 4.0 * d * hq * keys * B
+    tf = flops / (t_ext * 1e-3) / 1e12
+    return {"workload": "shared_prefix_extend", "batch": B, "prefix": P, "suffix": Sfx,
+            "num_q_heads": hq, "num_kv_heads": case.num_kv_heads, "head_dim": d,
+            "ms_per_call": round(t_ext, 5), "ms_per_step_with_append": round(t_step, 5),
+            "tflops": round(tf, 1), "useful_flops_per_call": flops,
+            "roofline": {"kernel": "paged_extend_attn", "bound": "tensor", "achieved": round(tf, 1),
+                         "peak": bf16, "unit": "TFLOP/s", "frac": round(tf / bf16, 4),
+                         "peak_source": f"{peak_src} (bf16_tflops burst)", "traffic": None}}
+
+
+def cpu_baseline_decode(case, budget_s=10.0):
+    """The fp64 C oracle (OpenMP over (request, head)) on this host, on whole passes
+    over the same decode layer until `budget_s` seconds have been spent."""
+    import oracle
+    from paged_kv_cache_285_gb300 import workloads as W
+    S = W.to_numpy_storage
+    k, v, q = S(case.k_cache), S(case.v_cache), S(case.q)
+    bt, sl = case.block_tables.cpu().numpy(), case.seq_lens.cpu().numpy()
+    app_b, dec_b = decode_step_bytes(case)
+    # sample: the first requests of the batch, enlarged until one pass takes >= 1/4 budget
+    nreq = 4
+    while True:
+        pairs = [(bb, h) for bb in range(nreq) for h in range(case.num_q_heads)]
+        t0 = time.perf_counter()
+        oracle.paged_decode(k, v, case.cache_dtype, case.k_scale, case.v_scale, q, case.act_dtype,
+                            bt, sl, case.num_q_heads, case.sm_scale, pairs=pairs)
+        dt = time.perf_counter() - t0
+        if dt >= budget_s / 4 or nreq >= len(sl):
+            break
+        nreq = min(len(sl), nreq * 2)
+    passes, tot = 1, dt
+    while tot < budget_s:
+        t0 = time.perf_counter()
+        oracle.paged_decode(k, v, case.cache_dtype, case.k_scale, case.v_scale, q, case.act_dtype,
+                            bt, sl, case.num_q_heads, case.sm_scale, pairs=pairs)
+        tot += time.perf_counter() - t0
+        passes += 1
+    frac = float(sl[:nreq].sum()) / float(sl.sum())
+    sample_bytes = dec_b * frac
+    return {"value": round(sample_bytes * passes / tot / 1e9, 4), "unit": "GB/s",
+            "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"fp64 C oracle decode of requests 0..{nreq - 1} of {len(sl)} "
+                      f"(all {case.num_q_heads} heads), {passes} passes in {tot:.1f} s"}
+
+
+def run_reference(args, world, rank):
+    """The fp64 CPU oracle timed as the reference arm (rank 0 only)."""
+    if rank != 0:
+        return None
+    from paged_kv_cache_285_gb300 import workloads as W
+    case = W.llama3_8b_decode(device="cpu") if args.workload == "llama3_8b_layer" else None
+    if case is None:
+        return {"impl": "reference", "unavailable": f"no oracle arm for workload {args.workload}"}
+    base = cpu_baseline_decode(case, budget_s=max(2.0, min(20.0, args.cpu_seconds)))
+    val = base["value"]
+    return {"impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "step": "decode attention, fp64 CPU oracle"},
+            "cpu_baseline": base,
+            "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
+    ap.add_argument("--workload", default="llama3_8b_layer",
+                    choices=["llama3_8b_layer", "fp8_70b_layer", "shared_prefix_decode", "tiny"])
+    ap.add_argument("--no-extend", dest="extend", action="store_false")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)
+    world, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        res = run_reference(args, world, rank)
+    else:
+        res = run_decode_bench(args, world, rank, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
