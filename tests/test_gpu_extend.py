@@ -1,0 +1,129 @@
+"""GPU parity of pkv_paged_extend_attn (suffix prefill over cached prefix
+blocks) against the fp64 oracle: ragged suffixes spanning several 128-row
+tiles, prefixes that end mid-block, every GQA group the kernel takes, both
+block sizes and 16-bit dtypes; the 1,900 + 100 case of the first page; and the
+256-request shared-prefix workload the benchmark times (sampled rows)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_285_gb300 as pkv
+from paged_kv_cache_285_gb300 import workloads as W
+from tests.pkv_testlib import BF16, E4M3, F16, assert_attention_close, to_f64
+
+pytestmark = pytest.mark.gpu
+S = W.to_numpy_storage
+
+
+def gpu_extend(case):
+    out = torch.full_like(case.q, float("nan"))
+    rows, hq, _ = case.q.shape
+    lse = torch.full((rows, hq), float("nan"), dtype=torch.float32, device="cuda")
+    suf = (case.q_indptr[1:] - case.q_indptr[:-1]).cpu()
+    tot = case.prefix_lens.cpu() + suf
+    pkv.paged_extend_attn(case.k_cache, case.v_cache, case.q, out, case.q_indptr,
+                          case.prefix_lens, case.block_tables, case.sm_scale,
+                          int(suf.max()), int(tot.max()), k_scale=case.k_scale,
+                          v_scale=case.v_scale, lse_out=lse)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def check(case, out, lse, what, rows=None):
+    args = (S(case.k_cache), S(case.v_cache), case.cache_dtype, case.k_scale, case.v_scale,
+            S(case.q), case.act_dtype, case.q_indptr.cpu().numpy(), case.prefix_lens.cpu().numpy(),
+            case.block_tables.cpu().numpy(), case.num_q_heads, case.sm_scale)
+    ref, ref_lse, st = oracle.paged_extend(*args, rows=rows)
+    assert st == 0
+    got, gl = to_f64(out), lse.cpu().double().numpy()
+    if rows is not None:
+        got = np.stack([got[r, h] for r, h in rows])
+        gl = np.array([gl[r, h] for r, h in rows])
+    assert_attention_close(got, ref, case.act_dtype, what=what)
+    assert np.max(np.abs(gl - ref_lse)) <= 1e-3, what
+
+
+CASES = [
+    # (prefix_lens, suffix_lens, hq, hkv, bs, dtype)
+    ([0], [5], 4, 1, 16, F16),
+    ([4], [1], 4, 1, 16, F16),
+    ([1900], [100], 32, 8, 16, BF16),
+    ([0, 13, 30, 200], [37, 19, 130, 1], 8, 2, 16, BF16),
+    ([100, 0], [300, 129], 8, 8, 32, F16),
+    ([17, 250], [64, 33], 16, 2, 16, BF16),
+    ([129, 64, 1], [200, 17, 256], 64, 8, 16, BF16),
+    ([500], [40], 4, 2, 32, BF16),
+]
+
+
+@pytest.mark.parametrize("cfg", CASES, ids=lambda c: f"P{c[0]}-S{c[1]}-h{c[2]}x{c[3]}-bs{c[4]}-d{c[5]}")
+def test_extend_small(cfg):
+    P, Sx, hq, hkv, bs, dt = cfg
+    case = W.extend_case(P, Sx, hq, hkv, 128, bs, dt, dt, seed=sum(P) + sum(Sx) + hq, device="cuda")
+    out, lse = gpu_extend(case)
+    check(case, out, lse, str(cfg))
+    assert pkv.get_device_error() == 0
+
+
+def test_extend_matches_full_prefill_rows():
+    # 1,900 cached + 100 suffix == rows 1,900..1,999 of prefilling all 2,000 tokens
+    ext = W.extend_case([1900], [100], 32, 8, 128, 16, BF16, BF16, seed=70, device="cuda")
+    out_e, lse_e = gpu_extend(ext)
+    full = W.PagedBatch  # same pool and table, prefix 0, 2,000 query rows
+    q_full = torch.zeros((2000, 32, 128), dtype=torch.bfloat16, device="cuda")
+    q_full[1900:] = ext.q
+    pre = W.ExtendCase(k_cache=ext.k_cache, v_cache=ext.v_cache, cache_dtype=BF16, act_dtype=BF16,
+                       k_scale=1.0, v_scale=1.0, block_tables=ext.block_tables, num_q_heads=32,
+                       sm_scale=ext.sm_scale,
+                       q_indptr=torch.tensor([0, 2000], dtype=torch.int32, device="cuda"),
+                       prefix_lens=torch.tensor([0], dtype=torch.int32, device="cuda"), q=q_full)
+    out_p, lse_p = gpu_extend(pre)
+    del full
+    a = to_f64(out_e)
+    b = to_f64(out_p[1900:])
+    assert np.max(np.abs(a - b)) <= 2e-3
+    check(ext, out_e, lse_e, "1900+100")
+
+
+def test_shared_prefix_extend_workload_sampled():
+    case = W.shared_prefix_extend(device="cuda")
+    out, lse = gpu_extend(case)
+    rng = np.random.default_rng(3)
+    rows = [(int(r), int(h)) for r, h in zip(rng.integers(0, case.q.shape[0], 96),
+                                              rng.integers(0, 32, 96))]
+    check(case, out, lse, "shared-prefix extend", rows=rows)
+    assert pkv.get_device_error() == 0
+
+
+def test_extend_after_bulk_append():
+    # the step the benchmark times: append the suffix K/V, then extend over the pool
+    case = W.extend_case([1900] * 4, [100] * 4, 32, 8, 128, 16, BF16, BF16, seed=71,
+                         device="cuda", shared_prefix=1900)
+    k0, v0 = S(case.k_cache), S(case.v_cache)
+    pkv.kv_append(case.k_cache, case.v_cache, case.suffix_k, case.suffix_v, case.suffix_slots)
+    out, lse = gpu_extend(case)
+    kr, vr, st = oracle.kv_append(k0, v0, BF16, 1, 1, S(case.suffix_k), S(case.suffix_v), BF16,
+                                  case.suffix_slots.cpu().numpy())
+    assert st == 0
+    ref, _, st = oracle.paged_extend(kr, vr, BF16, 1, 1, S(case.q), BF16, case.q_indptr.cpu().numpy(),
+                                     case.prefix_lens.cpu().numpy(), case.block_tables.cpu().numpy(),
+                                     32, case.sm_scale)
+    assert st == 0
+    assert_attention_close(to_f64(out), ref, BF16, what="append+extend")
+
+
+def test_extend_garbage_past_end_is_ignored():
+    case = W.extend_case([30], [20], 8, 2, 128, 16, BF16, BF16, seed=72, device="cuda")
+    total = 50
+    blk = int(case.block_tables[0, (total - 1) // 16])
+    case.k_cache[blk, :, total % 16:] = float("inf")
+    case.v_cache[blk, :, total % 16:] = float("nan")
+    out, lse = gpu_extend(case)
+    check(case, out, lse, "garbage tail")
+
+
+def test_extend_unsupported_combinations_raise():
+    case = W.extend_case([4], [4], 4, 1, 64, 16, F16, F16, seed=73, device="cuda")
+    with pytest.raises(pkv.PkvError):
+        gpu_extend(case)  # head_dim 64 is not built for extend
