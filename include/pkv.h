@@ -171,6 +171,42 @@ pkv_status pkv_paged_decode_attn(const pkv_cache_desc* desc, const void* k_cache
  * Supported: head_dim 128, block_size 16/32, num_q_heads/num_kv_heads in
  * {1, 2, 4, 8}, 16-bit caches and fp8.
  * ------------------------------------------------------------------------- */
+/* ---------------------------------------------------------------------------
+ * pkv_paged_decode_attn_noalloc -- the same decode as pkv_paged_decode_attn,
+ * for callers that cannot allocate device memory.
+ *
+ * The pages describe no such call; it exists for integration only.  Some
+ * callers have no way to obtain a workspace: a plugin inside an engine that
+ * owns all device memory and passes in only the tensors of the call, or a
+ * latency-critical path where cudaMalloc (which may synchronise the device or
+ * fail under memory pressure) is not allowed.  This entry point takes no
+ * workspace: the split-KV partials go to a scratch array compiled into the
+ * library, PKV_NOALLOC_SCRATCH_BYTES (16 MiB) per device, held by every GPU
+ * that loads the library until the process exits.  The call allocates
+ * nothing.
+ *
+ * Arguments, layouts and results are those of pkv_paged_decode_attn.
+ * Errors: PKV_ERR_WORKSPACE if the split plan for these arguments needs more
+ * than PKV_NOALLOC_SCRATCH_BYTES (pkv_decode_workspace_bytes() tells the
+ * size; a smaller num_splits, e.g. 1, needs none), before anything is
+ * enqueued; PKV_ERR_CUDA if the scratch address cannot be obtained.
+ * The first call on each device looks up the scratch array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.
+ * All calls on one device share the scratch array and leave their partials
+ * in it: calls whose work overlaps on the GPU (other streams, concurrent graph
+ * branches) race and may produce wrong results.  Serialise them.
+ * ------------------------------------------------------------------------- */
+#define PKV_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+pkv_status pkv_paged_decode_attn_noalloc(const pkv_cache_desc* desc, const void* k_cache,
+                                         const void* v_cache, const void* q, void* out,
+                                         pkv_dtype act_dtype, const int32_t* block_tables,
+                                         int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                         int32_t batch, int32_t num_q_heads, float sm_scale,
+                                         int32_t max_seq_len, int32_t num_splits,
+                                         float* lse_out, cudaStream_t stream);
+
 size_t pkv_extend_workspace_bytes(const pkv_cache_desc* desc, int32_t batch,
                                   int32_t num_q_heads, int32_t total_q_rows,
                                   int32_t max_total_len);
