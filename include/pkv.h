@@ -164,6 +164,7 @@ pkv_status pkv_paged_decode_attn(const pkv_cache_desc* desc, const void* k_cache
  * q, out:        [q_indptr[batch]][num_q_heads][head_dim] act dtype.
  * q_indptr:      int32 [batch+1], device, non-decreasing, q_indptr[0] = 0.
  * prefix_lens:   int32 [batch], device.
+ * sm_scale:      softmax scale, finite and > 0.
  * max_suffix_len / max_total_len: host-side upper bounds of S_b and P_b+S_b.
  * total_q_rows:  q_indptr[batch] (host value; sizes the grid).
  * lse_out:       nullable float [q_indptr[batch]][num_q_heads], natural log.

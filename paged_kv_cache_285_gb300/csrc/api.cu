@@ -109,23 +109,6 @@ pkv_status make_page_map(CUtensorMap* m, const void* base, const pkv_cache_desc*
   return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
 }
 
-// Query tile of the extend kernel: dims {head_dim, num_q_heads, rows}, box
-// {64 dims, group heads, 128/group rows}, so one box row is one packed
-// (token, head) row of the 128-row tile.
-pkv_status make_q_map(CUtensorMap* m, const void* q, int total_rows, int hq, int head_dim,
-                      int group) {
-  auto enc = encode_fn();
-  if (!enc) return PKV_ERR_CUDA;
-  cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)hq, (cuuint64_t)total_rows};
-  cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)hq * head_dim * 2};
-  cuuint32_t box[3] = {64u, (cuuint32_t)group, (cuuint32_t)(128 / group)};
-  cuuint32_t estr[3] = {1u, 1u, 1u};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(q), dims, strides, box,
-                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
-}
-
 int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
 struct DecodePlan {
@@ -317,7 +300,7 @@ pkv_status pkv_paged_extend_attn(const pkv_cache_desc* desc, const void* k_cache
   if (st != PKV_OK) return st;
   if ((st = check_act(desc, act_dtype)) != PKV_OK) return st;
   if (batch < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || total_q_rows < 0 ||
-      max_suffix_len < 0 || max_total_len < 0 || !std::isfinite(sm_scale))
+      max_suffix_len < 0 || max_total_len < 0 || !std::isfinite(sm_scale) || !(sm_scale > 0.f))
     return PKV_ERR_INVALID_ARG;
   if (num_q_heads % desc->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
   const int group = num_q_heads / desc->num_kv_heads;
@@ -331,9 +314,7 @@ pkv_status pkv_paged_extend_attn(const pkv_cache_desc* desc, const void* k_cache
   cudaError_t e;
   DeviceState* ds = device_state(&e);
   if (!ds) return PKV_ERR_CUDA;
-  CUtensorMap qmap, kmap, vmap;
-  if ((st = make_q_map(&qmap, q, total_q_rows, num_q_heads, desc->head_dim, group)) != PKV_OK)
-    return st;
+  CUtensorMap kmap, vmap;
   if ((st = make_page_map(&kmap, k_cache, desc)) != PKV_OK) return st;
   if ((st = make_page_map(&vmap, v_cache, desc)) != PKV_OK) return st;
   ExtendParams p;
@@ -358,8 +339,7 @@ pkv_status pkv_paged_extend_attn(const pkv_cache_desc* desc, const void* k_cache
   p.out_scale = desc->cache_dtype == PKV_FP8_E4M3 ? desc->v_scale : 1.0f;
   if (p.tiles_per_head > 65535 || desc->num_kv_heads > 65535 || batch > 65535)
     return PKV_ERR_UNSUPPORTED;
-  e = launch_extend(qmap, kmap, vmap, p, desc->head_dim, (int)desc->cache_dtype, (int)act_dtype,
-                    stream);
+  e = launch_extend(kmap, vmap, p, desc->head_dim, (int)desc->cache_dtype, (int)act_dtype, stream);
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

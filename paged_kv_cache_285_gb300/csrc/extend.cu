@@ -12,22 +12,32 @@
 // (token i, head j) attends to keys 0 .. prefix + i.  Keys are consumed in
 // tiles of 128 read through the block table.
 //
+// Shared-memory bandwidth is what limits this shape (each 128x128x128 MMA
+// pair reads 64 KB of operands), so everything that can live in TMEM does:
+// TMEM (512 columns) holds two S buffers (the f16 P of a tile overwrites the
+// first half of its own S buffer), the O accumulator and the Q tile, and the
+// MMAs read Q and P straight from TMEM (A operand in tensor memory).  Shared
+// memory holds only 3-stage K and V rings.
+//
 // Warp roles (256 threads):
-//   warp 0      TMA producer: the Q tile once (3-D map over q), then per key
-//               tile the K tile (double-buffered) and the V tile, each as
+//   warp 0      TMA producer: per key tile the K and V tiles, each as
 //               sixteen 16-token x 64-dim boxes addressed through the block
 //               table, 128-byte swizzled.
-//   warp 1      TMEM owner (512 columns: two S buffers + O) and, on one lane,
-//               the MMA issuer: S = Q K^T (M=128, N=128, K=128) into the free
-//               S buffer, then O += P V for the previous tile.
-//   warps 2-3   V^T builders: each V tile is transposed to [dim][key] and
-//               converted to f16 (ldmatrix.trans -> cvt -> stmatrix), zeroing
-//               keys past the sequence end, so that the PV product is a
-//               K-major f16 x f16 MMA.
-//   warps 4-7   softmax (one thread per row): S row from TMEM, causal mask on
-//               the diagonal tiles, running max with lazy rescaling (O in TMEM
-//               is rescaled only when the max grows by more than 2^8), P in
-//               f16 to shared memory, final O / l and LSE.
+//   warp 1      TMEM owner and, on one lane, the MMA issuer:
+//               S = Q K^T (A = Q in TMEM, B = K tile K-major, M=N=K=128) into
+//               the free S buffer, then O += P V for the previous tile
+//               (A = P in TMEM, B = the V tile as loaded, [key][dim], read as
+//               an MN-major operand).
+//   warps 2-3   V converters: bf16 V tiles are turned into f16 in place and
+//               keys past the sequence end are zeroed, so that the PV product
+//               is f16 x f16.
+//   warps 4-7   softmax (one thread per row): loads its Q row into TMEM, then
+//               per tile reads its 128-column S row from TMEM with one wait
+//               (TMEM load latency is paid once), takes the row max, writes
+//               2^(s - max) back over it as f16 P; causal mask on diagonal
+//               tiles, running max with lazy rescaling (O in TMEM is rescaled
+//               only when the max grows by more than 2^8); finally O / l and
+//               the LSE.
 // P is kept in f16 (11-bit significand) because bf16 P alone would put the
 // relative L2 error of the output near 1.5e-3.
 #include "internal.h"
@@ -42,30 +52,28 @@ constexpr int BM = 128;       // rows per tile
 constexpr int BN = 128;       // keys per tile
 constexpr int HD = 128;       // head dim
 constexpr int NTHREADS = 256;
-constexpr int TILE = BM * HD * 2;   // 32 KB: 128 x 128 16-bit elements
+constexpr int NCONV = 64;     // V converter threads (warps 2, 3)
+constexpr int NST = 3;        // K and V ring depth
+constexpr int TILE = BN * HD * 2;   // 32 KB: 128 x 128 16-bit elements
 constexpr int CHUNK = 16384;        // one 64-element column block [128 rows][128 B]
 
-constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + TILE;   // two stages
-constexpr int OFF_V = OFF_K + 2 * TILE;
-constexpr int OFF_VT = OFF_V + TILE;
-constexpr int OFF_P = OFF_VT + TILE;
-constexpr int OFF_BAR = OFF_P + TILE;
+constexpr int OFF_K = 0;
+constexpr int OFF_V = OFF_K + NST * TILE;
+constexpr int OFF_BAR = OFF_V + NST * TILE;
 enum {
-  B_Q = 0, B_KFULL = 1, B_KFREE = 3, B_VFULL = 5, B_VFREE = 6, B_VTFULL = 7,
-  B_SFULL = 8, B_SFREE = 10, B_PFULL = 12, B_PVDONE = 13, NBAR = 14
+  B_Q = 0,
+  B_KFULL = 1, B_KFREE = B_KFULL + NST,
+  B_VFULL = B_KFREE + NST, B_VFREE = B_VFULL + NST, B_VCONV = B_VFREE + NST,
+  B_SFULL = B_VCONV + NST, B_PFULL = B_SFULL + 2, B_PVDONE = B_PFULL + 2,
+  NBAR = B_PVDONE + 2
 };
 constexpr int OFF_TMEMSLOT = OFF_BAR + NBAR * 8;
 constexpr int SMEM_BYTES = OFF_TMEMSLOT + 16 + 1024;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_S = 0;     // S buffers at columns 0 and 128
-constexpr uint32_t TM_O = 256;   // O accumulator at column 256
+constexpr uint32_t TM_S = 0;     // S buffers at columns 0 and 128 (P: first 64 of each)
+constexpr uint32_t TM_O = 256;   // O accumulator, 128 columns
+constexpr uint32_t TM_Q = 384;   // Q tile as 64 columns of 16-bit pairs
 constexpr float kLn2f = 0.6931471805599453f;
-
-// byte offset of (row, 16-byte unit) in a [128 rows][128 B] 128B-swizzled block
-__device__ __forceinline__ uint32_t sw_off(int row, int unit) {
-  return (uint32_t)(row * 128 + ((unit ^ (row & 7)) << 4));
-}
 
 __device__ __forceinline__ void set_err(int32_t* err, int code) {
   if (err) atomicCAS(err, 0, code);
@@ -73,8 +81,8 @@ __device__ __forceinline__ void set_err(int32_t* err, int code) {
 
 template <int CT>
 __global__ void __launch_bounds__(NTHREADS, 1)
-extend_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-              const __grid_constant__ CUtensorMap vmap, const ExtendParams p) {
+extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+              const ExtendParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -105,23 +113,21 @@ extend_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
   const int T = (k_hi + BN - 1) / BN;
 
   if (threadIdx.x == 0) {
-    prefetch_tensormap(&qmap);
     prefetch_tensormap(&kmap);
     prefetch_tensormap(&vmap);
-    mbar_init(bar(B_Q), 1);
-    mbar_init(bar(B_KFULL), 1);
-    mbar_init(bar(B_KFULL + 1), 1);
-    mbar_init(bar(B_KFREE), 1);
-    mbar_init(bar(B_KFREE + 1), 1);
-    mbar_init(bar(B_VFULL), 1);
-    mbar_init(bar(B_VFREE), 2);
-    mbar_init(bar(B_VTFULL), 2);
-    mbar_init(bar(B_SFULL), 1);
-    mbar_init(bar(B_SFULL + 1), 1);
-    mbar_init(bar(B_SFREE), 4);
-    mbar_init(bar(B_SFREE + 1), 4);
-    mbar_init(bar(B_PFULL), 4);
-    mbar_init(bar(B_PVDONE), 1);
+    mbar_init(bar(B_Q), 4);
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(bar(B_KFULL + i), 1);
+      mbar_init(bar(B_KFREE + i), 1);
+      mbar_init(bar(B_VFULL + i), 1);
+      mbar_init(bar(B_VFREE + i), 1);
+      mbar_init(bar(B_VCONV + i), NCONV / 32);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(B_SFULL + i), 1);
+      mbar_init(bar(B_PFULL + i), 4);
+      mbar_init(bar(B_PVDONE + i), 1);
+    }
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -133,14 +139,10 @@ extend_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      mbar_arrive_expect_tx(bar(B_Q), TILE);
-      for (int c = 0; c < 2; ++c)
-        tma_load_3d(s_base + OFF_Q + c * CHUNK, &qmap, bar(B_Q), c * 64, g * G, row0 + i0);
-    }
     const int32_t* bt = p.block_tables + (int64_t)b * p.max_blocks;
     for (int kt = 0; kt < T && ok; ++kt) {
-      const int s = kt & 1;
+      const int s = kt % NST;
+      const uint32_t ph = (uint32_t)((kt / NST - 1) & 1);  // phase of the previous use
       const int key0 = kt * BN + 16 * (lane & 7);
       int blk = -1;
       if (lane < 8 && key0 < k_hi) {
@@ -152,13 +154,13 @@ extend_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
       }
       const int page = blk < 0 ? -1 : blk * p.num_kv_heads + g;
       const int rip = key0 & (bs - 1);
-      if (kt >= 2 && !mbar_wait(bar(B_KFREE + s), ((kt - 2) >> 1) & 1)) { ok = false; break; }
       int pg[8], rr[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         pg[j] = __shfl_sync(0xFFFFFFFFu, page, j);
         rr[j] = __shfl_sync(0xFFFFFFFFu, rip, j);
       }
+      if (kt >= NST && !mbar_wait(bar(B_KFREE + s), ph)) { ok = false; break; }
       if (lane == 0) {
         const uint32_t dst = s_base + OFF_K + s * TILE;
         mbar_arrive_expect_tx(bar(B_KFULL + s), TILE);
@@ -168,15 +170,15 @@ extend_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
           for (int c = 0; c < 2; ++c)
             tma_load_3d(dst + c * CHUNK + j * 2048, &kmap, bar(B_KFULL + s), c * 64, rr[j], pg[j]);
       }
-      if (kt >= 1 && !mbar_wait(bar(B_VFREE), (kt - 1) & 1)) { ok = false; break; }
+      if (kt >= NST && !mbar_wait(bar(B_VFREE + s), ph)) { ok = false; break; }
       if (lane == 0) {
-        const uint32_t dst = s_base + OFF_V;
-        mbar_arrive_expect_tx(bar(B_VFULL), TILE);
+        const uint32_t dst = s_base + OFF_V + s * TILE;
+        mbar_arrive_expect_tx(bar(B_VFULL + s), TILE);
 #pragma unroll
         for (int j = 0; j < 8; ++j)
 #pragma unroll
           for (int c = 0; c < 2; ++c)
-            tma_load_3d(dst + c * CHUNK + j * 2048, &vmap, bar(B_VFULL), c * 64, rr[j], pg[j]);
+            tma_load_3d(dst + c * CHUNK + j * 2048, &vmap, bar(B_VFULL + s), c * 64, rr[j], pg[j]);
       }
     }
   } else if (warp == 1) {
@@ -184,79 +186,81 @@ extend_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
     if (lane == 0) {
       constexpr uint32_t qk_fmt = (CT == DT_BF16) ? 1u : 0u;
       constexpr uint32_t idesc_qk = umma_idesc_f16(qk_fmt, qk_fmt, BM, BN);
-      constexpr uint32_t idesc_pv = umma_idesc_f16(0u, 0u, BM, HD);
+      // P (A, f16 in TMEM) x V (B, f16, MN-major: the V tile as loaded, [key][dim])
+      constexpr uint32_t idesc_pv = umma_idesc_f16(0u, 0u, BM, HD) | (1u << 16);
       auto issue_pv = [&](int u) -> bool {
-        if (!mbar_wait(bar(B_PFULL), u & 1)) return false;
-        if (!mbar_wait(bar(B_VTFULL), u & 1)) return false;
+        const int ub = u & 1, us = u % NST;
+        if (!mbar_wait(bar(B_PFULL + ub), (u >> 1) & 1)) return false;
+        if (!mbar_wait(bar(B_VCONV + us), (u / NST) & 1)) return false;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * CHUNK + (kk & 3) * 32;
-          umma_f16(tmem + TM_O, umma_desc_sw128(s_base + OFF_P + off),
-                   umma_desc_sw128(s_base + OFF_VT + off), idesc_pv, (u > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(bar(B_PVDONE));
+        for (int kk = 0; kk < BN / 16; ++kk)
+          umma_f16_ts(tmem + TM_O, tmem + TM_S + ub * BN + kk * 8,
+                      umma_desc_sw128_mn(s_base + OFF_V + us * TILE + kk * 2048, CHUNK), idesc_pv,
+                      (u > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(bar(B_PVDONE + ub));  // S/P buffer ub and O are free again
+        umma_commit(bar(B_VFREE + us));
         return true;
       };
       ok = mbar_wait(bar(B_Q), 0);
       for (int kt = 0; kt < T && ok; ++kt) {
-        const int s = kt & 1;
-        if (!mbar_wait(bar(B_KFULL + s), (kt >> 1) & 1)) { ok = false; break; }
-        if (kt >= 2 && !mbar_wait(bar(B_SFREE + s), ((kt - 2) >> 1) & 1)) { ok = false; break; }
+        const int sb = kt & 1, ks = kt % NST;
+        if (!mbar_wait(bar(B_KFULL + ks), (kt / NST) & 1)) { ok = false; break; }
+        // S buffer sb still holds P(kt-2) until PV(kt-2) completes
+        if (kt >= 2 && !mbar_wait(bar(B_PVDONE + sb), ((kt - 2) >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * CHUNK + (kk & 3) * 32;
-          umma_f16(tmem + TM_S + s * BN, umma_desc_sw128(s_base + OFF_Q + off),
-                   umma_desc_sw128(s_base + OFF_K + s * TILE + off), idesc_qk, kk > 0 ? 1u : 0u);
+          umma_f16_ts(tmem + TM_S + sb * BN, tmem + TM_Q + kk * 8,
+                      umma_desc_sw128(s_base + OFF_K + ks * TILE + off), idesc_qk, kk > 0 ? 1u : 0u);
         }
-        umma_commit(bar(B_SFULL + s));
-        umma_commit(bar(B_KFREE + s));
+        umma_commit(bar(B_SFULL + sb));
+        umma_commit(bar(B_KFREE + ks));
         if (kt >= 1 && !issue_pv(kt - 1)) { ok = false; break; }
       }
       if (ok) ok = issue_pv(T - 1);
     }
     __syncwarp();
   } else if (warp < 4) {
-    // ------------------------------------------------------------ V^T builders
+    // ------------------------------------------------------------ V converters
+    // In place, per 16-byte unit: bf16 -> f16 (the PV product is f16 x f16),
+    // and keys at or past the sequence end -> 0 (they may hold anything).
+    // The swizzle only permutes units inside a 128-byte key row, so the key
+    // of a unit is its byte offset / 128 within its column block.
     const int ct = threadIdx.x - 64;  // 0..63
     for (int kt = 0; kt < T && ok; ++kt) {
-      if (!mbar_wait(bar(B_VFULL), kt & 1)) { ok = false; break; }
-      if (kt >= 1 && !mbar_wait(bar(B_PVDONE), (kt - 1) & 1)) { ok = false; break; }
+      const int vs = kt % NST;
+      if (!mbar_wait(bar(B_VFULL + vs), (kt / NST) & 1)) { ok = false; break; }
       const int kbase = kt * BN;
-      // 64 groups of four 8x8 blocks; this warp takes 32 of them
-      for (int q = ct >> 5; q < 64; q += 2) {
-        const int kb2 = q >> 3, dq = q & 7;
-        const int jm = lane >> 3, rw = lane & 7;
-        // source: row = key, 16 B = 8 dims
-        const int key_s = kb2 * 16 + (jm >> 1) * 8 + rw;
-        const int dim_s = dq * 16 + (jm & 1) * 8;
-        uint32_t r[4];
-        ldsm_x4_t(s_base + OFF_V + (dim_s >> 6) * CHUNK + sw_off(key_s, (dim_s & 63) >> 3), r);
-        // r[j]: rows = dims db_j + gid, cols = keys kb_j + 2tig, +1
-        const int gid = lane >> 2, tig = lane & 3;
+      const bool tail = kbase + BN > kv_total;
+      if (CT == DT_BF16 || tail) {
+        uint8_t* vt = smem + OFF_V + vs * TILE;
+        constexpr int PER = TILE / 16 / NCONV;  // 32 units of 16 bytes per thread
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int kb_j = kb2 * 16 + (j >> 1) * 8;
-          uint32_t v = to_f16x2<CT == DT_BF16>(r[j]);
-          const int k0 = kbase + kb_j + 2 * tig;
-          if (k0 >= kv_total) v &= 0xFFFF0000u;
-          if (k0 + 1 >= kv_total) v &= 0x0000FFFFu;
-          r[j] = v;
-          (void)gid;
+        for (int h = 0; h < PER; h += 8) {
+          uint4 w[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) w[i] = *reinterpret_cast<const uint4*>(vt + (ct + (h + i) * NCONV) * 16);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int u = ct + (h + i) * NCONV;
+            const int key = kbase + ((u * 16) % CHUNK) / 128;
+            if (key >= kv_total) {
+              w[i] = make_uint4(0u, 0u, 0u, 0u);
+            } else if (CT == DT_BF16) {
+              w[i].x = to_f16x2<true>(w[i].x);
+              w[i].y = to_f16x2<true>(w[i].y);
+              w[i].z = to_f16x2<true>(w[i].z);
+              w[i].w = to_f16x2<true>(w[i].w);
+            }
+            *reinterpret_cast<uint4*>(vt + u * 16) = w[i];
+          }
         }
-        // destination: row = dim, 16 B = 8 keys
-        const int dim_d = dq * 16 + (jm & 1) * 8 + rw;
-        const int key_d = kb2 * 16 + (jm >> 1) * 8;
-        stsm_x4(s_base + OFF_VT + (key_d >> 6) * CHUNK + sw_off(dim_d, (key_d & 63) >> 3), r[0], r[1],
-                r[2], r[3]);
+        fence_async_smem();
       }
-      fence_async_smem();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(bar(B_VFREE));
-        mbar_arrive(bar(B_VTFULL));
-      }
+      if (lane == 0) mbar_arrive(bar(B_VCONV + vs));
     }
   } else {
     // ------------------------------------------------------------ softmax
@@ -264,86 +268,107 @@ extend_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
     const int r = qw * 32 + lane;
     const uint32_t lane_addr = (uint32_t)(qw * 32) << 16;
     const int lim = P + i0 + r / G;  // last key this row may see
+    const bool valid = (r / G) < ntok;
+    const int64_t qrow = (int64_t)(row0 + i0 + r / G) * p.num_q_heads + g * G + (r % G);
+    // Q row -> TMEM (64 columns of 16-bit pairs); rows past the suffix get zeros
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.q) + qrow * HD);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[16];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint4 w = valid ? __ldg(src + c * 4 + j) : make_uint4(0u, 0u, 0u, 0u);
+          v[4 * j] = w.x; v[4 * j + 1] = w.y; v[4 * j + 2] = w.z; v[4 * j + 3] = w.w;
+        }
+        tmem_st16(tmem + lane_addr + TM_Q + c * 16, v);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_Q));
+    }
     float m_run = -INFINITY, l_run = 0.f;
     for (int kt = 0; kt < T && ok; ++kt) {
-      const int s = kt & 1;
-      if (!mbar_wait(bar(B_SFULL + s), (kt >> 1) & 1)) { ok = false; break; }
+      const int sb = kt & 1;
+      if (!mbar_wait(bar(B_SFULL + sb), (kt >> 1) & 1)) { ok = false; break; }
       tc_fence_after();
-      float x[BN];
-      {
-        uint32_t raw[4][32];
+      const uint32_t srow = tmem + lane_addr + TM_S + sb * BN;
+      const int key0 = kt * BN;
+      const bool diag = key0 + BN - 1 > P + i0;  // tile reaches past some row's limit
+      // the whole S row: four 32-column loads, one wait
+      uint32_t raw[4][32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_addr + TM_S + s * BN + c * 32, raw[c]);
-        tmem_wait_ld();
+      for (int c = 0; c < 4; ++c) tmem_ld32(srow + c * 32, raw[c]);
+      tmem_wait_ld();
+      if (diag) {  // causal mask on the tile that reaches past some row's limit
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int j = 0; j < 32; ++j) x[c * 32 + j] = __uint_as_float(raw[c][j]);
+          for (int j = 0; j < 32; ++j)
+            if (key0 + c * 32 + j > lim) raw[c][j] = __float_as_uint(-INFINITY);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_SFREE + s));
-
-      const int key0 = kt * BN;
-      const bool need_mask = key0 + BN - 1 > P + i0;
-      float mt = -INFINITY;
+      // row max over 8 independent accumulators (one running max would be a
+      // 128-long dependent chain)
+      float mx[8];
 #pragma unroll
-      for (int j = 0; j < BN; ++j) {
-        float v = x[j] * p.scale_log2;
-        if (need_mask && key0 + j > lim) v = -INFINITY;
-        x[j] = v;
-        mt = fmaxf(mt, v);
-      }
+      for (int a = 0; a < 8; ++a) mx[a] = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int j = 0; j < 32; ++j) mx[j & 7] = fmaxf(mx[j & 7], __uint_as_float(raw[c][j]));
+      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * p.scale_log2;
       float m_new = m_run;
       if (mt > m_run + 8.f) m_new = mt;
       const float alpha = fast_exp2(m_run - m_new);
-      uint32_t pk[BN / 2];
-      float sum = 0.f;
-#pragma unroll
-      for (int j = 0; j < BN / 2; ++j) {
-        const float p0 = fast_exp2(x[2 * j] - m_new), p1 = fast_exp2(x[2 * j + 1] - m_new);
-        sum += p0 + p1;
-        pk[j] = pack2<false>(p0, p1);
-      }
-      l_run = l_run * alpha + sum;
-      if (kt >= 1) {
-        if (!mbar_wait(bar(B_PVDONE), (kt - 1) & 1)) { ok = false; break; }
+      const bool mine = (m_new != m_run);
+      if (kt >= 1 && __any_sync(0xFFFFFFFFu, mine)) {
+        // rescale O in TMEM: wait until PV(kt-1) has finished accumulating
+        if (!mbar_wait(bar(B_PVDONE + (sb ^ 1)), ((kt - 1) >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
-        const bool mine = (m_new != m_run);
-        if (__any_sync(0xFFFFFFFFu, mine)) {
-          const float f = mine ? alpha : 1.f;
+        const float f = mine ? alpha : 1.f;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tmem + lane_addr + TM_O + c * 32, o);
-            tmem_wait_ld();
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lane_addr + TM_O + c * 32, o);
+          tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * f);
-            tmem_st32(tmem + lane_addr + TM_O + c * 32, o);
-          }
-          tmem_wait_st();
+          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * f);
+          tmem_st32(tmem + lane_addr + TM_O + c * 32, o);
         }
+        tmem_wait_st();
       }
       m_run = m_new;
+      // p = 2^(s*scale - m) in f16, written over the first 64 columns of the S
+      // buffer (the whole row is already in registers)
+      float sm[8];
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const uint32_t addr = s_base + OFF_P + (u >> 3) * CHUNK + sw_off(r, u & 7);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * u]),
-                     "r"(pk[4 * u + 1]), "r"(pk[4 * u + 2]), "r"(pk[4 * u + 3])
-                     : "memory");
+      for (int a = 0; a < 8; ++a) sm[a] = 0.f;
+      const float sc = p.scale_log2, neg_m = -m_new;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float p0 = fast_exp2(fmaf(__uint_as_float(raw[c][2 * j]), sc, neg_m));
+          const float p1 = fast_exp2(fmaf(__uint_as_float(raw[c][2 * j + 1]), sc, neg_m));
+          sm[j & 7] += p0 + p1;
+          pk[j] = pack2<false>(p0, p1);
+        }
+        tmem_st16(srow + c * 16, pk);
       }
-      fence_async_smem();
+      const float sum = ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
+      l_run = l_run * alpha + sum;
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_PFULL));
+      if (lane == 0) mbar_arrive(bar(B_PFULL + sb));
     }
     // ---- epilogue: O / l -> out, LSE
-    if (ok && mbar_wait(bar(B_PVDONE), (T - 1) & 1)) {
+    if (ok && mbar_wait(bar(B_PVDONE + ((T - 1) & 1)), ((T - 1) >> 1) & 1)) {
       tc_fence_after();
-      const bool valid = (r / G) < ntok;
-      const int64_t orow = (int64_t)(row0 + i0 + r / G) * p.num_q_heads + g * G + (r % G);
-      const float inv = 1.f / l_run;
-      const float osc = inv * p.out_scale;
+      const float osc = p.out_scale / l_run;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t o[32];
@@ -355,12 +380,12 @@ extend_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ 
           for (int j = 0; j < 16; ++j)
             w[j] = pack2<CT == DT_BF16>(__uint_as_float(o[2 * j]) * osc,
                                         __uint_as_float(o[2 * j + 1]) * osc);
-          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.out) + orow * HD + c * 32);
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.out) + qrow * HD + c * 32);
 #pragma unroll
           for (int j = 0; j < 4; ++j) dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
         }
       }
-      if (valid && p.lse_out) p.lse_out[orow] = (m_run + log2f(l_run)) * kLn2f;
+      if (valid && p.lse_out) p.lse_out[qrow] = (m_run + log2f(l_run)) * kLn2f;
     } else {
       ok = false;
     }
@@ -383,21 +408,20 @@ bool extend_supported(int head_dim, int cache_dt, int act_dt, int group) {
   return group == 1 || group == 2 || group == 4 || group == 8;
 }
 
-cudaError_t launch_extend(const CUtensorMap& qmap, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                          const ExtendParams& p, int head_dim, int cache_dt, int act_dt,
-                          cudaStream_t stream) {
+cudaError_t launch_extend(const CUtensorMap& kmap, const CUtensorMap& vmap, const ExtendParams& p,
+                          int head_dim, int cache_dt, int act_dt, cudaStream_t stream) {
   if (!extend_supported(head_dim, cache_dt, act_dt, p.group)) return cudaErrorInvalidValue;
   dim3 grid(p.tiles_per_head, p.num_kv_heads, p.batch);
   if (cache_dt == DT_BF16) {
     auto k = extend_kernel<DT_BF16>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    k<<<grid, NTHREADS, SMEM_BYTES, stream>>>(qmap, kmap, vmap, p);
+    k<<<grid, NTHREADS, SMEM_BYTES, stream>>>(kmap, vmap, p);
   } else {
     auto k = extend_kernel<DT_F16>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    k<<<grid, NTHREADS, SMEM_BYTES, stream>>>(qmap, kmap, vmap, p);
+    k<<<grid, NTHREADS, SMEM_BYTES, stream>>>(kmap, vmap, p);
   }
   return cudaGetLastError();
 }

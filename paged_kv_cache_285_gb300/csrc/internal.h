@@ -78,9 +78,9 @@ cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap,
                           cudaStream_t stream);
 size_t decode_smem_bytes(int head_dim, int cache_dt);
 cudaError_t launch_append(const AppendParams& p, int cache_dt, int act_dt, cudaStream_t stream);
-cudaError_t launch_extend(const CUtensorMap& qmap, const CUtensorMap& kmap,
-                          const CUtensorMap& vmap, const ExtendParams& p, int head_dim,
-                          int cache_dt, int act_dt, cudaStream_t stream);
+cudaError_t launch_extend(const CUtensorMap& kmap, const CUtensorMap& vmap,
+                          const ExtendParams& p, int head_dim, int cache_dt, int act_dt,
+                          cudaStream_t stream);
 bool extend_supported(int head_dim, int cache_dt, int act_dt, int group);
 
 }  // namespace pkv
