@@ -12,34 +12,34 @@
 // (token i, head j) attends to keys 0 .. prefix + i.  Keys are consumed in
 // tiles of 128 read through the block table.
 //
-// Shared-memory bandwidth is what limits this shape (each 128x128x128 MMA
-// pair reads 64 KB of operands), so everything that can live in TMEM does:
-// TMEM (512 columns) holds two S buffers (the f16 P of a tile overwrites the
-// first half of its own S buffer), the O accumulator and the Q tile, and the
-// MMAs read Q and P straight from TMEM (A operand in tensor memory).  Shared
-// memory holds only 3-stage K and V rings.
+// Measured on this part, an MMA that reads its A operand from shared memory
+// runs at ~60% of the tensor peak for this shape, one that reads A from TMEM
+// at the full peak, so both A operands (Q for S = Q K^T, P for O += P V) live
+// in TMEM.  TMEM (512 columns): two fp32 S buffers, the O accumulator, the Q
+// tile and one f16 P tile.  An S buffer is released as soon as the softmax
+// has its row in registers, so S = Q K^T of tile k+2 never waits for a PV
+// product to drain; the P tile is rewritten once PV of the previous tile is
+// done.  Shared memory holds only 3-stage K and V rings.
 //
-// Warp roles (256 threads):
+// Warp roles (384 threads):
 //   warp 0      TMA producer: per key tile the K and V tiles, each as
 //               sixteen 16-token x 64-dim boxes addressed through the block
 //               table, 128-byte swizzled.
-//   warp 1      TMEM owner and, on one lane, the MMA issuer:
-//               S = Q K^T (A = Q in TMEM, B = K tile K-major, M=N=K=128) into
-//               the free S buffer, then O += P V for the previous tile
-//               (A = P in TMEM, B = the V tile as loaded, [key][dim], read as
-//               an MN-major operand).
-//   warps 2-3   V converters: bf16 V tiles are turned into f16 in place and
-//               keys past the sequence end are zeroed, so that the PV product
-//               is f16 x f16.
-//   warps 4-7   softmax (one thread per row): loads its Q row into TMEM, then
-//               per tile reads its 128-column S row from TMEM with one wait
-//               (TMEM load latency is paid once), takes the row max, writes
-//               2^(s - max) back over it as f16 P; causal mask on diagonal
-//               tiles, running max with lazy rescaling (O in TMEM is rescaled
-//               only when the max grows by more than 2^8); finally O / l and
-//               the LSE.
-// P is kept in f16 (11-bit significand) because bf16 P alone would put the
-// relative L2 error of the output near 1.5e-3.
+//   warp 1      TMEM owner and, on one lane, the MMA issuer: S = Q K^T
+//               (A = Q in TMEM, B = K tile K-major, M=N=K=128), then
+//               O += P V for the previous tile (A = P in TMEM, B = the V tile
+//               as loaded, [key][dim], read as an MN-major operand).
+//   warps 2-3,  V converters: bf16 V tiles are turned into f16 in place and
+//   8-11        keys past the sequence end are zeroed (they may hold NaN).
+//   warps 4-7   softmax (one thread per row): stores its Q row into TMEM,
+//               then per tile reads its 128-column S row from TMEM with one
+//               wait, takes the row max (causal mask on diagonal tiles), keeps
+//               a running max with lazy rescaling (O in TMEM is rescaled only
+//               when the max grows by more than 2^8) and writes f16 P; finally
+//               O / l and the LSE.
+// P is f16 (11 significant bits) because bf16 P alone would put the relative
+// L2 error of the output near 1.5e-3; V is therefore converted to f16 (bf16
+// values beyond +-65504 are outside this path's range).
 #include "internal.h"
 #include "ptx.cuh"
 #include "tcgen05.cuh"
@@ -51,8 +51,8 @@ namespace {
 constexpr int BM = 128;       // rows per tile
 constexpr int BN = 128;       // keys per tile
 constexpr int HD = 128;       // head dim
-constexpr int NTHREADS = 256;
-constexpr int NCONV = 64;     // V converter threads (warps 2, 3)
+constexpr int NTHREADS = 384;
+constexpr int NCONV = 192;    // V converter threads (warps 2, 3, 8-11)
 constexpr int NST = 3;        // K and V ring depth
 constexpr int TILE = BN * HD * 2;   // 32 KB: 128 x 128 16-bit elements
 constexpr int CHUNK = 16384;        // one 64-element column block [128 rows][128 B]
@@ -64,15 +64,16 @@ enum {
   B_Q = 0,
   B_KFULL = 1, B_KFREE = B_KFULL + NST,
   B_VFULL = B_KFREE + NST, B_VFREE = B_VFULL + NST, B_VCONV = B_VFREE + NST,
-  B_SFULL = B_VCONV + NST, B_PFULL = B_SFULL + 2, B_PVDONE = B_PFULL + 2,
-  NBAR = B_PVDONE + 2
+  B_SFULL = B_VCONV + NST, B_SFREE = B_SFULL + 2, B_PFULL = B_SFREE + 2, B_PVDONE = B_PFULL + 1,
+  NBAR = B_PVDONE + 1
 };
 constexpr int OFF_TMEMSLOT = OFF_BAR + NBAR * 8;
 constexpr int SMEM_BYTES = OFF_TMEMSLOT + 16 + 1024;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_S = 0;     // S buffers at columns 0 and 128 (P: first 64 of each)
+constexpr uint32_t TM_S = 0;     // two fp32 S buffers, columns 0 and 128
 constexpr uint32_t TM_O = 256;   // O accumulator, 128 columns
-constexpr uint32_t TM_Q = 384;   // Q tile as 64 columns of 16-bit pairs
+constexpr uint32_t TM_Q = 384;   // Q tile: 64 columns of 16-bit pairs
+constexpr uint32_t TM_P = 448;   // P tile: 64 columns of f16 pairs
 constexpr float kLn2f = 0.6931471805599453f;
 
 __device__ __forceinline__ void set_err(int32_t* err, int code) {
@@ -125,9 +126,10 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(B_SFULL + i), 1);
-      mbar_init(bar(B_PFULL + i), 4);
-      mbar_init(bar(B_PVDONE + i), 1);
+      mbar_init(bar(B_SFREE + i), 4);
     }
+    mbar_init(bar(B_PFULL), 4);
+    mbar_init(bar(B_PVDONE), 1);
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -189,16 +191,16 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       // P (A, f16 in TMEM) x V (B, f16, MN-major: the V tile as loaded, [key][dim])
       constexpr uint32_t idesc_pv = umma_idesc_f16(0u, 0u, BM, HD) | (1u << 16);
       auto issue_pv = [&](int u) -> bool {
-        const int ub = u & 1, us = u % NST;
-        if (!mbar_wait(bar(B_PFULL + ub), (u >> 1) & 1)) return false;
+        const int us = u % NST;
+        if (!mbar_wait(bar(B_PFULL), u & 1)) return false;
         if (!mbar_wait(bar(B_VCONV + us), (u / NST) & 1)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          umma_f16_ts(tmem + TM_O, tmem + TM_S + ub * BN + kk * 8,
+          umma_f16_ts(tmem + TM_O, tmem + TM_P + kk * 8,
                       umma_desc_sw128_mn(s_base + OFF_V + us * TILE + kk * 2048, CHUNK), idesc_pv,
                       (u > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar(B_PVDONE + ub));  // S/P buffer ub and O are free again
+        umma_commit(bar(B_PVDONE));  // P buffer and O are free again
         umma_commit(bar(B_VFREE + us));
         return true;
       };
@@ -206,8 +208,8 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       for (int kt = 0; kt < T && ok; ++kt) {
         const int sb = kt & 1, ks = kt % NST;
         if (!mbar_wait(bar(B_KFULL + ks), (kt / NST) & 1)) { ok = false; break; }
-        // S buffer sb still holds P(kt-2) until PV(kt-2) completes
-        if (kt >= 2 && !mbar_wait(bar(B_PVDONE + sb), ((kt - 2) >> 1) & 1)) { ok = false; break; }
+        // S buffer sb is free once the softmax has read S(kt-2) into registers
+        if (kt >= 2 && !mbar_wait(bar(B_SFREE + sb), ((kt - 2) >> 1) & 1)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
@@ -222,13 +224,13 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       if (ok) ok = issue_pv(T - 1);
     }
     __syncwarp();
-  } else if (warp < 4) {
+  } else if (warp < 4 || warp >= 8) {
     // ------------------------------------------------------------ V converters
     // In place, per 16-byte unit: bf16 -> f16 (the PV product is f16 x f16),
-    // and keys at or past the sequence end -> 0 (they may hold anything).
-    // The swizzle only permutes units inside a 128-byte key row, so the key
-    // of a unit is its byte offset / 128 within its column block.
-    const int ct = threadIdx.x - 64;  // 0..63
+    // and keys at or past the sequence end -> 0 (they may hold anything, and
+    // 0 * NaN is NaN).  The swizzle only permutes units inside a 128-byte key
+    // row, so the key of a unit is its byte offset / 128 within its block.
+    const int ct = warp < 4 ? threadIdx.x - 64 : threadIdx.x - 192;  // 0..191
     for (int kt = 0; kt < T && ok; ++kt) {
       const int vs = kt % NST;
       if (!mbar_wait(bar(B_VFULL + vs), (kt / NST) & 1)) { ok = false; break; }
@@ -236,26 +238,27 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       const bool tail = kbase + BN > kv_total;
       if (CT == DT_BF16 || tail) {
         uint8_t* vt = smem + OFF_V + vs * TILE;
-        constexpr int PER = TILE / 16 / NCONV;  // 32 units of 16 bytes per thread
+        constexpr int PER = (TILE / 16 + NCONV - 1) / NCONV;  // 11 units of 16 bytes
+        uint4 w[PER];
 #pragma unroll
-        for (int h = 0; h < PER; h += 8) {
-          uint4 w[8];
+        for (int i = 0; i < PER; ++i) {
+          const int u = ct + i * NCONV;
+          if (u < TILE / 16) w[i] = *reinterpret_cast<const uint4*>(vt + u * 16);
+        }
 #pragma unroll
-          for (int i = 0; i < 8; ++i) w[i] = *reinterpret_cast<const uint4*>(vt + (ct + (h + i) * NCONV) * 16);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int u = ct + (h + i) * NCONV;
-            const int key = kbase + ((u * 16) % CHUNK) / 128;
-            if (key >= kv_total) {
-              w[i] = make_uint4(0u, 0u, 0u, 0u);
-            } else if (CT == DT_BF16) {
-              w[i].x = to_f16x2<true>(w[i].x);
-              w[i].y = to_f16x2<true>(w[i].y);
-              w[i].z = to_f16x2<true>(w[i].z);
-              w[i].w = to_f16x2<true>(w[i].w);
-            }
-            *reinterpret_cast<uint4*>(vt + u * 16) = w[i];
+        for (int i = 0; i < PER; ++i) {
+          const int u = ct + i * NCONV;
+          if (u >= TILE / 16) break;
+          const int key = kbase + ((u * 16) % CHUNK) / 128;
+          if (key >= kv_total) {
+            w[i] = make_uint4(0u, 0u, 0u, 0u);
+          } else if (CT == DT_BF16) {
+            w[i].x = to_f16x2<true>(w[i].x);
+            w[i].y = to_f16x2<true>(w[i].y);
+            w[i].z = to_f16x2<true>(w[i].z);
+            w[i].w = to_f16x2<true>(w[i].w);
           }
+          *reinterpret_cast<uint4*>(vt + u * 16) = w[i];
         }
         fence_async_smem();
       }
@@ -270,7 +273,8 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
     const int lim = P + i0 + r / G;  // last key this row may see
     const bool valid = (r / G) < ntok;
     const int64_t qrow = (int64_t)(row0 + i0 + r / G) * p.num_q_heads + g * G + (r % G);
-    // Q row -> TMEM (64 columns of 16-bit pairs); rows past the suffix get zeros
+    // Q row -> TMEM (64 columns of 16-bit pairs, the QK A operand); rows
+    // past the suffix get zeros
     {
       const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.q) + qrow * HD);
 #pragma unroll
@@ -301,12 +305,16 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(srow + c * 32, raw[c]);
       tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_SFREE + sb));  // S is in registers: buffer free
       if (diag) {  // causal mask on the tile that reaches past some row's limit
+        const int nvis = lim - key0;  // keys key0 .. key0+nvis are visible
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            if (key0 + c * 32 + j > lim) raw[c][j] = __float_as_uint(-INFINITY);
+            if (c * 32 + j > nvis) raw[c][j] = __float_as_uint(-INFINITY);
       }
       // row max over 8 independent accumulators (one running max would be a
       // 128-long dependent chain)
@@ -325,10 +333,10 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       const bool mine = (m_new != m_run);
       if (kt >= 1 && __any_sync(0xFFFFFFFFu, mine)) {
         // rescale O in TMEM: wait until PV(kt-1) has finished accumulating
-        if (!mbar_wait(bar(B_PVDONE + (sb ^ 1)), ((kt - 1) >> 1) & 1)) { ok = false; break; }
+        if (!mbar_wait(bar(B_PVDONE), (kt - 1) & 1)) { ok = false; break; }
         tc_fence_after();
         const float f = mine ? alpha : 1.f;
-#pragma unroll
+#pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t o[32];
           tmem_ld32(tmem + lane_addr + TM_O + c * 32, o);
@@ -340,8 +348,10 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
         tmem_wait_st();
       }
       m_run = m_new;
-      // p = 2^(s*scale - m) in f16, written over the first 64 columns of the S
-      // buffer (the whole row is already in registers)
+      // p = 2^(s*scale - m) as f16 pairs, streamed 32 keys at a time into the P
+      // tile once PV(kt-1) has consumed P(kt-1)
+      if (kt >= 1 && !mbar_wait(bar(B_PVDONE), (kt - 1) & 1)) { ok = false; break; }
+      tc_fence_after();
       float sm[8];
 #pragma unroll
       for (int a = 0; a < 8; ++a) sm[a] = 0.f;
@@ -356,20 +366,20 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
           sm[j & 7] += p0 + p1;
           pk[j] = pack2<false>(p0, p1);
         }
-        tmem_st16(srow + c * 16, pk);
+        tmem_st16(tmem + lane_addr + TM_P + c * 16, pk);
       }
       const float sum = ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
       l_run = l_run * alpha + sum;
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_PFULL + sb));
+      if (lane == 0) mbar_arrive(bar(B_PFULL));
     }
     // ---- epilogue: O / l -> out, LSE
-    if (ok && mbar_wait(bar(B_PVDONE + ((T - 1) & 1)), ((T - 1) >> 1) & 1)) {
+    if (ok && mbar_wait(bar(B_PVDONE), (T - 1) & 1)) {
       tc_fence_after();
       const float osc = p.out_scale / l_run;
-#pragma unroll
+#pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t o[32];
         tmem_ld32(tmem + lane_addr + TM_O + c * 32, o);
