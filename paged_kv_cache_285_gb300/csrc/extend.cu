@@ -22,15 +22,15 @@
 // done.  Shared memory holds only 3-stage K and V rings.
 //
 // Warp roles (384 threads):
-//   warp 0      TMA producer: per key tile the K and V tiles, each as
-//               sixteen 16-token x 64-dim boxes addressed through the block
-//               table, 128-byte swizzled.
+//   warps 0,11  TMA producers for the K and the V ring: per key tile sixteen
+//               16-token x 64-dim boxes addressed through the block table
+//               (block ids prefetched into registers), 128-byte swizzled.
 //   warp 1      TMEM owner and, on one lane, the MMA issuer: S = Q K^T
 //               (A = Q in TMEM, B = K tile K-major, M=N=K=128), then
 //               O += P V for the previous tile (A = P in TMEM, B = the V tile
 //               as loaded, [key][dim], read as an MN-major operand).
 //   warps 2-3,  V converters: bf16 V tiles are turned into f16 in place and
-//   8-11        keys past the sequence end are zeroed (they may hold NaN).
+//   8-10        keys past the sequence end are zeroed (they may hold NaN).
 //   warps 4-7   softmax (one thread per row): stores its Q row into TMEM,
 //               then per tile reads its 128-column S row from TMEM with one
 //               wait, takes the row max (causal mask on diagonal tiles), keeps
@@ -52,7 +52,7 @@ constexpr int BM = 128;       // rows per tile
 constexpr int BN = 128;       // keys per tile
 constexpr int HD = 128;       // head dim
 constexpr int NTHREADS = 384;
-constexpr int NCONV = 192;    // V converter threads (warps 2, 3, 8-11)
+constexpr int NCONV = 160;    // V converter threads (warps 2, 3, 8-10)
 constexpr int NST = 3;        // K and V ring depth
 constexpr int TILE = BN * HD * 2;   // 32 KB: 128 x 128 16-bit elements
 constexpr int CHUNK = 16384;        // one 64-element column block [128 rows][128 B]
@@ -139,48 +139,49 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
   const uint32_t tmem = *tmem_slot;
   bool ok = true;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp == 0 || warp == 11) {
+    // ------------------------------------------------------------ producers
+    // warp 0 streams K tiles, warp 11 V tiles, each through its own ring, so
+    // that a K load never queues behind a V buffer that is still in use.
+    // Block ids: lane l holds sub-tile (32 w + l) of window w, the next
+    // window is fetched one window ahead.
+    const bool is_k = (warp == 0);
+    const CUtensorMap* map = is_k ? &kmap : &vmap;
+    const int full0 = is_k ? B_KFULL : B_VFULL, free0 = is_k ? B_KFREE : B_VFREE;
+    const uint32_t ring = s_base + (is_k ? OFF_K : OFF_V);
     const int32_t* bt = p.block_tables + (int64_t)b * p.max_blocks;
+    auto fetch = [&](int w) -> int {
+      const int key0 = (w * 32 + lane) * 16;  // sub-tile = 16 keys
+      int page = -1;
+      if (key0 < k_hi) {
+        const int blk = bt[key0 >> p.bs_shift];
+        if (blk < 0 || blk >= p.num_blocks) set_err(p.err, 1);  // TMA zero-fills page -1
+        else page = blk * p.num_kv_heads + g;
+      }
+      return page;
+    };
+    int win = 0, cur = fetch(0), nxt = fetch(1);
     for (int kt = 0; kt < T && ok; ++kt) {
       const int s = kt % NST;
-      const uint32_t ph = (uint32_t)((kt / NST - 1) & 1);  // phase of the previous use
-      const int key0 = kt * BN + 16 * (lane & 7);
-      int blk = -1;
-      if (lane < 8 && key0 < k_hi) {
-        blk = bt[key0 >> p.bs_shift];
-        if (blk < 0 || blk >= p.num_blocks) {
-          set_err(p.err, 1);
-          blk = -1;  // the TMA fills an out-of-range box with zeros
+      if ((kt >> 2) > win) {  // 4 tiles x 8 sub-tiles per window
+        cur = nxt;
+        ++win;
+        nxt = fetch(win + 1);
+      }
+      int pg[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) pg[j] = __shfl_sync(0xFFFFFFFFu, cur, (kt & 3) * 8 + j);
+      if (kt >= NST && !mbar_wait(bar(free0 + s), (uint32_t)((kt / NST - 1) & 1))) { ok = false; break; }
+      if (lane == 0) {
+        const uint32_t dst = ring + s * TILE;
+        mbar_arrive_expect_tx(bar(full0 + s), TILE);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int rip = (kt * BN + 16 * j) & (bs - 1);
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+            tma_load_3d(dst + c * CHUNK + j * 2048, map, bar(full0 + s), c * 64, rip, pg[j]);
         }
-      }
-      const int page = blk < 0 ? -1 : blk * p.num_kv_heads + g;
-      const int rip = key0 & (bs - 1);
-      int pg[8], rr[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        pg[j] = __shfl_sync(0xFFFFFFFFu, page, j);
-        rr[j] = __shfl_sync(0xFFFFFFFFu, rip, j);
-      }
-      if (kt >= NST && !mbar_wait(bar(B_KFREE + s), ph)) { ok = false; break; }
-      if (lane == 0) {
-        const uint32_t dst = s_base + OFF_K + s * TILE;
-        mbar_arrive_expect_tx(bar(B_KFULL + s), TILE);
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-#pragma unroll
-          for (int c = 0; c < 2; ++c)
-            tma_load_3d(dst + c * CHUNK + j * 2048, &kmap, bar(B_KFULL + s), c * 64, rr[j], pg[j]);
-      }
-      if (kt >= NST && !mbar_wait(bar(B_VFREE + s), ph)) { ok = false; break; }
-      if (lane == 0) {
-        const uint32_t dst = s_base + OFF_V + s * TILE;
-        mbar_arrive_expect_tx(bar(B_VFULL + s), TILE);
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-#pragma unroll
-          for (int c = 0; c < 2; ++c)
-            tma_load_3d(dst + c * CHUNK + j * 2048, &vmap, bar(B_VFULL + s), c * 64, rr[j], pg[j]);
       }
     }
   } else if (warp == 1) {
@@ -225,12 +226,12 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
     }
     __syncwarp();
   } else if (warp < 4 || warp >= 8) {
-    // ------------------------------------------------------------ V converters
+    // ------------------------------------------------------------ V converters (2, 3, 8-10)
     // In place, per 16-byte unit: bf16 -> f16 (the PV product is f16 x f16),
     // and keys at or past the sequence end -> 0 (they may hold anything, and
     // 0 * NaN is NaN).  The swizzle only permutes units inside a 128-byte key
     // row, so the key of a unit is its byte offset / 128 within its block.
-    const int ct = warp < 4 ? threadIdx.x - 64 : threadIdx.x - 192;  // 0..191
+    const int ct = warp < 4 ? threadIdx.x - 64 : threadIdx.x - 192;  // 0..159
     for (int kt = 0; kt < T && ok; ++kt) {
       const int vs = kt % NST;
       if (!mbar_wait(bar(B_VFULL + vs), (kt / NST) & 1)) { ok = false; break; }
@@ -238,7 +239,7 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       const bool tail = kbase + BN > kv_total;
       if (CT == DT_BF16 || tail) {
         uint8_t* vt = smem + OFF_V + vs * TILE;
-        constexpr int PER = (TILE / 16 + NCONV - 1) / NCONV;  // 11 units of 16 bytes
+        constexpr int PER = (TILE / 16 + NCONV - 1) / NCONV;  // 13 units of 16 bytes
         uint4 w[PER];
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
