@@ -6,37 +6,46 @@
 // is the one dense contraction of the path and runs on tcgen05 with TMEM
 // accumulators.
 //
-// One CTA owns a 128-row tile of packed (suffix token, query head) rows of
-// one (request, kv head): with a GQA group of G heads the tile holds 128/G
+// Work item: a 128-row tile of packed (suffix token, query head) rows of one
+// (request, kv head): with a GQA group of G heads the tile holds 128/G
 // consecutive suffix tokens x G heads, all sharing the same K/V.  Row r
 // (token i, head j) attends to keys 0 .. prefix + i.  Keys are consumed in
 // tiles of 128 read through the block table.
 //
+// The kernel is persistent: one CTA per SM walks the items with a fixed
+// stride, and every pipeline (K and V rings, S, P, O) runs straight through
+// item boundaries, so loading the next item's Q, block ids and first K/V
+// tiles, and writing the previous item's output, overlap the tensor work.
+//
 // Measured on this part, an MMA that reads its A operand from shared memory
-// runs at ~60% of the tensor peak for this shape, one that reads A from TMEM
-// at the full peak, so both A operands (Q for S = Q K^T, P for O += P V) live
-// in TMEM.  TMEM (512 columns): two fp32 S buffers, the O accumulator, the Q
-// tile and one f16 P tile.  An S buffer is released as soon as the softmax
-// has its row in registers, so S = Q K^T of tile k+2 never waits for a PV
-// product to drain; the P tile is rewritten once PV of the previous tile is
-// done.  Shared memory holds only 3-stage K and V rings.
+// runs well below the tensor peak for this shape, one that reads A from TMEM
+// at the peak, so both A operands (Q for S = Q K^T, P for O += P V) live in
+// TMEM.  TMEM: one fp32 S tile, the O accumulator, two Q tiles and two f16 P
+// tiles.  Q arrives by TMA in a shared-memory stage and is copied into the
+// TMEM Q tile of its item (tcgen05.cp).  The S tile is released as soon as the
+// softmax has its row in registers, so S = Q K^T of the next key tile runs
+// while the softmax works; P of key tile n goes to P buffer n mod 2 while
+// O += P V of tile n-1 reads the other.  Every reuse of a TMEM or
+// shared-memory buffer is ordered by an mbarrier.
 //
 // Warp roles (384 threads):
-//   warps 0,11  TMA producers for the K and the V ring: per key tile sixteen
-//               16-token x 64-dim boxes addressed through the block table
-//               (block ids prefetched into registers), 128-byte swizzled.
-//   warp 1      TMEM owner and, on one lane, the MMA issuer: S = Q K^T
-//               (A = Q in TMEM, B = K tile K-major, M=N=K=128), then
-//               O += P V for the previous tile (A = P in TMEM, B = the V tile
-//               as loaded, [key][dim], read as an MN-major operand).
+//   warp 0      TMA producer of the Q stage (per item) and of the K ring: per
+//               key tile sixteen 16-token x 64-dim boxes addressed through the
+//               block table (block ids prefetched into registers), 128-byte
+//               swizzled.
+//   warp 11     TMA producer of the V ring, the same way.
+//   warp 1      TMEM owner and, on one lane, the MMA issuer: Q stage -> TMEM,
+//               S = Q K^T (A = Q in TMEM, B = K tile K-major, M=N=K=128), then
+//               O += P V for the previous key tile (A = P in TMEM, B = the V
+//               tile as loaded, [key][dim], read as an MN-major operand).
 //   warps 2-3,  V converters: bf16 V tiles are turned into f16 in place and
 //   8-10        keys past the sequence end are zeroed (they may hold NaN).
-//   warps 4-7   softmax (one thread per row): stores its Q row into TMEM,
-//               then per tile reads its 128-column S row from TMEM with one
-//               wait, takes the row max (causal mask on diagonal tiles), keeps
-//               a running max with lazy rescaling (O in TMEM is rescaled only
-//               when the max grows by more than 2^8) and writes f16 P; finally
-//               O / l and the LSE.
+//   warps 4-7   softmax (one thread per row): per key tile reads its
+//               128-column S row from TMEM with one wait, takes the row max
+//               (causal mask on diagonal tiles), keeps a running max with lazy
+//               rescaling (O in TMEM is rescaled only when the max grows by
+//               more than 2^8) and writes f16 P; at the end of an item O / l
+//               and the LSE.
 // P is f16 (11 significant bits) because bf16 P alone would put the relative
 // L2 error of the output near 1.5e-3; V is therefore converted to f16 (bf16
 // values beyond +-65504 are outside this path's range).
@@ -52,38 +61,92 @@ constexpr int BM = 128;       // rows per tile
 constexpr int BN = 128;       // keys per tile
 constexpr int HD = 128;       // head dim
 constexpr int NTHREADS = 384;
-constexpr int NCONV = 160;    // V converter threads (warps 2, 3, 8-10)
+constexpr int NCONV = 128;    // V converter threads (warps 2, 3, 8, 9: one per SM sub-partition)
 constexpr int NST = 3;        // K and V ring depth
 constexpr int TILE = BN * HD * 2;   // 32 KB: 128 x 128 16-bit elements
 constexpr int CHUNK = 16384;        // one 64-element column block [128 rows][128 B]
 
 constexpr int OFF_K = 0;
 constexpr int OFF_V = OFF_K + NST * TILE;
-constexpr int OFF_BAR = OFF_V + NST * TILE;
+constexpr int OFF_Q = OFF_V + NST * TILE;   // Q stage, one tile
+constexpr int OFF_BAR = OFF_Q + TILE;
 enum {
-  B_Q = 0,
-  B_KFULL = 1, B_KFREE = B_KFULL + NST,
-  B_VFULL = B_KFREE + NST, B_VFREE = B_VFULL + NST, B_VCONV = B_VFREE + NST,
-  B_SFULL = B_VCONV + NST, B_SFREE = B_SFULL + 2, B_PFULL = B_SFREE + 2, B_PVDONE = B_PFULL + 1,
-  NBAR = B_PVDONE + 1
+  B_KFULL = 0, B_VFULL = B_KFULL + NST, B_VCONV = B_VFULL + NST,
+  // S(n) = Q K^T of key tile n done: S is readable, K stage n mod NST free
+  B_SDONE = B_VCONV + NST,
+  // O += P V of key tile n done: P buffer n mod 2, O and V stage n mod NST free
+  B_PVDONE = B_SDONE + NST,
+  B_SFREE = B_PVDONE + NST,   // softmax has S in registers
+  B_PFULL = B_SFREE + 1,      // [2] P buffer written
+  B_QFULL = B_PFULL + 2,      // Q stage loaded
+  B_QSFREE = B_QFULL + 1,     // Q stage copied into TMEM
+  B_QDONE = B_QSFREE + 1,     // [2] every S = Q K^T of the item using TMEM Q tile i done
+  B_OFREE = B_QDONE + 2,      // the item's O has been read out of TMEM
+  NBAR = B_OFREE + 1
 };
 constexpr int OFF_TMEMSLOT = OFF_BAR + NBAR * 8;
 constexpr int SMEM_BYTES = OFF_TMEMSLOT + 16 + 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TM_S = 0;     // two fp32 S buffers, columns 0 and 128
-constexpr uint32_t TM_O = 256;   // O accumulator, 128 columns
-constexpr uint32_t TM_Q = 384;   // Q tile: 64 columns of 16-bit pairs
-constexpr uint32_t TM_P = 448;   // P tile: 64 columns of f16 pairs
+constexpr uint32_t TM_S = 0;     // fp32 S tile, 128 columns
+constexpr uint32_t TM_O = 128;   // O accumulator, 128 columns
+constexpr uint32_t TM_Q = 256;   // two Q tiles of 64 columns of 16-bit pairs
+constexpr uint32_t TM_P = 384;   // two P tiles of 64 columns of f16 pairs
 constexpr float kLn2f = 0.6931471805599453f;
 
 __device__ __forceinline__ void set_err(int32_t* err, int code) {
   if (err) atomicCAS(err, 0, code);
 }
 
+// Per-request values an item needs, loaded one item ahead.
+struct ItemRaw {
+  int r0, r1, prefix;
+};
+
+struct Item {
+  int b, g, i0, ntok, P, S, row0, kv_total, k_hi, T;
+};
+
+__device__ __forceinline__ ItemRaw load_raw(const ExtendParams& p, int item) {
+  ItemRaw r{0, 0, 0};
+  if (item < p.num_items) {
+    const int b = item / (p.tiles_per_head * p.num_kv_heads);
+    r.r0 = __ldg(p.q_indptr + b);
+    r.r1 = __ldg(p.q_indptr + b + 1);
+    r.prefix = __ldg(p.prefix_lens + b);
+  }
+  return r;
+}
+
+// false: the tile holds no suffix rows (the same answer in every role)
+__device__ __forceinline__ bool derive(const ExtendParams& p, int item, const ItemRaw& r, Item& it) {
+  const int tile = item % p.tiles_per_head;
+  const int rest = item / p.tiles_per_head;
+  it.g = rest % p.num_kv_heads;
+  it.b = rest / p.num_kv_heads;
+  const int TOK = BM / p.group;
+  it.row0 = r.r0;
+  it.S = r.r1 - r.r0;
+  it.i0 = tile * TOK;
+  if (it.i0 >= it.S) return false;
+  it.ntok = min(TOK, it.S - it.i0);
+  it.P = r.prefix;
+  const int cap = p.max_blocks << p.bs_shift;
+  it.kv_total = it.P + it.S;
+  it.k_hi = it.P + it.i0 + it.ntok;  // keys this tile needs
+  if (it.P < 0 || it.kv_total > cap) {
+    set_err(p.err, 3);
+    it.kv_total = min(max(it.kv_total, 0), cap);
+    it.k_hi = min(max(it.k_hi, 1), max(cap, 1));
+  }
+  it.T = (it.k_hi + BN - 1) / BN;
+  return true;
+}
+
 template <int CT>
 __global__ void __launch_bounds__(NTHREADS, 1)
 extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-              const ExtendParams p) {
+              const __grid_constant__ CUtensorMap qmap, const ExtendParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -92,44 +155,29 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
   const uint32_t s_base = smem_u32(smem);
   auto bar = [&](int i) -> uint32_t { return smem_u32(&bars[i]); };
 
-  const int tile = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.group;
-  const int TOK = BM / G;
-  const int row0 = p.q_indptr[b];
-  const int S = p.q_indptr[b + 1] - row0;
-  const int i0 = tile * TOK;
-  if (i0 >= S) return;  // CTA-uniform: no tokens in this tile
-  const int ntok = min(TOK, S - i0);
-  const int P = p.prefix_lens[b];
-  const int bs = 1 << p.bs_shift;
-  const int cap = p.max_blocks * bs;
-  int kv_total = P + S;
-  int k_hi = P + i0 + ntok;  // keys this tile needs
-  if (P < 0 || kv_total > cap) {
-    if (threadIdx.x == 0) set_err(p.err, 3);
-    kv_total = min(max(kv_total, 0), cap);
-    k_hi = min(max(k_hi, 1), max(cap, 1));
-  }
-  const int T = (k_hi + BN - 1) / BN;
+  const int item0 = blockIdx.x, stride = gridDim.x;
 
   if (threadIdx.x == 0) {
     prefetch_tensormap(&kmap);
     prefetch_tensormap(&vmap);
-    mbar_init(bar(B_Q), 4);
+    prefetch_tensormap(&qmap);
     for (int i = 0; i < NST; ++i) {
       mbar_init(bar(B_KFULL + i), 1);
-      mbar_init(bar(B_KFREE + i), 1);
       mbar_init(bar(B_VFULL + i), 1);
-      mbar_init(bar(B_VFREE + i), 1);
       mbar_init(bar(B_VCONV + i), NCONV / 32);
+      mbar_init(bar(B_SDONE + i), 1);
+      mbar_init(bar(B_PVDONE + i), 1);
     }
+    mbar_init(bar(B_SFREE), 4);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(B_SFULL + i), 1);
-      mbar_init(bar(B_SFREE + i), 4);
+      mbar_init(bar(B_PFULL + i), 4);
+      mbar_init(bar(B_QDONE + i), 1);
     }
-    mbar_init(bar(B_PFULL), 4);
-    mbar_init(bar(B_PVDONE), 1);
+    mbar_init(bar(B_QFULL), 1);
+    mbar_init(bar(B_QSFREE), 1);
+    mbar_init(bar(B_OFREE), 4);
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -139,266 +187,370 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
   const uint32_t tmem = *tmem_slot;
   bool ok = true;
 
-  if (warp == 0 || warp == 11) {
-    // ------------------------------------------------------------ producers
-    // warp 0 streams K tiles, warp 11 V tiles, each through its own ring, so
-    // that a K load never queues behind a V buffer that is still in use.
-    // Block ids: lane l holds sub-tile (32 w + l) of window w, the next
-    // window is fetched one window ahead.
-    const bool is_k = (warp == 0);
-    const CUtensorMap* map = is_k ? &kmap : &vmap;
-    const int full0 = is_k ? B_KFULL : B_VFULL, free0 = is_k ? B_KFREE : B_VFREE;
-    const uint32_t ring = s_base + (is_k ? OFF_K : OFF_V);
-    const int32_t* bt = p.block_tables + (int64_t)b * p.max_blocks;
-    auto fetch = [&](int w) -> int {
-      const int key0 = (w * 32 + lane) * 16;  // sub-tile = 16 keys
-      int page = -1;
-      if (key0 < k_hi) {
-        const int blk = bt[key0 >> p.bs_shift];
-        if (blk < 0 || blk >= p.num_blocks) set_err(p.err, 1);  // TMA zero-fills page -1
-        else page = blk * p.num_kv_heads + g;
-      }
-      return page;
-    };
-    int win = 0, cur = fetch(0), nxt = fetch(1);
-    for (int kt = 0; kt < T && ok; ++kt) {
-      const int s = kt % NST;
-      if ((kt >> 2) > win) {  // 4 tiles x 8 sub-tiles per window
-        cur = nxt;
-        ++win;
-        nxt = fetch(win + 1);
-      }
-      int pg[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) pg[j] = __shfl_sync(0xFFFFFFFFu, cur, (kt & 3) * 8 + j);
-      if (kt >= NST && !mbar_wait(bar(free0 + s), (uint32_t)((kt / NST - 1) & 1))) { ok = false; break; }
-      if (lane == 0) {
-        const uint32_t dst = ring + s * TILE;
-        mbar_arrive_expect_tx(bar(full0 + s), TILE);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int rip = (kt * BN + 16 * j) & (bs - 1);
-#pragma unroll
-          for (int c = 0; c < 2; ++c)
-            tma_load_3d(dst + c * CHUNK + j * 2048, map, bar(full0 + s), c * 64, rip, pg[j]);
-        }
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t qk_fmt = (CT == DT_BF16) ? 1u : 0u;
-      constexpr uint32_t idesc_qk = umma_idesc_f16(qk_fmt, qk_fmt, BM, BN);
-      // P (A, f16 in TMEM) x V (B, f16, MN-major: the V tile as loaded, [key][dim])
-      constexpr uint32_t idesc_pv = umma_idesc_f16(0u, 0u, BM, HD) | (1u << 16);
-      auto issue_pv = [&](int u) -> bool {
-        const int us = u % NST;
-        if (!mbar_wait(bar(B_PFULL), u & 1)) return false;
-        if (!mbar_wait(bar(B_VCONV + us), (u / NST) & 1)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          umma_f16_ts(tmem + TM_O, tmem + TM_P + kk * 8,
-                      umma_desc_sw128_mn(s_base + OFF_V + us * TILE + kk * 2048, CHUNK), idesc_pv,
-                      (u > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(bar(B_PVDONE));  // P buffer and O are free again
-        umma_commit(bar(B_VFREE + us));
-        return true;
-      };
-      ok = mbar_wait(bar(B_Q), 0);
-      for (int kt = 0; kt < T && ok; ++kt) {
-        const int sb = kt & 1, ks = kt % NST;
-        if (!mbar_wait(bar(B_KFULL + ks), (kt / NST) & 1)) { ok = false; break; }
-        // S buffer sb is free once the softmax has read S(kt-2) into registers
-        if (kt >= 2 && !mbar_wait(bar(B_SFREE + sb), ((kt - 2) >> 1) & 1)) { ok = false; break; }
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * CHUNK + (kk & 3) * 32;
-          umma_f16_ts(tmem + TM_S + sb * BN, tmem + TM_Q + kk * 8,
-                      umma_desc_sw128(s_base + OFF_K + ks * TILE + off), idesc_qk, kk > 0 ? 1u : 0u);
-        }
-        umma_commit(bar(B_SFULL + sb));
-        umma_commit(bar(B_KFREE + ks));
-        if (kt >= 1 && !issue_pv(kt - 1)) { ok = false; break; }
-      }
-      if (ok) ok = issue_pv(T - 1);
-    }
-    __syncwarp();
-  } else if (warp < 4 || warp >= 8) {
-    // ------------------------------------------------------------ V converters (2, 3, 8-10)
-    // In place, per 16-byte unit: bf16 -> f16 (the PV product is f16 x f16),
-    // and keys at or past the sequence end -> 0 (they may hold anything, and
-    // 0 * NaN is NaN).  The swizzle only permutes units inside a 128-byte key
-    // row, so the key of a unit is its byte offset / 128 within its block.
-    const int ct = warp < 4 ? threadIdx.x - 64 : threadIdx.x - 192;  // 0..159
-    for (int kt = 0; kt < T && ok; ++kt) {
-      const int vs = kt % NST;
-      if (!mbar_wait(bar(B_VFULL + vs), (kt / NST) & 1)) { ok = false; break; }
-      const int kbase = kt * BN;
-      const bool tail = kbase + BN > kv_total;
-      if (CT == DT_BF16 || tail) {
-        uint8_t* vt = smem + OFF_V + vs * TILE;
-        constexpr int PER = (TILE / 16 + NCONV - 1) / NCONV;  // 13 units of 16 bytes
-        uint4 w[PER];
-#pragma unroll
-        for (int i = 0; i < PER; ++i) {
-          const int u = ct + i * NCONV;
-          if (u < TILE / 16) w[i] = *reinterpret_cast<const uint4*>(vt + u * 16);
-        }
-#pragma unroll
-        for (int i = 0; i < PER; ++i) {
-          const int u = ct + i * NCONV;
-          if (u >= TILE / 16) break;
-          const int key = kbase + ((u * 16) % CHUNK) / 128;
-          if (key >= kv_total) {
-            w[i] = make_uint4(0u, 0u, 0u, 0u);
-          } else if (CT == DT_BF16) {
-            w[i].x = to_f16x2<true>(w[i].x);
-            w[i].y = to_f16x2<true>(w[i].y);
-            w[i].z = to_f16x2<true>(w[i].z);
-            w[i].w = to_f16x2<true>(w[i].w);
-          }
-          *reinterpret_cast<uint4*>(vt + u * 16) = w[i];
-        }
-        fence_async_smem();
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_VCONV + vs));
-    }
-  } else {
+  // registers: launched with 168 per thread (384 x 168); the softmax
+  // warpgroup (warps 4-7) raises its budget to 248, the other two
+  // warpgroups lower theirs to 128: 128 + 248 + 128 = 3 x 168.
+  static_assert(128 + 248 + 128 == 3 * 168, "register split must equal the launch budget");
+  if (warp >= 4 && warp < 8) {
+    regs_inc<248>();
     // ------------------------------------------------------------ softmax
     const int qw = warp & 3;
     const int r = qw * 32 + lane;
     const uint32_t lane_addr = (uint32_t)(qw * 32) << 16;
-    const int lim = P + i0 + r / G;  // last key this row may see
-    const bool valid = (r / G) < ntok;
-    const int64_t qrow = (int64_t)(row0 + i0 + r / G) * p.num_q_heads + g * G + (r % G);
-    // Q row -> TMEM (64 columns of 16-bit pairs, the QK A operand); rows
-    // past the suffix get zeros
-    {
-      const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.q) + qrow * HD);
+    int n = 0;
+    // Output rows are written back late: the packed row of the previous item
+    // stays in registers and goes out in four groups of four 16-byte stores,
+    // one group per key tile of the next item, so the row-strided stores
+    // drain behind the softmax instead of stalling it at the item boundary.
+    uint32_t w[64];
+    uint4* pdst = nullptr;
+    int pstage = 4;  // next group to store; 4: nothing pending
+    auto store_group = [&]() {
+      if (pstage < 4) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[16];
+        for (int g4 = 0; g4 < 4; ++g4)
+          if (g4 == pstage) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint4 w = valid ? __ldg(src + c * 4 + j) : make_uint4(0u, 0u, 0u, 0u);
-          v[4 * j] = w.x; v[4 * j + 1] = w.y; v[4 * j + 2] = w.z; v[4 * j + 3] = w.w;
-        }
-        tmem_st16(tmem + lane_addr + TM_Q + c * 16, v);
+            for (int q = 0; q < 4; ++q)
+              pdst[4 * g4 + q] = make_uint4(w[16 * g4 + 4 * q], w[16 * g4 + 4 * q + 1],
+                                            w[16 * g4 + 4 * q + 2], w[16 * g4 + 4 * q + 3]);
+          }
+        ++pstage;
       }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_Q));
-    }
-    float m_run = -INFINITY, l_run = 0.f;
-    for (int kt = 0; kt < T && ok; ++kt) {
-      const int sb = kt & 1;
-      if (!mbar_wait(bar(B_SFULL + sb), (kt >> 1) & 1)) { ok = false; break; }
-      tc_fence_after();
-      const uint32_t srow = tmem + lane_addr + TM_S + sb * BN;
-      const int key0 = kt * BN;
-      const bool diag = key0 + BN - 1 > P + i0;  // tile reaches past some row's limit
-      // the whole S row: four 32-column loads, one wait
-      uint32_t raw[4][32];
+    };
+    ItemRaw nxt_raw = load_raw(p, item0);
+    for (int item = item0; ok && item < p.num_items; item += stride) {
+      const ItemRaw raw = nxt_raw;
+      nxt_raw = load_raw(p, item + stride);
+      Item it;
+      if (!derive(p, item, raw, it)) continue;
+      const int kdiag = it.P + it.i0;  // a row's last visible key is kdiag + its token
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int kt = 0; kt < it.T; ++kt, ++n) {
+        const int pb = n & 1;
+        if (!mbar_wait(bar(B_SDONE + n % NST), (n / NST) & 1)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t srow = tmem + lane_addr + TM_S;
+        const int key0 = kt * BN;
+        if (key0 + BN - 1 > kdiag) {
+          // causal mask on a tile that reaches past some row's limit (keys
+          // key0 .. key0+nvis are visible): applied in TMEM one 32-column
+          // chunk at a time, a short rolled loop that runs on one or two key
+          // tiles per item
+          const int nvis = kdiag + r / G - key0;
+          const uint32_t ninf = __float_as_uint(-INFINITY);
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t t[32];
+            tmem_ld32(srow + c * 32, t);
+            tmem_wait_ld();
+            const int lc = nvis - c * 32;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(srow + c * 32, raw[c]);
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_SFREE + sb));  // S is in registers: buffer free
-      if (diag) {  // causal mask on the tile that reaches past some row's limit
-        const int nvis = lim - key0;  // keys key0 .. key0+nvis are visible
+            for (int q = 0; q < 32; ++q) t[q] = (q > lc) ? ninf : t[q];
+            tmem_st32(srow + c * 32, t);
+          }
+          tmem_wait_st();
+        }
+        // the whole S row: four 32-column loads, one wait
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(srow + c * 32, sr[c]);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_SFREE));  // S is in registers: tile free
+        // row max: three-input max over 8 independent accumulators (one running
+        // max would be a 128-long dependent chain)
+        float mx[8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a) mx[a] = -INFINITY;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (c * 32 + j > nvis) raw[c][j] = __float_as_uint(-INFINITY);
-      }
-      // row max over 8 independent accumulators (one running max would be a
-      // 128-long dependent chain)
-      float mx[8];
+          for (int q = 0; q < 16; ++q)
+            mx[q & 7] = fmax3(mx[q & 7], __uint_as_float(sr[c][2 * q]), __uint_as_float(sr[c][2 * q + 1]));
+        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * p.scale_log2;
+        float m_new = m_run;
+        if (mt > m_run + 8.f) m_new = mt;
+        const float alpha = fast_exp2(m_run - m_new);
+        const bool mine = (m_new != m_run);
+        if (kt >= 1 && __any_sync(0xFFFFFFFFu, mine)) {
+          // rescale O in TMEM: wait until PV(n-1) has finished accumulating
+          if (!mbar_wait(bar(B_PVDONE + (n - 1) % NST), ((n - 1) / NST) & 1)) { ok = false; break; }
+          tc_fence_after();
+          const float f = mine ? alpha : 1.f;
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tmem + lane_addr + TM_O + c * 32, o);
+            tmem_wait_ld();
 #pragma unroll
-      for (int a = 0; a < 8; ++a) mx[a] = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int j = 0; j < 32; ++j) mx[j & 7] = fmaxf(mx[j & 7], __uint_as_float(raw[c][j]));
-      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * p.scale_log2;
-      float m_new = m_run;
-      if (mt > m_run + 8.f) m_new = mt;
-      const float alpha = fast_exp2(m_run - m_new);
-      const bool mine = (m_new != m_run);
-      if (kt >= 1 && __any_sync(0xFFFFFFFFu, mine)) {
-        // rescale O in TMEM: wait until PV(kt-1) has finished accumulating
-        if (!mbar_wait(bar(B_PVDONE), (kt - 1) & 1)) { ok = false; break; }
+            for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * f);
+            tmem_st32(tmem + lane_addr + TM_O + c * 32, o);
+          }
+          tmem_wait_st();
+        }
+        m_run = m_new;
+        // p = 2^(s*scale - m) as f16 pairs, streamed 32 keys at a time into P
+        // buffer pb once PV(n-2) has consumed P(n-2)
+        if (n >= 2 && !mbar_wait(bar(B_PVDONE + (n - 2) % NST), ((n - 2) / NST) & 1)) { ok = false; break; }
         tc_fence_after();
-        const float f = mine ? alpha : 1.f;
-#pragma unroll 1
+        // pairs of keys through the packed fp32 pipe: x = s * scale - m, p = 2^x
+        float2 sm[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) sm[a] = make_float2(0.f, 0.f);
+        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+        const float2 nm2 = make_float2(-m_new, -m_new);
+#pragma unroll
         for (int c = 0; c < 4; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tmem + lane_addr + TM_O + c * 32, o);
-          tmem_wait_ld();
+          uint32_t pk[16];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * f);
-          tmem_st32(tmem + lane_addr + TM_O + c * 32, o);
+          for (int q = 0; q < 16; ++q) {
+            const float2 x = __ffma2_rn(
+                make_float2(__uint_as_float(sr[c][2 * q]), __uint_as_float(sr[c][2 * q + 1])), sc2, nm2);
+            const float2 pe = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+            sm[q & 3] = __fadd2_rn(sm[q & 3], pe);
+            pk[q] = pack2<false>(pe.x, pe.y);
+          }
+          tmem_st16(tmem + lane_addr + TM_P + pb * 64 + c * 16, pk);
         }
+        const float sum = ((sm[0].x + sm[1].x) + (sm[2].x + sm[3].x)) +
+                          ((sm[0].y + sm[1].y) + (sm[2].y + sm[3].y));
+        l_run = l_run * alpha + sum;
         tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_PFULL + pb));
+        store_group();
       }
-      m_run = m_new;
-      // p = 2^(s*scale - m) as f16 pairs, streamed 32 keys at a time into the P
-      // tile once PV(kt-1) has consumed P(kt-1)
-      if (kt >= 1 && !mbar_wait(bar(B_PVDONE), (kt - 1) & 1)) { ok = false; break; }
+      if (!ok) break;
+      // ---- item epilogue: O out of TMEM (then O is free for the next item),
+      // O / l -> out, LSE
+      const int u = n - 1;  // last key tile of this item
+      if (!mbar_wait(bar(B_PVDONE + u % NST), (u / NST) & 1)) { ok = false; break; }
       tc_fence_after();
-      float sm[8];
-#pragma unroll
-      for (int a = 0; a < 8; ++a) sm[a] = 0.f;
-      const float sc = p.scale_log2, neg_m = -m_new;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float p0 = fast_exp2(fmaf(__uint_as_float(raw[c][2 * j]), sc, neg_m));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(raw[c][2 * j + 1]), sc, neg_m));
-          sm[j & 7] += p0 + p1;
-          pk[j] = pack2<false>(p0, p1);
-        }
-        tmem_st16(tmem + lane_addr + TM_P + c * 16, pk);
-      }
-      const float sum = ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
-      l_run = l_run * alpha + sum;
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_PFULL));
-    }
-    // ---- epilogue: O / l -> out, LSE
-    if (ok && mbar_wait(bar(B_PVDONE), (T - 1) & 1)) {
-      tc_fence_after();
+      while (pstage < 4) store_group();  // the previous item's row, if still pending
+      // O / l, packed to 16-bit, kept in registers; then O is free in TMEM
       const float osc = p.out_scale / l_run;
-#pragma unroll 1
+#pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t o[32];
         tmem_ld32(tmem + lane_addr + TM_O + c * 32, o);
         tmem_wait_ld();
-        if (valid) {
-          uint32_t w[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            w[j] = pack2<CT == DT_BF16>(__uint_as_float(o[2 * j]) * osc,
-                                        __uint_as_float(o[2 * j + 1]) * osc);
-          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.out) + qrow * HD + c * 32);
+        for (int q = 0; q < 16; ++q)
+          w[c * 16 + q] = pack2<CT == DT_BF16>(__uint_as_float(o[2 * q]) * osc,
+                                               __uint_as_float(o[2 * q + 1]) * osc);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_OFREE));
+      if ((r / G) < it.ntok) {
+        const int64_t qrow = (int64_t)(it.row0 + it.i0 + r / G) * p.num_q_heads + it.g * G + (r % G);
+        pdst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.out) + qrow * HD);
+        pstage = 0;
+        if (p.lse_out) p.lse_out[qrow] = (m_run + log2f(l_run)) * kLn2f;
+      }
+    }
+    while (pstage < 4) store_group();
+  } else {
+    regs_dec<128>();
+    if (warp == 0 || warp == 11) {
+      // ------------------------------------------------------------ producers
+      // warp 0 streams the Q stage and K tiles, warp 11 V tiles, each through
+      // its own ring, so that a K load never queues behind a V buffer that is
+      // still in use.  Block ids: lane l holds sub-tile (32 w + l) of window w,
+      // the next window is fetched one window ahead.
+      const bool is_k = (warp == 0);
+      const CUtensorMap* map = is_k ? &kmap : &vmap;
+      // a stage is free once the MMA that read it has completed
+      const int full0 = is_k ? B_KFULL : B_VFULL, free0 = is_k ? B_SDONE : B_PVDONE;
+      const uint32_t ring = s_base + (is_k ? OFF_K : OFF_V);
+      int n = 0, j = 0;  // key tiles and items so far
+      ItemRaw nxt_raw = load_raw(p, item0);
+      for (int item = item0; ok && item < p.num_items; item += stride) {
+        const ItemRaw raw = nxt_raw;
+        nxt_raw = load_raw(p, item + stride);
+        Item it;
+        if (!derive(p, item, raw, it)) continue;
+        if (is_k) {
+          if (lane == 0) {
+            // the Q stage is free once the previous item's Q is in TMEM
+            if (j >= 1 && !mbar_wait(bar(B_QSFREE), (j - 1) & 1)) ok = false;
+            if (ok) {
+              mbar_arrive_expect_tx(bar(B_QFULL), TILE);
+  #pragma unroll
+              for (int c = 0; c < 2; ++c)
+                tma_load_3d(s_base + OFF_Q + c * CHUNK, &qmap, bar(B_QFULL), c * 64, it.g * G,
+                            it.row0 + it.i0);
+            }
+          }
+          ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+          if (!ok) break;
+        }
+        const int32_t* bt = p.block_tables + (int64_t)it.b * p.max_blocks;
+        auto fetch = [&](int w) -> int {
+          const int key0 = (w * 32 + lane) * 16;  // sub-tile = 16 keys
+          int page = -1;
+          if (key0 < it.k_hi) {
+            const int blk = bt[key0 >> p.bs_shift];
+            if (blk < 0 || blk >= p.num_blocks) set_err(p.err, 1);  // TMA zero-fills page -1
+            else page = blk * p.num_kv_heads + it.g;
+          }
+          return page;
+        };
+        int win = 0, cur = fetch(0), nxt = fetch(1);
+        for (int kt = 0; kt < it.T; ++kt, ++n) {
+          const int s = n % NST;
+          if ((kt >> 2) > win) {  // 4 tiles x 8 sub-tiles per window
+            cur = nxt;
+            ++win;
+            nxt = fetch(win + 1);
+          }
+          int pg[8];
+  #pragma unroll
+          for (int q = 0; q < 8; ++q) pg[q] = __shfl_sync(0xFFFFFFFFu, cur, (kt & 3) * 8 + q);
+          if (n >= NST && !mbar_wait(bar(free0 + s), (uint32_t)((n / NST - 1) & 1))) { ok = false; break; }
+          if (lane == 0) {
+            const uint32_t dst = ring + s * TILE;
+            mbar_arrive_expect_tx(bar(full0 + s), TILE);
+  #pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const int rip = (kt * BN + 16 * q) & ((1 << p.bs_shift) - 1);
+  #pragma unroll
+              for (int c = 0; c < 2; ++c)
+                tma_load_3d(dst + c * CHUNK + q * 2048, map, bar(full0 + s), c * 64, rip, pg[q]);
+            }
+          }
+        }
+        ++j;
+      }
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t qk_fmt = (CT == DT_BF16) ? 1u : 0u;
+        constexpr uint32_t idesc_qk = umma_idesc_f16(qk_fmt, qk_fmt, BM, BN);
+        // P (A, f16 in TMEM) x V (B, f16, MN-major: the V tile as loaded, [key][dim])
+        constexpr uint32_t idesc_pv = umma_idesc_f16(0u, 0u, BM, HD) | (1u << 16);
+        // O += P V of key tile u; `first`: the first key tile of item ju, which
+        // overwrites O once the previous item's O has been read out
+        auto issue_pv = [&](int u, bool first, int ju) -> bool {
+          const int us = u % NST, pb = u & 1;  // V stage, P buffer
+          if (!mbar_wait(bar(B_PFULL + pb), (u >> 1) & 1)) return false;
+          if (!mbar_wait(bar(B_VCONV + us), (u / NST) & 1)) return false;
+          if (first && ju >= 1 && !mbar_wait(bar(B_OFREE), (ju - 1) & 1)) return false;
+          tc_fence_after();
+  #pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            umma_f16_ts(tmem + TM_O, tmem + TM_P + pb * 64 + kk * 8,
+                        umma_desc_sw128_mn(s_base + OFF_V + us * TILE + kk * 2048, CHUNK), idesc_pv,
+                        (!first || kk > 0) ? 1u : 0u);
+          umma_commit(bar(B_PVDONE + us));
+          return true;
+        };
+        int n = 0, j = 0;
+        bool have_prev = false, prev_first = false;
+        int prev_n = 0, prev_j = 0;
+        ItemRaw nxt_raw = load_raw(p, item0);
+        for (int item = item0; ok && item < p.num_items; item += stride) {
+          const ItemRaw raw = nxt_raw;
+          nxt_raw = load_raw(p, item + stride);
+          Item it;
+          if (!derive(p, item, raw, it)) continue;
+          const int qb = j & 1;
+          // Q stage -> TMEM Q tile qb, once the item two back is done with it
+          if (!mbar_wait(bar(B_QFULL), j & 1)) { ok = false; break; }
+          if (j >= 2 && !mbar_wait(bar(B_QDONE + qb), ((j - 2) >> 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+  #pragma unroll
+          for (int kk = 0; kk < HD / 16; ++kk)
+            tmem_cp_128x256b(tmem + TM_Q + qb * 64 + kk * 8,
+                             umma_desc_sw128(s_base + OFF_Q + (kk >> 2) * CHUNK + (kk & 3) * 32));
+          umma_commit(bar(B_QSFREE));
+          for (int kt = 0; kt < it.T; ++kt, ++n) {
+            const int ks = n % NST;
+            if (!mbar_wait(bar(B_KFULL + ks), (n / NST) & 1)) { ok = false; break; }
+            // the S tile is free once the softmax has read S(n-1) into registers
+            if (n >= 1 && !mbar_wait(bar(B_SFREE), (n - 1) & 1)) { ok = false; break; }
+            tc_fence_after();
+  #pragma unroll
+            for (int kk = 0; kk < HD / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * CHUNK + (kk & 3) * 32;
+              umma_f16_ts(tmem + TM_S, tmem + TM_Q + qb * 64 + kk * 8,
+                          umma_desc_sw128(s_base + OFF_K + ks * TILE + off), idesc_qk, kk > 0 ? 1u : 0u);
+            }
+            umma_commit(bar(B_SDONE + ks));
+            if (kt == it.T - 1) umma_commit(bar(B_QDONE + qb));
+            if (have_prev && !issue_pv(prev_n, prev_first, prev_j)) { ok = false; break; }
+            have_prev = true;
+            prev_n = n;
+            prev_first = (kt == 0);
+            prev_j = j;
+          }
+          ++j;
+        }
+        if (ok && have_prev) ok = issue_pv(prev_n, prev_first, prev_j);
+      }
+      __syncwarp();
+    } else if (warp != 10) {
+      // ------------------------------------------------------------ V converters (2, 3, 8, 9)
+      // In place, per 16-byte unit: bf16 -> f16 (the PV product is f16 x f16),
+      // and keys at or past the sequence end -> 0 (they may hold anything, and
+      // 0 * NaN is NaN).  The swizzle only permutes units inside a 128-byte key
+      // row, so the key of a unit is its byte offset / 128 within its block.
+      const int ct = warp < 4 ? threadIdx.x - 64 : threadIdx.x - 192;  // 0..127
+      constexpr int PER = TILE / 16 / NCONV;  // 16 units of 16 bytes per thread
+      static_assert(PER * NCONV * 16 == TILE, "converter units");
+      int n = 0;
+      ItemRaw nxt_raw = load_raw(p, item0);
+      for (int item = item0; ok && item < p.num_items; item += stride) {
+        const ItemRaw raw = nxt_raw;
+        nxt_raw = load_raw(p, item + stride);
+        Item it;
+        if (!derive(p, item, raw, it)) continue;
+        for (int kt = 0; kt < it.T; ++kt, ++n) {
+          const int vs = n % NST;
+          if (!mbar_wait(bar(B_VFULL + vs), (n / NST) & 1)) { ok = false; break; }
+          const int kbase = kt * BN;
+          uint4* vt = reinterpret_cast<uint4*>(smem + OFF_V + vs * TILE);
+          if (kbase + BN > it.kv_total) {  // tail tile: zero the keys past the end
+#pragma unroll 4
+            for (int i = 0; i < PER; ++i) {
+              const int u = ct + i * NCONV;
+              uint4 x = vt[u];
+              if (kbase + ((u * 16) % CHUNK) / 128 >= it.kv_total) {
+                x = make_uint4(0u, 0u, 0u, 0u);
+              } else if (CT == DT_BF16) {
+                x.x = to_f16x2<true>(x.x);
+                x.y = to_f16x2<true>(x.y);
+                x.z = to_f16x2<true>(x.z);
+                x.w = to_f16x2<true>(x.w);
+              }
+              vt[u] = x;
+            }
+            fence_async_smem();
+          } else if (CT == DT_BF16) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+            for (int h = 0; h < 2; ++h) {  // two batches of 8 loads in flight
+              uint4 x[PER / 2];
+#pragma unroll
+              for (int i = 0; i < PER / 2; ++i) x[i] = vt[ct + (h * (PER / 2) + i) * NCONV];
+#pragma unroll
+              for (int i = 0; i < PER / 2; ++i) {
+                x[i].x = to_f16x2<true>(x[i].x);
+                x[i].y = to_f16x2<true>(x[i].y);
+                x[i].z = to_f16x2<true>(x[i].z);
+                x[i].w = to_f16x2<true>(x[i].w);
+                vt[ct + (h * (PER / 2) + i) * NCONV] = x[i];
+              }
+            }
+            fence_async_smem();
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_VCONV + vs));
         }
       }
-      if (valid && p.lse_out) p.lse_out[qrow] = (m_run + log2f(l_run)) * kLn2f;
-    } else {
-      ok = false;
     }
   }
 
@@ -419,20 +571,22 @@ bool extend_supported(int head_dim, int cache_dt, int act_dt, int group) {
   return group == 1 || group == 2 || group == 4 || group == 8;
 }
 
-cudaError_t launch_extend(const CUtensorMap& kmap, const CUtensorMap& vmap, const ExtendParams& p,
-                          int head_dim, int cache_dt, int act_dt, cudaStream_t stream) {
+cudaError_t launch_extend(const CUtensorMap& kmap, const CUtensorMap& vmap, const CUtensorMap& qmap,
+                          const ExtendParams& p, int head_dim, int cache_dt, int act_dt,
+                          cudaStream_t stream) {
   if (!extend_supported(head_dim, cache_dt, act_dt, p.group)) return cudaErrorInvalidValue;
-  dim3 grid(p.tiles_per_head, p.num_kv_heads, p.batch);
+  if (p.num_items <= 0 || p.num_ctas <= 0) return cudaErrorInvalidValue;
+  const dim3 grid(p.num_ctas);
   if (cache_dt == DT_BF16) {
     auto k = extend_kernel<DT_BF16>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    k<<<grid, NTHREADS, SMEM_BYTES, stream>>>(kmap, vmap, p);
+    k<<<grid, NTHREADS, SMEM_BYTES, stream>>>(kmap, vmap, qmap, p);
   } else {
     auto k = extend_kernel<DT_F16>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    k<<<grid, NTHREADS, SMEM_BYTES, stream>>>(kmap, vmap, p);
+    k<<<grid, NTHREADS, SMEM_BYTES, stream>>>(kmap, vmap, qmap, p);
   }
   return cudaGetLastError();
 }

@@ -89,6 +89,27 @@ __device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// Copy a 128-row x 32-byte matrix from shared memory (described by `sdesc`,
+// the same descriptor an MMA operand would use) into TMEM lanes 0-127,
+// 8 columns from `taddr`: row i's bytes land in lane i in order, which is the
+// TMEM layout of a 16-bit A operand for 16 k values.  Ordered before MMAs that
+// this thread issues afterwards.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Per-warpgroup register budget (all four warps of the warpgroup execute it).
+// The increases of all warpgroups may not exceed what the decreases release
+// from the launch's threads x registers.
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // Arrive once on `bar` when every MMA this thread issued so far has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile(
