@@ -80,11 +80,9 @@ cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap,
                           cudaStream_t stream);
 size_t decode_smem_bytes(int head_dim, int cache_dt);
 cudaError_t launch_append(const AppendParams& p, int cache_dt, int act_dt, cudaStream_t stream);
-// kmap/vmap: page maps of the K and V caches; qmap: the query rows, dims
-// {head_dim, num_q_heads, total_rows}, box {64, group, 128 / group}.
-cudaError_t launch_extend(const CUtensorMap& kmap, const CUtensorMap& vmap,
-                          const CUtensorMap& qmap, const ExtendParams& p, int head_dim,
-                          int cache_dt, int act_dt, cudaStream_t stream);
+// kmap/vmap: page maps of the K and V caches.
+cudaError_t launch_extend(const CUtensorMap& kmap, const CUtensorMap& vmap, const ExtendParams& p,
+                          int head_dim, int cache_dt, int act_dt, cudaStream_t stream);
 bool extend_supported(int head_dim, int cache_dt, int act_dt, int group);
 
 }  // namespace pkv
