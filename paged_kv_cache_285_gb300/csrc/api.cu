@@ -110,6 +110,23 @@ pkv_status make_page_map(CUtensorMap* m, const void* base, const pkv_cache_desc*
   return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
 }
 
+// Query rows of the extend call as a 3-D map {head_dim, num_q_heads, rows}:
+// one box {64, group, 128 / group} is the 64-dim half of a 128-row tile of
+// (suffix token, head of the group) rows, 128-byte swizzled.
+pkv_status make_q_map(CUtensorMap* m, const void* q, int head_dim, int num_q_heads,
+                      int total_rows, int group) {
+  auto enc = encode_fn();
+  if (!enc) return PKV_ERR_CUDA;
+  cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_q_heads, (cuuint64_t)total_rows};
+  cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2u, (cuuint64_t)head_dim * 2u * (cuuint64_t)num_q_heads};
+  cuuint32_t box[3] = {64u, (cuuint32_t)group, (cuuint32_t)(128 / group)};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(q), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PKV_OK : PKV_ERR_CUDA;
+}
+
 int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
 struct DecodePlan {
@@ -315,9 +332,11 @@ pkv_status pkv_paged_extend_attn(const pkv_cache_desc* desc, const void* k_cache
   cudaError_t e;
   DeviceState* ds = device_state(&e);
   if (!ds) return PKV_ERR_CUDA;
-  CUtensorMap kmap, vmap;
+  CUtensorMap kmap, vmap, qmap;
   if ((st = make_page_map(&kmap, k_cache, desc)) != PKV_OK) return st;
   if ((st = make_page_map(&vmap, v_cache, desc)) != PKV_OK) return st;
+  if ((st = make_q_map(&qmap, q, desc->head_dim, num_q_heads, total_q_rows, group)) != PKV_OK)
+    return st;
   ExtendParams p;
   p.q_indptr = q_indptr;
   p.prefix_lens = prefix_lens;
@@ -338,11 +357,13 @@ pkv_status pkv_paged_extend_attn(const pkv_cache_desc* desc, const void* k_cache
   const double kscale = desc->cache_dtype == PKV_FP8_E4M3 ? (double)desc->k_scale : 1.0;
   p.scale_log2 = (float)((double)sm_scale * kscale * 1.4426950408889634);
   p.out_scale = desc->cache_dtype == PKV_FP8_E4M3 ? desc->v_scale : 1.0f;
-  const int64_t items = (int64_t)p.tiles_per_head * desc->num_kv_heads * batch;
+  // a work item is a pair of consecutive 128-row tiles of one (request, kv head)
+  const int64_t items = (int64_t)((p.tiles_per_head + 1) / 2) * desc->num_kv_heads * batch;
   if (items > INT32_MAX) return PKV_ERR_UNSUPPORTED;
   p.num_items = (int)items;
   p.num_ctas = (int)std::min<int64_t>(items, ds->sm_count > 0 ? ds->sm_count : 1);
-  e = launch_extend(kmap, vmap, p, desc->head_dim, (int)desc->cache_dtype, (int)act_dtype, stream);
+  e = launch_extend(kmap, vmap, qmap, p, desc->head_dim, (int)desc->cache_dtype, (int)act_dtype,
+                    stream);
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

@@ -68,7 +68,7 @@ struct ExtendParams {
   int bs_shift;
   int total_rows;
   int tiles_per_head;   // ceil(max_suffix_len * group / 128)
-  int num_items;        // tiles_per_head * num_kv_heads * batch
+  int num_items;        // ceil(tiles_per_head / 2) * num_kv_heads * batch (pairs of tiles)
   int num_ctas;         // persistent grid: min(num_items, SM count)
   float scale_log2;
   float out_scale;
@@ -80,9 +80,11 @@ cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap,
                           cudaStream_t stream);
 size_t decode_smem_bytes(int head_dim, int cache_dt);
 cudaError_t launch_append(const AppendParams& p, int cache_dt, int act_dt, cudaStream_t stream);
-// kmap/vmap: page maps of the K and V caches.
-cudaError_t launch_extend(const CUtensorMap& kmap, const CUtensorMap& vmap, const ExtendParams& p,
-                          int head_dim, int cache_dt, int act_dt, cudaStream_t stream);
+// kmap/vmap: page maps of the K and V caches; qmap: the query rows, dims
+// {head_dim, num_q_heads, total_rows}, box {64, group, 128 / group}.
+cudaError_t launch_extend(const CUtensorMap& kmap, const CUtensorMap& vmap,
+                          const CUtensorMap& qmap, const ExtendParams& p, int head_dim,
+                          int cache_dt, int act_dt, cudaStream_t stream);
 bool extend_supported(int head_dim, int cache_dt, int act_dt, int group);
 
 }  // namespace pkv
