@@ -96,6 +96,31 @@ def test_shared_prefix_extend_workload_sampled():
     assert pkv.get_device_error() == 0
 
 
+@pytest.mark.parametrize("hq,hkv", [(32, 8), (8, 8)], ids=["gqa4", "mha"])
+def test_extend_many_items_mixed_lengths(hq, hkv):
+    # Many more (request, kv head, row-tile pair) items than SMs, with key-tile
+    # counts from 1 to dozens per item and many empty row tiles (short
+    # suffixes next to long ones), so the persistent pipeline crosses item
+    # boundaries of every kind; rows are sampled against the oracle.
+    rng = np.random.default_rng(11)
+    B = 40
+    P = [int(x) for x in rng.integers(0, 3000, B)]
+    P[0], P[1] = 0, 0
+    Sx = [int(x) for x in rng.integers(1, 300, B)]
+    Sx[2], Sx[3] = 1, 2
+    case = W.extend_case(P, Sx, hq, hkv, 128, 16, BF16, BF16, seed=81 + hq, device="cuda")
+    out, lse = gpu_extend(case)
+    total_rows = case.q.shape[0]
+    rows = [(int(r), int(h)) for r, h in zip(rng.integers(0, total_rows, 300), rng.integers(0, hq, 300))]
+    # every request's first and last suffix row, too
+    starts = case.q_indptr.cpu().numpy()
+    for b in range(B):
+        rows.append((int(starts[b]), int(rng.integers(0, hq))))
+        rows.append((int(starts[b + 1]) - 1, int(rng.integers(0, hq))))
+    check(case, out, lse, f"many items {hq}x{hkv}", rows=rows)
+    assert pkv.get_device_error() == 0
+
+
 def test_extend_after_bulk_append():
     # the step the benchmark times: append the suffix K/V, then extend over the pool
     case = W.extend_case([1900] * 4, [100] * 4, 32, 8, 128, 16, BF16, BF16, seed=71,
