@@ -168,9 +168,20 @@ pkv_status pkv_paged_decode_attn(const pkv_cache_desc* desc, const void* k_cache
  * max_suffix_len / max_total_len: host-side upper bounds of S_b and P_b+S_b.
  * total_q_rows:  q_indptr[batch] (host value; sizes the grid).
  * lse_out:       nullable float [q_indptr[batch]][num_q_heads], natural log.
- * workspace:     pkv_extend_workspace_bytes() bytes (currently 0).
+ * workspace:     device memory of at least pkv_extend_workspace_bytes()
+ *                bytes, 256-byte aligned, owned by the caller; its contents
+ *                need no initialisation and are scratch after the call.  0
+ *                bytes (NULL allowed) for 16-bit caches.  For an fp8 cache it
+ *                holds a claim flag per physical block and 16-bit shadow K and
+ *                V pools of the activation dtype (4*num_blocks rounded up to
+ *                256, plus twice num_blocks*Hkv*bs*D*2 rounded up to 256):
+ *                every page a request of the call reads is widened there once
+ *                (exactly: e4m3 fits f16 and bf16) and the 16-bit kernel runs
+ *                on the shadow pools; k_scale and v_scale are applied to the
+ *                scores and the output.  Too small -> PKV_ERR_WORKSPACE.  Two
+ *                calls in flight must not share a workspace.
  * Supported: head_dim 128, block_size 16/32, num_q_heads/num_kv_heads in
- * {1, 2, 4, 8}, 16-bit caches and fp8.
+ * {1, 2, 4, 8}; cache dtype equal to the act dtype (f16, bf16) or fp8 e4m3.
  * ------------------------------------------------------------------------- */
 /* ---------------------------------------------------------------------------
  * pkv_paged_decode_attn_noalloc -- the same decode as pkv_paged_decode_attn,

@@ -129,6 +129,23 @@ pkv_status make_q_map(CUtensorMap* m, const void* q, int head_dim, int num_q_hea
 
 int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Workspace of an extend call over an fp8 cache: a claim flag per physical
+// block, then 16-bit shadow K and V pools with the cache's geometry.
+struct ExtendFp8Layout {
+  size_t flags = 0, k16 = 0, v16 = 0, total = 0;
+};
+ExtendFp8Layout fp8_layout(const pkv_cache_desc* d) {
+  ExtendFp8Layout l;
+  const size_t pool16 = (size_t)d->num_blocks * d->num_kv_heads * d->block_size * d->head_dim * 2;
+  l.flags = 0;
+  l.k16 = align256((size_t)d->num_blocks * 4);
+  l.v16 = l.k16 + align256(pool16);
+  l.total = l.v16 + align256(pool16);
+  return l;
+}
+
 struct DecodePlan {
   int chunk = 0;
   int splits = 0;
@@ -301,8 +318,10 @@ pkv_status pkv_paged_decode_attn(const pkv_cache_desc* desc, const void* k_cache
 
 size_t pkv_extend_workspace_bytes(const pkv_cache_desc* desc, int32_t batch, int32_t num_q_heads,
                                   int32_t total_q_rows, int32_t max_total_len) {
-  (void)desc; (void)batch; (void)num_q_heads; (void)total_q_rows; (void)max_total_len;
-  return 0;
+  (void)batch; (void)num_q_heads; (void)total_q_rows; (void)max_total_len;
+  if (check_desc(desc) != PKV_OK || desc->cache_dtype != PKV_FP8_E4M3) return 0;
+  const ExtendFp8Layout l = fp8_layout(desc);
+  return l.total;
 }
 
 pkv_status pkv_paged_extend_attn(const pkv_cache_desc* desc, const void* k_cache,
@@ -313,7 +332,6 @@ pkv_status pkv_paged_extend_attn(const pkv_cache_desc* desc, const void* k_cache
                                  float sm_scale, int32_t total_q_rows, int32_t max_suffix_len,
                                  int32_t max_total_len, float* lse_out, void* workspace,
                                  size_t workspace_bytes, cudaStream_t stream) {
-  (void)workspace; (void)workspace_bytes;
   pkv_status st = check_desc(desc);
   if (st != PKV_OK) return st;
   if ((st = check_act(desc, act_dtype)) != PKV_OK) return st;
@@ -322,7 +340,11 @@ pkv_status pkv_paged_extend_attn(const pkv_cache_desc* desc, const void* k_cache
     return PKV_ERR_INVALID_ARG;
   if (num_q_heads % desc->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
   const int group = num_q_heads / desc->num_kv_heads;
-  if (!extend_supported(desc->head_dim, (int)desc->cache_dtype, (int)act_dtype, group))
+  const bool fp8 = desc->cache_dtype == PKV_FP8_E4M3;
+  // an fp8 cache is read through 16-bit shadow pages of the activation dtype
+  pkv_cache_desc desc16 = *desc;
+  if (fp8) desc16.cache_dtype = act_dtype;
+  if (!extend_supported(desc->head_dim, (int)desc16.cache_dtype, (int)act_dtype, group))
     return PKV_ERR_UNSUPPORTED;
   if (batch == 0 || total_q_rows == 0 || max_suffix_len == 0) return PKV_OK;
   if (!k_cache || !v_cache || !q || !out || !block_tables || !q_indptr || !prefix_lens)
@@ -332,9 +354,38 @@ pkv_status pkv_paged_extend_attn(const pkv_cache_desc* desc, const void* k_cache
   cudaError_t e;
   DeviceState* ds = device_state(&e);
   if (!ds) return PKV_ERR_CUDA;
+  const void* k_pages = k_cache;
+  const void* v_pages = v_cache;
+  if (fp8) {
+    const ExtendFp8Layout l = fp8_layout(desc);
+    if (!workspace || workspace_bytes < l.total) return PKV_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return PKV_ERR_INVALID_ARG;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    DequantParams dp;
+    dp.k8 = static_cast<const uint8_t*>(k_cache);
+    dp.v8 = static_cast<const uint8_t*>(v_cache);
+    dp.k16 = reinterpret_cast<uint16_t*>(ws + l.k16);
+    dp.v16 = reinterpret_cast<uint16_t*>(ws + l.v16);
+    dp.flags = reinterpret_cast<int32_t*>(ws + l.flags);
+    dp.q_indptr = q_indptr;
+    dp.prefix_lens = prefix_lens;
+    dp.block_tables = block_tables;
+    dp.max_blocks = max_blocks_per_seq;
+    dp.num_blocks = desc->num_blocks;
+    dp.bs_shift = desc->block_size == 16 ? 4 : 5;
+    dp.page_elems = desc->num_kv_heads * desc->block_size * desc->head_dim;
+    if (cudaMemsetAsync(dp.flags, 0, (size_t)desc->num_blocks * 4, stream) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    // every table entry a request can read: the full table width (the kernel
+    // skips entries past each request's prefix + suffix)
+    if (launch_dequant_pages(dp, batch, max_blocks_per_seq, (int)act_dtype, stream) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    k_pages = dp.k16;
+    v_pages = dp.v16;
+  }
   CUtensorMap kmap, vmap, qmap;
-  if ((st = make_page_map(&kmap, k_cache, desc)) != PKV_OK) return st;
-  if ((st = make_page_map(&vmap, v_cache, desc)) != PKV_OK) return st;
+  if ((st = make_page_map(&kmap, k_pages, &desc16)) != PKV_OK) return st;
+  if ((st = make_page_map(&vmap, v_pages, &desc16)) != PKV_OK) return st;
   if ((st = make_q_map(&qmap, q, desc->head_dim, num_q_heads, total_q_rows, group)) != PKV_OK)
     return st;
   ExtendParams p;
@@ -362,7 +413,7 @@ pkv_status pkv_paged_extend_attn(const pkv_cache_desc* desc, const void* k_cache
   if (items > INT32_MAX) return PKV_ERR_UNSUPPORTED;
   p.num_items = (int)items;
   p.num_ctas = (int)std::min<int64_t>(items, ds->sm_count > 0 ? ds->sm_count : 1);
-  e = launch_extend(kmap, vmap, qmap, p, desc->head_dim, (int)desc->cache_dtype, (int)act_dtype,
+  e = launch_extend(kmap, vmap, qmap, p, desc->head_dim, (int)desc16.cache_dtype, (int)act_dtype,
                     stream);
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

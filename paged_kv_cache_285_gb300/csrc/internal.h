@@ -80,6 +80,24 @@ cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap,
                           cudaStream_t stream);
 size_t decode_smem_bytes(int head_dim, int cache_dt);
 cudaError_t launch_append(const AppendParams& p, int cache_dt, int act_dt, cudaStream_t stream);
+// fp8 pages read by an extend call -> 16-bit shadow pages (same layout).
+struct DequantParams {
+  const uint8_t* k8;          // fp8 K pool
+  const uint8_t* v8;          // fp8 V pool
+  uint16_t* k16;              // shadow K pool, activation dtype
+  uint16_t* v16;              // shadow V pool
+  int32_t* flags;             // [num_blocks], zero before the launch
+  const int32_t* q_indptr;
+  const int32_t* prefix_lens;
+  const int32_t* block_tables;
+  int max_blocks;
+  int num_blocks;
+  int bs_shift;
+  int page_elems;             // Hkv * block_size * head_dim
+};
+cudaError_t launch_dequant_pages(const DequantParams& p, int batch, int blocks_per_seq, int act_dt,
+                                 cudaStream_t stream);
+
 // kmap/vmap: page maps of the K and V caches; qmap: the query rows, dims
 // {head_dim, num_q_heads, total_rows}, box {64, group, 128 / group}.
 cudaError_t launch_extend(const CUtensorMap& kmap, const CUtensorMap& vmap,

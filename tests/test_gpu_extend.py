@@ -16,21 +16,26 @@ pytestmark = pytest.mark.gpu
 S = W.to_numpy_storage
 
 
-def gpu_extend(case):
+def gpu_extend(case, workspace="auto"):
     out = torch.full_like(case.q, float("nan"))
     rows, hq, _ = case.q.shape
     lse = torch.full((rows, hq), float("nan"), dtype=torch.float32, device="cuda")
     suf = (case.q_indptr[1:] - case.q_indptr[:-1]).cpu()
     tot = case.prefix_lens.cpu() + suf
+    if isinstance(workspace, str):
+        nbytes = pkv.extend_workspace_bytes(case.k_cache, int(suf.numel()), hq, rows, int(tot.max()),
+                                            k_scale=case.k_scale, v_scale=case.v_scale)
+        # filled with garbage: the call may not rely on its contents
+        workspace = torch.full((nbytes,), 0xA5, dtype=torch.uint8, device="cuda") if nbytes else None
     pkv.paged_extend_attn(case.k_cache, case.v_cache, case.q, out, case.q_indptr,
                           case.prefix_lens, case.block_tables, case.sm_scale,
                           int(suf.max()), int(tot.max()), k_scale=case.k_scale,
-                          v_scale=case.v_scale, lse_out=lse)
+                          v_scale=case.v_scale, lse_out=lse, workspace=workspace)
     torch.cuda.synchronize()
     return out, lse
 
 
-def check(case, out, lse, what, rows=None):
+def check(case, out, lse, what, rows=None, fp8=False):
     args = (S(case.k_cache), S(case.v_cache), case.cache_dtype, case.k_scale, case.v_scale,
             S(case.q), case.act_dtype, case.q_indptr.cpu().numpy(), case.prefix_lens.cpu().numpy(),
             case.block_tables.cpu().numpy(), case.num_q_heads, case.sm_scale)
@@ -40,8 +45,8 @@ def check(case, out, lse, what, rows=None):
     if rows is not None:
         got = np.stack([got[r, h] for r, h in rows])
         gl = np.array([gl[r, h] for r, h in rows])
-    assert_attention_close(got, ref, case.act_dtype, what=what)
-    assert np.max(np.abs(gl - ref_lse)) <= 1e-3, what
+    assert_attention_close(got, ref, case.act_dtype, fp8=fp8, what=what)
+    assert np.max(np.abs(gl - ref_lse)) <= (3e-2 if fp8 else 1e-3), what
 
 
 CASES = [
@@ -146,6 +151,61 @@ def test_extend_garbage_past_end_is_ignored():
     case.v_cache[blk, :, total % 16:] = float("nan")
     out, lse = gpu_extend(case)
     check(case, out, lse, "garbage tail")
+
+
+FP8_CASES = [
+    # (prefix_lens, suffix_lens, hq, hkv, bs, act dtype)
+    ([0, 13, 30, 200], [37, 19, 130, 1], 8, 2, 16, BF16),
+    ([1900], [100], 32, 8, 16, BF16),
+    ([100, 0], [300, 129], 8, 8, 32, F16),
+    ([129, 64, 1], [200, 17, 256], 64, 8, 16, BF16),
+]
+
+
+@pytest.mark.parametrize("cfg", FP8_CASES, ids=lambda c: f"fp8-P{c[0]}-S{c[1]}-h{c[2]}x{c[3]}-bs{c[4]}-a{c[5]}")
+def test_extend_fp8_cache(cfg):
+    # e4m3 pages with per-tensor scales: widened once per page into the
+    # workspace, then the 16-bit path; vs the oracle on the same dequantised
+    # values, fp8 bound
+    P, Sx, hq, hkv, bs, act = cfg
+    case = W.extend_case(P, Sx, hq, hkv, 128, bs, E4M3, act, seed=90 + sum(Sx), device="cuda")
+    out, lse = gpu_extend(case)
+    check(case, out, lse, "fp8 " + str(cfg), fp8=True)
+    assert pkv.get_device_error() == 0
+
+
+def test_extend_fp8_shared_prefix_pages_widened_once():
+    # 64 requests over one shared 1,900-token prefix: the shared pages are
+    # claimed by one CTA each; results match the oracle on sampled rows
+    case = W.extend_case([1900] * 64, [100] * 64, 32, 8, 128, 16, E4M3, BF16, seed=95,
+                         device="cuda", shared_prefix=1900)
+    out, lse = gpu_extend(case)
+    rng = np.random.default_rng(5)
+    rows = [(int(r), int(h)) for r, h in zip(rng.integers(0, case.q.shape[0], 96), rng.integers(0, 32, 96))]
+    check(case, out, lse, "fp8 shared prefix", rows=rows, fp8=True)
+    assert pkv.get_device_error() == 0
+
+
+def test_extend_fp8_garbage_past_end_is_ignored():
+    case = W.extend_case([30], [20], 8, 2, 128, 16, E4M3, BF16, seed=96, device="cuda")
+    total = 50
+    blk = int(case.block_tables[0, (total - 1) // 16])
+    case.k_cache[blk, :, total % 16:] = 0x7F  # e4m3 NaN codes
+    case.v_cache[blk, :, total % 16:] = 0xFF
+    out, lse = gpu_extend(case)
+    check(case, out, lse, "fp8 garbage tail", fp8=True)
+
+
+def test_extend_fp8_workspace_checks():
+    case = W.extend_case([16], [8], 8, 2, 128, 16, E4M3, BF16, seed=97, device="cuda")
+    need = pkv.extend_workspace_bytes(case.k_cache, 1, 8, 8, 24, k_scale=case.k_scale, v_scale=case.v_scale)
+    nb, hkv, bs, d = case.k_cache.shape
+    pool16 = nb * hkv * bs * d * 2
+    assert need == -(-nb * 4 // 256) * 256 + 2 * (-(-pool16 // 256) * 256)
+    with pytest.raises(pkv.PkvError):
+        gpu_extend(case, workspace=None)
+    with pytest.raises(pkv.PkvError):
+        gpu_extend(case, workspace=torch.empty(need - 256, dtype=torch.uint8, device="cuda"))
 
 
 def test_extend_unsupported_combinations_raise():
