@@ -409,7 +409,12 @@ def run_extend_bench(args, dev, bf16, bf16_sus, peak_src):
             "tflops": round(tf, 1), "useful_flops_per_call": flops,
             "roofline": {"kernel": "paged_extend_attn", "bound": "tensor", "achieved": round(tf, 1),
                          "peak": bf16, "unit": "TFLOP/s", "frac": round(tf / bf16, 4),
-                         "peak_source": f"{peak_src} (bf16_tflops burst)", "traffic": None}}
+                         "peak_source": f"{peak_src} (bf16_tflops burst)",
+                         "traffic": profiled_traffic(
+                             "extend_kernel_shared_prefix_extend.md",
+                             ["paged_kv_cache_285_gb300/csrc/extend.cu",
+                              "paged_kv_cache_285_gb300/csrc/ptx.cuh",
+                              "paged_kv_cache_285_gb300/csrc/tcgen05.cuh"])}}
 
 
 def cpu_baseline_decode(case, budget_s=10.0):
