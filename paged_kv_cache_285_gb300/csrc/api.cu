@@ -402,6 +402,7 @@ pkv_status pkv_paged_extend_attn(const pkv_cache_desc* desc, const void* k_cache
   p.num_q_heads = num_q_heads;
   p.num_kv_heads = desc->num_kv_heads;
   p.group = group;
+  p.out_32b = aligned(out, 32) ? 1 : 0;
   p.bs_shift = desc->block_size == 16 ? 4 : 5;
   p.total_rows = total_q_rows;
   p.tiles_per_head = ceil_div((int64_t)max_suffix_len * group, 128);

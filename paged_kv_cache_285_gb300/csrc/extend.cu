@@ -318,9 +318,17 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       if (lane == 0) mbar_arrive(bar(B_OFREE + x));
       if ((r / G) < it.ntok[x]) {
         const int64_t qrow = (int64_t)(it.row0 + i0x + r / G) * p.num_q_heads + it.g * G + (r % G);
-        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.out) + qrow * HD);
+        uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + qrow * HD;
+        if (p.out_32b) {
+          // 32-byte stores: half the L1 requests of 16-byte ones for the
+          // row-strided output
 #pragma unroll
-        for (int q = 0; q < 16; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+          for (int q = 0; q < 8; ++q) st_global_v8(dst + 16 * q, &w[8 * q]);
+        } else {
+          uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+          for (int q = 0; q < 16; ++q) d4[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+        }
         if (p.lse_out) p.lse_out[qrow] = (m_run + log2f(l_run)) * kLn2f;
       }
       ++js;

@@ -70,6 +70,7 @@ struct ExtendParams {
   int tiles_per_head;   // ceil(max_suffix_len * group / 128)
   int num_items;        // ceil(tiles_per_head / 2) * num_kv_heads * batch (pairs of tiles)
   int num_ctas;         // persistent grid: min(num_items, SM count)
+  int out_32b;          // out is 32-byte aligned: rows are written with 32-byte stores
   float scale_log2;
   float out_scale;
 };
