@@ -403,6 +403,7 @@ pkv_status pkv_paged_extend_attn(const pkv_cache_desc* desc, const void* k_cache
   p.num_kv_heads = desc->num_kv_heads;
   p.group = group;
   p.out_32b = aligned(out, 32) ? 1 : 0;
+  p.group_shift = group == 1 ? 0 : group == 2 ? 1 : group == 4 ? 2 : 3;
   p.bs_shift = desc->block_size == 16 ? 4 : 5;
   p.total_rows = total_q_rows;
   p.tiles_per_head = ceil_div((int64_t)max_suffix_len * group, 128);
@@ -413,6 +414,10 @@ pkv_status pkv_paged_extend_attn(const pkv_cache_desc* desc, const void* k_cache
   const int64_t items = (int64_t)((p.tiles_per_head + 1) / 2) * desc->num_kv_heads * batch;
   if (items > INT32_MAX) return PKV_ERR_UNSUPPORTED;
   p.num_items = (int)items;
+  const uint32_t pairs = (uint32_t)((p.tiles_per_head + 1) / 2);
+  p.div_pairs = make_fastdiv(pairs);
+  p.div_hkv = make_fastdiv((uint32_t)desc->num_kv_heads);
+  p.div_req = make_fastdiv(pairs * (uint32_t)desc->num_kv_heads);
   p.num_ctas = (int)std::min<int64_t>(items, ds->sm_count > 0 ? ds->sm_count : 1);
   e = launch_extend(kmap, vmap, qmap, p, desc->head_dim, (int)desc16.cache_dtype, (int)act_dtype,
                     stream);

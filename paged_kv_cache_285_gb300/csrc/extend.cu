@@ -100,12 +100,10 @@ struct Item {
   int b, g, i0, ntok[2], P, S, row0, kv_total, k_hi, T;
 };
 
-__device__ __forceinline__ int pairs_per_head(const ExtendParams& p) { return (p.tiles_per_head + 1) >> 1; }
-
 __device__ __forceinline__ ItemRaw load_raw(const ExtendParams& p, int item) {
   ItemRaw r{0, 0, 0};
   if (item < p.num_items) {
-    const int b = item / (pairs_per_head(p) * p.num_kv_heads);
+    const int b = (int)p.div_req.div((uint32_t)item);
     r.r0 = __ldg(p.q_indptr + b);
     r.r1 = __ldg(p.q_indptr + b + 1);
     r.prefix = __ldg(p.prefix_lens + b);
@@ -115,12 +113,11 @@ __device__ __forceinline__ ItemRaw load_raw(const ExtendParams& p, int item) {
 
 // false: tile A holds no suffix rows (the same answer in every role)
 __device__ __forceinline__ bool derive(const ExtendParams& p, int item, const ItemRaw& r, Item& it) {
-  const int pph = pairs_per_head(p);
-  const int pair = item % pph;
-  const int rest = item / pph;
-  it.g = rest % p.num_kv_heads;
-  it.b = rest / p.num_kv_heads;
-  const int TOK = BM / p.group;
+  const uint32_t rest = p.div_pairs.div((uint32_t)item);
+  const int pair = item - (int)(rest * p.div_pairs.d);
+  it.b = (int)p.div_hkv.div(rest);
+  it.g = (int)(rest - (uint32_t)it.b * p.div_hkv.d);
+  const int TOK = BM >> p.group_shift;
   it.row0 = r.r0;
   it.S = r.r1 - r.r0;
   it.i0 = 2 * pair * TOK;  // first token of tile A; tile B follows it
@@ -154,7 +151,8 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.group;
-  const int TOK = BM / G;
+  const int gs = p.group_shift;  // G = 1 << gs
+  const int TOK = BM >> gs;
   const int item0 = blockIdx.x, stride = gridDim.x;
 
   if (threadIdx.x == 0) {
@@ -219,7 +217,7 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
           // key0 .. key0+nvis are visible): applied in TMEM one 32-column
           // chunk at a time, a short rolled loop that runs on one or two key
           // tiles per item
-          const int nvis = kdiag + r / G - key0;
+          const int nvis = kdiag + (r >> gs) - key0;
           const uint32_t ninf = __float_as_uint(-INFINITY);
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
@@ -316,8 +314,8 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_OFREE + x));
-      if ((r / G) < it.ntok[x]) {
-        const int64_t qrow = (int64_t)(it.row0 + i0x + r / G) * p.num_q_heads + it.g * G + (r % G);
+      if ((r >> gs) < it.ntok[x]) {
+        const int64_t qrow = (int64_t)(it.row0 + i0x + (r >> gs)) * p.num_q_heads + it.g * G + (r & (G - 1));
         uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + qrow * HD;
         if (p.out_32b) {
           // 32-byte stores: half the L1 requests of 16-byte ones for the

@@ -51,6 +51,34 @@ struct AppendParams {
   float v_scale;
 };
 
+// Division of unsigned n < 2^31 by a divisor fixed for a launch, as a
+// multiply-high and a shift (Granlund & Montgomery, "Division by invariant
+// integers using multiplication", 1994): with l = ceil(log2 d) and
+// m = floor(2^32 (2^l - d) / d) + 1, n / d = (umulhi(n, m) + n) >> l.
+struct FastDiv {
+  uint32_t d, m, l;
+#ifdef __CUDACC__
+  __host__ __device__
+#endif
+  uint32_t div(uint32_t n) const {
+#ifdef __CUDA_ARCH__
+    return (__umulhi(n, m) + n) >> l;
+#else
+    return (uint32_t)((((uint64_t)n * m) >> 32) + n) >> l;
+#endif
+  }
+#ifdef __CUDACC__
+  __host__ __device__
+#endif
+  uint32_t mod(uint32_t n) const { return n - div(n) * d; }
+};
+inline FastDiv make_fastdiv(uint32_t d) {
+  FastDiv f{d, 0u, 0u};
+  while ((1ull << f.l) < d) ++f.l;
+  f.m = (uint32_t)((((uint64_t)1 << 32) * ((1ull << f.l) - d)) / d + 1);
+  return f;
+}
+
 struct ExtendParams {
   const int32_t* q_indptr;
   const int32_t* prefix_lens;
@@ -65,12 +93,16 @@ struct ExtendParams {
   int num_q_heads;
   int num_kv_heads;
   int group;
+  int group_shift;      // log2(group); the group is 1, 2, 4 or 8
   int bs_shift;
   int total_rows;
   int tiles_per_head;   // ceil(max_suffix_len * group / 128)
   int num_items;        // ceil(tiles_per_head / 2) * num_kv_heads * batch (pairs of tiles)
   int num_ctas;         // persistent grid: min(num_items, SM count)
   int out_32b;          // out is 32-byte aligned: rows are written with 32-byte stores
+  FastDiv div_pairs;    // by ceil(tiles_per_head / 2)
+  FastDiv div_hkv;      // by num_kv_heads
+  FastDiv div_req;      // by ceil(tiles_per_head / 2) * num_kv_heads (items per request)
   float scale_log2;
   float out_scale;
 };
