@@ -150,6 +150,37 @@ pkv_status pkv_paged_decode_attn(const pkv_cache_desc* desc, const void* k_cache
                                  cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * pkv_paged_decode_attn_append -- decode with the current token appended by
+ * the decode kernel itself.
+ *
+ * "KV Cache에 대해 알아보자 (Feat. Attention)", §3: each decode step adds the
+ * new token's K and V to the cache and then attends over the whole cache,
+ * the new token included.  This call does both in one launch: the same result
+ * and the same cache bytes as pkv_kv_append of k_new/v_new into the slot of
+ * position seq_lens[b]-1 (physical block block_tables[b][(n-1)/bs], offset
+ * (n-1) % bs) followed by pkv_paged_decode_attn, without the separate launch
+ * and the second read of the new rows.
+ *
+ * k_new, v_new:  [batch][num_kv_heads][head_dim] act dtype, device,
+ *                16-byte aligned; request b's row goes to position
+ *                seq_lens[b]-1 (requests with seq_lens[b] == 0 append nothing).
+ * k_cache, v_cache: written at those slots (fp8: e4m3(fp32(x) / scale),
+ *                correctly rounded division, saturating round-to-nearest-even,
+ *                exactly as pkv_kv_append); the slots must not be shared by
+ *                two requests of the call.
+ * Everything else as pkv_paged_decode_attn.  A slot whose block id lies
+ * outside the pool is not written and is reported in the device error word.
+ * ------------------------------------------------------------------------- */
+pkv_status pkv_paged_decode_attn_append(const pkv_cache_desc* desc, void* k_cache, void* v_cache,
+                                        const void* k_new, const void* v_new, const void* q,
+                                        void* out, pkv_dtype act_dtype,
+                                        const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                        const int32_t* seq_lens, int32_t batch,
+                                        int32_t num_q_heads, float sm_scale, int32_t max_seq_len,
+                                        int32_t num_splits, float* lse_out, void* workspace,
+                                        size_t workspace_bytes, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
  * pkv_paged_extend_attn -- suffix prefill over a cached prefix.
  *
  * "PagedAttention과 RadixAttention으로 LLM KV 캐시 최적화", section 03: when

@@ -67,6 +67,9 @@ def load():
         lib.pkv_paged_decode_attn.argtypes = [D, P, P, P, P, ctypes.c_int, P, I32, P, I32, I32, F,
                                               I32, I32, P, P, SZ, P]
         lib.pkv_paged_decode_attn.restype = ctypes.c_int
+        lib.pkv_paged_decode_attn_append.argtypes = [D, P, P, P, P, P, P, ctypes.c_int, P, I32, P,
+                                                      I32, I32, F, I32, I32, P, P, SZ, P]
+        lib.pkv_paged_decode_attn_append.restype = ctypes.c_int
         lib.pkv_extend_workspace_bytes.argtypes = [D, I32, I32, I32, I32]
         lib.pkv_extend_workspace_bytes.restype = SZ
         lib.pkv_paged_extend_attn.argtypes = [D, P, P, P, P, ctypes.c_int, P, P, P, I32, I32, I32,
@@ -162,6 +165,24 @@ def paged_decode_attn(k_cache, v_cache, q, out, block_tables, seq_lens, sm_scale
                                    float(sm_scale), int(max_seq_len), int(num_splits),
                                    _ptr(lse_out), _ptr(workspace), ws_bytes, _stream(stream))
     _check(st, "pkv_paged_decode_attn")
+
+
+def paged_decode_attn_append(k_cache, v_cache, k_new, v_new, q, out, block_tables, seq_lens,
+                             sm_scale, max_seq_len, k_scale=1.0, v_scale=1.0, num_splits=0,
+                             lse_out=None, workspace=None, stream=None):
+    """pkv_paged_decode_attn_append: k_new/v_new [B, Hkv, D] are written to position
+    seq_len-1 of each request and attended in the same launch."""
+    lib = load()
+    desc = _desc(k_cache, k_scale, v_scale)
+    b, hq, _ = q.shape
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib.pkv_paged_decode_attn_append(ctypes.byref(desc), _ptr(k_cache), _ptr(v_cache),
+                                          _ptr(k_new), _ptr(v_new), _ptr(q), _ptr(out),
+                                          _dtype_code(q), _ptr(block_tables),
+                                          int(block_tables.shape[1]), _ptr(seq_lens), b, hq,
+                                          float(sm_scale), int(max_seq_len), int(num_splits),
+                                          _ptr(lse_out), _ptr(workspace), ws_bytes, _stream(stream))
+    _check(st, "pkv_paged_decode_attn_append")
 
 
 def extend_workspace_bytes(k_cache, batch, num_q_heads, total_q_rows, max_total_len,

@@ -258,13 +258,16 @@ size_t pkv_decode_workspace_bytes(const pkv_cache_desc* desc, int32_t batch, int
   return plan_decode(desc, batch, num_q_heads, max_seq_len, num_splits, sms).ws_bytes;
 }
 
-pkv_status pkv_paged_decode_attn(const pkv_cache_desc* desc, const void* k_cache,
-                                 const void* v_cache, const void* q, void* out,
-                                 pkv_dtype act_dtype, const int32_t* block_tables,
-                                 int32_t max_blocks_per_seq, const int32_t* seq_lens,
-                                 int32_t batch, int32_t num_q_heads, float sm_scale,
-                                 int32_t max_seq_len, int32_t num_splits, float* lse_out,
-                                 void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+// Decode, optionally with the current token's K/V (k_new/v_new, [B][Hkv][D]
+// act dtype) appended to position seq_len-1 inside the decode kernel.
+static pkv_status decode_common(const pkv_cache_desc* desc, const void* k_cache,
+                                const void* v_cache, const void* k_new, const void* v_new,
+                                const void* q, void* out, pkv_dtype act_dtype,
+                                const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+                                float sm_scale, int32_t max_seq_len, int32_t num_splits,
+                                float* lse_out, void* workspace, size_t workspace_bytes,
+                                cudaStream_t stream) {
   pkv_status st = check_desc(desc);
   if (st != PKV_OK) return st;
   if ((st = check_act(desc, act_dtype)) != PKV_OK) return st;
@@ -280,6 +283,8 @@ pkv_status pkv_paged_decode_attn(const pkv_cache_desc* desc, const void* k_cache
     return PKV_ERR_INVALID_ARG;
   if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 4) || !aligned(out, 2))
     return PKV_ERR_INVALID_ARG;
+  if ((k_new == nullptr) != (v_new == nullptr)) return PKV_ERR_INVALID_ARG;
+  if (k_new && (!aligned(k_new, 16) || !aligned(v_new, 16))) return PKV_ERR_INVALID_ARG;
   cudaError_t e;
   DeviceState* ds = device_state(&e);
   if (!ds) return PKV_ERR_CUDA;
@@ -312,8 +317,40 @@ pkv_status pkv_paged_decode_attn(const pkv_cache_desc* desc, const void* k_cache
   const double kscale = desc->cache_dtype == PKV_FP8_E4M3 ? (double)desc->k_scale : 1.0;
   p.scale_log2 = (float)((double)sm_scale * kscale * 1.4426950408889634);
   p.out_scale = desc->cache_dtype == PKV_FP8_E4M3 ? desc->v_scale : 1.0f;
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.k_cache = const_cast<void*>(k_cache);
+  p.v_cache = const_cast<void*>(v_cache);
+  p.k_scale = desc->k_scale;
+  p.v_scale = desc->v_scale;
   e = launch_decode(kmap, vmap, p, desc->head_dim, (int)desc->cache_dtype, (int)act_dtype, stream);
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_paged_decode_attn(const pkv_cache_desc* desc, const void* k_cache,
+                                 const void* v_cache, const void* q, void* out,
+                                 pkv_dtype act_dtype, const int32_t* block_tables,
+                                 int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                 int32_t batch, int32_t num_q_heads, float sm_scale,
+                                 int32_t max_seq_len, int32_t num_splits, float* lse_out,
+                                 void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return decode_common(desc, k_cache, v_cache, nullptr, nullptr, q, out, act_dtype, block_tables,
+                       max_blocks_per_seq, seq_lens, batch, num_q_heads, sm_scale, max_seq_len,
+                       num_splits, lse_out, workspace, workspace_bytes, stream);
+}
+
+pkv_status pkv_paged_decode_attn_append(const pkv_cache_desc* desc, void* k_cache, void* v_cache,
+                                        const void* k_new, const void* v_new, const void* q,
+                                        void* out, pkv_dtype act_dtype,
+                                        const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                        const int32_t* seq_lens, int32_t batch,
+                                        int32_t num_q_heads, float sm_scale, int32_t max_seq_len,
+                                        int32_t num_splits, float* lse_out, void* workspace,
+                                        size_t workspace_bytes, cudaStream_t stream) {
+  if (!k_new || !v_new) return PKV_ERR_INVALID_ARG;
+  return decode_common(desc, k_cache, v_cache, k_new, v_new, q, out, act_dtype, block_tables,
+                       max_blocks_per_seq, seq_lens, batch, num_q_heads, sm_scale, max_seq_len,
+                       num_splits, lse_out, workspace, workspace_bytes, stream);
 }
 
 size_t pkv_extend_workspace_bytes(const pkv_cache_desc* desc, int32_t batch, int32_t num_q_heads,

@@ -100,6 +100,13 @@ __device__ __forceinline__ float load_act(const void* base, int64_t idx) {
   }
 }
 
+// A 16-bit activation value (its bits) widened to fp32.
+template <int AT>
+__device__ __forceinline__ float to_f32_bits(uint32_t bits16) {
+  if constexpr (AT == DT_BF16) return __uint_as_float(bits16 << 16);
+  else return __half2float(__ushort_as_half((unsigned short)bits16));
+}
+
 template <int HD, int CT, int AT, int NW, int NS>
 __global__ void __launch_bounds__(NW * 32)
 decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
@@ -137,6 +144,50 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
   const int nsub = (t1 - t0 + kSubTokens - 1) / kSubTokens;
   const int nsplit_b = (n + p.chunk - 1) / p.chunk;
   const int cnt = warp < nsub ? (nsub - warp + NW - 1) / NW : 0;
+
+  if (p.k_new != nullptr && split == nsplit_b - 1) {
+    // Fused append: this CTA covers position n-1, the current token; its K/V
+    // rows of kv head g go to their slot before any tile of this CTA is
+    // loaded (TMA reads the slot after the proxy fence and the barrier
+    // below).  Same bytes as the separate append: a 16-bit copy, or
+    // e4m3(fp32(x) / scale) with a correctly rounded division and a
+    // saturating round-to-nearest-even convert.
+    const int pos = n - 1;
+    const int blk = p.block_tables[(int64_t)b * p.max_blocks + (pos >> p.bs_shift)];
+    constexpr int VPR = HD / 8;  // 16-byte input vectors per row
+    if (blk < 0 || blk >= p.num_blocks) {
+      if (threadIdx.x == 0) set_err(p.err, 2);
+    } else if (threadIdx.x < 2 * VPR) {
+      const bool isv = threadIdx.x >= VPR;
+      const int e = (threadIdx.x % VPR) * 8;
+      const int64_t src = ((int64_t)b * p.num_kv_heads + g) * HD + e;
+      const int64_t dst = (((int64_t)blk * p.num_kv_heads + g) * bs + (pos & (bs - 1))) * HD + e;
+      const uint4 x = __ldg(reinterpret_cast<const uint4*>(
+          reinterpret_cast<const uint16_t*>(isv ? p.v_new : p.k_new) + src));
+      void* cache = isv ? p.v_cache : p.k_cache;
+      if constexpr (CT != DT_E4M3) {
+        *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(cache) + dst) = x;
+      } else {
+        const float sc = isv ? p.v_scale : p.k_scale;
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+        uint32_t o[2];
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          uint32_t ob = 0;
+#pragma unroll
+          for (int q2 = 0; q2 < 2; ++q2) {
+            const uint32_t ww = w[2 * h2 + q2];
+            const float a0 = __fdiv_rn(to_f32_bits<AT>(ww & 0xFFFFu), sc);
+            const float a1 = __fdiv_rn(to_f32_bits<AT>(ww >> 16), sc);
+            ob |= f32x2_to_e4m3x2(a0, a1) << (16 * q2);
+          }
+          o[h2] = ob;
+        }
+        *reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(cache) + dst) = make_uint2(o[0], o[1]);
+      }
+      fence_proxy_async_global();
+    }
+  }
 
   if (threadIdx.x == 0) {
     prefetch_tensormap(&kmap);

@@ -33,6 +33,14 @@ struct DecodeParams {
   int num_splits;     // S of the plan
   float scale_log2;   // sm_scale * log2(e) (* k_scale for fp8)
   float out_scale;    // v_scale for fp8, else 1
+  // fused append (nullable k_new): the current token's K/V rows [B][Hkv][D]
+  // in the act dtype, written to position seq_len-1 before it is read
+  const void* k_new;
+  const void* v_new;
+  void* k_cache;
+  void* v_cache;
+  float k_scale;      // fp8 store scales
+  float v_scale;
 };
 
 struct AppendParams {
