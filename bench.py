@@ -218,13 +218,20 @@ def run_decode_bench(args, world, rank, local):
                               case.seq_lens, case.sm_scale, max_len, k_scale=case.k_scale,
                               v_scale=case.v_scale, workspace=ws)
 
+    def fused():  # the current token appended by the decode kernel itself
+        pkv.paged_decode_attn_append(case.k_cache, case.v_cache, case.new_k, case.new_v, case.q,
+                                     out, case.block_tables, case.seq_lens, case.sm_scale,
+                                     max_len, k_scale=case.k_scale, v_scale=case.v_scale,
+                                     workspace=ws)
+
     for _ in range(args.warmup):
         append()
         decode()
+        fused()
     torch.cuda.synchronize()
     # The step's launches are captured once into CUDA graphs and replayed, so the
     # device time is not stretched by host-side enqueue cost (Python + ctypes).
-    g_step, g_dec = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    g_step, g_dec, g_fused = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     cap = torch.cuda.Stream()
     cap.wait_stream(stream)
     with torch.cuda.stream(cap):
@@ -233,14 +240,17 @@ def run_decode_bench(args, world, rank, local):
             decode()
         with torch.cuda.graph(g_dec, stream=cap):
             decode()
+        with torch.cuda.graph(g_fused, stream=cap):
+            fused()
     stream.wait_stream(cap)
     for _ in range(args.warmup):
         g_step.replay()
         g_dec.replay()
+        g_fused.replay()
     torch.cuda.synchronize()
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
@@ -254,14 +264,19 @@ def run_decode_bench(args, world, rank, local):
             ev[i][2].record(stream)
             g_dec.replay()                      # the decode call alone, for its roofline
             ev[i][3].record(stream)
+            flush()
+            ev[i][4].record(stream)
+            g_fused.replay()                    # the step with the append fused into decode
+            ev[i][5].record(stream)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
     barrier(world)
     step_ms = [e[0].elapsed_time(e[1]) for e in ev]
     dec_ms = [e[2].elapsed_time(e[3]) for e in ev]
-    ms_step = sum(step_ms) / K
+    fused_ms = [e[4].elapsed_time(e[5]) for e in ev]
+    ms_sep = max_over_ranks(sum(step_ms) / K, world)
     ms_dec = sum(dec_ms) / K
-    ms_step_max = max_over_ranks(ms_step, world)
+    ms_step_max = max_over_ranks(sum(fused_ms) / K, world)
 
     app_b, dec_b = decode_step_bytes(case)
     step_bytes = app_b + dec_b
@@ -269,7 +284,7 @@ def run_decode_bench(args, world, rank, local):
     value = world * step_bytes / (ms_step_max * 1e-3) / 1e9
     dec_gbs = dec_b / (ms_dec * 1e-3) / 1e9
     splits_plan = ws_bytes > 0
-    launches_per_step = 1 + 1 + (1 if splits_plan else 0)
+    dec_launches = 1 + (1 if splits_plan else 0)    # decode_kernel (+ merge_kernel)
 
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
@@ -281,12 +296,18 @@ def run_decode_bench(args, world, rank, local):
                    "block_size": case.block_size, "cache_dtype": W.DTYPE_NAME[case.cache_dtype],
                    "act_dtype": W.DTYPE_NAME[case.act_dtype],
                    "cached_tokens": int(case.seq_lens.sum()),
-                   "step": "kv_append(1 token/request) + paged_decode_attn, one CUDA graph",
+                   "step": "paged_decode_attn_append: the current token's K/V (1 per request) "
+                           "appended by the decode kernel, then attention; one CUDA graph",
                    "l2": "256 MiB buffer written then read between timed steps (outside the events)",
                    "parallelism": f"replicas x{world}"},
         "pct_of_peak": round(100.0 * value / world / hbm, 1),
         "tokens_per_s": round(world * b / (ms_step_max * 1e-3), 1),
-        "gpu_launches": 2 * launches_per_step * K - K,
+        # timed region per iteration: append + decode, decode alone, fused step
+        "gpu_launches": (1 + 3 * dec_launches) * K,
+        "separate_step": {"step": "kv_append + paged_decode_attn, one CUDA graph",
+                          "ms_per_step": round(ms_sep, 5),
+                          "value": round(world * step_bytes / (ms_sep * 1e-3) / 1e9, 1),
+                          "unit": "GB/s"},
     }
     traffic = profiled_traffic("decode_kernel_llama3_8b_layer.md",
                                ["paged_kv_cache_285_gb300/csrc/decode.cu",
@@ -302,7 +323,7 @@ def run_decode_bench(args, world, rank, local):
     res["wall_s_timed"] = round(t_wall, 3)
 
     # end to end through the C ABI with host buffers: per step the inputs of the
-    # step (q, the new token's K/V, its slot, seq_lens, block tables) go host->device
+    # step (q, the new token's K/V, seq_lens, block tables) go host->device
     # from pinned memory and the output comes back device->host
     res["e2e"] = e2e_decode(case, pkv, max_len, ws, out, stream, K, world)
     if args.extend and rank == 0 and world == 1:
@@ -314,7 +335,7 @@ def run_decode_bench(args, world, rank, local):
 
 def e2e_decode(case, pkv, max_len, ws, out, stream, K, world):
     host = {}
-    names = ["q", "new_k", "new_v", "slot_last", "seq_lens", "block_tables"]
+    names = ["q", "new_k", "new_v", "seq_lens", "block_tables"]
     for n in names:
         t = getattr(case, n)
         host[n] = t.to("cpu").pin_memory()
@@ -326,11 +347,10 @@ def e2e_decode(case, pkv, max_len, ws, out, stream, K, world):
     def step():
         for n in names:
             dev_t[n].copy_(host[n], non_blocking=True)
-        pkv.kv_append(case.k_cache, case.v_cache, dev_t["new_k"], dev_t["new_v"],
-                      dev_t["slot_last"], k_scale=case.k_scale, v_scale=case.v_scale)
-        pkv.paged_decode_attn(case.k_cache, case.v_cache, dev_t["q"], out,
-                              dev_t["block_tables"], dev_t["seq_lens"], case.sm_scale, max_len,
-                              k_scale=case.k_scale, v_scale=case.v_scale, workspace=ws)
+        pkv.paged_decode_attn_append(case.k_cache, case.v_cache, dev_t["new_k"], dev_t["new_v"],
+                                     dev_t["q"], out, dev_t["block_tables"], dev_t["seq_lens"],
+                                     case.sm_scale, max_len, k_scale=case.k_scale,
+                                     v_scale=case.v_scale, workspace=ws)
         out_h.copy_(out, non_blocking=True)
 
     for _ in range(3):
