@@ -52,7 +52,9 @@ typedef enum {
   PKV_ERR_INVALID_ARG = 1,   /* null pointer, negative size, Hq % Hkv != 0, ... */
   PKV_ERR_UNSUPPORTED = 2,   /* valid but not built: head_dim, block_size, dtype combo */
   PKV_ERR_WORKSPACE = 3,     /* workspace missing or smaller than *_workspace_bytes() */
-  PKV_ERR_CUDA = 4           /* a CUDA runtime/driver call or a launch failed */
+  PKV_ERR_CUDA = 4,          /* a CUDA runtime/driver call or a launch failed */
+  PKV_ERR_NO_SPACE = 5       /* prefix index: no free block even after evicting every
+                                unlocked leaf */
 } pkv_status;
 
 typedef enum { PKV_F16 = 0, PKV_BF16 = 1, PKV_FP8_E4M3 = 2 } pkv_dtype;
@@ -263,6 +265,83 @@ pkv_status pkv_paged_extend_attn(const pkv_cache_desc* desc, const void* k_cache
                                  int32_t max_suffix_len, int32_t max_total_len,
                                  float* lse_out, void* workspace, size_t workspace_bytes,
                                  cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Prefix index (host): radix tree over token ids with leaf-first LRU eviction.
+ *
+ * "PagedAttention과 RadixAttention으로 LLM KV 캐시 최적화", section 03: the KV
+ * of finished requests stays on token paths of a radix tree, a new request
+ * reuses the longest matching path and prefills only the rest, and when
+ * memory runs short unused leaf branches are evicted first (least recently
+ * used first) so that interior prefixes shared by many requests survive.
+ * With paged KV only whole blocks are shared: edge labels, matches and
+ * insertions are whole numbers of block_size tokens (a prefix that ends inside
+ * a block is matched up to the block before it).
+ *
+ * The index owns the physical block ids [0, num_blocks) of one cache pool.
+ * A block is free, held by the caller (pkv_radix_alloc, until pkv_radix_insert
+ * adopts it or pkv_radix_free returns it), or held by the tree (evictable once
+ * no match holds it).  All arrays here are host memory owned by the caller;
+ * the index keeps no pointer to them.  Not thread-safe.  The typical request:
+ *   match(tokens) -> P matched tokens, their blocks (locked);
+ *   alloc(blocks for the remaining tokens) -> block table = matched + new;
+ *   kv_append the suffix K/V, paged_extend_attn with prefix_len = P;
+ *   insert(tokens, block table) -> the tree adopts the new full blocks and
+ *   hands back any block it already held under the same tokens;
+ *   release(tokens, P) unlocks the matched path; free() the partial tail block
+ *   when the request is done with it.
+ * ------------------------------------------------------------------------- */
+typedef struct pkv_radix_index pkv_radix_index;
+
+typedef struct {
+  int32_t num_blocks;       /* pool size */
+  int32_t free_blocks;      /* not held by anyone */
+  int32_t tree_blocks;      /* held by the tree */
+  int32_t caller_blocks;    /* allocated and not yet inserted or freed */
+  int32_t nodes;            /* tree nodes (edges), the root not counted */
+  int32_t evictable_leaves; /* leaves that no match holds */
+} pkv_radix_stats_t;
+
+/* New index over block ids [0, num_blocks) of a pool with block_size tokens
+ * per block; every block starts free.  *out = NULL on error. */
+pkv_status pkv_radix_create(int32_t block_size, int32_t num_blocks, pkv_radix_index** out);
+void pkv_radix_destroy(pkv_radix_index* index);
+
+/* Longest cached prefix of tokens[0, num_tokens) in whole blocks: its length
+ * in *matched_tokens and its physical blocks, in order, in blocks_out (room for
+ * blocks_cap).  The path is locked (never evicted) until pkv_radix_release and
+ * marked as used now.  blocks_cap too small -> PKV_ERR_INVALID_ARG, nothing
+ * locked, *matched_tokens still set. */
+pkv_status pkv_radix_match(pkv_radix_index* index, const int32_t* tokens, int32_t num_tokens,
+                           int32_t* blocks_out, int32_t blocks_cap, int32_t* matched_tokens);
+
+/* Unlock a path locked by pkv_radix_match (same tokens, the matched length). */
+pkv_status pkv_radix_release(pkv_radix_index* index, const int32_t* tokens,
+                             int32_t matched_tokens);
+
+/* count free blocks for the caller, evicting unlocked leaves (least recently
+ * used first) as needed; PKV_ERR_NO_SPACE when even that is not enough (the
+ * evictions made so far stay made, nothing is allocated). */
+pkv_status pkv_radix_alloc(pkv_radix_index* index, int32_t count, int32_t* blocks_out);
+
+/* Return caller-held blocks to the pool. */
+pkv_status pkv_radix_free(pkv_radix_index* index, const int32_t* blocks, int32_t count);
+
+/* The tree takes the full blocks of tokens[0, num_tokens) with their physical
+ * blocks blocks[0, num_tokens / block_size): blocks it already holds under the
+ * same tokens stay the tree's; a caller block standing for such a block is
+ * freed and reported in released_out (room for num_tokens / block_size, may be
+ * NULL) / *num_released; the remaining blocks are adopted.  A partial last
+ * block is not taken.  Blocks that are free, or twice in the list ->
+ * PKV_ERR_INVALID_ARG with no change. */
+pkv_status pkv_radix_insert(pkv_radix_index* index, const int32_t* tokens, int32_t num_tokens,
+                            const int32_t* blocks, int32_t* released_out, int32_t* num_released);
+
+/* Evict unlocked leaves, least recently used first, until num_blocks blocks
+ * are freed or nothing is evictable; *freed = blocks freed. */
+pkv_status pkv_radix_evict(pkv_radix_index* index, int32_t num_blocks, int32_t* freed);
+
+pkv_status pkv_radix_stats(const pkv_radix_index* index, pkv_radix_stats_t* out);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* pkv_status_string(pkv_status status);

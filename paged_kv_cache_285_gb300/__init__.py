@@ -11,6 +11,9 @@ The three calls (names as in pkv.h without the ``pkv_`` prefix):
                           (GQA, split-KV, online softmax, LSE merge);
   * paged_extend_attn  -- suffix prefill over cached prefix blocks + causal
                           suffix.
+Also: paged_decode_attn_append (decode with the current token appended by the
+decode kernel) and RadixIndex (the host prefix index that hands out block
+tables and prefix lengths; host int32 arrays in, host arrays out).
 """
 from __future__ import annotations
 
@@ -22,13 +25,21 @@ import torch
 
 __all__ = ["F16", "BF16", "FP8_E4M3", "PkvError", "CacheDesc", "lib_path", "load",
            "kv_append", "paged_decode_attn", "paged_extend_attn", "decode_workspace_bytes",
-           "extend_workspace_bytes", "get_device_error", "status_string", "version"]
+           "extend_workspace_bytes", "get_device_error", "status_string", "version",
+           "paged_decode_attn_append", "RadixIndex", "NO_SPACE"]
 
 F16, BF16, FP8_E4M3 = 0, 1, 2
+NO_SPACE = 5  # PKV_ERR_NO_SPACE
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libpkv.so")
 _lib = None
 _lock = threading.Lock()
+
+
+class RadixStats(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int32), ("free_blocks", ctypes.c_int32),
+                ("tree_blocks", ctypes.c_int32), ("caller_blocks", ctypes.c_int32),
+                ("nodes", ctypes.c_int32), ("evictable_leaves", ctypes.c_int32)]
 
 
 class PkvError(RuntimeError):
@@ -81,6 +92,25 @@ def load():
         lib.pkv_get_device_error.restype = ctypes.c_int
         lib.pkv_version.argtypes = []
         lib.pkv_version.restype = I32
+        VP = ctypes.c_void_p
+        lib.pkv_radix_create.argtypes = [I32, I32, ctypes.POINTER(VP)]
+        lib.pkv_radix_create.restype = ctypes.c_int
+        lib.pkv_radix_destroy.argtypes = [VP]
+        lib.pkv_radix_destroy.restype = None
+        lib.pkv_radix_match.argtypes = [VP, P, I32, P, I32, ctypes.POINTER(I32)]
+        lib.pkv_radix_match.restype = ctypes.c_int
+        lib.pkv_radix_release.argtypes = [VP, P, I32]
+        lib.pkv_radix_release.restype = ctypes.c_int
+        lib.pkv_radix_alloc.argtypes = [VP, I32, P]
+        lib.pkv_radix_alloc.restype = ctypes.c_int
+        lib.pkv_radix_free.argtypes = [VP, P, I32]
+        lib.pkv_radix_free.restype = ctypes.c_int
+        lib.pkv_radix_insert.argtypes = [VP, P, I32, P, P, ctypes.POINTER(I32)]
+        lib.pkv_radix_insert.restype = ctypes.c_int
+        lib.pkv_radix_evict.argtypes = [VP, I32, ctypes.POINTER(I32)]
+        lib.pkv_radix_evict.restype = ctypes.c_int
+        lib.pkv_radix_stats.argtypes = [VP, ctypes.POINTER(RadixStats)]
+        lib.pkv_radix_stats.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -218,3 +248,83 @@ def get_device_error(clear=True, stream=None) -> int:
     _check(lib.pkv_get_device_error(ctypes.byref(w), int(bool(clear)), _stream(stream)),
            "pkv_get_device_error")
     return int(w.value)
+
+
+def _host_i32(a):
+    """Contiguous host int32 array and its address (numpy or a CPU tensor)."""
+    import numpy as np
+    if isinstance(a, torch.Tensor):
+        a = a.detach().to("cpu").numpy()
+    arr = np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+    return arr, (arr.ctypes.data if arr.size else None)
+
+
+class RadixIndex:
+    """pkv_radix_*: host prefix index over the block ids [0, num_blocks) of one pool.
+    Token and block lists are host int32 arrays; results are numpy int32 arrays."""
+
+    def __init__(self, block_size: int, num_blocks: int):
+        self._lib = load()
+        h = ctypes.c_void_p()
+        _check(self._lib.pkv_radix_create(int(block_size), int(num_blocks), ctypes.byref(h)),
+               "pkv_radix_create")
+        self._h = h
+        self.block_size = int(block_size)
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self._lib.pkv_radix_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def match(self, tokens):
+        """(matched_tokens, blocks): the locked longest cached whole-block prefix."""
+        import numpy as np
+        t, tp = _host_i32(tokens)
+        cap = t.size // self.block_size
+        out = np.zeros(max(cap, 1), dtype=np.int32)
+        m = ctypes.c_int32(0)
+        _check(self._lib.pkv_radix_match(self._h, tp, int(t.size), out.ctypes.data, cap, ctypes.byref(m)),
+               "pkv_radix_match")
+        return int(m.value), out[: m.value // self.block_size].copy()
+
+    def release(self, tokens, matched_tokens: int):
+        t, tp = _host_i32(tokens)
+        _check(self._lib.pkv_radix_release(self._h, tp, int(matched_tokens)), "pkv_radix_release")
+
+    def alloc(self, count: int):
+        import numpy as np
+        out = np.zeros(max(int(count), 1), dtype=np.int32)
+        _check(self._lib.pkv_radix_alloc(self._h, int(count), out.ctypes.data), "pkv_radix_alloc")
+        return out[: int(count)].copy()
+
+    def free(self, blocks):
+        b, bp = _host_i32(blocks)
+        _check(self._lib.pkv_radix_free(self._h, bp, int(b.size)), "pkv_radix_free")
+
+    def insert(self, tokens, blocks):
+        """Adopt the full blocks of a request; returns the caller blocks that were freed
+        because the tree already held the same tokens."""
+        import numpy as np
+        t, tp = _host_i32(tokens)
+        b, bp = _host_i32(blocks)
+        rel = np.zeros(max(t.size // self.block_size, 1), dtype=np.int32)
+        n = ctypes.c_int32(0)
+        _check(self._lib.pkv_radix_insert(self._h, tp, int(t.size), bp, rel.ctypes.data, ctypes.byref(n)),
+               "pkv_radix_insert")
+        return rel[: n.value].copy()
+
+    def evict(self, num_blocks: int) -> int:
+        f = ctypes.c_int32(0)
+        _check(self._lib.pkv_radix_evict(self._h, int(num_blocks), ctypes.byref(f)), "pkv_radix_evict")
+        return int(f.value)
+
+    def stats(self) -> dict:
+        st = RadixStats()
+        _check(self._lib.pkv_radix_stats(self._h, ctypes.byref(st)), "pkv_radix_stats")
+        return {k: int(getattr(st, k)) for k, _ in RadixStats._fields_}

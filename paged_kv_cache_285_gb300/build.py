@@ -1,6 +1,6 @@
 """Build libpkv.so in-tree with nvcc for sm_103a.
 
-Each .cu under csrc/ is compiled in parallel to an object under _build/, then
+Each .cu (and host-only .cpp) under csrc/ is compiled in parallel to an object under _build/, then
 linked (static CUDA runtime) into paged_kv_cache_285_gb300/libpkv.so.
 """
 from __future__ import annotations
@@ -31,7 +31,8 @@ def nvcc() -> str:
 
 
 def _sources():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    # CUDA translation units and host-only C++ (compiled by nvcc's host compiler)
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def _headers():
@@ -53,7 +54,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     jobs = []
     objs = []
     for src in _sources():
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(BUILD, os.path.splitext(os.path.basename(src))[0] + ".o")
         objs.append(obj)
         if force or _stale(obj, [src] + headers):
             jobs.append([cc, *ARCH, *FLAGS, *extra_flags, "-c", src, "-o", obj])
