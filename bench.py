@@ -328,6 +328,8 @@ def run_decode_bench(args, world, rank, local):
     res["e2e"] = e2e_decode(case, pkv, max_len, ws, out, stream, K, world)
     if args.extend and rank == 0 and world == 1:
         res["extend"] = run_extend_bench(args, dev, bf16, bf16_sus, peak_src)
+    if rank == 0 and world == 1:
+        res["prefix_index"] = run_prefix_index_bench()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline_decode(case, budget_s=args.cpu_seconds)
     return res
@@ -435,6 +437,45 @@ def run_extend_bench(args, dev, bf16, bf16_sus, peak_src):
                              ["paged_kv_cache_285_gb300/csrc/extend.cu",
                               "paged_kv_cache_285_gb300/csrc/ptx.cuh",
                               "paged_kv_cache_285_gb300/csrc/tcgen05.cuh"])}}
+
+
+def run_prefix_index_bench(n_requests=20000, seed=0):
+    """The host prefix index (RadixIndex) on a chat-like trace: 64 system prompts
+    of 1,000 tokens, a question of 10..200 tokens per request, 16-token blocks, a
+    pool of 8,192 blocks so that eviction runs; every request does match, alloc,
+    insert, release and frees its partial tail, through the public binding."""
+    import numpy as np
+    import paged_kv_cache_285_gb300 as pkv
+    rng = np.random.default_rng(seed)
+    bs, pool = 16, 8192
+    prompts = [rng.integers(0, 32000, 1000).astype(np.int32) for _ in range(64)]
+    reqs = [np.concatenate([prompts[rng.integers(0, 64)],
+                            rng.integers(0, 32000, rng.integers(10, 201)).astype(np.int32)])
+            for _ in range(n_requests)]
+    x = pkv.RadixIndex(bs, pool)
+    hit = total = refused = 0
+    t0 = time.perf_counter()
+    for t in reqs:
+        m, blk = x.match(t)
+        try:
+            new = x.alloc(-(-len(t) // bs) - len(blk))
+        except pkv.PkvError:
+            x.release(t, m)
+            refused += 1
+            continue
+        table = np.concatenate([blk, new])
+        x.insert(t, table)
+        x.release(t, m)
+        if len(t) % bs:
+            x.free(table[-1:])
+        hit += m
+        total += len(t)
+    dt = time.perf_counter() - t0
+    return {"workload": "64 x 1,000-token system prompts + 10..200-token questions, bs 16, "
+                        "8,192-block pool", "requests": n_requests,
+            "requests_per_s": round(n_requests / dt, 1),
+            "cached_token_frac": round(hit / max(total, 1), 4), "refused": refused,
+            "note": "host C++ index driven through the Python binding (5 calls per request)"}
 
 
 def cpu_baseline_decode(case, budget_s=10.0):
