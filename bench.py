@@ -330,6 +330,7 @@ def run_decode_bench(args, world, rank, local):
         res["extend"] = run_extend_bench(args, dev, bf16, bf16_sus, peak_src)
     if rank == 0 and world == 1:
         res["prefix_index"] = run_prefix_index_bench()
+        res["chain_hash"] = run_chain_hash_bench(dev, hbm, peak_src)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline_decode(case, budget_s=args.cpu_seconds)
     return res
@@ -476,6 +477,41 @@ def run_prefix_index_bench(n_requests=20000, seed=0):
             "requests_per_s": round(n_requests / dt, 1),
             "cached_token_frac": round(hit / max(total, 1), 4), "refused": refused,
             "note": "host C++ index driven through the Python binding (5 calls per request)"}
+
+
+def run_chain_hash_bench(dev, hbm, peak_src, n=20, seed=0):
+    """pkv_chain_hash over a prefill batch: 1,024 requests of 4,096 token ids,
+    16-token blocks, a salt per request; algorithmic bytes = the token ids read
+    (4 B each) + the hashes written (8 B per block) + offsets and salts."""
+    import paged_kv_cache_285_gb300 as pkv
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    B, L, bs = 1024, 4096, 16
+    toks = torch.randint(0, 128256, (B * L,), generator=g, dtype=torch.int32).to(dev)
+    indptr = (torch.arange(B + 1, dtype=torch.int32) * L).to(dev)
+    salts = torch.randint(-2**62, 2**62, (B,), generator=g, dtype=torch.int64).to(dev)
+    hashes = torch.empty((B, L // bs), dtype=torch.int64, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        pkv.chain_hash(toks, indptr, bs, hashes, salts=salts)
+    flush = L2Flush(dev)
+    tot = 0.0
+    for _ in range(n):
+        flush()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        pkv.chain_hash(toks, indptr, bs, hashes, salts=salts)
+        e1.record(stream)
+        e1.synchronize()
+        tot += e0.elapsed_time(e1)
+    ms = tot / n
+    nbytes = 4 * B * L + 8 * B * (L // bs) + 4 * (B + 1) + 8 * B
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": "1,024 requests x 4,096 token ids, 16-token blocks, salted",
+            "ms_per_call": round(ms, 5), "tokens_per_s": round(B * L / (ms * 1e-3), 1),
+            "achieved_gbs": round(gbs, 1), "hbm_peak_gbs": hbm, "frac_of_hbm": round(gbs / hbm, 4),
+            "peak_source": f"{peak_src} (hbm_gbs)", "algorithmic_bytes": nbytes,
+            "l2": "256 MiB buffer written then read between calls"}
 
 
 def cpu_baseline_decode(case, budget_s=10.0):

@@ -65,6 +65,7 @@ typedef enum { PKV_F16 = 0, PKV_BF16 = 1, PKV_FP8_E4M3 = 2 } pkv_dtype;
 #define PKV_DEVERR_BAD_SLOT 2      /* slot_mapping entry outside the pool */
 #define PKV_DEVERR_BAD_LENGTH 3    /* seq_len / prefix+suffix beyond the table or hint */
 #define PKV_DEVERR_TIMEOUT 4       /* a bounded wait on an asynchronous copy ran out */
+#define PKV_DEVERR_TOO_MANY_BLOCKS 5 /* chain hash: a request has more full blocks than max_blocks */
 
 /* Description of one layer's KV pool.
  *   head_dim in {64, 128}; block_size in {16, 32};
@@ -342,6 +343,36 @@ pkv_status pkv_radix_insert(pkv_radix_index* index, const int32_t* tokens, int32
 pkv_status pkv_radix_evict(pkv_radix_index* index, int32_t num_blocks, int32_t* freed);
 
 pkv_status pkv_radix_stats(const pkv_radix_index* index, pkv_radix_stats_t* out);
+
+/* ---------------------------------------------------------------------------
+ * pkv_chain_hash -- chain hashes of full KV blocks (block identifiers).
+ *
+ * "PagedAttention과 RadixAttention으로 LLM KV 캐시 최적화", section 05: a
+ * block's hash combines its parent block's hash with the block's token ids
+ * (and optional extra data), so equal token prefixes give equal chains and a
+ * request's first miss marks where new blocks begin; section 06: a per-tenant
+ * salt in the identifier keeps tenants apart.  The pages fix no hash; this one
+ * (G = 0x9E3779B97F4A7C15, mix = the SplitMix64 finalizer):
+ *   content(block) = c after c = mix(c + G + (uint32)token) over the block's
+ *                    tokens, from c = 0;
+ *   h[0] = mix((salt ^ content(block 0)) + G),
+ *   h[i] = mix((h[i-1] ^ content(block i)) + G).
+ * Extra data (a LoRA or multimodal id) belongs in the salt.
+ *
+ * tokens:        int32 [token_indptr[batch]], device; request b owns
+ *                tokens[token_indptr[b] .. token_indptr[b+1]).
+ * token_indptr:  int32 [batch+1], device, non-decreasing.
+ * salts:         uint64 [batch], device, or NULL (salt 0).
+ * hashes:        uint64 [batch][max_blocks], device: request b's full blocks
+ *                (len / block_size of them) get hashes[b][0 ..); a partial
+ *                last block gets none; other entries are left untouched.  A
+ *                request with more full blocks than max_blocks gets the first
+ *                max_blocks and PKV_DEVERR_TOO_MANY_BLOCKS in the error word.
+ * block_size:    1 .. 4096 tokens.
+ * ------------------------------------------------------------------------- */
+pkv_status pkv_chain_hash(const int32_t* tokens, const int32_t* token_indptr, int32_t batch,
+                          int32_t block_size, const uint64_t* salts, uint64_t* hashes,
+                          int32_t max_blocks, cudaStream_t stream);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* pkv_status_string(pkv_status status);

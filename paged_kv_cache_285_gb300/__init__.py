@@ -12,8 +12,9 @@ The three calls (names as in pkv.h without the ``pkv_`` prefix):
   * paged_extend_attn  -- suffix prefill over cached prefix blocks + causal
                           suffix.
 Also: paged_decode_attn_append (decode with the current token appended by the
-decode kernel) and RadixIndex (the host prefix index that hands out block
-tables and prefix lengths; host int32 arrays in, host arrays out).
+decode kernel), RadixIndex (the host prefix index that hands out block
+tables and prefix lengths; host int32 arrays in, host arrays out) and
+chain_hash (salted chain hashes of full blocks, as block identifiers).
 """
 from __future__ import annotations
 
@@ -26,7 +27,7 @@ import torch
 __all__ = ["F16", "BF16", "FP8_E4M3", "PkvError", "CacheDesc", "lib_path", "load",
            "kv_append", "paged_decode_attn", "paged_extend_attn", "decode_workspace_bytes",
            "extend_workspace_bytes", "get_device_error", "status_string", "version",
-           "paged_decode_attn_append", "RadixIndex", "NO_SPACE"]
+           "paged_decode_attn_append", "RadixIndex", "NO_SPACE", "chain_hash"]
 
 F16, BF16, FP8_E4M3 = 0, 1, 2
 NO_SPACE = 5  # PKV_ERR_NO_SPACE
@@ -92,6 +93,8 @@ def load():
         lib.pkv_get_device_error.restype = ctypes.c_int
         lib.pkv_version.argtypes = []
         lib.pkv_version.restype = I32
+        lib.pkv_chain_hash.argtypes = [P, P, I32, I32, P, P, I32, P]
+        lib.pkv_chain_hash.restype = ctypes.c_int
         VP = ctypes.c_void_p
         lib.pkv_radix_create.argtypes = [I32, I32, ctypes.POINTER(VP)]
         lib.pkv_radix_create.restype = ctypes.c_int
@@ -239,6 +242,21 @@ def paged_extend_attn(k_cache, v_cache, q, out, q_indptr, prefix_lens, block_tab
                                    int(max_total_len), _ptr(lse_out), _ptr(workspace), ws_bytes,
                                    _stream(stream))
     _check(st, "pkv_paged_extend_attn")
+
+
+def chain_hash(tokens, token_indptr, block_size, hashes, salts=None, stream=None):
+    """pkv_chain_hash: tokens int32 [T], token_indptr int32 [B+1], hashes int64 [B, max_blocks]
+    (uint64 bits), salts int64 [B] (uint64 bits) or None; all device tensors."""
+    lib = load()
+    b = int(token_indptr.shape[0]) - 1
+    if tokens.dtype != torch.int32 or token_indptr.dtype != torch.int32 or token_indptr.dim() != 1:
+        raise ValueError("tokens and token_indptr must be int32 (token_indptr 1-D)")
+    if hashes.dtype != torch.int64 or hashes.dim() != 2 or hashes.shape[0] != b:
+        raise ValueError("hashes must be int64 [batch, max_blocks]")
+    if salts is not None and (salts.dtype != torch.int64 or tuple(salts.shape) != (b,)):
+        raise ValueError("salts must be int64 [batch]")
+    _check(lib.pkv_chain_hash(_ptr(tokens), _ptr(token_indptr), b, int(block_size), _ptr(salts),
+                              _ptr(hashes), int(hashes.shape[1]), _stream(stream)), "pkv_chain_hash")
 
 
 def get_device_error(clear=True, stream=None) -> int:

@@ -186,6 +186,29 @@ DecodePlan plan_decode(const pkv_cache_desc* d, int batch, int hq, int max_seq_l
 
 extern "C" {
 
+pkv_status pkv_chain_hash(const int32_t* tokens, const int32_t* token_indptr, int32_t batch,
+                          int32_t block_size, const uint64_t* salts, uint64_t* hashes,
+                          int32_t max_blocks, cudaStream_t stream) {
+  if (batch < 0 || block_size <= 0 || block_size > 4096 || max_blocks < 0) return PKV_ERR_INVALID_ARG;
+  if (batch == 0 || max_blocks == 0) return PKV_OK;
+  if (!tokens || !token_indptr || !hashes) return PKV_ERR_INVALID_ARG;
+  if (!aligned(hashes, 8) || (salts && !aligned(salts, 8)) || !aligned(tokens, 4))
+    return PKV_ERR_INVALID_ARG;
+  cudaError_t e;
+  DeviceState* ds = device_state(&e);
+  if (!ds) return PKV_ERR_CUDA;
+  ChainHashParams p;
+  p.tokens = tokens;
+  p.token_indptr = token_indptr;
+  p.salts = salts;
+  p.hashes = hashes;
+  p.err = ds->err;
+  p.block_size = block_size;
+  p.max_blocks = max_blocks;
+  e = launch_chain_hash(p, batch, stream);
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
 const char* pkv_status_string(pkv_status s) {
   switch (s) {
     case PKV_OK: return "PKV_OK";
@@ -318,13 +341,15 @@ static pkv_status decode_common(const pkv_cache_desc* desc, const void* k_cache,
   const double kscale = desc->cache_dtype == PKV_FP8_E4M3 ? (double)desc->k_scale : 1.0;
   p.scale_log2 = (float)((double)sm_scale * kscale * 1.4426950408889634);
   p.out_scale = desc->cache_dtype == PKV_FP8_E4M3 ? desc->v_scale : 1.0f;
-  p.k_new = k_new;
-  p.v_new = v_new;
-  p.k_cache = const_cast<void*>(k_cache);
-  p.v_cache = const_cast<void*>(v_cache);
-  p.k_scale = desc->k_scale;
-  p.v_scale = desc->v_scale;
-  e = launch_decode(kmap, vmap, p, desc->head_dim, (int)desc->cache_dtype, (int)act_dtype, stream);
+  DecodeAppendParams ap;
+  ap.k_new = k_new;
+  ap.v_new = v_new;
+  ap.k_cache = const_cast<void*>(k_cache);
+  ap.v_cache = const_cast<void*>(v_cache);
+  ap.k_scale = desc->k_scale;
+  ap.v_scale = desc->v_scale;
+  e = launch_decode(kmap, vmap, p, ap, desc->head_dim, (int)desc->cache_dtype, (int)act_dtype,
+                    stream);
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

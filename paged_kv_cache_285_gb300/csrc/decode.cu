@@ -110,7 +110,7 @@ __device__ __forceinline__ float to_f32_bits(uint32_t bits16) {
 template <int HD, int CT, int AT, int NW, int NS>
 __global__ void __launch_bounds__(NW * 32)
 decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-              const DecodeParams p) {
+              const DecodeParams p, const DecodeAppendParams ap) {
   using C = DecodeCfg<HD, CT, NW, NS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -145,7 +145,7 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
   const int nsplit_b = (n + p.chunk - 1) / p.chunk;
   const int cnt = warp < nsub ? (nsub - warp + NW - 1) / NW : 0;
 
-  if (p.k_new != nullptr && split == nsplit_b - 1) {
+  if (ap.k_new != nullptr && split == nsplit_b - 1) {
     // Fused append: this CTA covers position n-1, the current token; its K/V
     // rows of kv head g go to their slot before any tile of this CTA is
     // loaded (TMA reads the slot after the proxy fence and the barrier
@@ -163,12 +163,12 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       const int64_t src = ((int64_t)b * p.num_kv_heads + g) * HD + e;
       const int64_t dst = (((int64_t)blk * p.num_kv_heads + g) * bs + (pos & (bs - 1))) * HD + e;
       const uint4 x = __ldg(reinterpret_cast<const uint4*>(
-          reinterpret_cast<const uint16_t*>(isv ? p.v_new : p.k_new) + src));
-      void* cache = isv ? p.v_cache : p.k_cache;
+          reinterpret_cast<const uint16_t*>(isv ? ap.v_new : ap.k_new) + src));
+      void* cache = isv ? ap.v_cache : ap.k_cache;
       if constexpr (CT != DT_E4M3) {
         *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(cache) + dst) = x;
       } else {
-        const float sc = isv ? p.v_scale : p.k_scale;
+        const float sc = isv ? ap.v_scale : ap.k_scale;
         const uint32_t w[4] = {x.x, x.y, x.z, x.w};
         uint32_t o[2];
 #pragma unroll
@@ -543,14 +543,15 @@ constexpr int stages_for() {
 
 template <int HD, int CT, int AT>
 cudaError_t launch_decode_t(const CUtensorMap& kmap, const CUtensorMap& vmap,
-                            const DecodeParams& p, cudaStream_t stream) {
+                            const DecodeParams& p, const DecodeAppendParams& ap,
+                            cudaStream_t stream) {
   constexpr int NS = stages_for<HD, CT>();
   using C = DecodeCfg<HD, CT, kNW, NS>;
   auto kern = decode_kernel<HD, CT, AT, kNW, NS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(p.num_splits, p.num_kv_heads, p.batch);
-  kern<<<grid, kNW * 32, C::SMEM, stream>>>(kmap, vmap, p);
+  kern<<<grid, kNW * 32, C::SMEM, stream>>>(kmap, vmap, p, ap);
   e = cudaGetLastError();
   if (e != cudaSuccess || p.num_splits <= 1) return e;
   const int64_t pairs = (int64_t)p.batch * p.num_q_heads;
@@ -573,10 +574,11 @@ size_t decode_smem_bytes(int head_dim, int cache_dt) {
 }
 
 cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
-                          int head_dim, int cache_dt, int act_dt, cudaStream_t stream) {
+                          const DecodeAppendParams& ap, int head_dim, int cache_dt, int act_dt,
+                          cudaStream_t stream) {
 #define PKV_DEC(HD, CT, AT)                                              \
   if (head_dim == HD && cache_dt == CT && act_dt == AT)                  \
-    return launch_decode_t<HD, CT, AT>(kmap, vmap, p, stream);
+    return launch_decode_t<HD, CT, AT>(kmap, vmap, p, ap, stream);
   PKV_DEC(64, DT_F16, DT_F16)
   PKV_DEC(64, DT_BF16, DT_BF16)
   PKV_DEC(64, DT_E4M3, DT_F16)

@@ -33,8 +33,13 @@ struct DecodeParams {
   int num_splits;     // S of the plan
   float scale_log2;   // sm_scale * log2(e) (* k_scale for fp8)
   float out_scale;    // v_scale for fp8, else 1
-  // fused append (nullable k_new): the current token's K/V rows [B][Hkv][D]
-  // in the act dtype, written to position seq_len-1 before it is read
+};
+
+// Fused append of a decode call (k_new null: none): the current token's K/V
+// rows [B][Hkv][D] in the act dtype, written to position seq_len-1 before it
+// is read.  A kernel argument of its own: widening DecodeParams changes how
+// the decode loop is register-allocated.
+struct DecodeAppendParams {
   const void* k_new;
   const void* v_new;
   void* k_cache;
@@ -117,10 +122,22 @@ struct ExtendParams {
 
 // Each returns a cudaError_t from the launch.
 cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap,
-                          const DecodeParams& p, int head_dim, int cache_dt, int act_dt,
-                          cudaStream_t stream);
+                          const DecodeParams& p, const DecodeAppendParams& ap, int head_dim,
+                          int cache_dt, int act_dt, cudaStream_t stream);
 size_t decode_smem_bytes(int head_dim, int cache_dt);
 cudaError_t launch_append(const AppendParams& p, int cache_dt, int act_dt, cudaStream_t stream);
+// Chain hashes of the full blocks of each request's token ids.
+struct ChainHashParams {
+  const int32_t* tokens;        // [token_indptr[batch]]
+  const int32_t* token_indptr;  // [batch + 1]
+  const uint64_t* salts;        // [batch] or null (salt 0)
+  uint64_t* hashes;             // [batch][max_blocks]
+  int32_t* err;                 // device error word
+  int block_size;
+  int max_blocks;
+};
+cudaError_t launch_chain_hash(const ChainHashParams& p, int batch, cudaStream_t stream);
+
 // fp8 pages read by an extend call -> 16-bit shadow pages (same layout).
 struct DequantParams {
   const uint8_t* k8;          // fp8 K pool
