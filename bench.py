@@ -311,7 +311,8 @@ def run_decode_bench(args, world, rank, local):
     }
     traffic = profiled_traffic("decode_kernel_llama3_8b_layer.md",
                                ["paged_kv_cache_285_gb300/csrc/decode.cu",
-                                "paged_kv_cache_285_gb300/csrc/ptx.cuh"]) \
+                                "paged_kv_cache_285_gb300/csrc/ptx.cuh",
+                                "paged_kv_cache_285_gb300/csrc/internal.h"]) \
         if args.workload == "llama3_8b_layer" else None
     res["roofline"] = {"kernel": "paged_decode_attn (decode_kernel + merge_kernel)",
                        "bound": "hbm", "achieved": round(dec_gbs, 1), "peak": hbm,
@@ -437,7 +438,8 @@ def run_extend_bench(args, dev, bf16, bf16_sus, peak_src):
                              "extend_kernel_shared_prefix_extend.md",
                              ["paged_kv_cache_285_gb300/csrc/extend.cu",
                               "paged_kv_cache_285_gb300/csrc/ptx.cuh",
-                              "paged_kv_cache_285_gb300/csrc/tcgen05.cuh"])}}
+                              "paged_kv_cache_285_gb300/csrc/tcgen05.cuh",
+                              "paged_kv_cache_285_gb300/csrc/internal.h"])}}
 
 
 def run_prefix_index_bench(n_requests=20000, seed=0):
@@ -511,6 +513,7 @@ def run_chain_hash_bench(dev, hbm, peak_src, n=20, seed=0):
             "ms_per_call": round(ms, 5), "tokens_per_s": round(B * L / (ms * 1e-3), 1),
             "achieved_gbs": round(gbs, 1), "hbm_peak_gbs": hbm, "frac_of_hbm": round(gbs / hbm, 4),
             "peak_source": f"{peak_src} (hbm_gbs)", "algorithmic_bytes": nbytes,
+            "bound": "latency: each request's chain is %d dependent hash steps" % (L // bs),
             "l2": "256 MiB buffer written then read between calls"}
 
 

@@ -13,7 +13,8 @@
 //                    unsigned 32-bit value), c starting at 0, G = 0x9E3779B97F4A7C15
 //   h_i = mix((h_{i-1} ^ content(block i)) + G), h_{-1} = the request's salt
 // (extra data goes into the salt).  Two levels so that the block contents
-// hash in parallel and only the cheap chain step is sequential.
+// hash in parallel and only the cheap chain step is sequential: one pass
+// hashes every block's contents at once, a second runs each request's chain.
 #include "internal.h"
 
 namespace pkv {
@@ -21,16 +22,8 @@ namespace pkv {
 namespace {
 
 constexpr uint64_t kGolden = 0x9E3779B97F4A7C15ull;
-constexpr int kThreads = 64;         // warp 0: chain; warp 1: block contents
-constexpr int kRoundBlocks = 32;     // blocks per round, one per content lane
-constexpr int kRoundTokens = 1024;   // tokens staged per round (fewer blocks if larger)
-constexpr int kStages = 3;           // token buffers: copy r+2, hash r+1, (free)
-
-// Blocks per round: one per content lane, at most kRoundTokens tokens, at least 1.
-__host__ __device__ __forceinline__ int round_blocks(int block_size) {
-  const int c = kRoundTokens / block_size;
-  return c < 1 ? 1 : (c > kRoundBlocks ? kRoundBlocks : c);
-}
+constexpr int kContentThreads = 128;  // blocks per CTA of the content pass
+constexpr int kMaxChunkCtas = 16;     // content-pass CTAs per request, at most
 
 __device__ __forceinline__ uint64_t mix64(uint64_t z) {
   z ^= z >> 30;
@@ -41,105 +34,149 @@ __device__ __forceinline__ uint64_t mix64(uint64_t z) {
   return z;
 }
 
-__device__ __forceinline__ void cp_async4(void* dst_smem, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+// Full blocks of request b (at most max_blocks; more sets the error word when
+// `report`).
+__device__ __forceinline__ int64_t full_blocks(const ChainHashParams& p, int b, int64_t* base,
+                                               bool report) {
+  *base = p.token_indptr[b];
+  const int64_t len = (int64_t)p.token_indptr[b + 1] - *base;
+  int64_t n = len > 0 ? len / p.block_size : 0;
+  if (n > p.max_blocks) {
+    if (report && p.err) atomicCAS(p.err, 0, 5);
+    n = p.max_blocks;
+  }
+  return n;
+}
+
+// Pass 1, all blocks in parallel: CTA (b, y) folds the tokens of blocks
+// y * kContentThreads + threadIdx.x, then every gridDim.y * kContentThreads
+// further, of request b into their content hashes, stored where the blocks'
+// chain hashes go.
+__global__ void __launch_bounds__(kContentThreads) block_content_kernel(const ChainHashParams p) {
+  const int b = blockIdx.x;
+  int64_t base;
+  const int64_t nblk = full_blocks(p, b, &base, blockIdx.y == 0 && threadIdx.x == 0);
+  const int bs = p.block_size;
+  for (int64_t j = (int64_t)blockIdx.y * kContentThreads + threadIdx.x; j < nblk;
+       j += (int64_t)gridDim.y * kContentThreads) {
+    const int32_t* t = p.tokens + base + j * bs;
+    uint64_t c = 0;
+    if ((bs & 3) == 0 && (reinterpret_cast<uintptr_t>(t) & 15) == 0) {
+      const int4* t4 = reinterpret_cast<const int4*>(t);
+      for (int k = 0; k < bs / 4; ++k) {
+        const int4 v = __ldg(t4 + k);
+        c = mix64(c + kGolden + (uint64_t)(uint32_t)v.x);
+        c = mix64(c + kGolden + (uint64_t)(uint32_t)v.y);
+        c = mix64(c + kGolden + (uint64_t)(uint32_t)v.z);
+        c = mix64(c + kGolden + (uint64_t)(uint32_t)v.w);
+      }
+    } else {
+      for (int k = 0; k < bs; ++k) c = mix64(c + kGolden + (uint64_t)(uint32_t)__ldg(t + k));
+    }
+    p.hashes[(int64_t)b * p.max_blocks + j] = c;
+  }
+}
+
+__device__ __forceinline__ void cp_async8(void* dst_smem, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(
                    static_cast<uint32_t>(__cvta_generic_to_shared(dst_smem))),
                "l"(src)
                : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void cp_async_wait_1() {
-  asm volatile("cp.async.wait_group 1;" ::: "memory");
-}
 
-// One CTA of two warps per request, in rounds of round_blocks() blocks.  In
-// round r the whole CTA starts the asynchronous copy of round r+2's tokens
-// into shared memory, warp 1 hashes the contents of round r+1 (one block per
-// lane), and lane 0 of warp 0 runs the chain over round r's contents; warp 0
-// then stores round r's hashes with coalesced writes.  Only the chain is
-// sequential, so a request takes about (its blocks) x (one chain step).
-__global__ void __launch_bounds__(kThreads) chain_hash_kernel(const ChainHashParams p) {
-  extern __shared__ int32_t tok_s[];  // kStages x round_blocks x block_size tokens
-  __shared__ uint64_t content_s[2][kRoundBlocks];
-  __shared__ uint64_t chain_s[kRoundBlocks];
-  const int b = blockIdx.x;
+// Pass 2, one lane per request: the chain over the contents of pass 1, in
+// place.  Only this step is sequential; one warp instruction advances 32
+// requests' chains.  The contents go through shared memory in tiles of 32
+// requests x 32 blocks, four buffers deep: while warp 0 chains tile t (lane
+// l along row l), warp 1 writes tile t-1 back and starts copying tile t+2
+// in, both row-wise (coalesced), so a copy has a whole tile's time to land.  Rows are padded to 33 entries, so lane l's column
+// reads hit distinct banks.
+constexpr int kTile = 32;
+constexpr int kBufs = 4;
+__global__ void __launch_bounds__(64) chain_kernel(const ChainHashParams p, int batch) {
+  __shared__ uint64_t tile[kBufs][kTile][kTile + 1];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bs = p.block_size;
-  const int cb = round_blocks(bs);
-  const int stage_tok = cb * bs;
-  const int64_t base = p.token_indptr[b];
-  const int64_t len = (int64_t)p.token_indptr[b + 1] - base;
-  int64_t nblk = len > 0 ? len / bs : 0;
-  if (nblk > p.max_blocks) {
-    if (threadIdx.x == 0 && p.err) atomicCAS(p.err, 0, 5);
-    nblk = p.max_blocks;
-  }
-  const int64_t nrounds = (nblk + cb - 1) / cb;
-  auto nb_of = [&](int64_t r) -> int {
-    const int64_t left = nblk - r * cb;
-    return (int)(left < cb ? left : cb);
-  };
-  // Start the copy of round r's tokens (an empty group past the end keeps the
-  // group count per thread uniform).
-  auto copy_round = [&](int64_t r) {
-    if (r < nrounds) {
-      const int ntok = nb_of(r) * bs;
-      const int32_t* src = p.tokens + base + r * (int64_t)stage_tok;
-      int32_t* dst = tok_s + (int)(r % kStages) * stage_tok;
-      for (int i = threadIdx.x; i < ntok; i += kThreads) cp_async4(dst + i, src + i);
+  const int b0 = blockIdx.x * kTile;
+  const int nrows = batch - b0 < kTile ? batch - b0 : kTile;
+  const int b = b0 + lane;
+  int64_t base;
+  const int nblk = lane < nrows ? (int)full_blocks(p, b, &base, false) : 0;  // <= max_blocks
+  const int ntile = (__reduce_max_sync(0xffffffffu, nblk) + kTile - 1) / kTile;
+  int nr[kTile];  // every row's length, in registers (rows past the batch: 0)
+#pragma unroll
+  for (int r = 0; r < kTile; ++r) nr[r] = __shfl_sync(0xffffffffu, nblk, r);
+  uint64_t* const rows = p.hashes + (int64_t)b0 * p.max_blocks;
+  // warp 1: start copying tile t in (row r, columns lane); one group per
+  // call, empty past the end, so that "all but the newest group" is tile t-1
+  auto fetch = [&](int t) {
+    if (t < ntile) {
+      const int j = t * kTile + lane;
+#pragma unroll
+      for (int r = 0; r < kTile; ++r)
+        if (j < nr[r]) cp_async8(&tile[t % kBufs][r][lane], rows + (int64_t)r * p.max_blocks + j);
     }
-    cp_async_commit();
+    asm volatile("cp.async.commit_group;" ::: "memory");
   };
-  auto hash_round = [&](int64_t r) {  // warp 1
-    if (r < nrounds && lane < nb_of(r)) {
-      const int32_t* t = tok_s + (int)(r % kStages) * stage_tok + lane * bs;
-      uint64_t c = 0;
-      for (int j = 0; j < bs; ++j) c = mix64(c + kGolden + (uint64_t)(uint32_t)t[j]);
-      content_s[r & 1][lane] = c;
-    }
+  auto landed_but_newest = [&]() {
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
+    __syncwarp();
+  };
+  // warp 1: write tile t back
+  auto store = [&](int t) {
+    const int j = t * kTile + lane;
+#pragma unroll
+    for (int r = 0; r < kTile; ++r)
+      if (j < nr[r]) rows[(int64_t)r * p.max_blocks + j] = tile[t % kBufs][r][lane];
   };
 
-  copy_round(0);
-  copy_round(1);
-  cp_async_wait_1();
+  if (warp == 1) {
+    fetch(0);
+    fetch(1);
+    landed_but_newest();  // tile 0
+  }
   __syncthreads();
-  if (warp == 1) hash_round(0);
-  uint64_t h = p.salts ? p.salts[b] : 0ull;  // lane 0 of warp 0 carries the chain
-  for (int64_t r = 0; r < nrounds; ++r) {
-    copy_round(r + 2);
-    cp_async_wait_1();  // this thread's copies of round r+1 have landed
-    __syncthreads();    // ... and everyone's; round r's contents are complete
-    if (warp == 1) {
-      hash_round(r + 1);
-    } else {
-      const int nb = nb_of(r);
-      if (lane == 0) {
-        const uint64_t* cs = content_s[r & 1];
-        for (int i = 0; i < nb; ++i) {
-          h = mix64((h ^ cs[i]) + kGolden);
-          chain_s[i] = h;
+  uint64_t h = (lane < nrows && p.salts) ? p.salts[b] : 0ull;  // warp 0's chains
+  for (int t = 0; t < ntile; ++t) {
+    if (warp == 0) {
+      uint64_t* row = tile[t % kBufs][lane];
+      int kend = nblk - t * kTile;  // this lane's blocks in tile t
+      kend = kend < 0 ? 0 : (kend > kTile ? kTile : kend);
+      int k0 = 0;
+      for (; k0 + 8 <= kend; k0 += 8) {  // 8 contents to registers, then 8 steps
+        uint64_t c[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) c[k] = row[k0 + k];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          h = mix64((h ^ c[k]) + kGolden);
+          row[k0 + k] = h;
         }
       }
-      __syncwarp();
-      if (lane < nb) p.hashes[(int64_t)b * p.max_blocks + r * cb + lane] = chain_s[lane];
-      __syncwarp();
+      for (; k0 < kend; ++k0) {
+        h = mix64((h ^ row[k0]) + kGolden);
+        row[k0] = h;
+      }
+    } else {
+      if (t >= 1) store(t - 1);
+      fetch(t + 2);
+      landed_but_newest();  // tile t+1
     }
+    __syncthreads();  // tile t chained, tile t+1 in, tile t-1 out
   }
+  if (warp == 1 && ntile > 0) store(ntile - 1);
 }
 
 }  // namespace
 
 cudaError_t launch_chain_hash(const ChainHashParams& p, int batch, cudaStream_t stream) {
-  if (batch <= 0) return cudaSuccess;
-  const size_t smem = (size_t)kStages * round_blocks(p.block_size) * p.block_size * sizeof(int32_t);
-  if (smem > 40 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(chain_hash_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-  }
-  chain_hash_kernel<<<batch, kThreads, smem, stream>>>(p);
+  if (batch <= 0 || p.max_blocks <= 0) return cudaSuccess;
+  // at most kMaxChunkCtas CTAs per request; the device knows the lengths
+  const int64_t chunks = ((int64_t)p.max_blocks + kContentThreads - 1) / kContentThreads;
+  const dim3 grid1((unsigned)batch, (unsigned)(chunks < kMaxChunkCtas ? chunks : kMaxChunkCtas));
+  block_content_kernel<<<grid1, kContentThreads, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  chain_kernel<<<(unsigned)((batch + kTile - 1) / kTile), 64, 0, stream>>>(p, batch);
   return cudaGetLastError();
 }
 
