@@ -48,3 +48,10 @@ def test_block_size_one_chain_is_a_fold_over_tokens():
     for x in t:
         h = ch.mix(((h ^ ch.mix(0 + ch.G + x)) + ch.G) & ch.M64)
     assert ch.chain(t, 1)[-1] == h
+
+
+def test_token_ids_enter_as_unsigned_32_bit_values():
+    # an int32 token id is read as its unsigned 32-bit value, not sign-extended
+    assert ch.chain([-1] * 4, 4) == ch.chain([0xFFFFFFFF] * 4, 4)
+    assert ch.content([-1]) == ch.mix(ch.G + 0xFFFFFFFF)
+    assert ch.content([-1]) != ch.mix((ch.G + ch.M64) & ch.M64)
