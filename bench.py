@@ -332,6 +332,7 @@ def run_decode_bench(args, world, rank, local):
     if rank == 0 and world == 1:
         res["prefix_index"] = run_prefix_index_bench()
         res["chain_hash"] = run_chain_hash_bench(dev, hbm, peak_src)
+        res["shared_prefix_decode"] = run_shared_prefix_bench(dev, hbm, peak_src)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline_decode(case, budget_s=args.cpu_seconds)
     return res
@@ -479,6 +480,85 @@ def run_prefix_index_bench(n_requests=20000, seed=0):
             "requests_per_s": round(n_requests / dt, 1),
             "cached_token_frac": round(hit / max(total, 1), 4), "refused": refused,
             "note": "host C++ index driven through the Python binding (5 calls per request)"}
+
+
+def run_shared_prefix_bench(dev, hbm, peak_src, n=20):
+    """Decode of 256 requests sharing one 1,000-token prompt (62 shared 16-token
+    blocks + an 8-token tail in each request's own block), own tokens U[32, 256],
+    32 q / 8 kv heads, d128, bf16: plain paged_decode_attn (every request reads
+    the prefix) against paged_decode_attn_shared_prefix (the prefix once per
+    group on the tensor cores, LSE merge), both in CUDA graphs, L2 flushed."""
+    import paged_kv_cache_285_gb300 as pkv
+    from paged_kv_cache_285_gb300 import workloads as W
+    case = W.shared_prefix_decode(device="cuda")
+    b, hq, hkv, d, bs = case.q.shape[0], case.num_q_heads, case.num_kv_heads, case.head_dim, 16
+    lens = case.seq_lens.tolist()
+    max_len = max(lens)
+    prefix = 1000
+    shared = (prefix // bs) * bs
+    gi = torch.tensor([0, b], dtype=torch.int32, device=dev)
+    gp = torch.tensor([prefix], dtype=torch.int32, device=dev)
+    out_p, out_c = torch.empty_like(case.q), torch.empty_like(case.q)
+    ws_p = torch.empty(max(pkv.decode_workspace_bytes(case.k_cache, b, hq, max_len, 0), 256),
+                       dtype=torch.uint8, device=dev)
+    ws_c = torch.empty(pkv.shared_prefix_decode_workspace_bytes(case.k_cache, b, hq,
+                                                                max_len - prefix, 0),
+                       dtype=torch.uint8, device=dev)
+
+    def plain():
+        pkv.paged_decode_attn(case.k_cache, case.v_cache, case.q, out_p, case.block_tables,
+                              case.seq_lens, case.sm_scale, max_len, workspace=ws_p)
+
+    def cascade():
+        pkv.paged_decode_attn_shared_prefix(case.k_cache, case.v_cache, case.q, out_c,
+                                            case.block_tables, case.seq_lens, case.sm_scale, gi,
+                                            gp, b, max_len - prefix, workspace=ws_c)
+
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        plain()
+        cascade()
+    torch.cuda.synchronize()
+    graphs = []
+    cap = torch.cuda.Stream()
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        for fn in (plain, cascade):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
+                fn()
+            graphs.append(g)
+    stream.wait_stream(cap)
+    flush = L2Flush(dev)
+    tot = [0.0, 0.0]
+    for _ in range(n):
+        for k, g in enumerate(graphs):
+            flush()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            e1.synchronize()
+            tot[k] += e0.elapsed_time(e1)
+    ms_p, ms_c = tot[0] / n, tot[1] / n
+    kv_tok = hkv * d * 2 * 2  # K + V bytes per token (bf16)
+    qo = 2 * b * hq * d * 2
+    logical = sum(lens) * kv_tok + qo
+    unique = (shared + sum(x - shared for x in lens)) * kv_tok + qo
+    diff = (out_p.float() - out_c.float()).abs().max().item()
+    return {"workload": "256 requests sharing one 1,000-token prompt (62 shared blocks), own "
+                        "tokens U[32,256], 32q/8kv, d128, bf16, bs16",
+            "plain_ms": round(ms_p, 5), "shared_prefix_ms": round(ms_c, 5),
+            "speedup": round(ms_p / ms_c, 3),
+            "logical_bytes": logical, "unique_bytes": unique,
+            "plain_gbs_logical": round(logical / (ms_p * 1e-3) / 1e9, 1),
+            "shared_prefix_gbs_logical": round(logical / (ms_c * 1e-3) / 1e9, 1),
+            "shared_prefix_gbs_unique": round(unique / (ms_c * 1e-3) / 1e9, 1),
+            "shared_prefix_frac_of_hbm_unique": round(unique / (ms_c * 1e-3) / 1e9 / hbm, 4),
+            "peak_source": f"{peak_src} (hbm_gbs)",
+            "max_abs_diff_plain_vs_shared_prefix": diff,
+            "l2": "256 MiB buffer written then read between calls"}
 
 
 def run_chain_hash_bench(dev, hbm, peak_src, n=20, seed=0):

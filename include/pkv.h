@@ -20,9 +20,11 @@
  *                     a negative slot means "do not write this token"
  *   GQA: query head h reads kv head h / (num_q_heads / num_kv_heads).
  *
- * Ownership: the caller owns and allocates every buffer, including the
- * workspace.  The library allocates no device memory and keeps no state
- * besides a per-device cache of the SM count.
+ * Ownership: the caller owns and allocates every device buffer, including
+ * the workspace; the library allocates no device memory.  Its own state: a
+ * per-device cache of the SM count, the device error word and the scratch
+ * array of pkv_paged_decode_attn_noalloc (module globals), and the host
+ * objects of the prefix index (pkv_radix_create .. pkv_radix_destroy).
  *
  * Execution: every call only validates its arguments on the host and enqueues
  * kernels on `stream`; it returns before the GPU work finishes.  Buffers must
@@ -182,6 +184,56 @@ pkv_status pkv_paged_decode_attn_append(const pkv_cache_desc* desc, void* k_cach
                                         int32_t num_q_heads, float sm_scale, int32_t max_seq_len,
                                         int32_t num_splits, float* lse_out, void* workspace,
                                         size_t workspace_bytes, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * pkv_paged_decode_attn_shared_prefix -- decode for groups of requests that
+ * share a cached prefix, the prefix attended once per group.
+ *
+ * "KV Cache 완전 정리 — PagedAttention vs RadixAttention, SGLang이 빠른 이유",
+ * section "RadixAttention — SGLang의 혁신", and "PagedAttention과
+ * RadixAttention으로 LLM KV 캐시 최적화", section 03: many requests share one
+ * long prefix (a system prompt) whose KV blocks are stored once.  Plain
+ * decode reads those blocks once per request; this call computes the
+ * prefix's attention for all (request, head) rows of a group in one dense
+ * pass on the tensor cores, attends each request's own tokens with the
+ * split-KV decode kernel, and merges the parts with their log-sum-exps,
+ * which equals attention over the whole sequence up to rounding.
+ *
+ * Groups: request b belongs to group g when group_indptr[g] <= b <
+ * group_indptr[g+1]; group_indptr (int32 [num_groups+1], device) rises from 0
+ * to batch.  group_prefix_lens (int32 [num_groups], device): P_g, the tokens
+ * every member of the group holds with the same K/V (0 = none).  Only whole
+ * blocks are shared: with W_g = floor(P_g / block_size) * block_size, tokens
+ * 0 .. W_g-1 of every member are read once for the group, through the block
+ * table of its first member (block_tables[group_indptr[g]]; the other
+ * members' entries for them are not read), and tokens W_g .. seq_lens[b]-1
+ * through the member's own table.  P_g <= seq_lens[b] for every member (else
+ * the device error word reports PKV_DEVERR_BAD_LENGTH).
+ *
+ * k_new, v_new:  nullable together; as pkv_paged_decode_attn_append (the
+ *                current token, position seq_lens[b]-1, must lie at or after
+ *                W_g).
+ * max_group_size: host bound of the members per group (sizes the prefix pass).
+ * max_suffix_len: host bound of seq_lens[b] - P_g (sizes the split plan).
+ * num_splits:    as pkv_paged_decode_attn, for the members' own tokens.
+ * workspace:     pkv_shared_prefix_decode_workspace_bytes() bytes, 256-byte
+ *                aligned (always needed).
+ * q:             16-byte aligned.  Everything else as pkv_paged_decode_attn.
+ * Supported: head_dim 128, f16 or bf16 cache with the same act dtype,
+ * block_size 16/32, num_q_heads/num_kv_heads in {1, 2, 4, 8}, sm_scale > 0.
+ * ------------------------------------------------------------------------- */
+size_t pkv_shared_prefix_decode_workspace_bytes(const pkv_cache_desc* desc, int32_t batch,
+                                                int32_t num_q_heads, int32_t max_suffix_len,
+                                                int32_t num_splits);
+
+pkv_status pkv_paged_decode_attn_shared_prefix(
+    const pkv_cache_desc* desc, void* k_cache, void* v_cache, const void* k_new,
+    const void* v_new, const void* q, void* out, pkv_dtype act_dtype,
+    const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+    int32_t batch, int32_t num_q_heads, float sm_scale, const int32_t* group_indptr,
+    const int32_t* group_prefix_lens, int32_t num_groups, int32_t max_group_size,
+    int32_t max_suffix_len, int32_t num_splits, float* lse_out, void* workspace,
+    size_t workspace_bytes, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
  * pkv_paged_extend_attn -- suffix prefill over a cached prefix.

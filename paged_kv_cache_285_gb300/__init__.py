@@ -12,7 +12,8 @@ The three calls (names as in pkv.h without the ``pkv_`` prefix):
   * paged_extend_attn  -- suffix prefill over cached prefix blocks + causal
                           suffix.
 Also: paged_decode_attn_append (decode with the current token appended by the
-decode kernel), RadixIndex (the host prefix index that hands out block
+decode kernel), paged_decode_attn_shared_prefix (decode for groups of requests
+sharing a prefix, the prefix attended once per group), RadixIndex (the host prefix index that hands out block
 tables and prefix lengths; host int32 arrays in, host arrays out) and
 chain_hash (salted chain hashes of full blocks, as block identifiers).
 """
@@ -27,7 +28,8 @@ import torch
 __all__ = ["F16", "BF16", "FP8_E4M3", "PkvError", "CacheDesc", "lib_path", "load",
            "kv_append", "paged_decode_attn", "paged_extend_attn", "decode_workspace_bytes",
            "extend_workspace_bytes", "get_device_error", "status_string", "version",
-           "paged_decode_attn_append", "RadixIndex", "NO_SPACE", "chain_hash"]
+           "paged_decode_attn_append", "RadixIndex", "NO_SPACE", "chain_hash",
+           "paged_decode_attn_shared_prefix", "shared_prefix_decode_workspace_bytes"]
 
 F16, BF16, FP8_E4M3 = 0, 1, 2
 NO_SPACE = 5  # PKV_ERR_NO_SPACE
@@ -93,6 +95,12 @@ def load():
         lib.pkv_get_device_error.restype = ctypes.c_int
         lib.pkv_version.argtypes = []
         lib.pkv_version.restype = I32
+        lib.pkv_shared_prefix_decode_workspace_bytes.argtypes = [D, I32, I32, I32, I32]
+        lib.pkv_shared_prefix_decode_workspace_bytes.restype = SZ
+        lib.pkv_paged_decode_attn_shared_prefix.argtypes = [D, P, P, P, P, P, P, ctypes.c_int, P,
+                                                             I32, P, I32, I32, F, P, P, I32, I32,
+                                                             I32, I32, P, P, SZ, P]
+        lib.pkv_paged_decode_attn_shared_prefix.restype = ctypes.c_int
         lib.pkv_chain_hash.argtypes = [P, P, I32, I32, P, P, I32, P]
         lib.pkv_chain_hash.restype = ctypes.c_int
         VP = ctypes.c_void_p
@@ -216,6 +224,39 @@ def paged_decode_attn_append(k_cache, v_cache, k_new, v_new, q, out, block_table
                                           float(sm_scale), int(max_seq_len), int(num_splits),
                                           _ptr(lse_out), _ptr(workspace), ws_bytes, _stream(stream))
     _check(st, "pkv_paged_decode_attn_append")
+
+
+def shared_prefix_decode_workspace_bytes(k_cache, batch, num_q_heads, max_suffix_len,
+                                         num_splits=0) -> int:
+    lib = load()
+    desc = _desc(k_cache, 1.0, 1.0)
+    return int(lib.pkv_shared_prefix_decode_workspace_bytes(ctypes.byref(desc), batch, num_q_heads,
+                                                            max_suffix_len, num_splits))
+
+
+def paged_decode_attn_shared_prefix(k_cache, v_cache, q, out, block_tables, seq_lens, sm_scale,
+                                    group_indptr, group_prefix_lens, max_group_size,
+                                    max_suffix_len, k_new=None, v_new=None, num_splits=0,
+                                    lse_out=None, workspace=None, stream=None):
+    """pkv_paged_decode_attn_shared_prefix: requests [group_indptr[g], group_indptr[g+1])
+    share their first group_prefix_lens[g] tokens (read through the group's first member's
+    block table), attended once per group; k_new/v_new as paged_decode_attn_append."""
+    lib = load()
+    desc = _desc(k_cache, 1.0, 1.0)
+    b, hq, _ = q.shape
+    ng = int(group_indptr.shape[0]) - 1
+    if group_indptr.dtype != torch.int32 or group_prefix_lens.dtype != torch.int32:
+        raise ValueError("group_indptr and group_prefix_lens must be int32")
+    if tuple(group_prefix_lens.shape) != (ng,):
+        raise ValueError("group_prefix_lens must be int32 [num_groups]")
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib.pkv_paged_decode_attn_shared_prefix(
+        ctypes.byref(desc), _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new), _ptr(q),
+        _ptr(out), _dtype_code(q), _ptr(block_tables), int(block_tables.shape[1]), _ptr(seq_lens),
+        b, hq, float(sm_scale), _ptr(group_indptr), _ptr(group_prefix_lens), ng,
+        int(max_group_size), int(max_suffix_len), int(num_splits), _ptr(lse_out),
+        _ptr(workspace), ws_bytes, _stream(stream))
+    _check(st, "pkv_paged_decode_attn_shared_prefix")
 
 
 def extend_workspace_bytes(k_cache, batch, num_q_heads, total_q_rows, max_total_len,

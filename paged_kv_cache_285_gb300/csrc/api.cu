@@ -282,6 +282,157 @@ size_t pkv_decode_workspace_bytes(const pkv_cache_desc* desc, int32_t batch, int
   return plan_decode(desc, batch, num_q_heads, max_seq_len, num_splits, sms).ws_bytes;
 }
 
+}  // extern "C"
+
+// Plan of a shared-prefix decode: the decode split plan over the requests'
+// own tokens, partials for one more slot (the shared prefix's) per (request,
+// head), always merged.
+static DecodePlan plan_cascade(const pkv_cache_desc* d, int batch, int hq, int max_suffix_len,
+                               int forced, int sm_count) {
+  // a member's own tokens start at its group's prefix rounded down to whole
+  // blocks: up to block_size - 1 more than seq_len - prefix
+  DecodePlan pl = plan_decode(d, batch, hq, max_suffix_len + d->block_size - 1, forced, sm_count);
+  const size_t slots = (size_t)pl.splits + 1;
+  pl.ws_lse_offset = align256((size_t)batch * hq * slots * d->head_dim * sizeof(float));
+  pl.ws_bytes = pl.ws_lse_offset + (size_t)batch * hq * slots * sizeof(float);
+  return pl;
+}
+
+extern "C" {
+
+size_t pkv_shared_prefix_decode_workspace_bytes(const pkv_cache_desc* desc, int32_t batch,
+                                                int32_t num_q_heads, int32_t max_suffix_len,
+                                                int32_t num_splits) {
+  if (check_desc(desc) != PKV_OK || batch <= 0 || num_q_heads <= 0 || max_suffix_len < 0 ||
+      num_splits < 0)
+    return 0;
+  cudaError_t e;
+  DeviceState* ds = device_state(&e);
+  const int sms = ds ? ds->sm_count : 0;
+  return plan_cascade(desc, batch, num_q_heads, max_suffix_len, num_splits, sms).ws_bytes;
+}
+
+pkv_status pkv_paged_decode_attn_shared_prefix(
+    const pkv_cache_desc* desc, void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+    const void* q, void* out, pkv_dtype act_dtype, const int32_t* block_tables,
+    int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
+    float sm_scale, const int32_t* group_indptr, const int32_t* group_prefix_lens,
+    int32_t num_groups, int32_t max_group_size, int32_t max_suffix_len, int32_t num_splits,
+    float* lse_out, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  pkv_status st = check_desc(desc);
+  if (st != PKV_OK) return st;
+  if ((st = check_act(desc, act_dtype)) != PKV_OK) return st;
+  if (batch < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || num_groups < 0 ||
+      max_group_size < 0 || max_suffix_len < 0 || num_splits < 0 || !std::isfinite(sm_scale) ||
+      !(sm_scale > 0.f))
+    return PKV_ERR_INVALID_ARG;
+  if (num_q_heads % desc->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+  const int group = num_q_heads / desc->num_kv_heads;
+  if (!extend_supported(desc->head_dim, (int)desc->cache_dtype, (int)act_dtype, group))
+    return PKV_ERR_UNSUPPORTED;
+  if (batch == 0) return PKV_OK;
+  if (num_groups == 0 || max_group_size == 0) return PKV_ERR_INVALID_ARG;
+  if (batch > 65535 || desc->num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
+  if (!k_cache || !v_cache || !q || !out || !block_tables || !seq_lens || !group_indptr ||
+      !group_prefix_lens)
+    return PKV_ERR_INVALID_ARG;
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 16) || !aligned(out, 2))
+    return PKV_ERR_INVALID_ARG;
+  if ((k_new == nullptr) != (v_new == nullptr)) return PKV_ERR_INVALID_ARG;
+  if (k_new && (!aligned(k_new, 16) || !aligned(v_new, 16))) return PKV_ERR_INVALID_ARG;
+  cudaError_t e;
+  DeviceState* ds = device_state(&e);
+  if (!ds) return PKV_ERR_CUDA;
+  const DecodePlan pl = plan_cascade(desc, batch, num_q_heads, max_suffix_len, num_splits,
+                                     ds->sm_count);
+  if (!workspace || workspace_bytes < pl.ws_bytes || !aligned(workspace, 256))
+    return PKV_ERR_WORKSPACE;
+  if (pl.splits > 65535) return PKV_ERR_UNSUPPORTED;
+  CUtensorMap kmap, vmap, qmap;
+  if ((st = make_page_map(&kmap, k_cache, desc)) != PKV_OK) return st;
+  if ((st = make_page_map(&vmap, v_cache, desc)) != PKV_OK) return st;
+  if ((st = make_q_map(&qmap, q, desc->head_dim, num_q_heads, batch, group)) != PKV_OK) return st;
+  float* ws_o = reinterpret_cast<float*>(workspace);
+  float* ws_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + pl.ws_lse_offset);
+  const int slots = pl.splits + 1;
+  const float scale_log2 = (float)((double)sm_scale * 1.4426950408889634);
+
+  // 1. the shared prefixes, once per group, on the tensor cores -> slot 0
+  ExtendParams pe;
+  pe.q_indptr = group_indptr;
+  pe.prefix_lens = group_prefix_lens;
+  pe.block_tables = block_tables;
+  pe.q = q;
+  pe.out = nullptr;
+  pe.lse_out = nullptr;
+  pe.err = ds->err;
+  pe.max_blocks = max_blocks_per_seq;
+  pe.num_blocks = desc->num_blocks;
+  pe.batch = num_groups;
+  pe.num_q_heads = num_q_heads;
+  pe.num_kv_heads = desc->num_kv_heads;
+  pe.group = group;
+  pe.out_32b = 0;
+  pe.group_shift = group == 1 ? 0 : group == 2 ? 1 : group == 4 ? 2 : 3;
+  pe.bs_shift = desc->block_size == 16 ? 4 : 5;
+  pe.total_rows = batch;
+  pe.tiles_per_head = ceil_div((int64_t)max_group_size * group, 128);
+  pe.scale_log2 = scale_log2;
+  pe.out_scale = 1.0f;
+  const int64_t items = (int64_t)((pe.tiles_per_head + 1) / 2) * desc->num_kv_heads * num_groups;
+  if (items > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  pe.num_items = (int)items;
+  const uint32_t pairs = (uint32_t)((pe.tiles_per_head + 1) / 2);
+  pe.div_pairs = make_fastdiv(pairs);
+  pe.div_hkv = make_fastdiv((uint32_t)desc->num_kv_heads);
+  pe.div_req = make_fastdiv(pairs * (uint32_t)desc->num_kv_heads);
+  pe.num_ctas = (int)std::min<int64_t>(items, ds->sm_count > 0 ? ds->sm_count : 1);
+  ExtendPartialParams pp;
+  pp.o = ws_o;
+  pp.lse = ws_lse;
+  pp.o_stride = (int64_t)slots * desc->head_dim;
+  pp.lse_stride = slots;
+  e = launch_extend_prefix_pass(kmap, vmap, qmap, pe, pp, desc->head_dim, (int)desc->cache_dtype,
+                                (int)act_dtype, stream);
+  if (e != cudaSuccess) return PKV_ERR_CUDA;
+
+  // 2. each request's own tokens (current token appended first) -> slots 1..,
+  //    then the merge of all slots
+  DecodeParams p;
+  p.block_tables = block_tables;
+  p.seq_lens = seq_lens;
+  p.q = q;
+  p.out = out;
+  p.lse_out = lse_out;
+  p.ws_o = ws_o;
+  p.ws_lse = ws_lse;
+  p.err = ds->err;
+  p.max_blocks = max_blocks_per_seq;
+  p.num_blocks = desc->num_blocks;
+  p.batch = batch;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = desc->num_kv_heads;
+  p.group = group;
+  p.bs_shift = desc->block_size == 16 ? 4 : 5;
+  p.chunk = pl.chunk;
+  p.num_splits = pl.splits;
+  p.scale_log2 = scale_log2;
+  p.out_scale = 1.0f;
+  DecodeExtraParams ap{};
+  ap.k_new = k_new;
+  ap.v_new = v_new;
+  ap.k_cache = k_cache;
+  ap.v_cache = v_cache;
+  ap.k_scale = desc->k_scale;
+  ap.v_scale = desc->v_scale;
+  ap.group_indptr = group_indptr;
+  ap.group_prefix_lens = group_prefix_lens;
+  ap.num_groups = num_groups;
+  e = launch_decode_cascade(kmap, vmap, p, ap, desc->head_dim, (int)desc->cache_dtype,
+                            (int)act_dtype, stream);
+  return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
 // Decode, optionally with the current token's K/V (k_new/v_new, [B][Hkv][D]
 // act dtype) appended to position seq_len-1 inside the decode kernel.
 static pkv_status decode_common(const pkv_cache_desc* desc, const void* k_cache,
@@ -341,7 +492,7 @@ static pkv_status decode_common(const pkv_cache_desc* desc, const void* k_cache,
   const double kscale = desc->cache_dtype == PKV_FP8_E4M3 ? (double)desc->k_scale : 1.0;
   p.scale_log2 = (float)((double)sm_scale * kscale * 1.4426950408889634);
   p.out_scale = desc->cache_dtype == PKV_FP8_E4M3 ? desc->v_scale : 1.0f;
-  DecodeAppendParams ap;
+  DecodeExtraParams ap{};
   ap.k_new = k_new;
   ap.v_new = v_new;
   ap.k_cache = const_cast<void*>(k_cache);

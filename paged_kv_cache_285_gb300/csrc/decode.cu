@@ -107,10 +107,24 @@ __device__ __forceinline__ float to_f32_bits(uint32_t bits16) {
   else return __half2float(__ushort_as_half((unsigned short)bits16));
 }
 
-template <int HD, int CT, int AT, int NW, int NS>
+// Shared-prefix length of request b's group (group_indptr is non-decreasing
+// from 0 to batch; the search stays inside the arrays whatever they hold).
+__device__ __forceinline__ int group_prefix_len(const DecodeExtraParams& ap, int b) {
+  int lo = 0, hi = ap.num_groups;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(ap.group_indptr + mid) <= b) lo = mid;
+    else hi = mid;
+  }
+  return __ldg(ap.group_prefix_lens + lo);
+}
+
+// CASC: a cascade launch (tokens from the group's shared prefix on, partials
+// in workspace slots 1.., always merged).
+template <int HD, int CT, int AT, int NW, int NS, bool CASC>
 __global__ void __launch_bounds__(NW * 32)
 decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-              const DecodeParams p, const DecodeAppendParams ap) {
+              const DecodeParams p, const DecodeExtraParams ap) {
   using C = DecodeCfg<HD, CT, NW, NS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -124,14 +138,26 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
   const int bs = 1 << p.bs_shift;
 
   int n = p.seq_lens[b];
-  const int cap = min(p.max_blocks * bs, p.num_splits * p.chunk);
+  int tb = 0;  // first token of this launch (cascade: the end of the shared prefix)
+  if constexpr (CASC) tb = group_prefix_len(ap, b);
+  const int cap = min(p.max_blocks * bs, (tb > 0 ? tb : 0) + p.num_splits * p.chunk);
   if (n < 0 || n > cap) {
     if (threadIdx.x == 0 && split == 0) set_err(p.err, 3);
     n = n < 0 ? 0 : cap;
   }
-  const int t0 = split * p.chunk;
+  if constexpr (CASC) {
+    if (tb < 0 || tb > n) {
+      if (threadIdx.x == 0 && split == 0) set_err(p.err, 3);
+      tb = tb < 0 ? 0 : n;
+    }
+    tb = (tb >> p.bs_shift) << p.bs_shift;  // only whole blocks are shared
+  }
+  const int t0 = tb + split * p.chunk;
   if (t0 >= n) {
-    if (split == 0) {  // empty sequence: out = 0, lse = -inf
+    if constexpr (CASC) {
+      // nothing after the prefix; the current token cannot be appended there
+      if (ap.k_new != nullptr && split == 0 && n > 0 && threadIdx.x == 0) set_err(p.err, 3);
+    } else if (split == 0) {  // empty sequence: out = 0, lse = -inf
       for (int idx = threadIdx.x; idx < G * HD; idx += NW * 32) {
         const int h = g * G + idx / HD;
         store_act<AT>(p.out, ((int64_t)b * p.num_q_heads + h) * HD + idx % HD, 0.f);
@@ -142,7 +168,7 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
   }
   const int t1 = min(n, t0 + p.chunk);
   const int nsub = (t1 - t0 + kSubTokens - 1) / kSubTokens;
-  const int nsplit_b = (n + p.chunk - 1) / p.chunk;
+  const int nsplit_b = (n - tb + p.chunk - 1) / p.chunk;
   const int cnt = warp < nsub ? (nsub - warp + NW - 1) / NW : 0;
 
   if (ap.k_new != nullptr && split == nsplit_b - 1) {
@@ -462,7 +488,9 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
   }
   __syncthreads();
 
-  const bool direct = (nsplit_b == 1);
+  const bool direct = !CASC && (nsplit_b == 1);
+  constexpr int kSlot0 = CASC ? 1 : 0;  // cascade: slot 0 holds the shared prefix
+  const int nslots = p.num_splits + kSlot0;
   for (int idx = threadIdx.x; idx < G * HD; idx += NW * 32) {
     const int jh = idx / HD, d = idx % HD;
     float mstar = -INFINITY;
@@ -483,38 +511,53 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       store_act<AT>(p.out, bh * HD + d, res);
       if (p.lse_out && d == 0) p.lse_out[bh] = lse2 * kLn2;
     } else {
-      p.ws_o[(bh * p.num_splits + split) * HD + d] = res;
-      if (d == 0) p.ws_lse[bh * p.num_splits + split] = lse2;
+      p.ws_o[(bh * nslots + kSlot0 + split) * HD + d] = res;
+      if (d == 0) p.ws_lse[bh * nslots + kSlot0 + split] = lse2;
     }
   }
 }
 
 // Merge the splits of one (request, head) per warp:
 //   lse* = log2 sum_s 2^lse_s,  out = sum_s 2^(lse_s - lse*) o_s.
-template <int HD, int AT>
-__global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p) {
+// Cascade: slot 0 (the group's shared prefix, when it has one) and slots
+// 1 .. of the request's own tokens.
+template <int HD, int AT, bool CASC>
+__global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, const DecodeExtraParams ap) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t bh = (int64_t)blockIdx.x * 4 + warp;
   if (bh >= (int64_t)p.batch * p.num_q_heads) return;
   const int b = (int)(bh / p.num_q_heads);
   const int bs = 1 << p.bs_shift;
   int n = p.seq_lens[b];
-  const int cap = min(p.max_blocks * bs, p.num_splits * p.chunk);
+  int tb = 0;
+  if constexpr (CASC) tb = group_prefix_len(ap, b);
+  const int cap = min(p.max_blocks * bs, (tb > 0 ? tb : 0) + p.num_splits * p.chunk);
   n = n < 0 ? 0 : (n > cap ? cap : n);
-  const int ns = (n + p.chunk - 1) / p.chunk;
-  if (ns <= 1) return;  // written directly by the split kernel
-  const float* lse = p.ws_lse + bh * p.num_splits;
+  tb = tb < 0 ? 0 : (tb > n ? n : tb);
+  tb = (tb >> p.bs_shift) << p.bs_shift;
+  const int ns = (n - tb + p.chunk - 1) / p.chunk;
+  if (!CASC && ns <= 1) return;  // written directly by the split kernel
+  constexpr int kSlot0 = CASC ? 1 : 0;
+  const int nslots = p.num_splits + kSlot0;
+  const int s_lo = (CASC && tb > 0) ? 0 : kSlot0, s_hi = kSlot0 + ns;
+  constexpr int PER = HD / 32;
+  if (s_lo >= s_hi) {  // no token at all: out = 0, lse = -inf
+#pragma unroll
+    for (int k = 0; k < PER; ++k) store_act<AT>(p.out, bh * HD + lane * PER + k, 0.f);
+    if (p.lse_out && lane == 0) p.lse_out[bh] = -INFINITY;
+    return;
+  }
+  const float* lse = p.ws_lse + bh * nslots;
   float m = -INFINITY;
-  for (int s = lane; s < ns; s += 32) m = fmaxf(m, lse[s]);
+  for (int s = s_lo + lane; s < s_hi; s += 32) m = fmaxf(m, lse[s]);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
-  constexpr int PER = HD / 32;
   float o[PER];
 #pragma unroll
   for (int k = 0; k < PER; ++k) o[k] = 0.f;
   float L = 0.f;
-  const float* po = p.ws_o + bh * p.num_splits * HD + lane * PER;
-  for (int s = 0; s < ns; ++s) {
+  const float* po = p.ws_o + bh * nslots * HD + lane * PER;
+  for (int s = s_lo; s < s_hi; ++s) {
     const float w = fast_exp2(lse[s] - m);
     L += w;
     if constexpr (PER == 4) {
@@ -541,21 +584,21 @@ constexpr int stages_for() {
   return ns < 2 ? 2 : (ns > 8 ? 8 : ns);
 }
 
-template <int HD, int CT, int AT>
+template <int HD, int CT, int AT, bool CASC>
 cudaError_t launch_decode_t(const CUtensorMap& kmap, const CUtensorMap& vmap,
-                            const DecodeParams& p, const DecodeAppendParams& ap,
+                            const DecodeParams& p, const DecodeExtraParams& ap,
                             cudaStream_t stream) {
   constexpr int NS = stages_for<HD, CT>();
   using C = DecodeCfg<HD, CT, kNW, NS>;
-  auto kern = decode_kernel<HD, CT, AT, kNW, NS>;
+  auto kern = decode_kernel<HD, CT, AT, kNW, NS, CASC>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(p.num_splits, p.num_kv_heads, p.batch);
   kern<<<grid, kNW * 32, C::SMEM, stream>>>(kmap, vmap, p, ap);
   e = cudaGetLastError();
-  if (e != cudaSuccess || p.num_splits <= 1) return e;
+  if (e != cudaSuccess || (!CASC && p.num_splits <= 1)) return e;
   const int64_t pairs = (int64_t)p.batch * p.num_q_heads;
-  merge_kernel<HD, AT><<<(unsigned)((pairs + 3) / 4), 128, 0, stream>>>(p);
+  merge_kernel<HD, AT, CASC><<<(unsigned)((pairs + 3) / 4), 128, 0, stream>>>(p, ap);
   return cudaGetLastError();
 }
 
@@ -574,11 +617,11 @@ size_t decode_smem_bytes(int head_dim, int cache_dt) {
 }
 
 cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, const DecodeParams& p,
-                          const DecodeAppendParams& ap, int head_dim, int cache_dt, int act_dt,
+                          const DecodeExtraParams& ap, int head_dim, int cache_dt, int act_dt,
                           cudaStream_t stream) {
 #define PKV_DEC(HD, CT, AT)                                              \
   if (head_dim == HD && cache_dt == CT && act_dt == AT)                  \
-    return launch_decode_t<HD, CT, AT>(kmap, vmap, p, ap, stream);
+    return launch_decode_t<HD, CT, AT, false>(kmap, vmap, p, ap, stream);
   PKV_DEC(64, DT_F16, DT_F16)
   PKV_DEC(64, DT_BF16, DT_BF16)
   PKV_DEC(64, DT_E4M3, DT_F16)
@@ -588,6 +631,17 @@ cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, cons
   PKV_DEC(128, DT_E4M3, DT_F16)
   PKV_DEC(128, DT_E4M3, DT_BF16)
 #undef PKV_DEC
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_decode_cascade(const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                  const DecodeParams& p, const DecodeExtraParams& ap, int head_dim,
+                                  int cache_dt, int act_dt, cudaStream_t stream) {
+  if (head_dim != 128 || act_dt != cache_dt) return cudaErrorInvalidValue;
+  if (!ap.group_indptr || !ap.group_prefix_lens || ap.num_groups <= 0 || !p.ws_o)
+    return cudaErrorInvalidValue;
+  if (cache_dt == DT_F16) return launch_decode_t<128, DT_F16, DT_F16, true>(kmap, vmap, p, ap, stream);
+  if (cache_dt == DT_BF16) return launch_decode_t<128, DT_BF16, DT_BF16, true>(kmap, vmap, p, ap, stream);
   return cudaErrorInvalidValue;
 }
 

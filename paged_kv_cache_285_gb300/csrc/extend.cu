@@ -45,6 +45,13 @@
 // P is f16 (11 significant bits) because bf16 P alone would put the relative
 // L2 error of the output near 1.5e-3; V is therefore converted to f16 (bf16
 // values beyond +-65504 are outside this path's range).
+//
+// Prefix pass (PP = true), for decode over a prefix shared by a group of
+// requests: each group is one pseudo-request whose rows are the group
+// members' query vectors (one token each), keys are the group's P shared
+// tokens read through its first member's block table, every row sees all P
+// of them and no other, and each row's result leaves as an fp32 partial
+// (O / l and the base-2 LSE) for an LSE merge with the member's own tokens.
 #include "internal.h"
 #include "ptx.cuh"
 #include "tcgen05.cuh"
@@ -111,7 +118,9 @@ __device__ __forceinline__ ItemRaw load_raw(const ExtendParams& p, int item) {
   return r;
 }
 
-// false: tile A holds no suffix rows (the same answer in every role)
+// false: the item has no work (the same answer in every role): tile A holds no
+// suffix rows, or, in the prefix pass, the group shares no prefix
+template <bool PP>
 __device__ __forceinline__ bool derive(const ExtendParams& p, int item, const ItemRaw& r, Item& it) {
   const uint32_t rest = p.div_pairs.div((uint32_t)item);
   const int pair = item - (int)(rest * p.div_pairs.d);
@@ -126,8 +135,20 @@ __device__ __forceinline__ bool derive(const ExtendParams& p, int item, const It
   it.ntok[1] = max(0, min(TOK, it.S - it.i0 - TOK));
   it.P = r.prefix;
   const int cap = p.max_blocks << p.bs_shift;
-  it.kv_total = it.P + it.S;
-  it.k_hi = it.P + it.i0 + it.ntok[0] + it.ntok[1];  // keys the pair needs
+  if constexpr (PP) {
+    // the group's first member supplies the block table and must exist
+    if (it.row0 < 0 || it.row0 >= p.total_rows) {
+      set_err(p.err, 3);
+      return false;
+    }
+    it.P = (it.P >> p.bs_shift) << p.bs_shift;  // only whole blocks are shared
+    if (it.P <= 0) return false;
+    it.kv_total = it.P;
+    it.k_hi = it.P;
+  } else {
+    it.kv_total = it.P + it.S;
+    it.k_hi = it.P + it.i0 + it.ntok[0] + it.ntok[1];  // keys the pair needs
+  }
   if (it.P < 0 || it.kv_total > cap) {
     set_err(p.err, 3);
     it.kv_total = min(max(it.kv_total, 0), cap);
@@ -137,10 +158,11 @@ __device__ __forceinline__ bool derive(const ExtendParams& p, int item, const It
   return true;
 }
 
-template <int CT>
+template <int CT, bool PP>
 __global__ void __launch_bounds__(NTHREADS, 1)
 extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-              const __grid_constant__ CUtensorMap qmap, const ExtendParams p) {
+              const __grid_constant__ CUtensorMap qmap, const ExtendParams p,
+              const ExtendPartialParams pp) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -204,9 +226,10 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       const ItemRaw raw = nxt_raw;
       nxt_raw = load_raw(p, item + stride);
       Item it;
-      if (!derive(p, item, raw, it)) continue;
+      if (!derive<PP>(p, item, raw, it)) continue;
       const int i0x = it.i0 + x * TOK;  // first token of this tile
-      const int kdiag = it.P + i0x;     // a row's last visible key is kdiag + its token
+      // a row's last visible key is kdiag + its token (prefix pass: P - 1 for all)
+      const int kdiag = PP ? it.P - 1 : it.P + i0x;
       float m_run = -INFINITY, l_run = 0.f;
       for (int kt = 0; kt < it.T; ++kt, ++n) {
         if (!mbar_wait(bar(B_SDONE + x), n & 1)) { ok = false; break; }
@@ -217,7 +240,7 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
           // key0 .. key0+nvis are visible): applied in TMEM one 32-column
           // chunk at a time, a short rolled loop that runs on one or two key
           // tiles per item
-          const int nvis = kdiag + (r >> gs) - key0;
+          const int nvis = kdiag + (PP ? 0 : (r >> gs)) - key0;
           const uint32_t ninf = __float_as_uint(-INFINITY);
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
@@ -298,36 +321,60 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       // item), O / l -> out, LSE
       if (!mbar_wait(bar(B_ODONE), js & 1)) { ok = false; break; }
       tc_fence_after();
-      // O / l packed to 16-bit in registers; then O_x is free in TMEM
       const float osc = p.out_scale / l_run;
-      uint32_t w[64];
+      if constexpr (PP) {
+        // fp32 O / l straight from TMEM, 32 columns at a time, then the LSE
+        const int req = it.row0 + i0x + (r >> gs);  // the group member of this row
+        const bool valid = (r >> gs) < it.ntok[x] && req >= 0 && req < p.total_rows;
+        const int64_t qrow = (int64_t)req * p.num_q_heads + it.g * G + (r & (G - 1));
+        float* dst = pp.o + qrow * pp.o_stride;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tmem_ld32(orow + c * 32, o);
+          tmem_wait_ld();
+          if (valid) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t o[32];
-        tmem_ld32(orow + c * 32, o);
-        tmem_wait_ld();
+            for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * osc);
 #pragma unroll
-        for (int q = 0; q < 16; ++q)
-          w[c * 16 + q] = pack2<CT == DT_BF16>(__uint_as_float(o[2 * q]) * osc,
-                                               __uint_as_float(o[2 * q + 1]) * osc);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_OFREE + x));
-      if ((r >> gs) < it.ntok[x]) {
-        const int64_t qrow = (int64_t)(it.row0 + i0x + (r >> gs)) * p.num_q_heads + it.g * G + (r & (G - 1));
-        uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + qrow * HD;
-        if (p.out_32b) {
-          // 32-byte stores: half the L1 requests of 16-byte ones for the
-          // row-strided output
-#pragma unroll
-          for (int q = 0; q < 8; ++q) st_global_v8(dst + 16 * q, &w[8 * q]);
-        } else {
-          uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-          for (int q = 0; q < 16; ++q) d4[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+            for (int q = 0; q < 4; ++q) st_global_v8(dst + c * 32 + 8 * q, &o[8 * q]);
+          }
         }
-        if (p.lse_out) p.lse_out[qrow] = (m_run + log2f(l_run)) * kLn2f;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_OFREE + x));
+        if (valid) pp.lse[qrow * pp.lse_stride] = m_run + log2f(l_run);
+      } else {
+        // O / l packed to 16-bit in registers; then O_x is free in TMEM
+        uint32_t w[64];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tmem_ld32(orow + c * 32, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int q = 0; q < 16; ++q)
+            w[c * 16 + q] = pack2<CT == DT_BF16>(__uint_as_float(o[2 * q]) * osc,
+                                                 __uint_as_float(o[2 * q + 1]) * osc);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_OFREE + x));
+        if ((r >> gs) < it.ntok[x]) {
+          const int64_t qrow = (int64_t)(it.row0 + i0x + (r >> gs)) * p.num_q_heads + it.g * G + (r & (G - 1));
+          uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + qrow * HD;
+          if (p.out_32b) {
+            // 32-byte stores: half the L1 requests of 16-byte ones for the
+            // row-strided output
+#pragma unroll
+            for (int q = 0; q < 8; ++q) st_global_v8(dst + 16 * q, &w[8 * q]);
+          } else {
+            uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) d4[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+          }
+          if (p.lse_out) p.lse_out[qrow] = (m_run + log2f(l_run)) * kLn2f;
+        }
       }
       ++js;
     }
@@ -368,9 +415,10 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
         const ItemRaw raw = nxt_raw;
         nxt_raw = load_raw(p, item + stride);
         Item it;
-        if (!derive(p, item, raw, it)) continue;
+        if (!derive<PP>(p, item, raw, it)) continue;
         if (is_k && !load_q(it, j, 0)) { ok = false; break; }
-        const int32_t* bt = p.block_tables + (int64_t)it.b * p.max_blocks;
+        // prefix pass: the group's first member's table (row0 = its index)
+        const int32_t* bt = p.block_tables + (int64_t)(PP ? it.row0 : it.b) * p.max_blocks;
         auto fetch = [&](int wi) -> int {
           const int key0 = (wi * 32 + lane) * 16;  // sub-tile = 16 keys
           int page = -1;
@@ -460,7 +508,7 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
         const ItemRaw raw = nxt_raw;
         nxt_raw = load_raw(p, item + stride);
         Item it;
-        if (!derive(p, item, raw, it)) continue;
+        if (!derive<PP>(p, item, raw, it)) continue;
         const int qa = (2 * j) % NQB, qb = (2 * j + 1) % NQB;
         for (int kt = 0; kt < it.T; ++kt, ++n) {
           if (have_prev && !issue_pv(0, prev_n, prev_first, prev_j)) { ok = false; break; }
@@ -511,7 +559,7 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
         const ItemRaw raw = nxt_raw;
         nxt_raw = load_raw(p, item + stride);
         Item it;
-        if (!derive(p, item, raw, it)) continue;
+        if (!derive<PP>(p, item, raw, it)) continue;
         for (int kt = 0; kt < it.T; ++kt, ++n) {
           const int vs = n % NST;
           if (!mbar_wait(bar(B_VFULL + vs), (n / NST) & 1)) { ok = false; break; }
@@ -574,24 +622,37 @@ bool extend_supported(int head_dim, int cache_dt, int act_dt, int group) {
   return group == 1 || group == 2 || group == 4 || group == 8;
 }
 
-cudaError_t launch_extend(const CUtensorMap& kmap, const CUtensorMap& vmap, const CUtensorMap& qmap,
-                          const ExtendParams& p, int head_dim, int cache_dt, int act_dt,
-                          cudaStream_t stream) {
+namespace {
+
+template <bool PP>
+cudaError_t launch_extend_t(const CUtensorMap& kmap, const CUtensorMap& vmap, const CUtensorMap& qmap,
+                            const ExtendParams& p, const ExtendPartialParams& pp, int head_dim,
+                            int cache_dt, int act_dt, cudaStream_t stream) {
   if (!extend_supported(head_dim, cache_dt, act_dt, p.group)) return cudaErrorInvalidValue;
   if (p.num_items <= 0 || p.num_ctas <= 0) return cudaErrorInvalidValue;
   const dim3 grid(p.num_ctas);
-  if (cache_dt == DT_BF16) {
-    auto k = extend_kernel<DT_BF16>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    k<<<grid, NTHREADS, SMEM_BYTES, stream>>>(kmap, vmap, qmap, p);
-  } else {
-    auto k = extend_kernel<DT_F16>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    k<<<grid, NTHREADS, SMEM_BYTES, stream>>>(kmap, vmap, qmap, p);
-  }
+  auto k = cache_dt == DT_BF16 ? extend_kernel<DT_BF16, PP> : extend_kernel<DT_F16, PP>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  k<<<grid, NTHREADS, SMEM_BYTES, stream>>>(kmap, vmap, qmap, p, pp);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_extend(const CUtensorMap& kmap, const CUtensorMap& vmap, const CUtensorMap& qmap,
+                          const ExtendParams& p, int head_dim, int cache_dt, int act_dt,
+                          cudaStream_t stream) {
+  return launch_extend_t<false>(kmap, vmap, qmap, p, ExtendPartialParams{}, head_dim, cache_dt,
+                                act_dt, stream);
+}
+
+cudaError_t launch_extend_prefix_pass(const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                      const CUtensorMap& qmap, const ExtendParams& p,
+                                      const ExtendPartialParams& pp, int head_dim, int cache_dt,
+                                      int act_dt, cudaStream_t stream) {
+  if (!pp.o || !pp.lse) return cudaErrorInvalidValue;
+  return launch_extend_t<true>(kmap, vmap, qmap, p, pp, head_dim, cache_dt, act_dt, stream);
 }
 
 }  // namespace pkv

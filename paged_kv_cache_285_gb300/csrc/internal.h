@@ -35,17 +35,26 @@ struct DecodeParams {
   float out_scale;    // v_scale for fp8, else 1
 };
 
-// Fused append of a decode call (k_new null: none): the current token's K/V
-// rows [B][Hkv][D] in the act dtype, written to position seq_len-1 before it
-// is read.  A kernel argument of its own: widening DecodeParams changes how
-// the decode loop is register-allocated.
-struct DecodeAppendParams {
+// Per-call extras of a decode launch, a kernel argument of their own:
+// widening DecodeParams changes how the decode loop is register-allocated.
+//  - fused append (k_new null: none): the current token's K/V rows
+//    [B][Hkv][D] in the act dtype, written to position seq_len-1 before it is
+//    read;
+//  - shared-prefix groups (cascade launches only): requests
+//    [group_indptr[g], group_indptr[g+1]) share their first
+//    group_prefix_lens[g] tokens, which a prefix pass attends once for the
+//    group; the decode then covers each request's tokens from there on and
+//    its partials start at workspace slot 1 (slot 0 is the prefix's).
+struct DecodeExtraParams {
   const void* k_new;
   const void* v_new;
   void* k_cache;
   void* v_cache;
   float k_scale;      // fp8 store scales
   float v_scale;
+  const int32_t* group_indptr;       // [num_groups + 1]
+  const int32_t* group_prefix_lens;  // [num_groups]
+  int num_groups;
 };
 
 struct AppendParams {
@@ -120,10 +129,27 @@ struct ExtendParams {
   float out_scale;
 };
 
+// Partial output of the extend kernel's prefix pass: row q (request b, head h:
+// q = b * num_q_heads + h) writes O / l to o[q * o_stride .. + head_dim) and
+// the base-2 LSE to lse[q * lse_stride] (o 32-byte aligned, o_stride a
+// multiple of 8).
+struct ExtendPartialParams {
+  float* o;
+  float* lse;
+  int64_t o_stride;
+  int64_t lse_stride;
+};
+
 // Each returns a cudaError_t from the launch.
 cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap,
-                          const DecodeParams& p, const DecodeAppendParams& ap, int head_dim,
+                          const DecodeParams& p, const DecodeExtraParams& ap, int head_dim,
                           int cache_dt, int act_dt, cudaStream_t stream);
+// Decode over each request's tokens after its group's shared prefix, partials
+// in slots 1.. of the workspace, then the merge with slot 0 (the prefix
+// pass's); head_dim 128, 16-bit caches.
+cudaError_t launch_decode_cascade(const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                  const DecodeParams& p, const DecodeExtraParams& ap, int head_dim,
+                                  int cache_dt, int act_dt, cudaStream_t stream);
 size_t decode_smem_bytes(int head_dim, int cache_dt);
 cudaError_t launch_append(const AppendParams& p, int cache_dt, int act_dt, cudaStream_t stream);
 // Chain hashes of the full blocks of each request's token ids.
@@ -161,6 +187,12 @@ cudaError_t launch_dequant_pages(const DequantParams& p, int batch, int blocks_p
 cudaError_t launch_extend(const CUtensorMap& kmap, const CUtensorMap& vmap,
                           const CUtensorMap& qmap, const ExtendParams& p, int head_dim,
                           int cache_dt, int act_dt, cudaStream_t stream);
+// The prefix pass: ExtendParams over groups (q_indptr = group offsets into
+// the batch, prefix_lens = the groups' shared prefix lengths); see extend.cu.
+cudaError_t launch_extend_prefix_pass(const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                      const CUtensorMap& qmap, const ExtendParams& p,
+                                      const ExtendPartialParams& pp, int head_dim, int cache_dt,
+                                      int act_dt, cudaStream_t stream);
 bool extend_supported(int head_dim, int cache_dt, int act_dt, int group);
 
 }  // namespace pkv

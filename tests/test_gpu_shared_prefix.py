@@ -1,0 +1,204 @@
+"""GPU parity of pkv_paged_decode_attn_shared_prefix (decode for groups of
+requests that share a cached prefix, the prefix attended once per group on
+the tensor cores and merged by LSE with each request's own tokens) against
+the fp64 oracle's plain decode over every request's whole sequence.
+
+"KV Cache 완전 정리 — PagedAttention vs RadixAttention, SGLang이 빠른 이유",
+section "RadixAttention — SGLang의 혁신" (many requests, one shared prompt);
+"PagedAttention과 RadixAttention으로 LLM KV 캐시 최적화", section 03.
+Groups share their whole prefix blocks (the members' tables point at the
+first member's blocks) and hold copies of the prefix's partial last block, as
+a paged cache stores a shared prefix."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_285_gb300 as pkv
+from paged_kv_cache_285_gb300 import workloads as W
+from tests.pkv_testlib import BF16, F16, assert_attention_close, to_f64
+
+pytestmark = pytest.mark.gpu
+S = W.to_numpy_storage
+
+
+def grouped_case(groups, suffixes, hq, hkv, bs, dt, seed):
+    """groups: [(members, P)]; suffixes: one own-token count per request (>= 0)."""
+    lens = []
+    it = iter(suffixes)
+    for size, prefix in groups:
+        lens += [prefix + next(it) for _ in range(size)]
+    case = W.decode_case(lens, hq, hkv, 128, bs, dt, dt, seed=seed, device="cuda")
+    tables = case.block_tables.cpu()
+    indptr, plens, start = [0], [], 0
+    for size, prefix in groups:
+        full, tail = prefix // bs, prefix % bs
+        for m in range(start + 1, start + size):
+            tables[m, :full] = tables[start, :full]
+            if tail:
+                src, dst = int(tables[start, full]), int(tables[m, full])
+                case.k_cache[dst, :, :tail] = case.k_cache[src, :, :tail]
+                case.v_cache[dst, :, :tail] = case.v_cache[src, :, :tail]
+        start += size
+        indptr.append(start)
+        plens.append(prefix)
+    case.block_tables = tables.to("cuda")
+    gi = torch.tensor(indptr, dtype=torch.int32, device="cuda")
+    gp = torch.tensor(plens, dtype=torch.int32, device="cuda")
+    max_group = max(size for size, _ in groups)
+    max_suffix = max(n - plens[g] for g, (a, e) in enumerate(zip(indptr[:-1], indptr[1:]))
+                     for n in lens[a:e])
+    return case, gi, gp, max_group, max_suffix
+
+
+def run_cascade(case, gi, gp, max_group, max_suffix, splits=0, append=False):
+    b = case.q.shape[0]
+    out = torch.full_like(case.q, float("nan"))
+    lse = torch.full((b, case.num_q_heads), float("nan"), dtype=torch.float32, device="cuda")
+    nbytes = pkv.shared_prefix_decode_workspace_bytes(case.k_cache, b, case.num_q_heads,
+                                                      max_suffix, splits)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    kw = dict(k_new=case.new_k, v_new=case.new_v) if append else {}
+    pkv.paged_decode_attn_shared_prefix(case.k_cache, case.v_cache, case.q, out, case.block_tables,
+                                        case.seq_lens, case.sm_scale, gi, gp, max_group,
+                                        max_suffix, num_splits=splits, lse_out=lse, workspace=ws,
+                                        **kw)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def oracle_ref(case, pools=None, pairs=None):
+    k, v = (S(case.k_cache), S(case.v_cache)) if pools is None else pools
+    ref, ref_lse, st = oracle.paged_decode(k, v, case.cache_dtype, 1.0, 1.0, S(case.q),
+                                           case.act_dtype, case.block_tables.cpu().numpy(),
+                                           case.seq_lens.cpu().numpy(), case.num_q_heads,
+                                           case.sm_scale, pairs=pairs)
+    assert st == 0
+    return ref, ref_lse
+
+
+def check(case, out, lse, what, pools=None):
+    ref, ref_lse = oracle_ref(case, pools)
+    assert_attention_close(to_f64(out), ref, case.act_dtype, what=what)
+    gl = lse.cpu().double().numpy()
+    fin = np.isfinite(ref_lse)
+    assert np.all(np.isfinite(gl) == fin), what
+    assert np.max(np.abs(gl[fin] - ref_lse[fin]), initial=0) <= 1e-3, what
+
+
+def rand_suffixes(n, lo, hi, seed):
+    return np.random.default_rng(seed).integers(lo, hi + 1, n).tolist()
+
+
+CASES = [
+    # (groups [(members, P)], suffix range, hq, hkv, bs, dtype)
+    ([(64, 500)], (1, 300), 32, 8, 16, BF16),
+    ([(1, 0), (5, 100), (70, 1000), (3, 37), (1, 16), (2, 0)], (1, 200), 8, 2, 16, F16),
+    ([(40, 256)], (1, 90), 64, 8, 32, BF16),
+    ([(9, 48), (7, 480)], (1, 70), 8, 8, 16, F16),
+    ([(33, 160), (2, 64)], (1, 50), 16, 8, 32, BF16),
+]
+
+
+@pytest.mark.parametrize("splits", [0, 1, 3])
+@pytest.mark.parametrize("cfg", CASES, ids=lambda c: f"g{len(c[0])}-h{c[2]}x{c[3]}-bs{c[4]}-d{c[5]}")
+def test_groups_match_oracle(cfg, splits):
+    groups, (lo, hi), hq, hkv, bs, dt = cfg
+    nreq = sum(s for s, _ in groups)
+    case, gi, gp, mg, ms = grouped_case(groups, rand_suffixes(nreq, lo, hi, nreq + splits), hq,
+                                        hkv, bs, dt, seed=nreq + hq + splits)
+    out, lse = run_cascade(case, gi, gp, mg, ms, splits)
+    check(case, out, lse, f"{cfg} splits={splits}")
+    assert pkv.get_device_error() == 0
+
+
+def test_members_with_no_own_tokens():
+    # seq_len == the shared prefix (whole blocks): only the prefix pass contributes
+    case, gi, gp, mg, ms = grouped_case([(4, 64), (3, 96)], [0, 5, 0, 31, 0, 0, 1], 8, 2, 16,
+                                        BF16, seed=11)
+    out, lse = run_cascade(case, gi, gp, mg, ms)
+    check(case, out, lse, "no own tokens")
+    assert pkv.get_device_error() == 0
+
+
+def test_fused_append_matches_append_then_oracle():
+    groups = [(20, 320), (6, 40)]
+    suf = rand_suffixes(26, 1, 120, 5)
+    case, gi, gp, mg, ms = grouped_case(groups, suf, 32, 8, 16, BF16, seed=21)
+    k0, v0 = S(case.k_cache), S(case.v_cache)
+    out, lse = run_cascade(case, gi, gp, mg, ms, append=True)
+    kr, vr, st = oracle.kv_append(k0, v0, case.cache_dtype, 1.0, 1.0, S(case.new_k),
+                                  S(case.new_v), case.act_dtype, case.slot_last.cpu().numpy())
+    assert st == 0
+    assert np.array_equal(kr, S(case.k_cache)) and np.array_equal(vr, S(case.v_cache))
+    check(case, out, lse, "fused append", pools=(kr, vr))
+    assert pkv.get_device_error() == 0
+
+
+def test_no_shared_prefix_equals_plain_decode():
+    # every group's prefix 0: the cascade is plain split decode + merge
+    case, gi, gp, mg, ms = grouped_case([(3, 0), (5, 0)], [100, 7, 64, 1, 300, 33, 16, 90], 32, 8,
+                                        16, F16, seed=31)
+    out, lse = run_cascade(case, gi, gp, mg, ms, splits=2)
+    check(case, out, lse, "prefix 0")
+    assert pkv.get_device_error() == 0
+
+
+def test_shared_prefix_decode_workload_sampled():
+    # the benchmark layer: 256 requests, one 1,000-token prompt (62 shared blocks +
+    # an 8-token tail in each request's own block), own tokens U[32, 256]
+    case = W.shared_prefix_decode(device="cuda")
+    b = case.q.shape[0]
+    gi = torch.tensor([0, b], dtype=torch.int32, device="cuda")
+    gp = torch.tensor([1000], dtype=torch.int32, device="cuda")
+    ms = int(case.seq_lens.max()) - 1000
+    out, lse = run_cascade(case, gi, gp, b, ms)
+    pairs = [(r, h) for r in (0, 1, 77, 128, 255) for h in (0, 5, 31)]
+    ref, ref_lse = oracle_ref(case, pairs=pairs)
+    got = np.stack([to_f64(out)[r, h] for r, h in pairs])
+    assert_attention_close(got, ref, case.act_dtype, what="shared prefix workload")
+    gl = np.array([float(lse[r, h]) for r, h in pairs])
+    assert np.max(np.abs(gl - ref_lse)) <= 1e-3
+    # and the plain decode on the same inputs agrees within the same bound
+    plain = torch.empty_like(case.q)
+    ws = torch.empty(max(pkv.decode_workspace_bytes(case.k_cache, b, case.num_q_heads,
+                                                    int(case.seq_lens.max()), 0), 1),
+                     dtype=torch.uint8, device="cuda")
+    pkv.paged_decode_attn(case.k_cache, case.v_cache, case.q, plain, case.block_tables,
+                          case.seq_lens, case.sm_scale, int(case.seq_lens.max()), workspace=ws)
+    torch.cuda.synchronize()
+    d = (to_f64(plain) - to_f64(out))
+    assert np.max(np.abs(d)) <= 8e-3
+    assert pkv.get_device_error() == 0
+
+
+def test_prefix_longer_than_a_member_is_reported():
+    # P_g above one member's seq_len: flagged in the device error word, no fault
+    case, gi, gp, mg, ms = grouped_case([(3, 64)], [40, 40, 40], 8, 2, 16, F16, seed=41)
+    case.seq_lens[2] = 50  # < 64
+    run_cascade(case, gi, gp, mg, ms)
+    assert pkv.get_device_error() == 3
+
+
+def test_unsupported_and_bad_arguments_are_refused_on_the_host():
+    c64 = W.decode_case([40, 50], 4, 1, 64, 16, F16, F16, seed=1, device="cuda")
+    gi = torch.tensor([0, 2], dtype=torch.int32, device="cuda")
+    gp = torch.tensor([32], dtype=torch.int32, device="cuda")
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    with pytest.raises(pkv.PkvError) as e:  # head_dim 64 has no prefix pass
+        pkv.paged_decode_attn_shared_prefix(c64.k_cache, c64.v_cache, c64.q, torch.empty_like(c64.q),
+                                            c64.block_tables, c64.seq_lens, c64.sm_scale, gi, gp,
+                                            2, 20, workspace=ws)
+    assert e.value.status == 2
+    c = W.decode_case([40, 50], 8, 2, 128, 16, BF16, BF16, seed=2, device="cuda")
+    small = torch.empty(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.paged_decode_attn_shared_prefix(c.k_cache, c.v_cache, c.q, torch.empty_like(c.q),
+                                            c.block_tables, c.seq_lens, c.sm_scale, gi, gp, 2, 20,
+                                            workspace=small)
+    assert e.value.status == 3
+    with pytest.raises(pkv.PkvError) as e:  # a negative softmax scale
+        pkv.paged_decode_attn_shared_prefix(c.k_cache, c.v_cache, c.q, torch.empty_like(c.q),
+                                            c.block_tables, c.seq_lens, -0.1, gi, gp, 2, 20,
+                                            workspace=ws)
+    assert e.value.status == 1
