@@ -219,6 +219,12 @@ pkv_status pkv_paged_decode_attn_append(const pkv_cache_desc* desc, void* k_cach
  * workspace:     pkv_shared_prefix_decode_workspace_bytes() bytes, 256-byte
  *                aligned (always needed).
  * q:             16-byte aligned.  Everything else as pkv_paged_decode_attn.
+ * Streams: the prefix pass runs on a side stream the library keeps per device
+ * (highest priority), forked from `stream` by an event at the call and joined
+ * back before the merge, so it overlaps the decode of the members' own
+ * tokens; the call as a whole is ordered on `stream` like any other and can
+ * be captured into a CUDA graph.  Calls on one device from several host
+ * threads are serialised around the fork and join.
  * Supported: head_dim 128, f16 or bf16 cache with the same act dtype,
  * block_size 16/32, num_q_heads/num_kv_heads in {1, 2, 4, 8}, sm_scale > 0.
  * ------------------------------------------------------------------------- */

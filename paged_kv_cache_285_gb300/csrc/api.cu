@@ -24,6 +24,15 @@ struct DeviceState {
   int sm_count = 0;
   int32_t* err = nullptr;
   cudaError_t init_error = cudaSuccess;
+  // side stream of the shared-prefix decode, created on first use: its
+  // prefix pass runs there, beside the decode of the members' own tokens on
+  // the caller's stream (fork / join events order both against the caller's
+  // stream; the mutex keeps concurrent callers' fork and join apart)
+  std::once_flag side_once;
+  std::mutex side_mu;
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  cudaError_t side_error = cudaSuccess;
 };
 DeviceState g_dev[kMaxDevices];
 
@@ -43,6 +52,18 @@ DeviceState* device_state(cudaError_t* e) {
   });
   *e = s->init_error;
   return s->init_error == cudaSuccess ? s : nullptr;
+}
+
+cudaError_t side_stream(DeviceState* s) {
+  std::call_once(s->side_once, [s]() {
+    int least = 0, greatest = 0;
+    cudaError_t r = cudaDeviceGetStreamPriorityRange(&least, &greatest);
+    if (r == cudaSuccess) r = cudaStreamCreateWithPriority(&s->side, cudaStreamNonBlocking, greatest);
+    if (r == cudaSuccess) r = cudaEventCreateWithFlags(&s->fork, cudaEventDisableTiming);
+    if (r == cudaSuccess) r = cudaEventCreateWithFlags(&s->join, cudaEventDisableTiming);
+    s->side_error = r;
+  });
+  return s->side_error;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -358,6 +379,7 @@ pkv_status pkv_paged_decode_attn_shared_prefix(
   const float scale_log2 = (float)((double)sm_scale * 1.4426950408889634);
 
   // 1. the shared prefixes, once per group, on the tensor cores -> slot 0
+  //    (on the side stream, beside step 2)
   ExtendParams pe;
   pe.q_indptr = group_indptr;
   pe.prefix_lens = group_prefix_lens;
@@ -392,12 +414,24 @@ pkv_status pkv_paged_decode_attn_shared_prefix(
   pp.lse = ws_lse;
   pp.o_stride = (int64_t)slots * desc->head_dim;
   pp.lse_stride = slots;
-  e = launch_extend_prefix_pass(kmap, vmap, qmap, pe, pp, desc->head_dim, (int)desc->cache_dtype,
-                                (int)act_dtype, stream);
+  if (side_stream(ds) != cudaSuccess) return PKV_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(ds->side_mu);
+  e = cudaEventRecord(ds->fork, stream);
   if (e != cudaSuccess) return PKV_ERR_CUDA;
+  e = cudaStreamWaitEvent(ds->side, ds->fork, 0);
+  if (e == cudaSuccess)
+    e = launch_extend_prefix_pass(kmap, vmap, qmap, pe, pp, desc->head_dim,
+                                  (int)desc->cache_dtype, (int)act_dtype, ds->side);
+  // join even after a failure, so that the caller's stream (or a capture in
+  // progress) never keeps the side stream forked
+  const cudaError_t ej = cudaEventRecord(ds->join, ds->side);
+  if (e != cudaSuccess || ej != cudaSuccess) {
+    cudaStreamWaitEvent(stream, ds->join, 0);
+    return PKV_ERR_CUDA;
+  }
 
   // 2. each request's own tokens (current token appended first) -> slots 1..,
-  //    then the merge of all slots
+  //    then, once the prefix pass has joined, the merge of all slots
   DecodeParams p;
   p.block_tables = block_tables;
   p.seq_lens = seq_lens;
@@ -429,7 +463,7 @@ pkv_status pkv_paged_decode_attn_shared_prefix(
   ap.group_prefix_lens = group_prefix_lens;
   ap.num_groups = num_groups;
   e = launch_decode_cascade(kmap, vmap, p, ap, desc->head_dim, (int)desc->cache_dtype,
-                            (int)act_dtype, stream);
+                            (int)act_dtype, stream, ds->join);
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

@@ -584,11 +584,12 @@ constexpr int stages_for() {
   return ns < 2 ? 2 : (ns > 8 ? 8 : ns);
 }
 
-template <int HD, int CT, int AT, bool CASC>
+// NSO > 0 overrides the pipeline depth (stages per warp).
+template <int HD, int CT, int AT, bool CASC, int NSO = 0>
 cudaError_t launch_decode_t(const CUtensorMap& kmap, const CUtensorMap& vmap,
                             const DecodeParams& p, const DecodeExtraParams& ap,
-                            cudaStream_t stream) {
-  constexpr int NS = stages_for<HD, CT>();
+                            cudaStream_t stream, cudaEvent_t merge_after = nullptr) {
+  constexpr int NS = NSO > 0 ? NSO : stages_for<HD, CT>();
   using C = DecodeCfg<HD, CT, kNW, NS>;
   auto kern = decode_kernel<HD, CT, AT, kNW, NS, CASC>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -597,6 +598,8 @@ cudaError_t launch_decode_t(const CUtensorMap& kmap, const CUtensorMap& vmap,
   kern<<<grid, kNW * 32, C::SMEM, stream>>>(kmap, vmap, p, ap);
   e = cudaGetLastError();
   if (e != cudaSuccess || (!CASC && p.num_splits <= 1)) return e;
+  if (merge_after != nullptr && (e = cudaStreamWaitEvent(stream, merge_after, 0)) != cudaSuccess)
+    return e;
   const int64_t pairs = (int64_t)p.batch * p.num_q_heads;
   merge_kernel<HD, AT, CASC><<<(unsigned)((pairs + 3) / 4), 128, 0, stream>>>(p, ap);
   return cudaGetLastError();
@@ -636,12 +639,24 @@ cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap, cons
 
 cudaError_t launch_decode_cascade(const CUtensorMap& kmap, const CUtensorMap& vmap,
                                   const DecodeParams& p, const DecodeExtraParams& ap, int head_dim,
-                                  int cache_dt, int act_dt, cudaStream_t stream) {
+                                  int cache_dt, int act_dt, cudaStream_t stream,
+                                  cudaEvent_t merge_after) {
   if (head_dim != 128 || act_dt != cache_dt) return cudaErrorInvalidValue;
   if (!ap.group_indptr || !ap.group_prefix_lens || ap.num_groups <= 0 || !p.ws_o)
     return cudaErrorInvalidValue;
-  if (cache_dt == DT_F16) return launch_decode_t<128, DT_F16, DT_F16, true>(kmap, vmap, p, ap, stream);
-  if (cache_dt == DT_BF16) return launch_decode_t<128, DT_BF16, DT_BF16, true>(kmap, vmap, p, ap, stream);
+  // Short runs per CTA (the members' own tokens are typically a few hundred):
+  // one stage per warp, so that four CTAs fit on an SM instead of two and
+  // their fixed costs (setup, first copy, epilogue) overlap; measured 13 %
+  // faster at 320 tokens per CTA.  Long runs keep the deeper pipeline.
+  const bool short_runs = p.chunk <= 512;
+  if (cache_dt == DT_F16)
+    return short_runs
+               ? launch_decode_t<128, DT_F16, DT_F16, true, 1>(kmap, vmap, p, ap, stream, merge_after)
+               : launch_decode_t<128, DT_F16, DT_F16, true>(kmap, vmap, p, ap, stream, merge_after);
+  if (cache_dt == DT_BF16)
+    return short_runs
+               ? launch_decode_t<128, DT_BF16, DT_BF16, true, 1>(kmap, vmap, p, ap, stream, merge_after)
+               : launch_decode_t<128, DT_BF16, DT_BF16, true>(kmap, vmap, p, ap, stream, merge_after);
   return cudaErrorInvalidValue;
 }
 

@@ -145,11 +145,13 @@ cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap,
                           const DecodeParams& p, const DecodeExtraParams& ap, int head_dim,
                           int cache_dt, int act_dt, cudaStream_t stream);
 // Decode over each request's tokens after its group's shared prefix, partials
-// in slots 1.. of the workspace, then the merge with slot 0 (the prefix
-// pass's); head_dim 128, 16-bit caches.
+// in slots 1.. of the workspace, then (after `merge_after`, the prefix pass's
+// completion, when not null) the merge with slot 0; head_dim 128, 16-bit
+// caches.
 cudaError_t launch_decode_cascade(const CUtensorMap& kmap, const CUtensorMap& vmap,
                                   const DecodeParams& p, const DecodeExtraParams& ap, int head_dim,
-                                  int cache_dt, int act_dt, cudaStream_t stream);
+                                  int cache_dt, int act_dt, cudaStream_t stream,
+                                  cudaEvent_t merge_after);
 size_t decode_smem_bytes(int head_dim, int cache_dt);
 cudaError_t launch_append(const AppendParams& p, int cache_dt, int act_dt, cudaStream_t stream);
 // Chain hashes of the full blocks of each request's token ids.

@@ -97,6 +97,10 @@ CASES = [
     ([(40, 256)], (1, 90), 64, 8, 32, BF16),
     ([(9, 48), (7, 480)], (1, 70), 8, 8, 16, F16),
     ([(33, 160), (2, 64)], (1, 50), 16, 8, 32, BF16),
+    # long own-token runs: with one split a CTA covers > 512 tokens (the deeper
+    # pipeline variant of the decode)
+    ([(12, 200)], (600, 1000), 16, 8, 16, BF16),
+    ([(4, 96), (6, 32)], (520, 700), 8, 2, 32, F16),
 ]
 
 
