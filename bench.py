@@ -339,19 +339,36 @@ def run_decode_bench(args, world, rank, local):
 
 
 def e2e_decode(case, pkv, max_len, ws, out, stream, K, world):
-    host = {}
+    """The fused decode step through the public API from host buffers: each step's
+    inputs (q, the current token's K/V, seq_lens, block tables) sit in one pinned
+    staging buffer (256-byte-aligned views) and go to the device in one copy; the
+    output comes back in one copy."""
     names = ["q", "new_k", "new_v", "seq_lens", "block_tables"]
+    offs, total = {}, 0
     for n in names:
         t = getattr(case, n)
-        host[n] = t.to("cpu").pin_memory()
-    dev_t = {n: torch.empty_like(getattr(case, n)) for n in names}
+        offs[n] = total
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    host_buf = torch.empty(total, dtype=torch.uint8).pin_memory()
+    dev_buf = torch.empty(total, dtype=torch.uint8, device=out.device)
+
+    def views(buf):
+        v = {}
+        for n in names:
+            t = getattr(case, n)
+            nb = t.numel() * t.element_size()
+            v[n] = buf[offs[n]:offs[n] + nb].view(t.dtype).view(t.shape)
+        return v
+
+    host, dev_t = views(host_buf), views(dev_buf)
+    for n in names:
+        host[n].copy_(getattr(case, n).cpu())
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+    h2d = total
     d2h = out_h.numel() * out_h.element_size()
 
     def step():
-        for n in names:
-            dev_t[n].copy_(host[n], non_blocking=True)
+        dev_buf.copy_(host_buf, non_blocking=True)
         pkv.paged_decode_attn_append(case.k_cache, case.v_cache, dev_t["new_k"], dev_t["new_v"],
                                      dev_t["q"], out, dev_t["block_tables"], dev_t["seq_lens"],
                                      case.sm_scale, max_len, k_scale=case.k_scale,
