@@ -131,7 +131,9 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::AREA);
 
-  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  // split is the slowest grid dimension: every request's first chunk runs
+  // before any second chunk, so the partial and empty last splits form the tail
+  const int g = blockIdx.x, b = blockIdx.y, split = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
   const int G = p.group;
@@ -578,9 +580,13 @@ constexpr int kNW = 4;
 
 template <int HD, int CT>
 constexpr int stages_for() {
-  // ~24 KB of copies in flight per warp; 2 CTAs per SM fit beside each other.
+  // ~12 KB of copies in flight per warp (at least two stages): CTAs of 48-64 KB,
+  // so three or four share an SM (four is also the register limit at ~123
+  // registers).  More CTAs in flight beat deeper pipelines: on GB300, fp8 d128
+  // at 3 stages took 180 us where 6 took 206 us (70B-shaped layer), bf16 d128
+  // at 2 stages 98.6 us where 3 took 99.2 us (8B-shaped layer).
   constexpr int st = DecodeCfg<HD, CT, kNW, 1>::STAGEB;
-  constexpr int ns = (24 * 1024) / st;
+  constexpr int ns = (12 * 1024) / st;
   return ns < 2 ? 2 : (ns > 8 ? 8 : ns);
 }
 
@@ -594,7 +600,7 @@ cudaError_t launch_decode_t(const CUtensorMap& kmap, const CUtensorMap& vmap,
   auto kern = decode_kernel<HD, CT, AT, kNW, NS, CASC>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.num_splits, p.num_kv_heads, p.batch);
+  dim3 grid(p.num_kv_heads, p.batch, p.num_splits);
   kern<<<grid, kNW * 32, C::SMEM, stream>>>(kmap, vmap, p, ap);
   e = cudaGetLastError();
   if (e != cudaSuccess || (!CASC && p.num_splits <= 1)) return e;
