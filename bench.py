@@ -397,7 +397,8 @@ def e2e_decode(case, pkv, max_len, ws, out, stream, K, world):
 
 def run_extend_bench(args, dev, bf16, bf16_sus, peak_src):
     """paged_extend_attn on 256 requests x 100 suffix tokens over a shared 1,900-token
-    prefix (useful causal flops only), with the suffix's kv_append in the step."""
+    prefix (useful causal flops only); the step with the suffix's kv_append as a
+    separate launch and as paged_extend_attn_append (written by the extend kernel)."""
     import paged_kv_cache_285_gb300 as pkv
     from paged_kv_cache_285_gb300 import workloads as W
     try:
@@ -420,14 +421,20 @@ def run_extend_bench(args, dev, bf16, bf16_sus, peak_src):
         extend()
     except pkv.PkvError as e:
         return {"status": "not built", "error": str(e)}
+    def fused():
+        pkv.paged_extend_attn_append(case.k_cache, case.v_cache, case.suffix_k, case.suffix_v,
+                                     case.q, out, case.q_indptr, case.prefix_lens,
+                                     case.block_tables, case.sm_scale, Sfx, P + Sfx)
+
     for _ in range(3):
         append()
         extend()
+        fused()
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
     n = max(5, min(50, args.steps))
     flush = L2Flush(dev)
-    t_ext = t_step = 0.0
+    t_ext = t_step = t_fused = 0.0
     for _ in range(n):
         flush()
         e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
@@ -439,8 +446,16 @@ def run_extend_bench(args, dev, bf16, bf16_sus, peak_src):
         e2.synchronize()
         t_ext += e1.elapsed_time(e2)
         t_step += e0.elapsed_time(e2)
+        flush()
+        e3, e4 = (torch.cuda.Event(enable_timing=True) for _ in range(2))
+        e3.record(stream)
+        fused()
+        e4.record(stream)
+        e4.synchronize()
+        t_fused += e3.elapsed_time(e4)
     t_ext /= n
     t_step /= n
+    t_fused /= n
     hq, d = case.num_q_heads, case.head_dim
     keys = sum(P + i + 1 for i in range(Sfx))
     flops = 4.0 * d * hq * keys * B
@@ -448,6 +463,7 @@ def run_extend_bench(args, dev, bf16, bf16_sus, peak_src):
     return {"workload": "shared_prefix_extend", "batch": B, "prefix": P, "suffix": Sfx,
             "num_q_heads": hq, "num_kv_heads": case.num_kv_heads, "head_dim": d,
             "ms_per_call": round(t_ext, 5), "ms_per_step_with_append": round(t_step, 5),
+            "ms_per_step_fused_append": round(t_fused, 5),
             "tflops": round(tf, 1), "useful_flops_per_call": flops,
             "roofline": {"kernel": "paged_extend_attn", "bound": "tensor", "achieved": round(tf, 1),
                          "peak": bf16, "unit": "TFLOP/s", "frac": round(tf / bf16, 4),

@@ -326,6 +326,38 @@ pkv_status pkv_paged_extend_attn(const pkv_cache_desc* desc, const void* k_cache
                                  cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * pkv_paged_extend_attn_append -- suffix prefill with the suffix's K/V written
+ * into the cache by the same call.
+ *
+ * "KV Cache에 대해 알아보자 (Feat. Attention)", §3: the K/V of every processed
+ * token go into the cache; "PagedAttention과 RadixAttention으로 LLM KV 캐시
+ * 최적화", section 03: only the suffix after the cached prefix is computed.
+ * Same result and same cache bytes as pkv_kv_append of k_new/v_new into
+ * positions prefix_lens[b] + i of request b (physical block
+ * block_tables[b][(prefix_lens[b]+i)/bs], offset (prefix_lens[b]+i) % bs)
+ * followed by pkv_paged_extend_attn, in one call without a slot mapping: the
+ * append kernel derives each row's slot from q_indptr, prefix_lens and the
+ * block table, then the extend kernel runs (two launches in stream order).
+ * Writing the rows from inside the extend kernel was built and measured
+ * slower (the extra warp code displaced the softmax loop's instructions).
+ *
+ * k_new, v_new:  [total_q_rows][num_kv_heads][head_dim], the cache dtype,
+ *                device, 16-byte aligned; row q_indptr[b] + i is suffix token
+ *                i of request b.
+ * Everything else as pkv_paged_extend_attn.  16-bit caches only
+ * (PKV_ERR_UNSUPPORTED for fp8).  A suffix slot whose block id lies outside
+ * the pool is not written and is reported in the device error word.
+ * ------------------------------------------------------------------------- */
+pkv_status pkv_paged_extend_attn_append(const pkv_cache_desc* desc, void* k_cache, void* v_cache,
+                                        const void* k_new, const void* v_new, const void* q,
+                                        void* out, pkv_dtype act_dtype, const int32_t* q_indptr,
+                                        const int32_t* prefix_lens, const int32_t* block_tables,
+                                        int32_t max_blocks_per_seq, int32_t batch,
+                                        int32_t num_q_heads, float sm_scale, int32_t total_q_rows,
+                                        int32_t max_suffix_len, int32_t max_total_len,
+                                        float* lse_out, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Prefix index (host): radix tree over token ids with leaf-first LRU eviction.
  *
  * "PagedAttention과 RadixAttention으로 LLM KV 캐시 최적화", section 03: the KV

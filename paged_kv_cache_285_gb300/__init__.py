@@ -11,11 +11,13 @@ The three calls (names as in pkv.h without the ``pkv_`` prefix):
                           (GQA, split-KV, online softmax, LSE merge);
   * paged_extend_attn  -- suffix prefill over cached prefix blocks + causal
                           suffix.
-Also: paged_decode_attn_append (decode with the current token appended by the
-decode kernel), paged_decode_attn_shared_prefix (decode for groups of requests
-sharing a prefix, the prefix attended once per group), RadixIndex (the host prefix index that hands out block
-tables and prefix lengths; host int32 arrays in, host arrays out) and
-chain_hash (salted chain hashes of full blocks, as block identifiers).
+Also: paged_decode_attn_append and paged_extend_attn_append (the new tokens'
+K/V written into the cache by the same call; in decode by the attention
+kernel itself), paged_decode_attn_shared_prefix
+(decode for groups of requests sharing a prefix, the prefix attended once per
+group), RadixIndex (the host prefix index that hands out block tables and
+prefix lengths; host int32 arrays in, host arrays out) and chain_hash (salted
+chain hashes of full blocks, as block identifiers).
 """
 from __future__ import annotations
 
@@ -29,7 +31,8 @@ __all__ = ["F16", "BF16", "FP8_E4M3", "PkvError", "CacheDesc", "lib_path", "load
            "kv_append", "paged_decode_attn", "paged_extend_attn", "decode_workspace_bytes",
            "extend_workspace_bytes", "get_device_error", "status_string", "version",
            "paged_decode_attn_append", "RadixIndex", "NO_SPACE", "chain_hash",
-           "paged_decode_attn_shared_prefix", "shared_prefix_decode_workspace_bytes"]
+           "paged_decode_attn_shared_prefix", "shared_prefix_decode_workspace_bytes",
+           "paged_extend_attn_append"]
 
 F16, BF16, FP8_E4M3 = 0, 1, 2
 NO_SPACE = 5  # PKV_ERR_NO_SPACE
@@ -89,6 +92,9 @@ def load():
         lib.pkv_paged_extend_attn.argtypes = [D, P, P, P, P, ctypes.c_int, P, P, P, I32, I32, I32,
                                               F, I32, I32, I32, P, P, SZ, P]
         lib.pkv_paged_extend_attn.restype = ctypes.c_int
+        lib.pkv_paged_extend_attn_append.argtypes = [D, P, P, P, P, P, P, ctypes.c_int, P, P, P, I32,
+                                                     I32, I32, F, I32, I32, I32, P, P]
+        lib.pkv_paged_extend_attn_append.restype = ctypes.c_int
         lib.pkv_status_string.argtypes = [ctypes.c_int]
         lib.pkv_status_string.restype = ctypes.c_char_p
         lib.pkv_get_device_error.argtypes = [ctypes.POINTER(I32), I32, P]
@@ -283,6 +289,24 @@ def paged_extend_attn(k_cache, v_cache, q, out, q_indptr, prefix_lens, block_tab
                                    int(max_total_len), _ptr(lse_out), _ptr(workspace), ws_bytes,
                                    _stream(stream))
     _check(st, "pkv_paged_extend_attn")
+
+
+def paged_extend_attn_append(k_cache, v_cache, k_new, v_new, q, out, q_indptr, prefix_lens,
+                             block_tables, sm_scale, max_suffix_len, max_total_len, lse_out=None,
+                             stream=None):
+    """pkv_paged_extend_attn_append: k_new/v_new [sum S, Hkv, D] (the cache dtype) are written
+    to positions prefix_lens[b] + i and attended in the same call (16-bit caches)."""
+    lib = load()
+    desc = _desc(k_cache, 1.0, 1.0)
+    rows, hq, _ = q.shape
+    batch = int(prefix_lens.shape[0])
+    st = lib.pkv_paged_extend_attn_append(ctypes.byref(desc), _ptr(k_cache), _ptr(v_cache),
+                                          _ptr(k_new), _ptr(v_new), _ptr(q), _ptr(out),
+                                          _dtype_code(q), _ptr(q_indptr), _ptr(prefix_lens),
+                                          _ptr(block_tables), int(block_tables.shape[1]), batch,
+                                          hq, float(sm_scale), rows, int(max_suffix_len),
+                                          int(max_total_len), _ptr(lse_out), _stream(stream))
+    _check(st, "pkv_paged_extend_attn_append")
 
 
 def chain_hash(tokens, token_indptr, block_size, hashes, salts=None, stream=None):

@@ -274,7 +274,7 @@ pkv_status pkv_kv_append(const pkv_cache_desc* desc, void* k_cache, void* v_cach
   cudaError_t e;
   DeviceState* ds = device_state(&e);
   if (!ds) return PKV_ERR_CUDA;
-  AppendParams p;
+  AppendParams p{};
   p.k_cache = k_cache;
   p.v_cache = v_cache;
   p.k_new = k_new;
@@ -409,7 +409,7 @@ pkv_status pkv_paged_decode_attn_shared_prefix(
   pe.div_hkv = make_fastdiv((uint32_t)desc->num_kv_heads);
   pe.div_req = make_fastdiv(pairs * (uint32_t)desc->num_kv_heads);
   pe.num_ctas = (int)std::min<int64_t>(items, ds->sm_count > 0 ? ds->sm_count : 1);
-  ExtendPartialParams pp;
+  ExtendPartialParams pp{};
   pp.o = ws_o;
   pp.lse = ws_lse;
   pp.o_stride = (int64_t)slots * desc->head_dim;
@@ -572,14 +572,19 @@ size_t pkv_extend_workspace_bytes(const pkv_cache_desc* desc, int32_t batch, int
   return l.total;
 }
 
-pkv_status pkv_paged_extend_attn(const pkv_cache_desc* desc, const void* k_cache,
-                                 const void* v_cache, const void* q, void* out,
-                                 pkv_dtype act_dtype, const int32_t* q_indptr,
-                                 const int32_t* prefix_lens, const int32_t* block_tables,
-                                 int32_t max_blocks_per_seq, int32_t batch, int32_t num_q_heads,
-                                 float sm_scale, int32_t total_q_rows, int32_t max_suffix_len,
-                                 int32_t max_total_len, float* lse_out, void* workspace,
-                                 size_t workspace_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+// Extend, optionally with the suffix's K/V (k_new/v_new, [rows][Hkv][D] in
+// the cache dtype) written into the cache by the extend kernel.
+static pkv_status extend_common(const pkv_cache_desc* desc, const void* k_cache,
+                                const void* v_cache, const void* k_new, const void* v_new,
+                                const void* q, void* out, pkv_dtype act_dtype,
+                                const int32_t* q_indptr, const int32_t* prefix_lens,
+                                const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                int32_t batch, int32_t num_q_heads, float sm_scale,
+                                int32_t total_q_rows, int32_t max_suffix_len,
+                                int32_t max_total_len, float* lse_out, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream) {
   pkv_status st = check_desc(desc);
   if (st != PKV_OK) return st;
   if ((st = check_act(desc, act_dtype)) != PKV_OK) return st;
@@ -667,9 +672,67 @@ pkv_status pkv_paged_extend_attn(const pkv_cache_desc* desc, const void* k_cache
   p.div_hkv = make_fastdiv((uint32_t)desc->num_kv_heads);
   p.div_req = make_fastdiv(pairs * (uint32_t)desc->num_kv_heads);
   p.num_ctas = (int)std::min<int64_t>(items, ds->sm_count > 0 ? ds->sm_count : 1);
+  if (k_new) {
+    // the suffix's K/V first (its slots computed from the extend layout), then
+    // the extend kernel reads them back; two launches in stream order
+    AppendParams ap{};
+    ap.k_cache = const_cast<void*>(k_cache);
+    ap.v_cache = const_cast<void*>(v_cache);
+    ap.k_new = k_new;
+    ap.v_new = v_new;
+    ap.slots = nullptr;
+    ap.err = ds->err;
+    ap.num_tokens = total_q_rows;
+    ap.num_kv_heads = desc->num_kv_heads;
+    ap.head_dim = desc->head_dim;
+    ap.block_size = desc->block_size;
+    ap.num_blocks = desc->num_blocks;
+    ap.k_scale = desc->k_scale;
+    ap.v_scale = desc->v_scale;
+    ap.q_indptr = q_indptr;
+    ap.prefix_lens = prefix_lens;
+    ap.block_tables = block_tables;
+    ap.batch = batch;
+    ap.max_blocks = max_blocks_per_seq;
+    e = launch_append(ap, (int)desc->cache_dtype, (int)act_dtype, stream);
+    if (e != cudaSuccess) return PKV_ERR_CUDA;
+  }
   e = launch_extend(kmap, vmap, qmap, p, desc->head_dim, (int)desc16.cache_dtype, (int)act_dtype,
                     stream);
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+extern "C" {
+
+pkv_status pkv_paged_extend_attn(const pkv_cache_desc* desc, const void* k_cache,
+                                 const void* v_cache, const void* q, void* out,
+                                 pkv_dtype act_dtype, const int32_t* q_indptr,
+                                 const int32_t* prefix_lens, const int32_t* block_tables,
+                                 int32_t max_blocks_per_seq, int32_t batch, int32_t num_q_heads,
+                                 float sm_scale, int32_t total_q_rows, int32_t max_suffix_len,
+                                 int32_t max_total_len, float* lse_out, void* workspace,
+                                 size_t workspace_bytes, cudaStream_t stream) {
+  return extend_common(desc, k_cache, v_cache, nullptr, nullptr, q, out, act_dtype, q_indptr,
+                       prefix_lens, block_tables, max_blocks_per_seq, batch, num_q_heads,
+                       sm_scale, total_q_rows, max_suffix_len, max_total_len, lse_out, workspace,
+                       workspace_bytes, stream);
+}
+
+pkv_status pkv_paged_extend_attn_append(const pkv_cache_desc* desc, void* k_cache, void* v_cache,
+                                        const void* k_new, const void* v_new, const void* q,
+                                        void* out, pkv_dtype act_dtype, const int32_t* q_indptr,
+                                        const int32_t* prefix_lens, const int32_t* block_tables,
+                                        int32_t max_blocks_per_seq, int32_t batch,
+                                        int32_t num_q_heads, float sm_scale, int32_t total_q_rows,
+                                        int32_t max_suffix_len, int32_t max_total_len,
+                                        float* lse_out, cudaStream_t stream) {
+  if (!k_new || !v_new) return PKV_ERR_INVALID_ARG;
+  if (check_desc(desc) == PKV_OK && desc->cache_dtype == PKV_FP8_E4M3) return PKV_ERR_UNSUPPORTED;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16)) return PKV_ERR_INVALID_ARG;
+  return extend_common(desc, k_cache, v_cache, k_new, v_new, q, out, act_dtype, q_indptr,
+                       prefix_lens, block_tables, max_blocks_per_seq, batch, num_q_heads,
+                       sm_scale, total_q_rows, max_suffix_len, max_total_len, lse_out, nullptr, 0,
+                       stream);
 }
 
 }  // extern "C"

@@ -62,7 +62,7 @@ struct AppendParams {
   void* v_cache;
   const void* k_new;
   const void* v_new;
-  const int64_t* slots;
+  const int64_t* slots;          // null: slots from the extend layout below
   int32_t* err;
   int64_t num_tokens;
   int num_kv_heads;
@@ -71,6 +71,13 @@ struct AppendParams {
   int num_blocks;
   float k_scale;
   float v_scale;
+  // slots == null: token t is suffix row t of an extend call (request b with
+  // q_indptr[b] <= t < q_indptr[b+1]) at position prefix_lens[b] + t - q_indptr[b]
+  const int32_t* q_indptr;
+  const int32_t* prefix_lens;
+  const int32_t* block_tables;
+  int batch;
+  int max_blocks;
 };
 
 // Division of unsigned n < 2^31 by a divisor fixed for a launch, as a

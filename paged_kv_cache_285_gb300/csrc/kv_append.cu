@@ -34,7 +34,26 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
   const int64_t row = idx / vpr;
   const int g = (int)(row % p.num_kv_heads);
   const int64_t t = row / p.num_kv_heads;
-  const int64_t slot = p.slots[t];
+  int64_t slot;
+  if (p.slots) {
+    slot = p.slots[t];
+  } else {
+    int lo = 0, hi = p.batch;  // the request of suffix row t
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(p.q_indptr + mid) <= t) lo = mid;
+      else hi = mid;
+    }
+    const int64_t pos = (int64_t)__ldg(p.prefix_lens + lo) + (t - __ldg(p.q_indptr + lo));
+    const int64_t lb = pos / p.block_size;
+    if (pos < 0 || lb >= p.max_blocks) {
+      if (v == 0 && p.err) atomicCAS(p.err, 0, 3);
+      return;
+    }
+    const int32_t b = __ldg(p.block_tables + (int64_t)lo * p.max_blocks + lb);
+    // a negative block id is outside the pool too (reported below)
+    slot = (b < 0 ? (int64_t)p.num_blocks : (int64_t)b) * p.block_size + pos % p.block_size;
+  }
   if (slot < 0) return;
   const int64_t blk = slot / p.block_size, off = slot % p.block_size;
   if (blk >= p.num_blocks) {
