@@ -52,10 +52,22 @@ def peaks():
 
 
 def src_hash(*rel):
+    """Hash of the sources a kernel is built from; "path#A,B" takes only the
+    definitions of structs A and B from that file (the parameter layouts the
+    kernel reads)."""
     h = hashlib.sha256()
     for r in rel:
-        with open(os.path.join(ROOT, r), "rb") as f:
-            h.update(f.read())
+        path, _, structs = r.partition("#")
+        with open(os.path.join(ROOT, path), "rb") as f:
+            data = f.read()
+        if structs:
+            text = data.decode("utf-8")
+            parts = []
+            for name in structs.split(","):
+                i = text.index("struct " + name + " {")
+                parts.append(text[i:text.index("\n};", i) + 3])
+            data = "\n".join(parts).encode("utf-8")
+        h.update(data)
     return h.hexdigest()[:16]
 
 
@@ -312,7 +324,8 @@ def run_decode_bench(args, world, rank, local):
     traffic = profiled_traffic("decode_kernel_llama3_8b_layer.md",
                                ["paged_kv_cache_285_gb300/csrc/decode.cu",
                                 "paged_kv_cache_285_gb300/csrc/ptx.cuh",
-                                "paged_kv_cache_285_gb300/csrc/internal.h"]) \
+                                "paged_kv_cache_285_gb300/csrc/internal.h"
+                                "#DecodeParams,DecodeExtraParams"]) \
         if args.workload == "llama3_8b_layer" else None
     res["roofline"] = {"kernel": "paged_decode_attn (decode_kernel + merge_kernel)",
                        "bound": "hbm", "achieved": round(dec_gbs, 1), "peak": hbm,
@@ -473,7 +486,8 @@ def run_extend_bench(args, dev, bf16, bf16_sus, peak_src):
                              ["paged_kv_cache_285_gb300/csrc/extend.cu",
                               "paged_kv_cache_285_gb300/csrc/ptx.cuh",
                               "paged_kv_cache_285_gb300/csrc/tcgen05.cuh",
-                              "paged_kv_cache_285_gb300/csrc/internal.h"])}}
+                              "paged_kv_cache_285_gb300/csrc/internal.h"
+                              "#ExtendParams,ExtendPartialParams,FastDiv"])}}
 
 
 def run_prefix_index_bench(n_requests=20000, seed=0):
