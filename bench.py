@@ -470,6 +470,10 @@ def run_extend_bench(args, dev, bf16, bf16_sus, peak_src):
     t_step /= n
     t_fused /= n
     hq, d = case.num_q_heads, case.head_dim
+    # the suffix's kv_append: K and V rows read from the inputs and written to the cache
+    t_app = t_step - t_ext
+    app_bytes = rows * case.num_kv_heads * d * 2 * 2 * 2 + 8 * rows
+    hbm = peaks()[0]
     keys = sum(P + i + 1 for i in range(Sfx))
     flops = 4.0 * d * hq * keys * B
     tf = flops / (t_ext * 1e-3) / 1e12
@@ -477,6 +481,9 @@ def run_extend_bench(args, dev, bf16, bf16_sus, peak_src):
             "num_q_heads": hq, "num_kv_heads": case.num_kv_heads, "head_dim": d,
             "ms_per_call": round(t_ext, 5), "ms_per_step_with_append": round(t_step, 5),
             "ms_per_step_fused_append": round(t_fused, 5),
+            "kv_append": {"tokens": rows, "ms": round(t_app, 5), "bytes": app_bytes,
+                          "gbs": round(app_bytes / (t_app * 1e-3) / 1e9, 1),
+                          "frac_of_hbm": round(app_bytes / (t_app * 1e-3) / 1e9 / hbm, 4)},
             "tflops": round(tf, 1), "useful_flops_per_call": flops,
             "roofline": {"kernel": "paged_extend_attn", "bound": "tensor", "achieved": round(tf, 1),
                          "peak": bf16, "unit": "TFLOP/s", "frac": round(tf / bf16, 4),
