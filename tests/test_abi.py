@@ -110,3 +110,43 @@ class torch_free_cache:
 
     def dim(self):
         return 4
+
+
+def _shared(lib, desc, hq=8, act=1, batch=2, groups=1, scale=0.1, ws=None, ws_bytes=0):
+    return lib.pkv_paged_decode_attn_shared_prefix(
+        ctypes.byref(desc), FAKE, FAKE, None, None, FAKE, FAKE, act, FAKE, 4, FAKE, batch, hq,
+        scale, FAKE, FAKE, groups, 2, 100, 0, None, ws, ws_bytes, None)
+
+
+def test_shared_prefix_decode_argument_errors(lib):
+    assert _shared(lib, _desc(head_dim=64)) == 2              # no prefix pass at d64
+    assert _shared(lib, _desc(cache_dtype=2)) == 2            # fp8 cache
+    assert _shared(lib, _desc(), scale=-0.1) == 1             # the prefix pass needs scale > 0
+    assert _shared(lib, _desc(), hq=3) == 1                   # Hq % Hkv != 0
+    assert _shared(lib, _desc(), groups=0) == 1               # requests but no group
+    assert _shared(lib, _desc(), batch=0) == 0                # empty batch: nothing to do
+    # forced 2 splits over the members' own tokens (bound 100, + 15 for the prefix rounded
+    # down to whole blocks): 8 tiles -> 4 per split; slots = 2 + the prefix's
+    d = _desc()
+    assert lib.pkv_shared_prefix_decode_workspace_bytes(ctypes.byref(d), 2, 8, 100, 2) == \
+        2 * 8 * 3 * 128 * 4 + 2 * 8 * 3 * 4
+
+
+def test_chain_hash_and_extend_append_argument_errors(lib):
+    call = lambda tokens=FAKE, indptr=FAKE, b=2, bs=16, hashes=FAKE, mb=8: lib.pkv_chain_hash(
+        tokens, indptr, b, bs, None, hashes, mb, None)
+    assert call(bs=0) == 1
+    assert call(bs=5000) == 1
+    assert call(b=-1) == 1
+    assert call(b=0) == 0 and call(mb=0) == 0
+    assert call(tokens=None) == 1
+    import torch
+    with pytest.raises(ValueError):  # int64 token ids: refused by the binding
+        pkv.chain_hash(torch.zeros(4, dtype=torch.int64), torch.zeros(2, dtype=torch.int32), 16,
+                       torch.zeros((1, 1), dtype=torch.int64))
+    d8 = _desc(cache_dtype=2)
+    ext = lambda desc, kn=FAKE: lib.pkv_paged_extend_attn_append(
+        ctypes.byref(desc), FAKE, FAKE, kn, kn, FAKE, FAKE, 1, FAKE, FAKE, FAKE, 4, 1, 4, 0.1, 10,
+        10, 100, None, None)
+    assert ext(d8) == 2                                       # fp8 cache
+    assert ext(_desc(), kn=None) == 1                         # the suffix K/V are required
