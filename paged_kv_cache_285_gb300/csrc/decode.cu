@@ -109,7 +109,9 @@ __device__ __forceinline__ float to_f32_bits(uint32_t bits16) {
 
 // Shared-prefix length of request b's group (group_indptr is non-decreasing
 // from 0 to batch; the search stays inside the arrays whatever they hold).
+// A request that no group covers gets -1: no shared prefix, reported.
 __device__ __forceinline__ int group_prefix_len(const DecodeExtraParams& ap, int b) {
+  if (b < __ldg(ap.group_indptr) || b >= __ldg(ap.group_indptr + ap.num_groups)) return -1;
   int lo = 0, hi = ap.num_groups;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;

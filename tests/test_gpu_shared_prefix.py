@@ -206,3 +206,15 @@ def test_unsupported_and_bad_arguments_are_refused_on_the_host():
                                             c.block_tables, c.seq_lens, -0.1, gi, gp, 2, 20,
                                             workspace=ws)
     assert e.value.status == 1
+
+
+def test_request_outside_every_group_is_reported():
+    # groups cover requests 0..2 of 5: requests 3 and 4 attend their whole sequence through
+    # their own tables (correct values) and the device error word reports the gap
+    case, gi, gp, mg, ms = grouped_case([(3, 64), (1, 0), (1, 0)], [20, 30, 40, 50, 60], 8, 2, 16,
+                                        BF16, seed=51)
+    gi = gi[:2].contiguous()   # [0, 3]: one group only
+    gp = gp[:1].contiguous()
+    out, lse = run_cascade(case, gi, gp, mg, max(ms, 124))
+    check(case, out, lse, "uncovered requests")
+    assert pkv.get_device_error() == 3
