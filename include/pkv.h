@@ -208,7 +208,9 @@ pkv_status pkv_paged_decode_attn_append(const pkv_cache_desc* desc, void* k_cach
  * table of its first member (block_tables[group_indptr[g]]; the other
  * members' entries for them are not read), and tokens W_g .. seq_lens[b]-1
  * through the member's own table.  P_g <= seq_lens[b] for every member (else
- * the device error word reports PKV_DEVERR_BAD_LENGTH).
+ * the device error word reports PKV_DEVERR_BAD_LENGTH).  A request that no
+ * group covers is attended over its whole sequence through its own table and
+ * reported the same way.
  *
  * k_new, v_new:  nullable together; as pkv_paged_decode_attn_append (the
  *                current token, position seq_lens[b]-1, must lie at or after
