@@ -552,6 +552,25 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, const 
     return;
   }
   const float* lse = p.ws_lse + bh * nslots;
+  const float* po = p.ws_o + bh * nslots * HD + lane * PER;
+  // the first kPre partials are loaded together with the LSEs (they do not
+  // depend on the max), so the merge waits on one round trip, not two
+  constexpr int kPre = 8;
+  float pre[kPre][PER];
+#pragma unroll
+  for (int k = 0; k < kPre; ++k) {
+    if (s_lo + k < s_hi) {
+#pragma unroll
+      for (int e = 0; e < PER; ++e) pre[k][e] = 0.f;
+      if constexpr (PER == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(po + (int64_t)(s_lo + k) * HD);
+        pre[k][0] = v.x; pre[k][1] = v.y; pre[k][2] = v.z; pre[k][3] = v.w;
+      } else {
+        const float2 v = *reinterpret_cast<const float2*>(po + (int64_t)(s_lo + k) * HD);
+        pre[k][0] = v.x; pre[k][1] = v.y;
+      }
+    }
+  }
   float m = -INFINITY;
   for (int s = s_lo + lane; s < s_hi; s += 32) m = fmaxf(m, lse[s]);
 #pragma unroll
@@ -560,8 +579,16 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, const 
 #pragma unroll
   for (int k = 0; k < PER; ++k) o[k] = 0.f;
   float L = 0.f;
-  const float* po = p.ws_o + bh * nslots * HD + lane * PER;
-  for (int s = s_lo; s < s_hi; ++s) {
+#pragma unroll
+  for (int k = 0; k < kPre; ++k) {
+    if (s_lo + k < s_hi) {
+      const float w = fast_exp2(lse[s_lo + k] - m);
+      L += w;
+#pragma unroll
+      for (int e = 0; e < PER; ++e) o[e] += w * pre[k][e];
+    }
+  }
+  for (int s = s_lo + kPre; s < s_hi; ++s) {  // plans with more than kPre splits
     const float w = fast_exp2(lse[s] - m);
     L += w;
     if constexpr (PER == 4) {
