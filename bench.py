@@ -346,6 +346,7 @@ def run_decode_bench(args, world, rank, local):
         res["prefix_index"] = run_prefix_index_bench()
         res["chain_hash"] = run_chain_hash_bench(dev, hbm, peak_src)
         res["shared_prefix_decode"] = run_shared_prefix_bench(dev, hbm, peak_src)
+        res["more_decode_configs"] = run_more_decode_configs_bench(dev, hbm, peak_src)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline_decode(case, budget_s=args.cpu_seconds)
     return res
@@ -646,6 +647,79 @@ def run_shared_prefix_bench(dev, hbm, peak_src, n=20):
             "peak_source": f"{peak_src} (hbm_gbs)",
             "max_abs_diff_plain_vs_shared_prefix": diff,
             "l2": "256 MiB buffer written then read between calls"}
+
+
+def run_more_decode_configs_bench(dev, hbm, peak_src, n=10):
+    """Two more of the pages' workload shapes, timed like the headline step (each
+    request's current token appended by the decode kernel, then attention; one
+    CUDA graph; L2 flushed between steps): the Llama-2-70B-shaped fp8 layer, and
+    the long-context step over all 32 layers of 4 x 100,000 tokens."""
+    import paged_kv_cache_285_gb300 as pkv
+    from paged_kv_cache_285_gb300 import workloads as W
+    stream = torch.cuda.current_stream(dev)
+    flush = L2Flush(dev)
+
+    def prepare(case, max_len):
+        b = case.q.shape[0]
+        out = torch.empty_like(case.q)
+        wsb = pkv.decode_workspace_bytes(case.k_cache, b, case.num_q_heads, max_len, 0,
+                                         case.k_scale, case.v_scale)
+        ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
+        return lambda: pkv.paged_decode_attn_append(
+            case.k_cache, case.v_cache, case.new_k, case.new_v, case.q, out, case.block_tables,
+            case.seq_lens, case.sm_scale, max_len, k_scale=case.k_scale, v_scale=case.v_scale,
+            workspace=ws)
+
+    def time_step(fns):
+        for _ in range(3):
+            for f in fns:
+                f()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                for f in fns:
+                    f()
+        stream.wait_stream(cap)
+        g.replay()
+        tot = 0.0
+        for _ in range(n):
+            flush()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            e1.synchronize()
+            tot += e0.elapsed_time(e1)
+        return tot / n
+
+    res = {}
+    case = W.fp8_70b_decode(device="cuda")
+    ms = time_step([prepare(case, 4096)])
+    nbytes = sum(decode_step_bytes(case))
+    res["fp8_70b_layer"] = {
+        "workload": "128 requests x 4,096 tokens, 64q/8kv, d128, fp8_e4m3 K/V, bf16 q/out, bs16",
+        "ms_per_step": round(ms, 5), "step_bytes": nbytes,
+        "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+        "frac_of_hbm": round(nbytes / (ms * 1e-3) / 1e9 / hbm, 4)}
+    del case
+    torch.cuda.empty_cache()
+    cases = W.long_context_layers(device="cuda")
+    ms = time_step([prepare(c, 100_000) for c in cases])
+    nbytes = sum(sum(decode_step_bytes(c)) for c in cases)
+    res["long_context_32_layers"] = {
+        "workload": "4 requests x 100,000 tokens, 32 layers (one pool each), 32q/8kv, d128, fp16, bs32",
+        "ms_per_step": round(ms, 5), "step_bytes": nbytes,
+        "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+        "frac_of_hbm": round(nbytes / (ms * 1e-3) / 1e9 / hbm, 4),
+        "tokens_per_s": round(4 / (ms * 1e-3), 1)}
+    del cases
+    torch.cuda.empty_cache()
+    res["peak_source"] = f"{peak_src} (hbm_gbs)"
+    return res
 
 
 def run_chain_hash_bench(dev, hbm, peak_src, n=20, seed=0):
