@@ -619,18 +619,18 @@ constexpr int stages_for() {
   return ns < 2 ? 2 : (ns > 8 ? 8 : ns);
 }
 
-// NSO > 0 overrides the pipeline depth (stages per warp).
-template <int HD, int CT, int AT, bool CASC, int NSO = 0>
+// NSO > 0 overrides the pipeline depth (stages per warp), NW the warps per CTA.
+template <int HD, int CT, int AT, bool CASC, int NSO = 0, int NW = kNW>
 cudaError_t launch_decode_t(const CUtensorMap& kmap, const CUtensorMap& vmap,
                             const DecodeParams& p, const DecodeExtraParams& ap,
                             cudaStream_t stream, cudaEvent_t merge_after = nullptr) {
   constexpr int NS = NSO > 0 ? NSO : stages_for<HD, CT>();
-  using C = DecodeCfg<HD, CT, kNW, NS>;
-  auto kern = decode_kernel<HD, CT, AT, kNW, NS, CASC>;
+  using C = DecodeCfg<HD, CT, NW, NS>;
+  auto kern = decode_kernel<HD, CT, AT, NW, NS, CASC>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   dim3 grid(p.num_kv_heads, p.batch, p.num_splits);
-  kern<<<grid, kNW * 32, C::SMEM, stream>>>(kmap, vmap, p, ap);
+  kern<<<grid, NW * 32, C::SMEM, stream>>>(kmap, vmap, p, ap);
   e = cudaGetLastError();
   if (e != cudaSuccess || (!CASC && p.num_splits <= 1)) return e;
   if (merge_after != nullptr && (e = cudaStreamWaitEvent(stream, merge_after, 0)) != cudaSuccess)
@@ -680,17 +680,21 @@ cudaError_t launch_decode_cascade(const CUtensorMap& kmap, const CUtensorMap& vm
   if (!ap.group_indptr || !ap.group_prefix_lens || ap.num_groups <= 0 || !p.ws_o)
     return cudaErrorInvalidValue;
   // Short runs per CTA (the members' own tokens are typically a few hundred):
-  // one stage per warp, so that four CTAs fit on an SM instead of two and
-  // their fixed costs (setup, first copy, epilogue) overlap; measured 13 %
-  // faster at 320 tokens per CTA.  Long runs keep the deeper pipeline.
+  // small CTAs of two warps with two stages each (~33 KB), so that many fit
+  // on an SM and their fixed costs (setup, first copy, epilogue) overlap.
+  // Shared-prompt layer, 320 tokens per CTA: 50.5 us, against 51.5 (2 warps,
+  // 1 stage), 53.1 (4 warps, 1 stage), 59.6 (4 warps, 3 stages) and 65.5
+  // (8 warps, 1 stage).  Long runs keep the plain decode's configuration.
   const bool short_runs = p.chunk <= 512;
   if (cache_dt == DT_F16)
     return short_runs
-               ? launch_decode_t<128, DT_F16, DT_F16, true, 1>(kmap, vmap, p, ap, stream, merge_after)
+               ? launch_decode_t<128, DT_F16, DT_F16, true, 2, 2>(kmap, vmap, p, ap, stream,
+                                                                 merge_after)
                : launch_decode_t<128, DT_F16, DT_F16, true>(kmap, vmap, p, ap, stream, merge_after);
   if (cache_dt == DT_BF16)
     return short_runs
-               ? launch_decode_t<128, DT_BF16, DT_BF16, true, 1>(kmap, vmap, p, ap, stream, merge_after)
+               ? launch_decode_t<128, DT_BF16, DT_BF16, true, 2, 2>(kmap, vmap, p, ap, stream,
+                                                                   merge_after)
                : launch_decode_t<128, DT_BF16, DT_BF16, true>(kmap, vmap, p, ap, stream, merge_after);
   return cudaErrorInvalidValue;
 }
