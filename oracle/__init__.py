@@ -11,6 +11,11 @@ Two independent implementations live here:
 * ``ref_numpy.py`` (NumPy, fp64) -- a second, separately written version used
   only to cross-check the C code on small cases.
 
+Beside the attention oracle, plain-Python references of the block-identity
+parts: ``chain_hash_ref.py`` (salted chain hashes of full blocks) and
+``prefix_match_ref.py`` (the longest cached prefix at block granularity, by
+brute force).
+
 Sources of the definitions (page title, section):
   * "KV Cache에 대해 알아보자 (Feat. Attention)", §1: softmax(QK^T/sqrt(d_k))V.
   * "PagedAttention과 RadixAttention으로 LLM KV 캐시 최적화", section 02:

@@ -12,6 +12,7 @@ import numpy as np
 import pytest
 
 import paged_kv_cache_285_gb300 as pkv
+from oracle.prefix_match_ref import common_blocks, longest_block_prefix
 
 pytestmark = pytest.mark.filterwarnings("ignore")
 
@@ -166,10 +167,22 @@ def test_insert_releases_duplicate_blocks_and_rejects_bad_input():
     assert st["free_blocks"] + st["tree_blocks"] + st["caller_blocks"] == 16
 
 
+def test_brute_force_model_on_hand_cases():
+    # the reference itself, on cases worked by hand
+    assert common_blocks([1, 2, 3, 4, 5, 6], [1, 2, 3, 4, 9, 6], 2) == 2
+    assert common_blocks([1, 2, 3], [1, 2, 3, 4], 2) == 1      # partial blocks never count
+    assert common_blocks([7, 7], [8, 7], 1) == 0
+    stored = [([1, 2, 3, 4], [10, 11]), ([1, 2, 3, 4, 5, 6], [20, 21, 22])]
+    assert longest_block_prefix(stored, [1, 2, 3, 4, 5, 6, 7], 2) == (3, [20, 21, 22])
+    assert longest_block_prefix(stored, [1, 2, 3, 4, 9, 9], 2) == (2, [10, 11])  # earliest wins
+    assert longest_block_prefix(stored, [5, 5], 2) == (0, [])
+
+
 def test_random_workload_against_brute_force_model():
     # without eviction (a pool large enough), every match equals the longest
-    # whole-block common prefix with any sequence served before, and returns
-    # the blocks that sequence was given; the pool is accounted exactly
+    # whole-block common prefix with any sequence served before (the brute-force
+    # reference in oracle/prefix_match_ref.py), and returns the blocks that
+    # sequence was given; the pool is accounted exactly
     rng = np.random.default_rng(7)
     bs = 4
     x = pkv.RadixIndex(bs, 200000)
@@ -179,18 +192,10 @@ def test_random_workload_against_brute_force_model():
         base = bases[rng.integers(0, len(bases))]
         tail = rng.integers(0, 5, rng.integers(0, 30)).astype(np.int32)
         t = np.concatenate([base[: rng.integers(0, len(base) + 1)], tail]).astype(np.int32)
-        nb = len(t) // bs
-        best, best_tab = 0, None
-        for s, tab in stored:
-            k = 0
-            while k < nb and k < len(s) // bs and np.array_equal(s[k * bs:(k + 1) * bs], t[k * bs:(k + 1) * bs]):
-                k += 1
-            if k > best:
-                best, best_tab = k, tab
+        best, best_blocks = longest_block_prefix(stored, t, bs)
         m, blk = x.match(t)
         assert m == best * bs, it
-        if best:
-            assert list(blk) == list(best_tab[:best]), it
+        assert list(blk) == best_blocks, it
         x.release(t, m)
         _, table = serve(x, t)
         stored.append((t, table))
