@@ -173,6 +173,13 @@ def _desc(k_cache: torch.Tensor, k_scale: float, v_scale: float) -> CacheDesc:
     return CacheDesc(nb, bs, hkv, d, _dtype_code(k_cache), float(k_scale), float(v_scale))
 
 
+def _need(dtype, **tensors):
+    """The index tensors of a call must have the dtype the C ABI reads."""
+    for name, t in tensors.items():
+        if t is not None and t.dtype != dtype:
+            raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
 def _check(status: int, what: str):
     if status != 0:
         raise PkvError(status, what)
@@ -181,6 +188,7 @@ def _check(status: int, what: str):
 def kv_append(k_cache, v_cache, k_new, v_new, slot_mapping, k_scale=1.0, v_scale=1.0,
               stream=None):
     """pkv_kv_append: k_new/v_new [T, Hkv, D] act dtype, slot_mapping int64 [T]."""
+    _need(torch.int64, slot_mapping=slot_mapping)
     lib = load()
     desc = _desc(k_cache, k_scale, v_scale)
     st = lib.pkv_kv_append(ctypes.byref(desc), _ptr(k_cache), _ptr(v_cache), _ptr(k_new),
@@ -202,6 +210,7 @@ def paged_decode_attn(k_cache, v_cache, q, out, block_tables, seq_lens, sm_scale
                       stream=None):
     """pkv_paged_decode_attn: q/out [B, Hq, D]; block_tables int32 [B, W]; seq_lens int32 [B].
     ``workspace`` is a uint8 device tensor of at least decode_workspace_bytes() bytes."""
+    _need(torch.int32, block_tables=block_tables, seq_lens=seq_lens)
     lib = load()
     desc = _desc(k_cache, k_scale, v_scale)
     b, hq, _ = q.shape
@@ -219,6 +228,7 @@ def paged_decode_attn_append(k_cache, v_cache, k_new, v_new, q, out, block_table
                              lse_out=None, workspace=None, stream=None):
     """pkv_paged_decode_attn_append: k_new/v_new [B, Hkv, D] are written to position
     seq_len-1 of each request and attended in the same launch."""
+    _need(torch.int32, block_tables=block_tables, seq_lens=seq_lens)
     lib = load()
     desc = _desc(k_cache, k_scale, v_scale)
     b, hq, _ = q.shape
@@ -247,6 +257,7 @@ def paged_decode_attn_shared_prefix(k_cache, v_cache, q, out, block_tables, seq_
     """pkv_paged_decode_attn_shared_prefix: requests [group_indptr[g], group_indptr[g+1])
     share their first group_prefix_lens[g] tokens (read through the group's first member's
     block table), attended once per group; k_new/v_new as paged_decode_attn_append."""
+    _need(torch.int32, block_tables=block_tables, seq_lens=seq_lens)
     lib = load()
     desc = _desc(k_cache, 1.0, 1.0)
     b, hq, _ = q.shape
@@ -277,6 +288,7 @@ def paged_extend_attn(k_cache, v_cache, q, out, q_indptr, prefix_lens, block_tab
                       max_suffix_len, max_total_len, k_scale=1.0, v_scale=1.0, lse_out=None,
                       workspace=None, stream=None):
     """pkv_paged_extend_attn: q/out [sum S, Hq, D]; q_indptr int32 [B+1]; prefix_lens int32 [B]."""
+    _need(torch.int32, q_indptr=q_indptr, prefix_lens=prefix_lens, block_tables=block_tables)
     lib = load()
     desc = _desc(k_cache, k_scale, v_scale)
     rows, hq, _ = q.shape
@@ -296,6 +308,7 @@ def paged_extend_attn_append(k_cache, v_cache, k_new, v_new, q, out, q_indptr, p
                              stream=None):
     """pkv_paged_extend_attn_append: k_new/v_new [sum S, Hkv, D] (the cache dtype) are written
     to positions prefix_lens[b] + i and attended in the same call (16-bit caches)."""
+    _need(torch.int32, q_indptr=q_indptr, prefix_lens=prefix_lens, block_tables=block_tables)
     lib = load()
     desc = _desc(k_cache, 1.0, 1.0)
     rows, hq, _ = q.shape

@@ -150,3 +150,18 @@ def test_chain_hash_and_extend_append_argument_errors(lib):
         10, 100, None, None)
     assert ext(d8) == 2                                       # fp8 cache
     assert ext(_desc(), kn=None) == 1                         # the suffix K/V are required
+
+
+def test_binding_refuses_wrong_index_dtypes():
+    import torch
+    c = torch.zeros((4, 2, 16, 128), dtype=torch.bfloat16)
+    q = torch.zeros((2, 4, 128), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):  # int64 block tables
+        pkv.paged_decode_attn(c, c, q, q, torch.zeros((2, 4), dtype=torch.int64),
+                              torch.zeros(2, dtype=torch.int32), 0.1, 64)
+    with pytest.raises(ValueError):  # int32 slots
+        pkv.kv_append(c, c, q, q, torch.zeros(2, dtype=torch.int32))
+    with pytest.raises(ValueError):  # int64 prefix lengths
+        pkv.paged_extend_attn(c, c, q, q, torch.zeros(3, dtype=torch.int32),
+                              torch.zeros(2, dtype=torch.int64),
+                              torch.zeros((2, 4), dtype=torch.int32), 0.1, 1, 64)
