@@ -172,6 +172,7 @@ struct DecodePlan {
   int splits = 0;
   size_t ws_bytes = 0;
   size_t ws_lse_offset = 0;
+  size_t ws_span_offset = 0;  // cascade: int2 (first own token, length) per request
 };
 
 // Split plan: the sequence is cut into runs of `chunk` tokens (a multiple of
@@ -315,7 +316,8 @@ static DecodePlan plan_cascade(const pkv_cache_desc* d, int batch, int hq, int m
   DecodePlan pl = plan_decode(d, batch, hq, max_suffix_len + d->block_size - 1, forced, sm_count);
   const size_t slots = (size_t)pl.splits + 1;
   pl.ws_lse_offset = align256((size_t)batch * hq * slots * d->head_dim * sizeof(float));
-  pl.ws_bytes = pl.ws_lse_offset + (size_t)batch * hq * slots * sizeof(float);
+  pl.ws_span_offset = align256(pl.ws_lse_offset + (size_t)batch * hq * slots * sizeof(float));
+  pl.ws_bytes = pl.ws_span_offset + (size_t)batch * 2 * sizeof(int32_t);
   return pl;
 }
 
@@ -462,6 +464,7 @@ pkv_status pkv_paged_decode_attn_shared_prefix(
   ap.group_indptr = group_indptr;
   ap.group_prefix_lens = group_prefix_lens;
   ap.num_groups = num_groups;
+  ap.ws_span = reinterpret_cast<int2*>(static_cast<uint8_t*>(workspace) + pl.ws_span_offset);
   e = launch_decode_cascade(kmap, vmap, p, ap, desc->head_dim, (int)desc->cache_dtype,
                             (int)act_dtype, stream, ds->join);
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;

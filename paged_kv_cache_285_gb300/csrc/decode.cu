@@ -155,6 +155,8 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       tb = tb < 0 ? 0 : n;
     }
     tb = (tb >> p.bs_shift) << p.bs_shift;  // only whole blocks are shared
+    // the merge reads the request's span from here instead of searching again
+    if (split == 0 && g == 0 && threadIdx.x == 0) ap.ws_span[b] = make_int2(tb, n);
   }
   const int t0 = tb + split * p.chunk;
   if (t0 >= n) {
@@ -531,14 +533,18 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, const 
   const int64_t bh = (int64_t)blockIdx.x * 4 + warp;
   if (bh >= (int64_t)p.batch * p.num_q_heads) return;
   const int b = (int)(bh / p.num_q_heads);
-  const int bs = 1 << p.bs_shift;
-  int n = p.seq_lens[b];
-  int tb = 0;
-  if constexpr (CASC) tb = group_prefix_len(ap, b);
-  const int cap = min(p.max_blocks * bs, (tb > 0 ? tb : 0) + p.num_splits * p.chunk);
-  n = n < 0 ? 0 : (n > cap ? cap : n);
-  tb = tb < 0 ? 0 : (tb > n ? n : tb);
-  tb = (tb >> p.bs_shift) << p.bs_shift;
+  int n, tb = 0;
+  if constexpr (CASC) {
+    // (first own token, clamped length) as the split kernel settled them
+    const int2 span = ap.ws_span[b];
+    tb = span.x;
+    n = span.y;
+  } else {
+    const int bs = 1 << p.bs_shift;
+    n = p.seq_lens[b];
+    const int cap = min(p.max_blocks * bs, p.num_splits * p.chunk);
+    n = n < 0 ? 0 : (n > cap ? cap : n);
+  }
   const int ns = (n - tb + p.chunk - 1) / p.chunk;
   if (!CASC && ns <= 1) return;  // written directly by the split kernel
   constexpr int kSlot0 = CASC ? 1 : 0;

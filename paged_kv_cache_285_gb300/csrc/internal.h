@@ -55,6 +55,7 @@ struct DecodeExtraParams {
   const int32_t* group_indptr;       // [num_groups + 1]
   const int32_t* group_prefix_lens;  // [num_groups]
   int num_groups;
+  int2* ws_span;                     // [batch] (first own token, length), for the merge
 };
 
 struct AppendParams {

@@ -128,8 +128,9 @@ def test_shared_prefix_decode_argument_errors(lib):
     # forced 2 splits over the members' own tokens (bound 100, + 15 for the prefix rounded
     # down to whole blocks): 8 tiles -> 4 per split; slots = 2 + the prefix's
     d = _desc()
+    # (+ 256-byte alignment, then one int2 span per request)
     assert lib.pkv_shared_prefix_decode_workspace_bytes(ctypes.byref(d), 2, 8, 100, 2) == \
-        2 * 8 * 3 * 128 * 4 + 2 * 8 * 3 * 4
+        2 * 8 * 3 * 128 * 4 + 256 + 2 * 8
 
 
 def test_chain_hash_and_extend_append_argument_errors(lib):
