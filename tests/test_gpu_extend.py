@@ -59,6 +59,8 @@ CASES = [
     ([17, 250], [64, 33], 16, 2, 16, BF16),
     ([129, 64, 1], [200, 17, 256], 64, 8, 16, BF16),
     ([500], [40], 4, 2, 32, BF16),
+    # requests with no suffix rows between others (equal q_indptr entries)
+    ([40, 7, 0, 300, 0], [0, 50, 0, 3, 0], 8, 2, 16, BF16),
 ]
 
 
@@ -68,6 +70,16 @@ def test_extend_small(cfg):
     case = W.extend_case(P, Sx, hq, hkv, 128, bs, dt, dt, seed=sum(P) + sum(Sx) + hq, device="cuda")
     out, lse = gpu_extend(case)
     check(case, out, lse, str(cfg))
+    assert pkv.get_device_error() == 0
+
+
+
+def test_extend_with_no_suffix_rows_is_a_no_op():
+    # every request fully cached: nothing to compute, nothing written, no error
+    case = W.extend_case([33, 0, 200], [0, 0, 0], 8, 2, 128, 16, BF16, BF16, seed=9, device="cuda")
+    assert case.q.shape[0] == 0
+    out, lse = gpu_extend(case)
+    assert out.shape[0] == 0 and lse.shape[0] == 0
     assert pkv.get_device_error() == 0
 
 

@@ -53,6 +53,8 @@ CASES = [
     ([100, 0], [300, 129], 8, 8, 32, F16),
     ([129, 64, 1], [200, 17, 256], 64, 8, 16, BF16),
     ([511, 7], [700, 64], 16, 4, 32, BF16),
+    # requests with no suffix rows: the slot search must skip them
+    ([40, 7, 0, 300, 0], [0, 50, 0, 3, 0], 8, 2, 16, BF16),
 ]
 
 
