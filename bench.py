@@ -347,6 +347,7 @@ def run_decode_bench(args, world, rank, local):
         res["chain_hash"] = run_chain_hash_bench(dev, hbm, peak_src)
         res["shared_prefix_decode"] = run_shared_prefix_bench(dev, hbm, peak_src)
         res["more_decode_configs"] = run_more_decode_configs_bench(dev, hbm, peak_src)
+        res["append_fill"] = run_append_fill_bench(dev, hbm, peak_src)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline_decode(case, budget_s=args.cpu_seconds)
     return res
@@ -756,6 +757,58 @@ def run_chain_hash_bench(dev, hbm, peak_src, n=20, seed=0):
             "peak_source": f"{peak_src} (hbm_gbs)", "algorithmic_bytes": nbytes,
             "bound": "latency: each request's chain is %d dependent hash steps" % (L // bs),
             "l2": "256 MiB buffer written then read between calls"}
+
+
+def run_append_fill_bench(dev, hbm, peak_src, n=10):
+    """pkv_kv_append as a bulk fill: every position of a layer's context written in
+    one call (the Llama-3-8B-shaped layer kept in bf16, the Llama-2-70B-shaped
+    layer stored as fp8 e4m3); algorithmic bytes = the K and V rows read (bf16) +
+    the slot ids (8 B per token) + the K and V rows written (cache dtype)."""
+    import paged_kv_cache_285_gb300 as pkv
+    from paged_kv_cache_285_gb300 import workloads as W
+    stream = torch.cuda.current_stream(dev)
+    flush = L2Flush(dev)
+    res = {}
+    layers = (
+        ("llama3_8b_layer_bf16", W.llama3_8b_decode,
+         "64 requests, n ~ U[512,4096], 8 kv heads, d128, bf16 -> bf16 cache, bs16"),
+        ("llama2_70b_layer_fp8", W.fp8_70b_decode,
+         "128 requests x 4,096 tokens, 8 kv heads, d128, bf16 -> fp8_e4m3 cache, bs16"))
+    for name, make, what in layers:
+        case = make(device=dev)
+        slots = W.context_slots(case)
+        t, hkv, d = slots.numel(), case.k_cache.shape[1], case.k_cache.shape[3]
+        g = torch.Generator(device=dev).manual_seed(7)
+        nk = torch.randn((t, hkv, d), generator=g, device=dev).to(torch.bfloat16)
+        nv = torch.randn((t, hkv, d), generator=g, device=dev).to(torch.bfloat16)
+
+        def call():
+            pkv.kv_append(case.k_cache, case.v_cache, nk, nv, slots, k_scale=case.k_scale,
+                          v_scale=case.v_scale)
+
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        tot = 0.0
+        for _ in range(n):
+            flush()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            call()
+            e1.record(stream)
+            e1.synchronize()
+            tot += e0.elapsed_time(e1)
+        ms = tot / n
+        nbytes = t * hkv * d * (2 + case.k_cache.element_size()) * 2 + 8 * t
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res[name] = {"workload": what, "tokens": t, "ms_per_call": round(ms, 5),
+                     "bytes": nbytes, "gbs": round(gbs, 1), "frac_of_hbm": round(gbs / hbm, 4)}
+        del case, slots, nk, nv
+        torch.cuda.empty_cache()
+    res["peak_source"] = f"{peak_src} (hbm_gbs)"
+    res["l2"] = "256 MiB buffer written then read between calls"
+    return res
 
 
 def cpu_baseline_decode(case, budget_s=10.0):

@@ -58,29 +58,6 @@ struct DecodeExtraParams {
   int2* ws_span;                     // [batch] (first own token, length), for the merge
 };
 
-struct AppendParams {
-  void* k_cache;
-  void* v_cache;
-  const void* k_new;
-  const void* v_new;
-  const int64_t* slots;          // null: slots from the extend layout below
-  int32_t* err;
-  int64_t num_tokens;
-  int num_kv_heads;
-  int head_dim;
-  int block_size;
-  int num_blocks;
-  float k_scale;
-  float v_scale;
-  // slots == null: token t is suffix row t of an extend call (request b with
-  // q_indptr[b] <= t < q_indptr[b+1]) at position prefix_lens[b] + t - q_indptr[b]
-  const int32_t* q_indptr;
-  const int32_t* prefix_lens;
-  const int32_t* block_tables;
-  int batch;
-  int max_blocks;
-};
-
 // Division of unsigned n < 2^31 by a divisor fixed for a launch, as a
 // multiply-high and a shift (Granlund & Montgomery, "Division by invariant
 // integers using multiplication", 1994): with l = ceil(log2 d) and
@@ -108,6 +85,33 @@ inline FastDiv make_fastdiv(uint32_t d) {
   f.m = (uint32_t)((((uint64_t)1 << 32) * ((1ull << f.l) - d)) / d + 1);
   return f;
 }
+
+struct AppendParams {
+  void* k_cache;
+  void* v_cache;
+  const void* k_new;
+  const void* v_new;
+  const int64_t* slots;          // null: slots from the extend layout below
+  int32_t* err;
+  int64_t num_tokens;
+  int num_kv_heads;
+  int head_dim;
+  int block_size;
+  int num_blocks;
+  float k_scale;
+  float v_scale;
+  // slots == null: token t is suffix row t of an extend call (request b with
+  // q_indptr[b] <= t < q_indptr[b+1]) at position prefix_lens[b] + t - q_indptr[b]
+  const int32_t* q_indptr;
+  const int32_t* prefix_lens;
+  const int32_t* block_tables;
+  int batch;
+  int max_blocks;
+  // set by the launcher
+  int bs_shift;       // log2(block_size)
+  int rows_fit32;     // num_tokens * num_kv_heads < 2^31
+  FastDiv div_hkv;    // by num_kv_heads
+};
 
 struct ExtendParams {
   const int32_t* q_indptr;

@@ -24,16 +24,25 @@ __device__ __forceinline__ float act_to_f32(uint16_t bits) {
   else return __half2float(__ushort_as_half(bits));
 }
 
-template <int CT, int AT>
+template <int CT, int AT, int HD>
 __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
-  const int vpr = p.head_dim / 8;  // 16-byte input vectors per row
+  constexpr int VPR = HD / 8;  // 16-byte input vectors per row (a power of two)
   const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t total = p.num_tokens * p.num_kv_heads * vpr;
+  const int64_t total = p.num_tokens * p.num_kv_heads * VPR;
   if (idx >= total) return;
-  const int v = (int)(idx % vpr);
-  const int64_t row = idx / vpr;
-  const int g = (int)(row % p.num_kv_heads);
-  const int64_t t = row / p.num_kv_heads;
+  const int v = (int)(idx & (VPR - 1));
+  const int64_t row = (int64_t)((uint64_t)idx / VPR);  // (token, kv head) row
+  int64_t t;
+  int g;
+  if (p.rows_fit32) {  // row < 2^31: the kv-head split as a multiply-high
+    const uint32_t q = p.div_hkv.div((uint32_t)row);
+    t = q;
+    g = (int)((uint32_t)row - q * (uint32_t)p.num_kv_heads);
+  } else {
+    t = row / p.num_kv_heads;
+    g = (int)(row - t * p.num_kv_heads);
+  }
+  const int64_t bmask = p.block_size - 1;  // block sizes are powers of two
   int64_t slot;
   if (p.slots) {
     slot = p.slots[t];
@@ -45,23 +54,22 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
       else hi = mid;
     }
     const int64_t pos = (int64_t)__ldg(p.prefix_lens + lo) + (t - __ldg(p.q_indptr + lo));
-    const int64_t lb = pos / p.block_size;
-    if (pos < 0 || lb >= p.max_blocks) {
+    if (pos < 0 || (pos >> p.bs_shift) >= p.max_blocks) {
       if (v == 0 && p.err) atomicCAS(p.err, 0, 3);
       return;
     }
-    const int32_t b = __ldg(p.block_tables + (int64_t)lo * p.max_blocks + lb);
+    const int32_t b = __ldg(p.block_tables + (int64_t)lo * p.max_blocks + (pos >> p.bs_shift));
     // a negative block id is outside the pool too (reported below)
-    slot = (b < 0 ? (int64_t)p.num_blocks : (int64_t)b) * p.block_size + pos % p.block_size;
+    slot = ((b < 0 ? (int64_t)p.num_blocks : (int64_t)b) << p.bs_shift) + (pos & bmask);
   }
   if (slot < 0) return;
-  const int64_t blk = slot / p.block_size, off = slot % p.block_size;
+  const int64_t blk = slot >> p.bs_shift, off = slot & bmask;
   if (blk >= p.num_blocks) {
     if (v == 0 && p.err) atomicCAS(p.err, 0, 2);
     return;
   }
-  const int64_t src = (t * p.num_kv_heads + g) * p.head_dim + v * 8;
-  const int64_t dst = ((blk * p.num_kv_heads + g) * p.block_size + off) * p.head_dim + v * 8;
+  const int64_t src = idx * 8;  // row * HD + v * 8
+  const int64_t dst = (((blk * p.num_kv_heads + g) << p.bs_shift) + off) * HD + v * 8;
   const uint4 kx = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.k_new) + src));
   const uint4 vx = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.v_new) + src));
   if constexpr (CT != DT_E4M3) {
@@ -93,11 +101,16 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
 }
 
 template <int CT, int AT>
-cudaError_t launch_append_t(const AppendParams& p, cudaStream_t stream) {
-  const int64_t total = p.num_tokens * p.num_kv_heads * (p.head_dim / 8);
+cudaError_t launch_append_t(const AppendParams& in, cudaStream_t stream) {
+  const int64_t total = in.num_tokens * in.num_kv_heads * (in.head_dim / 8);
   if (total == 0) return cudaSuccess;
+  AppendParams p = in;
+  p.bs_shift = p.block_size == 16 ? 4 : 5;
+  p.rows_fit32 = p.num_tokens * p.num_kv_heads < ((int64_t)1 << 31) ? 1 : 0;
+  p.div_hkv = make_fastdiv((uint32_t)p.num_kv_heads);
   const unsigned blocks = (unsigned)((total + 255) / 256);
-  append_kernel<CT, AT><<<blocks, 256, 0, stream>>>(p);
+  if (p.head_dim == 64) append_kernel<CT, AT, 64><<<blocks, 256, 0, stream>>>(p);
+  else append_kernel<CT, AT, 128><<<blocks, 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -146,6 +146,19 @@ def _slots(tables, positions, bs):
     return torch.where(inside & (blk >= 0), slot, torch.full_like(slot, -1))
 
 
+def context_slots(case):
+    """Slot of every cached position of a decode case, request by request
+    (position t of request b -> block_tables[b][t // bs] * bs + t % bs): the
+    slot mapping of a kv_append that fills each request's whole context."""
+    lens = case.seq_lens.to(torch.int64)
+    bs = case.k_cache.shape[2]
+    starts = torch.cumsum(lens, 0) - lens
+    rows_b = torch.repeat_interleave(torch.arange(lens.numel(), device=lens.device), lens)
+    pos = torch.arange(rows_b.numel(), device=lens.device) - starts[rows_b]
+    blk = case.block_tables.to(torch.int64)[rows_b, pos // bs]
+    return blk * bs + pos % bs
+
+
 def _replicate_prefix_tail(case_k, case_v, tables, prefix, bs):
     """Same K/V for the prefix's tail tokens in every request's private block."""
     tail = prefix % bs

@@ -80,3 +80,59 @@ def test_zero_tokens_is_noop():
                   case.slot_last[:0])
     torch.cuda.synchronize()
     np.testing.assert_array_equal(S(case.k_cache), before)
+
+
+def _fill_inputs(case, seed):
+    slots = W.context_slots(case)
+    t, hkv, d = slots.numel(), case.k_cache.shape[1], case.k_cache.shape[3]
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    new_k = torch.randn((t, hkv, d), generator=g, device="cuda").to(torch.bfloat16)
+    new_v = torch.randn((t, hkv, d), generator=g, device="cuda").to(torch.bfloat16)
+    return slots, new_k, new_v
+
+
+def test_full_context_fill_llama3_8b_layer():
+    # every position of the Llama-3-8B-shaped layer (64 requests, ~147k tokens) in one call:
+    # each slot's row holds its input row bit for bit, every other byte of the pool is unchanged
+    case = W.llama3_8b_decode(device="cuda")
+    slots, new_k, new_v = _fill_inputs(case, 60)
+    nb, hkv, bs, d = case.k_cache.shape
+    k0, v0 = case.k_cache.clone(), case.v_cache.clone()
+    pkv.kv_append(case.k_cache, case.v_cache, new_k, new_v, slots)
+    torch.cuda.synchronize()
+    written = torch.zeros(nb * bs, dtype=torch.bool, device="cuda")
+    written[slots] = True
+    assert int(written.sum()) == slots.numel()  # the slot mapping has no repeats
+    for pool, before, new in ((case.k_cache, k0, new_k), (case.v_cache, v0, new_v)):
+        assert torch.equal(pool[slots // bs, :, slots % bs, :].view(torch.int16), new.view(torch.int16))
+        rows = pool.permute(0, 2, 1, 3).reshape(nb * bs, hkv, d)
+        rows0 = before.permute(0, 2, 1, 3).reshape(nb * bs, hkv, d)
+        assert torch.equal(rows[~written].view(torch.int16), rows0[~written].view(torch.int16))
+    assert pkv.get_device_error() == 0
+
+
+def test_full_context_fill_fp8_70b_layer_sampled():
+    # the Llama-2-70B-shaped layer (128 x 4,096 tokens) stored as fp8 e4m3 in one call;
+    # 514 sampled rows (the first and last among them) against the oracle's encoder
+    case = W.fp8_70b_decode(device="cuda")
+    slots, new_k, new_v = _fill_inputs(case, 61)
+    nb, hkv, bs, d = case.k_cache.shape
+    pkv.kv_append(case.k_cache, case.v_cache, new_k, new_v, slots, k_scale=case.k_scale,
+                  v_scale=case.v_scale)
+    torch.cuda.synchronize()
+    t = slots.numel()
+    rng = np.random.default_rng(61)
+    idx = np.unique(np.concatenate([[0, t - 1], rng.choice(t, 512, replace=False)]))
+    n = idx.size
+    nblk = -(-n // bs)
+    small = np.zeros((nblk, hkv, bs, d), dtype=np.uint8)
+    sel = torch.as_tensor(idx, device="cuda")
+    kr, vr, st = oracle.kv_append(small, small.copy(), E4M3, case.k_scale, case.v_scale,
+                                  S(new_k[sel]), S(new_v[sel]), BF16, np.arange(n, dtype=np.int64))
+    assert st == 0
+    ss = slots[sel]
+    for pool, ref in ((case.k_cache, kr), (case.v_cache, vr)):
+        got = S(pool[ss // bs, :, ss % bs, :])
+        want = ref.transpose(0, 2, 1, 3).reshape(nblk * bs, hkv, d)[:n]
+        np.testing.assert_array_equal(got, want)
+    assert pkv.get_device_error() == 0
