@@ -136,3 +136,44 @@ def test_full_context_fill_fp8_70b_layer_sampled():
         want = ref.transpose(0, 2, 1, 3).reshape(nblk * bs, hkv, d)[:n]
         np.testing.assert_array_equal(got, want)
     assert pkv.get_device_error() == 0
+
+
+# K and V scales of the exhaustive fp8 store tests: ordinary amax / 448 values (random and
+# round ones), scale 1, the ends of the range where the store skips its division, and
+# scales outside it
+_FP8_SCALES = [(1.0, 3.0), (1 / 448, 5 / 448), (4 / 448, 4.7316 / 448), (0.83 / 448, 13.1 / 448),
+               (2.0 ** -64, 2.0 ** 64), (2.0 ** -70, 1e30), (3e-30, 0.3), (7.0, 2.0 ** -60)]
+
+
+def _all_patterns(adt, nan):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    exp_mask, man_mask = (0x7F80, 0x007F) if adt == BF16 else (0x7C00, 0x03FF)
+    is_nan = ((bits & exp_mask) == exp_mask) & ((bits & man_mask) != 0)
+    sel = bits[is_nan] if nan else bits[~is_nan]
+    d = 128
+    sel = np.resize(sel, -(-sel.size // d) * d)  # whole rows (repeats a few patterns)
+    tdt = torch.bfloat16 if adt == BF16 else torch.float16
+    return torch.from_numpy(sel.view(np.int16).copy()).view(tdt).reshape(-1, 1, d)
+
+
+@pytest.mark.parametrize("adt", [BF16, F16])
+def test_fp8_store_every_finite_and_infinite_input(adt):
+    # every non-NaN 16-bit pattern, K and V with different scales, against the oracle's
+    # e4m3(fp32(x) / scale): the store's division-free path and its fallback agree with it
+    x = _all_patterns(adt, nan=False)
+    rows, bs = x.shape[0], 16
+    slots = torch.arange(rows, dtype=torch.int64, device="cuda")
+    for ks, vs in _FP8_SCALES:
+        k = torch.zeros((-(-rows // bs), 1, bs, 128), dtype=torch.uint8, device="cuda")
+        v = torch.zeros_like(k)
+        assert _check_append(k, v, E4M3, ks, vs, x.cuda(), x.flip(0).cuda(), adt, slots) == 0
+
+
+@pytest.mark.parametrize("adt", [BF16, F16])
+def test_fp8_store_nan_inputs(adt):
+    x = _all_patterns(adt, nan=True)
+    rows, bs = x.shape[0], 16
+    slots = torch.arange(rows, dtype=torch.int64, device="cuda")
+    k = torch.zeros((-(-rows // bs), 1, bs, 128), dtype=torch.uint8, device="cuda")
+    v = torch.zeros_like(k)
+    assert _check_append(k, v, E4M3, 1 / 448, 1.0, x.cuda(), x.cuda(), adt, slots) == 0
