@@ -87,6 +87,9 @@ def load():
         lib.pkv_paged_decode_attn_append.argtypes = [D, P, P, P, P, P, P, ctypes.c_int, P, I32, P,
                                                       I32, I32, F, I32, I32, P, P, SZ, P]
         lib.pkv_paged_decode_attn_append.restype = ctypes.c_int
+        lib.pkv_paged_decode_attn_noalloc.argtypes = [D, P, P, P, P, ctypes.c_int, P, I32, P, I32,
+                                                       I32, F, I32, I32, P, P]
+        lib.pkv_paged_decode_attn_noalloc.restype = ctypes.c_int
         lib.pkv_extend_workspace_bytes.argtypes = [D, I32, I32, I32, I32]
         lib.pkv_extend_workspace_bytes.restype = SZ
         lib.pkv_paged_extend_attn.argtypes = [D, P, P, P, P, ctypes.c_int, P, P, P, I32, I32, I32,
@@ -180,6 +183,70 @@ def _need(dtype, **tensors):
             raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
 
 
+def _shape(name, t, shape, dtype=None):
+    """A tensor argument must have the shape (and dtype) the call derives from the others: the
+    C ABI takes bare pointers and cannot see how large a buffer is."""
+    if t is None:
+        return
+    want = tuple(int(x) for x in shape)
+    if tuple(t.shape) != want:
+        raise ValueError(f"{name} must have shape {want}, got {tuple(t.shape)}")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _cache_pair(k_cache, v_cache):
+    """K and V pools [num_blocks, num_kv_heads, block_size, head_dim] of one dtype; returns
+    (num_kv_heads, head_dim)."""
+    if k_cache.dim() != 4:
+        raise ValueError("cache must be [num_blocks, num_kv_heads, block_size, head_dim]")
+    _shape("v_cache", v_cache, k_cache.shape, k_cache.dtype)
+    return int(k_cache.shape[1]), int(k_cache.shape[3])
+
+
+def _rows(name, t, head_dim):
+    """[rows, heads, head_dim] activations; returns (rows, heads)."""
+    if t.dim() != 3 or int(t.shape[2]) != head_dim:
+        raise ValueError(f"{name} must be [rows, heads, {head_dim}], got {tuple(t.shape)}")
+    return int(t.shape[0]), int(t.shape[1])
+
+
+def _table(name, t, rows):
+    if t.dim() != 2 or int(t.shape[0]) != rows:
+        raise ValueError(f"{name} must be [{rows}, max_blocks_per_seq], got {tuple(t.shape)}")
+
+
+def _decode_shapes(k_cache, v_cache, q, out, block_tables, seq_lens, lse_out, k_new=None,
+                   v_new=None):
+    """Shapes of a decode call; returns (batch, num_q_heads)."""
+    hkv, d = _cache_pair(k_cache, v_cache)
+    b, hq = _rows("q", q, d)
+    _shape("out", out, q.shape, q.dtype)
+    _table("block_tables", block_tables, b)
+    _shape("seq_lens", seq_lens, (b,))
+    _shape("lse_out", lse_out, (b, hq), torch.float32)
+    _shape("k_new", k_new, (b, hkv, d), q.dtype)
+    _shape("v_new", v_new, (b, hkv, d), q.dtype)
+    return b, hq
+
+
+def _extend_shapes(k_cache, v_cache, q, out, q_indptr, prefix_lens, block_tables, lse_out,
+                   k_new=None, v_new=None):
+    """Shapes of an extend call; returns (total_q_rows, num_q_heads, batch)."""
+    hkv, d = _cache_pair(k_cache, v_cache)
+    rows, hq = _rows("q", q, d)
+    _shape("out", out, q.shape, q.dtype)
+    if prefix_lens.dim() != 1:
+        raise ValueError("prefix_lens must be [batch]")
+    batch = int(prefix_lens.shape[0])
+    _shape("q_indptr", q_indptr, (batch + 1,))
+    _table("block_tables", block_tables, batch)
+    _shape("lse_out", lse_out, (rows, hq), torch.float32)
+    _shape("k_new", k_new, (rows, hkv, d), q.dtype)
+    _shape("v_new", v_new, (rows, hkv, d), q.dtype)
+    return rows, hq, batch
+
+
 def _check(status: int, what: str):
     if status != 0:
         raise PkvError(status, what)
@@ -189,6 +256,12 @@ def kv_append(k_cache, v_cache, k_new, v_new, slot_mapping, k_scale=1.0, v_scale
               stream=None):
     """pkv_kv_append: k_new/v_new [T, Hkv, D] act dtype, slot_mapping int64 [T]."""
     _need(torch.int64, slot_mapping=slot_mapping)
+    hkv, d = _cache_pair(k_cache, v_cache)
+    if slot_mapping.dim() != 1:
+        raise ValueError("slot_mapping must be [num_tokens]")
+    t = int(slot_mapping.shape[0])
+    _shape("k_new", k_new, (t, hkv, d))
+    _shape("v_new", v_new, (t, hkv, d), k_new.dtype)
     lib = load()
     desc = _desc(k_cache, k_scale, v_scale)
     st = lib.pkv_kv_append(ctypes.byref(desc), _ptr(k_cache), _ptr(v_cache), _ptr(k_new),
@@ -211,9 +284,9 @@ def paged_decode_attn(k_cache, v_cache, q, out, block_tables, seq_lens, sm_scale
     """pkv_paged_decode_attn: q/out [B, Hq, D]; block_tables int32 [B, W]; seq_lens int32 [B].
     ``workspace`` is a uint8 device tensor of at least decode_workspace_bytes() bytes."""
     _need(torch.int32, block_tables=block_tables, seq_lens=seq_lens)
+    b, hq = _decode_shapes(k_cache, v_cache, q, out, block_tables, seq_lens, lse_out)
     lib = load()
     desc = _desc(k_cache, k_scale, v_scale)
-    b, hq, _ = q.shape
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     st = lib.pkv_paged_decode_attn(ctypes.byref(desc), _ptr(k_cache), _ptr(v_cache), _ptr(q),
                                    _ptr(out), _dtype_code(q), _ptr(block_tables),
@@ -229,9 +302,10 @@ def paged_decode_attn_append(k_cache, v_cache, k_new, v_new, q, out, block_table
     """pkv_paged_decode_attn_append: k_new/v_new [B, Hkv, D] are written to position
     seq_len-1 of each request and attended in the same launch."""
     _need(torch.int32, block_tables=block_tables, seq_lens=seq_lens)
+    b, hq = _decode_shapes(k_cache, v_cache, q, out, block_tables, seq_lens, lse_out, k_new,
+                           v_new)
     lib = load()
     desc = _desc(k_cache, k_scale, v_scale)
-    b, hq, _ = q.shape
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     st = lib.pkv_paged_decode_attn_append(ctypes.byref(desc), _ptr(k_cache), _ptr(v_cache),
                                           _ptr(k_new), _ptr(v_new), _ptr(q), _ptr(out),
@@ -240,6 +314,23 @@ def paged_decode_attn_append(k_cache, v_cache, k_new, v_new, q, out, block_table
                                           float(sm_scale), int(max_seq_len), int(num_splits),
                                           _ptr(lse_out), _ptr(workspace), ws_bytes, _stream(stream))
     _check(st, "pkv_paged_decode_attn_append")
+
+
+def paged_decode_attn_noalloc(k_cache, v_cache, q, out, block_tables, seq_lens, sm_scale,
+                              max_seq_len, k_scale=1.0, v_scale=1.0, num_splits=0, lse_out=None,
+                              stream=None):
+    """pkv_paged_decode_attn_noalloc: paged_decode_attn with the split partials in the library's
+    own scratch array (no workspace; calls on one device must not overlap)."""
+    _need(torch.int32, block_tables=block_tables, seq_lens=seq_lens)
+    b, hq = _decode_shapes(k_cache, v_cache, q, out, block_tables, seq_lens, lse_out)
+    lib = load()
+    desc = _desc(k_cache, k_scale, v_scale)
+    st = lib.pkv_paged_decode_attn_noalloc(ctypes.byref(desc), _ptr(k_cache), _ptr(v_cache),
+                                           _ptr(q), _ptr(out), _dtype_code(q), _ptr(block_tables),
+                                           int(block_tables.shape[1]), _ptr(seq_lens), b, hq,
+                                           float(sm_scale), int(max_seq_len), int(num_splits),
+                                           _ptr(lse_out), _stream(stream))
+    _check(st, "pkv_paged_decode_attn_noalloc")
 
 
 def shared_prefix_decode_workspace_bytes(k_cache, batch, num_q_heads, max_suffix_len,
@@ -258,9 +349,12 @@ def paged_decode_attn_shared_prefix(k_cache, v_cache, q, out, block_tables, seq_
     share their first group_prefix_lens[g] tokens (read through the group's first member's
     block table), attended once per group; k_new/v_new as paged_decode_attn_append."""
     _need(torch.int32, block_tables=block_tables, seq_lens=seq_lens)
+    b, hq = _decode_shapes(k_cache, v_cache, q, out, block_tables, seq_lens, lse_out, k_new,
+                           v_new)
     lib = load()
     desc = _desc(k_cache, 1.0, 1.0)
-    b, hq, _ = q.shape
+    if group_indptr.dim() != 1:
+        raise ValueError("group_indptr must be int32 [num_groups + 1]")
     ng = int(group_indptr.shape[0]) - 1
     if group_indptr.dtype != torch.int32 or group_prefix_lens.dtype != torch.int32:
         raise ValueError("group_indptr and group_prefix_lens must be int32")
@@ -289,10 +383,10 @@ def paged_extend_attn(k_cache, v_cache, q, out, q_indptr, prefix_lens, block_tab
                       workspace=None, stream=None):
     """pkv_paged_extend_attn: q/out [sum S, Hq, D]; q_indptr int32 [B+1]; prefix_lens int32 [B]."""
     _need(torch.int32, q_indptr=q_indptr, prefix_lens=prefix_lens, block_tables=block_tables)
+    rows, hq, batch = _extend_shapes(k_cache, v_cache, q, out, q_indptr, prefix_lens,
+                                     block_tables, lse_out)
     lib = load()
     desc = _desc(k_cache, k_scale, v_scale)
-    rows, hq, _ = q.shape
-    batch = int(prefix_lens.shape[0])
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     st = lib.pkv_paged_extend_attn(ctypes.byref(desc), _ptr(k_cache), _ptr(v_cache), _ptr(q),
                                    _ptr(out), _dtype_code(q), _ptr(q_indptr), _ptr(prefix_lens),
@@ -306,13 +400,13 @@ def paged_extend_attn(k_cache, v_cache, q, out, q_indptr, prefix_lens, block_tab
 def paged_extend_attn_append(k_cache, v_cache, k_new, v_new, q, out, q_indptr, prefix_lens,
                              block_tables, sm_scale, max_suffix_len, max_total_len, lse_out=None,
                              stream=None):
-    """pkv_paged_extend_attn_append: k_new/v_new [sum S, Hkv, D] (the cache dtype) are written
+    """pkv_paged_extend_attn_append: k_new/v_new [sum S, Hkv, D] (the cache dtype = q's) are written
     to positions prefix_lens[b] + i and attended in the same call (16-bit caches)."""
     _need(torch.int32, q_indptr=q_indptr, prefix_lens=prefix_lens, block_tables=block_tables)
+    rows, hq, batch = _extend_shapes(k_cache, v_cache, q, out, q_indptr, prefix_lens,
+                                     block_tables, lse_out, k_new, v_new)
     lib = load()
     desc = _desc(k_cache, 1.0, 1.0)
-    rows, hq, _ = q.shape
-    batch = int(prefix_lens.shape[0])
     st = lib.pkv_paged_extend_attn_append(ctypes.byref(desc), _ptr(k_cache), _ptr(v_cache),
                                           _ptr(k_new), _ptr(v_new), _ptr(q), _ptr(out),
                                           _dtype_code(q), _ptr(q_indptr), _ptr(prefix_lens),

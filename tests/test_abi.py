@@ -6,6 +6,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import paged_kv_cache_285_gb300 as pkv
 from paged_kv_cache_285_gb300 import build as pkv_build
@@ -166,3 +167,43 @@ def test_binding_refuses_wrong_index_dtypes():
         pkv.paged_extend_attn(c, c, q, q, torch.zeros(3, dtype=torch.int32),
                               torch.zeros(2, dtype=torch.int64),
                               torch.zeros((2, 4), dtype=torch.int32), 0.1, 1, 64)
+
+
+def test_binding_refuses_inconsistent_shapes(lib):
+    # the C ABI takes bare pointers, so the binding checks every tensor against the others
+    # before anything is launched (CPU tensors: consistent ones stop at the device check)
+    c = torch.zeros((4, 2, 16, 128), dtype=torch.bfloat16)
+    q = torch.zeros((3, 8, 128), dtype=torch.bfloat16)
+    kn = torch.zeros((3, 2, 128), dtype=torch.bfloat16)
+    bt = torch.zeros((3, 4), dtype=torch.int32)
+    sl = torch.zeros(3, dtype=torch.int32)
+    ip = torch.zeros(4, dtype=torch.int32)
+    gi = torch.zeros(2, dtype=torch.int32)
+    gp = torch.zeros(1, dtype=torch.int32)
+    bad = [
+        ("v_cache", lambda: pkv.paged_decode_attn(c, c[:3], q, q, bt, sl, 0.1, 64)),
+        ("out", lambda: pkv.paged_decode_attn(c, c, q, q[:2], bt, sl, 0.1, 64)),
+        ("out", lambda: pkv.paged_decode_attn(c, c, q, q.float(), bt, sl, 0.1, 64)),
+        ("q", lambda: pkv.paged_decode_attn(c, c, q[..., :64], q[..., :64], bt, sl, 0.1, 64)),
+        ("block_tables", lambda: pkv.paged_decode_attn(c, c, q, q, bt[:2], sl, 0.1, 64)),
+        ("seq_lens", lambda: pkv.paged_decode_attn(c, c, q, q, bt, sl[:2], 0.1, 64)),
+        ("lse_out", lambda: pkv.paged_decode_attn(c, c, q, q, bt, sl, 0.1, 64,
+                                                  lse_out=torch.zeros((3, 7)))),
+        ("k_new", lambda: pkv.paged_decode_attn_append(c, c, kn[:2], kn[:2], q, q, bt, sl, 0.1, 64)),
+        ("seq_lens", lambda: pkv.paged_decode_attn_noalloc(c, c, q, q, bt, sl[:2], 0.1, 64)),
+        ("k_new", lambda: pkv.paged_decode_attn_shared_prefix(c, c, q, q, bt, sl, 0.1, gi, gp, 3, 64,
+                                                              k_new=kn[:1], v_new=kn[:1])),
+        ("k_new", lambda: pkv.kv_append(c, c, kn, kn, torch.zeros(2, dtype=torch.int64))),
+        ("v_new", lambda: pkv.kv_append(c, c, kn, kn.half(), torch.zeros(3, dtype=torch.int64))),
+        ("q_indptr", lambda: pkv.paged_extend_attn(c, c, q, q, ip[:3], sl, bt, 0.1, 8, 64)),
+        ("block_tables", lambda: pkv.paged_extend_attn(c, c, q, q, ip, sl, bt[:1], 0.1, 8, 64)),
+        ("k_new", lambda: pkv.paged_extend_attn_append(c, c, kn[:2], kn[:2], q, q, ip, sl, bt, 0.1,
+                                                       8, 64)),
+    ]
+    for name, call in bad:
+        with pytest.raises(ValueError, match=name):
+            call()
+    with pytest.raises(ValueError, match="device tensors"):
+        pkv.paged_decode_attn(c, c, q, q, bt, sl, 0.1, 64)
+    with pytest.raises(ValueError, match="device tensors"):
+        pkv.paged_extend_attn_append(c, c, kn, kn, q, q, ip, sl, bt, 0.1, 8, 64)
