@@ -568,7 +568,23 @@ def run_prefix_index_bench(n_requests=20000, seed=0):
                         "8,192-block pool", "requests": n_requests,
             "requests_per_s": round(n_requests / dt, 1),
             "cached_token_frac": round(hit / max(total, 1), 4), "refused": refused,
-            "note": "host C++ index driven through the Python binding (5 calls per request)"}
+            "note": "host C++ index driven through the Python binding (5 calls per request)",
+            "native_c_abi": _radix_trace_native(n_requests)}
+
+
+def _radix_trace_native(n_requests):
+    """The same trace recipe replayed by the library's own C++ driver (radix_trace, built
+    with libpkv.so): the index's throughput without the binding's per-call overhead."""
+    exe = os.path.join(os.path.dirname(os.path.abspath(__file__)), "paged_kv_cache_285_gb300",
+                       "radix_trace")
+    if not os.path.exists(exe):
+        return {"status": "not built"}
+    r = subprocess.run([exe, str(n_requests)], capture_output=True, text=True, timeout=120)
+    if r.returncode != 0:
+        return {"status": f"exit {r.returncode}"}
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    d["note"] = "C++ driver through the C ABI, std::mt19937_64 trace of the same recipe"
+    return d
 
 
 def run_shared_prefix_bench(dev, hbm, peak_src, n=20):

@@ -226,3 +226,20 @@ def test_random_workload_with_eviction_keeps_the_pool_consistent():
     # every tree block is unlocked and evictable at the end
     x.evict(pool)
     assert x.stats()["tree_blocks"] == 0 and x.stats()["free_blocks"] == pool
+
+
+def test_native_trace_driver():
+    # the C++ replay that bench.py reports: builds with the library, runs the whole trace
+    # through the C ABI without an error, refuses no request, and reuses the shared prompts
+    import json
+    import subprocess
+
+    from paged_kv_cache_285_gb300 import build as pkv_build
+    pkv_build.build()
+    r = subprocess.run([pkv_build.TRACE_BIN, "3000"], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    d = json.loads(r.stdout)
+    assert d["requests"] == 3000 and d["refused"] == 0
+    # 64 prompts of 1,000 tokens (62 whole blocks each) under 10..200 new tokens: once every
+    # prompt is cached, about 992 of ~1,105 tokens of a request come from the index
+    assert 0.8 < d["cached_token_frac"] < 0.9
