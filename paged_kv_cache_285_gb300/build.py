@@ -78,10 +78,15 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         run([cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs])
         os.replace(tmp, LIB)
     if force or _stale(TRACE_BIN, [TRACE_SRC, LIB]):
+        # an auxiliary benchmark driver: if it does not build, the library still stands
+        # (bench.py then reports it as not built)
         tmp = TRACE_BIN + f".tmp{os.getpid()}"
-        run([cc, "-O3", "-std=c++17", f"-I{INCLUDE}", TRACE_SRC, "-o", tmp, f"-L{HERE}", "-lpkv",
-             "-Xlinker", "-rpath", "-Xlinker", "$ORIGIN"])
-        os.replace(tmp, TRACE_BIN)
+        try:
+            run([cc, "-O3", "-std=c++17", f"-I{INCLUDE}", TRACE_SRC, "-o", tmp, f"-L{HERE}",
+                 "-lpkv", "-Xlinker", "-rpath", "-Xlinker", "$ORIGIN"])
+            os.replace(tmp, TRACE_BIN)
+        except RuntimeError:
+            sys.stderr.write("radix_trace was not built; the library is unaffected\n")
     return LIB
 
 
