@@ -579,10 +579,13 @@ def _radix_trace_native(n_requests):
                        "radix_trace")
     if not os.path.exists(exe):
         return {"status": "not built"}
-    r = subprocess.run([exe, str(n_requests)], capture_output=True, text=True, timeout=120)
-    if r.returncode != 0:
-        return {"status": f"exit {r.returncode}"}
-    d = json.loads(r.stdout.strip().splitlines()[-1])
+    try:
+        r = subprocess.run([exe, str(n_requests)], capture_output=True, text=True, timeout=120)
+        if r.returncode != 0:
+            return {"status": f"exit {r.returncode}"}
+        d = json.loads(r.stdout.strip().splitlines()[-1])
+    except (subprocess.SubprocessError, ValueError, IndexError) as e:
+        return {"status": f"failed: {e}"}
     d["note"] = "C++ driver through the C ABI, std::mt19937_64 trace of the same recipe"
     return d
 
