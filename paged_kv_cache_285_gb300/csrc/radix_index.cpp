@@ -29,10 +29,33 @@ namespace {
 
 enum : uint8_t { kFree = 0, kCaller = 1, kTree = 2 };
 
+// One block of token ids, viewed in place (a lookup key that allocates nothing).
+struct BlockView {
+  const int32_t* p;
+  int32_t n;
+};
+
+// Lexicographic order of token blocks, comparable across stored keys and views.
+struct BlockLess {
+  using is_transparent = void;
+  static bool less(const int32_t* a, size_t na, const int32_t* b, size_t nb) {
+    return std::lexicographical_compare(a, a + na, b, b + nb);
+  }
+  bool operator()(const std::vector<int32_t>& a, const std::vector<int32_t>& b) const {
+    return less(a.data(), a.size(), b.data(), b.size());
+  }
+  bool operator()(const std::vector<int32_t>& a, const BlockView& b) const {
+    return less(a.data(), a.size(), b.p, (size_t)b.n);
+  }
+  bool operator()(const BlockView& a, const std::vector<int32_t>& b) const {
+    return less(a.p, (size_t)a.n, b.data(), b.size());
+  }
+};
+
 struct Node {
   std::vector<int32_t> tokens;  // edge label: a whole number of blocks of token ids
   std::vector<int32_t> blocks;  // physical block of each block of the label
-  std::map<std::vector<int32_t>, std::unique_ptr<Node>> children;  // by first block's tokens
+  std::map<std::vector<int32_t>, std::unique_ptr<Node>, BlockLess> children;  // by first block
   Node* parent = nullptr;
   uint64_t last_use = 0;
   int64_t locks = 0;
@@ -53,9 +76,7 @@ struct pkv_radix_index {
   int64_t tree_blocks = 0;
   std::set<std::pair<uint64_t, Node*>> evictable;  // unlocked leaves, least recently used first
 
-  std::vector<int32_t> key_at(const int32_t* tokens, int64_t blk) const {
-    return std::vector<int32_t>(tokens + blk * bs, tokens + (blk + 1) * bs);
-  }
+  BlockView key_at(const int32_t* tokens, int64_t blk) const { return {tokens + blk * bs, bs}; }
 
   // Keep a node's entry in the evictable set in step with its state.
   void refresh(Node* n) {
@@ -82,7 +103,7 @@ struct pkv_radix_index {
     m->last_use = n->last_use;
     m->locks = n->locks;  // every lock through n also runs through m
     Node* parent = n->parent;
-    auto& slot = parent->children[std::vector<int32_t>(n->tokens.begin(), n->tokens.begin() + bs)];
+    auto& slot = parent->children.find(key_at(n->tokens.data(), 0))->second;
     std::unique_ptr<Node> lower = std::move(slot);
     lower->tokens.erase(lower->tokens.begin(), lower->tokens.begin() + k * bs);
     lower->blocks.erase(lower->blocks.begin(), lower->blocks.begin() + k);
@@ -136,7 +157,7 @@ struct pkv_radix_index {
     }
     tree_blocks -= (int64_t)n->blocks.size();
     Node* parent = n->parent;
-    parent->children.erase(std::vector<int32_t>(n->tokens.begin(), n->tokens.begin() + bs));
+    parent->children.erase(parent->children.find(key_at(n->tokens.data(), 0)));
     --nodes;
     refresh(parent);
     return true;
@@ -287,7 +308,9 @@ pkv_status pkv_radix_insert(pkv_radix_index* x, const int32_t* tokens, int32_t n
     for (int32_t b : l->blocks) x->state[b] = kTree;
     x->tree_blocks += nblk - r.second;
     l->parent = r.first;
-    r.first->children.emplace(x->key_at(tokens, r.second), std::move(leaf));
+    r.first->children.emplace(
+        std::vector<int32_t>(tokens + r.second * x->bs, tokens + (r.second + 1) * x->bs),
+        std::move(leaf));
     ++x->nodes;
     x->refresh(r.first);
     x->touch(l);
