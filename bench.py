@@ -186,6 +186,14 @@ def max_over_ranks(x: float, world: int) -> float:
 
 
 # ---------------------------------------------------------------------------------
+def extend_useful_flops(prefix_lens, suffix_lens, num_q_heads, head_dim):
+    """Useful flops of a suffix prefill: suffix row i of a request with prefix P sees P + i + 1
+    keys, and each (row, head, key) costs 2 * head_dim for the score and 2 * head_dim for its
+    share of P V (padding rows and masked keys a kernel computes are not counted)."""
+    keys = sum(p * s + s * (s + 1) // 2 for p, s in zip(prefix_lens, suffix_lens))
+    return 4.0 * head_dim * num_q_heads * keys
+
+
 def decode_step_bytes(case):
     """Algorithmic HBM bytes of one step: append of B tokens + decode over sum(seq_lens)."""
     from paged_kv_cache_285_gb300 import workloads as W
@@ -509,8 +517,7 @@ def run_extend_bench(args, dev, bf16, bf16_sus, peak_src):
     t_app = t_step - t_ext
     app_bytes = rows * case.num_kv_heads * d * 2 * 2 * 2 + 8 * rows
     hbm = peaks()[0]
-    keys = sum(P + i + 1 for i in range(Sfx))
-    flops = 4.0 * d * hq * keys * B
+    flops = extend_useful_flops([P] * B, [Sfx] * B, hq, d)
     tf = flops / (t_ext * 1e-3) / 1e12
     return {"workload": "shared_prefix_extend", "batch": B, "prefix": P, "suffix": Sfx,
             "num_q_heads": hq, "num_kv_heads": case.num_kv_heads, "head_dim": d,
