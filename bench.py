@@ -38,6 +38,9 @@ import torch  # noqa: E402
 METRIC = "paged decode attn HBM GB/s (% of GB300 peak) & tokens/s; extend TFLOP/s"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+# GB300 datasheet figures (context beside the measured peaks): HBM3e bandwidth and dense bf16
+NOMINAL_HBM_GBS = 7900.0
+NOMINAL_BF16_TFLOPS = 2250.0
 
 
 # ---------------------------------------------------------------------------------
@@ -297,6 +300,8 @@ def run_decode_bench(args, world, rank, local):
     ms_sep = max_over_ranks(sum(step_ms) / K, world)
     ms_dec = sum(dec_ms) / K
     ms_step_max = max_over_ranks(sum(fused_ms) / K, world)
+    ms_step_med = max_over_ranks(_median(fused_ms), world)
+    ms_dec_med = _median(dec_ms)
 
     app_b, dec_b = decode_step_bytes(case)
     step_bytes = app_b + dec_b
@@ -309,6 +314,8 @@ def run_decode_bench(args, world, rank, local):
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step_max, 5),
+        "ms_per_step_median": round(ms_step_med, 5),
+        "value_median": round(world * step_bytes / (ms_step_med * 1e-3) / 1e9, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": W.DTYPE_NAME[case.cache_dtype],
         "data": "synthetic (seeded N(0,1) K/V/q, random block permutation)",
         "config": {"workload": args.workload, "batch": b, "num_q_heads": case.num_q_heads,
@@ -339,6 +346,9 @@ def run_decode_bench(args, world, rank, local):
                        "bound": "hbm", "achieved": round(dec_gbs, 1), "peak": hbm,
                        "unit": "GB/s", "frac": round(dec_gbs / hbm, 4),
                        "peak_source": f"{peak_src} (hbm_gbs)",
+                       "achieved_median": round(dec_b / (ms_dec_med * 1e-3) / 1e9, 1),
+                       "frac_of_nominal": round(dec_gbs / NOMINAL_HBM_GBS, 4),
+                       "nominal_peak": NOMINAL_HBM_GBS,
                        "algorithmic_bytes_per_launch": dec_b,
                        "traffic": traffic}
     res["clocks"] = clk.summary()
@@ -451,10 +461,70 @@ def e2e_decode(case, pkv, max_len, ws, out, stream, K, world):
             "launch": "the step (copies + API call) captured once as a CUDA graph and replayed"}
 
 
+def _median(xs):
+    ys = sorted(xs)
+    n = len(ys)
+    return ys[n // 2] if n % 2 else 0.5 * (ys[n // 2 - 1] + ys[n // 2])
+
+
+def _time_extend_case(case, P, Sfx, n, flush, with_append):
+    """Mean and median device time of paged_extend_attn on `case` (L2 flushed before each
+    call); with_append: also the step with the suffix's kv_append before it and the one-call
+    paged_extend_attn_append.  Returns a dict of lists of ms."""
+    import paged_kv_cache_285_gb300 as pkv
+    out = torch.empty_like(case.q)
+    sc = dict(k_scale=case.k_scale, v_scale=case.v_scale)
+
+    def append():
+        pkv.kv_append(case.k_cache, case.v_cache, case.suffix_k, case.suffix_v, case.suffix_slots,
+                      **sc)
+
+    def extend():
+        pkv.paged_extend_attn(case.k_cache, case.v_cache, case.q, out, case.q_indptr,
+                              case.prefix_lens, case.block_tables, case.sm_scale, Sfx, P + Sfx,
+                              **sc)
+
+    def fused():
+        pkv.paged_extend_attn_append(case.k_cache, case.v_cache, case.suffix_k, case.suffix_v,
+                                     case.q, out, case.q_indptr, case.prefix_lens,
+                                     case.block_tables, case.sm_scale, Sfx, P + Sfx, **sc)
+
+    for _ in range(3):
+        if with_append:
+            append()
+            fused()
+        extend()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    t = {"extend": [], "step": [], "fused": []}
+    for _ in range(n):
+        flush()
+        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        e0.record(stream)
+        if with_append:
+            append()
+        e1.record(stream)
+        extend()
+        e2.record(stream)
+        e2.synchronize()
+        t["extend"].append(e1.elapsed_time(e2))
+        t["step"].append(e0.elapsed_time(e2))
+        if with_append:
+            flush()
+            e3, e4 = (torch.cuda.Event(enable_timing=True) for _ in range(2))
+            e3.record(stream)
+            fused()
+            e4.record(stream)
+            e4.synchronize()
+            t["fused"].append(e3.elapsed_time(e4))
+    return t
+
+
 def run_extend_bench(args, dev, bf16, bf16_sus, peak_src):
     """paged_extend_attn on 256 requests x 100 suffix tokens over a shared 1,900-token
     prefix (useful causal flops only); the step with the suffix's kv_append as a
-    separate launch and as paged_extend_attn_append (written by the extend kernel)."""
+    separate launch and as paged_extend_attn_append.  The same workload is also timed with
+    an fp8 e4m3 cache (bf16 queries) and at head_dim 64."""
     import paged_kv_cache_285_gb300 as pkv
     from paged_kv_cache_285_gb300 import workloads as W
     try:
@@ -462,56 +532,18 @@ def run_extend_bench(args, dev, bf16, bf16_sus, peak_src):
     except Exception as e:  # pragma: no cover
         return {"error": str(e)}
     rows = case.q.shape[0]
-    out = torch.empty_like(case.q)
     P, Sfx = 1900, 100
     B = case.prefix_lens.shape[0]
-
-    def append():
-        pkv.kv_append(case.k_cache, case.v_cache, case.suffix_k, case.suffix_v, case.suffix_slots)
-
-    def extend():
-        pkv.paged_extend_attn(case.k_cache, case.v_cache, case.q, out, case.q_indptr,
-                              case.prefix_lens, case.block_tables, case.sm_scale, Sfx, P + Sfx)
-
-    try:
-        extend()
-    except pkv.PkvError as e:
-        return {"status": "not built", "error": str(e)}
-    def fused():
-        pkv.paged_extend_attn_append(case.k_cache, case.v_cache, case.suffix_k, case.suffix_v,
-                                     case.q, out, case.q_indptr, case.prefix_lens,
-                                     case.block_tables, case.sm_scale, Sfx, P + Sfx)
-
-    for _ in range(3):
-        append()
-        extend()
-        fused()
-    torch.cuda.synchronize()
-    stream = torch.cuda.current_stream()
     n = max(5, min(50, args.steps))
     flush = L2Flush(dev)
-    t_ext = t_step = t_fused = 0.0
-    for _ in range(n):
-        flush()
-        e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
-        e0.record(stream)
-        append()
-        e1.record(stream)
-        extend()
-        e2.record(stream)
-        e2.synchronize()
-        t_ext += e1.elapsed_time(e2)
-        t_step += e0.elapsed_time(e2)
-        flush()
-        e3, e4 = (torch.cuda.Event(enable_timing=True) for _ in range(2))
-        e3.record(stream)
-        fused()
-        e4.record(stream)
-        e4.synchronize()
-        t_fused += e3.elapsed_time(e4)
-    t_ext /= n
-    t_step /= n
-    t_fused /= n
+    try:
+        t = _time_extend_case(case, P, Sfx, n, flush, True)
+    except pkv.PkvError as e:
+        return {"status": "not built", "error": str(e)}
+    t_ext = sum(t["extend"]) / n
+    t_step = sum(t["step"]) / n
+    t_fused = sum(t["fused"]) / n
+    med_ext = _median(t["extend"])
     hq, d = case.num_q_heads, case.head_dim
     # the suffix's kv_append: K and V rows read from the inputs and written to the cache
     t_app = t_step - t_ext
@@ -519,24 +551,52 @@ def run_extend_bench(args, dev, bf16, bf16_sus, peak_src):
     hbm = peaks()[0]
     flops = extend_useful_flops([P] * B, [Sfx] * B, hq, d)
     tf = flops / (t_ext * 1e-3) / 1e12
-    return {"workload": "shared_prefix_extend", "batch": B, "prefix": P, "suffix": Sfx,
-            "num_q_heads": hq, "num_kv_heads": case.num_kv_heads, "head_dim": d,
-            "ms_per_call": round(t_ext, 5), "ms_per_step_with_append": round(t_step, 5),
-            "ms_per_step_fused_append": round(t_fused, 5),
-            "kv_append": {"tokens": rows, "ms": round(t_app, 5), "bytes": app_bytes,
-                          "gbs": round(app_bytes / (t_app * 1e-3) / 1e9, 1),
-                          "frac_of_hbm": round(app_bytes / (t_app * 1e-3) / 1e9 / hbm, 4)},
-            "tflops": round(tf, 1), "useful_flops_per_call": flops,
-            "roofline": {"kernel": "paged_extend_attn", "bound": "tensor", "achieved": round(tf, 1),
-                         "peak": bf16, "unit": "TFLOP/s", "frac": round(tf / bf16, 4),
-                         "peak_source": f"{peak_src} (bf16_tflops burst)",
-                         "traffic": profiled_traffic(
-                             "extend_kernel_shared_prefix_extend.md",
-                             ["paged_kv_cache_285_gb300/csrc/extend.cu",
-                              "paged_kv_cache_285_gb300/csrc/ptx.cuh",
-                              "paged_kv_cache_285_gb300/csrc/tcgen05.cuh",
-                              "paged_kv_cache_285_gb300/csrc/internal.h"
-                              "#ExtendParams,ExtendPartialParams,FastDiv"])}}
+    res = {"workload": "shared_prefix_extend", "batch": B, "prefix": P, "suffix": Sfx,
+           "num_q_heads": hq, "num_kv_heads": case.num_kv_heads, "head_dim": d,
+           "ms_per_call": round(t_ext, 5), "ms_per_call_median": round(med_ext, 5),
+           "ms_per_step_with_append": round(t_step, 5),
+           "ms_per_step_fused_append": round(t_fused, 5),
+           "kv_append": {"tokens": rows, "ms": round(t_app, 5), "bytes": app_bytes,
+                         "gbs": round(app_bytes / (t_app * 1e-3) / 1e9, 1),
+                         "frac_of_hbm": round(app_bytes / (t_app * 1e-3) / 1e9 / hbm, 4)},
+           "tflops": round(tf, 1), "tflops_median": round(flops / (med_ext * 1e-3) / 1e12, 1),
+           "useful_flops_per_call": flops,
+           "roofline": {"kernel": "paged_extend_attn", "bound": "tensor", "achieved": round(tf, 1),
+                        "peak": bf16, "unit": "TFLOP/s", "frac": round(tf / bf16, 4),
+                        "peak_source": f"{peak_src} (bf16_tflops burst)",
+                        "frac_of_nominal": round(tf / NOMINAL_BF16_TFLOPS, 4),
+                        "nominal_peak": NOMINAL_BF16_TFLOPS,
+                        "traffic": profiled_traffic(
+                            "extend_kernel_shared_prefix_extend.md",
+                            ["paged_kv_cache_285_gb300/csrc/extend.cu",
+                             "paged_kv_cache_285_gb300/csrc/ptx.cuh",
+                             "paged_kv_cache_285_gb300/csrc/tcgen05.cuh",
+                             "paged_kv_cache_285_gb300/csrc/internal.h"
+                             "#ExtendParams,ExtendPartialParams,FastDiv"])}}
+    del case
+    # the same workload over an fp8 cache (codes widened inside the kernel) and at d64
+    for key, cdt, hd in (("extend_fp8", W.E4M3, 128), ("extend_d64", W.BF16, 64)):
+        try:
+            c = W.extend_case([P] * B, [Sfx] * B, hq, 8, hd, 16, cdt, W.BF16, seed=3,
+                              device="cuda", shared_prefix=P)
+            tt = _time_extend_case(c, P, Sfx, n, flush, False)
+        except pkv.PkvError as e:
+            res[key] = {"status": "failed", "error": str(e)}
+            continue
+        te, tm = sum(tt["extend"]) / n, _median(tt["extend"])
+        fl = extend_useful_flops([P] * B, [Sfx] * B, hq, hd)
+        tfx = fl / (te * 1e-3) / 1e12
+        res[key] = {"cache_dtype": W.DTYPE_NAME[cdt], "act_dtype": "bf16", "head_dim": hd,
+                    "ms_per_call": round(te, 5), "ms_per_call_median": round(tm, 5),
+                    "useful_flops_per_call": fl, "tflops": round(tfx, 1),
+                    "frac": round(tfx / bf16, 4), "frac_of_nominal": round(tfx / NOMINAL_BF16_TFLOPS, 4),
+                    "peak_source": f"{peak_src} (bf16_tflops burst)",
+                    "workspace_bytes": pkv.extend_workspace_bytes(c.k_cache, B, hq, rows, P + Sfx,
+                                                                  k_scale=c.k_scale,
+                                                                  v_scale=c.v_scale),
+                    "cache_bytes": 2 * c.k_cache.numel() * c.k_cache.element_size()}
+        del c
+    return res
 
 
 def run_prefix_index_bench(n_requests=20000, seed=0):
@@ -579,12 +639,35 @@ def run_prefix_index_bench(n_requests=20000, seed=0):
             "native_c_abi": _radix_trace_native(n_requests)}
 
 
+def _build_radix_trace():
+    """Compile bench_native/radix_trace.cpp (a benchmark driver, not part of the library)
+    against libpkv.so; returns the executable's path or None."""
+    import shutil
+    here = os.path.dirname(os.path.abspath(__file__))
+    src = os.path.join(here, "bench_native", "radix_trace.cpp")
+    libdir = os.path.join(here, "paged_kv_cache_285_gb300")
+    exe = os.path.join(here, "bench_native", "radix_trace")
+    if os.path.exists(exe) and os.path.getmtime(exe) >= max(
+            os.path.getmtime(src), os.path.getmtime(os.path.join(libdir, "libpkv.so"))):
+        return exe
+    cxx = shutil.which("g++") or shutil.which("c++")
+    if cxx is None:
+        return None
+    tmp = exe + f".tmp{os.getpid()}"
+    r = subprocess.run([cxx, "-O3", "-std=c++17", f"-I{os.path.join(here, 'include')}",
+                        "-I/usr/local/cuda/include", src, "-o", tmp, f"-L{libdir}", "-lpkv",
+                        f"-Wl,-rpath,{libdir}"], capture_output=True, text=True)
+    if r.returncode != 0:
+        return None
+    os.replace(tmp, exe)
+    return exe
+
+
 def _radix_trace_native(n_requests):
-    """The same trace recipe replayed by the library's own C++ driver (radix_trace, built
-    with libpkv.so): the index's throughput without the binding's per-call overhead."""
-    exe = os.path.join(os.path.dirname(os.path.abspath(__file__)), "paged_kv_cache_285_gb300",
-                       "radix_trace")
-    if not os.path.exists(exe):
+    """The same trace recipe replayed by a C++ driver (bench_native/radix_trace.cpp) through
+    the C ABI: the index's throughput without the binding's per-call overhead."""
+    exe = _build_radix_trace()
+    if exe is None:
         return {"status": "not built"}
     try:
         r = subprocess.run([exe, str(n_requests)], capture_output=True, text=True, timeout=120)
@@ -616,7 +699,7 @@ def run_shared_prefix_bench(dev, hbm, peak_src, n=20):
     out_p, out_c = torch.empty_like(case.q), torch.empty_like(case.q)
     ws_p = torch.empty(max(pkv.decode_workspace_bytes(case.k_cache, b, hq, max_len, 0), 256),
                        dtype=torch.uint8, device=dev)
-    ws_c = torch.empty(pkv.shared_prefix_decode_workspace_bytes(case.k_cache, b, hq,
+    ws_c = torch.empty(pkv.shared_prefix_decode_workspace_bytes(case.k_cache, b, hq, prefix,
                                                                 max_len - prefix, 0),
                        dtype=torch.uint8, device=dev)
 
@@ -627,7 +710,7 @@ def run_shared_prefix_bench(dev, hbm, peak_src, n=20):
     def cascade():
         pkv.paged_decode_attn_shared_prefix(case.k_cache, case.v_cache, case.q, out_c,
                                             case.block_tables, case.seq_lens, case.sm_scale, gi,
-                                            gp, b, max_len - prefix, workspace=ws_c)
+                                            gp, b, prefix, max_len - prefix, workspace=ws_c)
 
     stream = torch.cuda.current_stream(dev)
     for _ in range(3):

@@ -139,7 +139,11 @@ pkv_status pkv_kv_append(const pkv_cache_desc* desc, void* k_cache, void* v_cach
  * workspace:     device scratch of pkv_decode_workspace_bytes() bytes (may be
  *                NULL when that is 0).  Concurrent calls need separate
  *                workspaces.
- * Supported: head_dim 64/128, block_size 16/32, num_q_heads/num_kv_heads <= 8.
+ * Supported: head_dim 64/128, block_size 16/32, any GQA group
+ * num_q_heads/num_kv_heads.  One CTA takes up to 8 query heads of a kv head:
+ * a group of more than 8 is split into chunks of 8 heads whose CTAs each read
+ * the kv head's pages (K/V bytes are read once per chunk, mostly from L2
+ * after the first).
  * ------------------------------------------------------------------------- */
 size_t pkv_decode_workspace_bytes(const pkv_cache_desc* desc, int32_t batch,
                                   int32_t num_q_heads, int32_t max_seq_len,
@@ -186,98 +190,6 @@ pkv_status pkv_paged_decode_attn_append(const pkv_cache_desc* desc, void* k_cach
                                         size_t workspace_bytes, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
- * pkv_paged_decode_attn_shared_prefix -- decode for groups of requests that
- * share a cached prefix, the prefix attended once per group.
- *
- * "KV Cache 완전 정리 — PagedAttention vs RadixAttention, SGLang이 빠른 이유",
- * section "RadixAttention — SGLang의 혁신", and "PagedAttention과
- * RadixAttention으로 LLM KV 캐시 최적화", section 03: many requests share one
- * long prefix (a system prompt) whose KV blocks are stored once.  Plain
- * decode reads those blocks once per request; this call computes the
- * prefix's attention for all (request, head) rows of a group in one dense
- * pass on the tensor cores, attends each request's own tokens with the
- * split-KV decode kernel, and merges the parts with their log-sum-exps,
- * which equals attention over the whole sequence up to rounding.
- *
- * Groups: request b belongs to group g when group_indptr[g] <= b <
- * group_indptr[g+1]; group_indptr (int32 [num_groups+1], device) rises from 0
- * to batch.  group_prefix_lens (int32 [num_groups], device): P_g, the tokens
- * every member of the group holds with the same K/V (0 = none).  Only whole
- * blocks are shared: with W_g = floor(P_g / block_size) * block_size, tokens
- * 0 .. W_g-1 of every member are read once for the group, through the block
- * table of its first member (block_tables[group_indptr[g]]; the other
- * members' entries for them are not read), and tokens W_g .. seq_lens[b]-1
- * through the member's own table.  P_g <= seq_lens[b] for every member (else
- * the device error word reports PKV_DEVERR_BAD_LENGTH).  A request that no
- * group covers is attended over its whole sequence through its own table and
- * reported the same way.
- *
- * k_new, v_new:  nullable together; as pkv_paged_decode_attn_append (the
- *                current token, position seq_lens[b]-1, must lie at or after
- *                W_g).
- * max_group_size: host bound of the members per group (sizes the prefix pass).
- * max_suffix_len: host bound of seq_lens[b] - P_g (sizes the split plan).
- * num_splits:    as pkv_paged_decode_attn, for the members' own tokens.
- * workspace:     pkv_shared_prefix_decode_workspace_bytes() bytes, 256-byte
- *                aligned (always needed).
- * q:             16-byte aligned.  Everything else as pkv_paged_decode_attn.
- * Streams: the prefix pass runs on a side stream the library keeps per device
- * (highest priority), forked from `stream` by an event at the call and joined
- * back before the merge, so it overlaps the decode of the members' own
- * tokens; the call as a whole is ordered on `stream` like any other and can
- * be captured into a CUDA graph.  Calls on one device from several host
- * threads are serialised around the fork and join.
- * Supported: head_dim 128, f16 or bf16 cache with the same act dtype,
- * block_size 16/32, num_q_heads/num_kv_heads in {1, 2, 4, 8}, sm_scale > 0.
- * ------------------------------------------------------------------------- */
-size_t pkv_shared_prefix_decode_workspace_bytes(const pkv_cache_desc* desc, int32_t batch,
-                                                int32_t num_q_heads, int32_t max_suffix_len,
-                                                int32_t num_splits);
-
-pkv_status pkv_paged_decode_attn_shared_prefix(
-    const pkv_cache_desc* desc, void* k_cache, void* v_cache, const void* k_new,
-    const void* v_new, const void* q, void* out, pkv_dtype act_dtype,
-    const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
-    int32_t batch, int32_t num_q_heads, float sm_scale, const int32_t* group_indptr,
-    const int32_t* group_prefix_lens, int32_t num_groups, int32_t max_group_size,
-    int32_t max_suffix_len, int32_t num_splits, float* lse_out, void* workspace,
-    size_t workspace_bytes, cudaStream_t stream);
-
-/* ---------------------------------------------------------------------------
- * pkv_paged_extend_attn -- suffix prefill over a cached prefix.
- *
- * "PagedAttention과 RadixAttention으로 LLM KV 캐시 최적화", section 03: when
- * the longest cached prefix of a request has P tokens, only the remaining
- * suffix is computed (2,000-token request with 1,900 cached -> 100 prefilled).
- * Request b owns query rows q_indptr[b] .. q_indptr[b+1]-1; its row i sits at
- * position P_b + i (P_b = prefix_lens[b]) and attends to keys 0 .. P_b + i:
- * every cached prefix token plus the suffix causally.  The suffix's own K/V
- * must already be in the cache at positions P_b .. P_b+S_b-1 (pkv_kv_append
- * first), so every key is read through the block table.
- *
- * q, out:        [q_indptr[batch]][num_q_heads][head_dim] act dtype.
- * q_indptr:      int32 [batch+1], device, non-decreasing, q_indptr[0] = 0.
- * prefix_lens:   int32 [batch], device.
- * sm_scale:      softmax scale, finite and > 0.
- * max_suffix_len / max_total_len: host-side upper bounds of S_b and P_b+S_b.
- * total_q_rows:  q_indptr[batch] (host value; sizes the grid).
- * lse_out:       nullable float [q_indptr[batch]][num_q_heads], natural log.
- * workspace:     device memory of at least pkv_extend_workspace_bytes()
- *                bytes, 256-byte aligned, owned by the caller; its contents
- *                need no initialisation and are scratch after the call.  0
- *                bytes (NULL allowed) for 16-bit caches.  For an fp8 cache it
- *                holds a claim flag per physical block and 16-bit shadow K and
- *                V pools of the activation dtype (4*num_blocks rounded up to
- *                256, plus twice num_blocks*Hkv*bs*D*2 rounded up to 256):
- *                every page a request of the call reads is widened there once
- *                (exactly: e4m3 fits f16 and bf16) and the 16-bit kernel runs
- *                on the shadow pools; k_scale and v_scale are applied to the
- *                scores and the output.  Too small -> PKV_ERR_WORKSPACE.  Two
- *                calls in flight must not share a workspace.
- * Supported: head_dim 128, block_size 16/32, num_q_heads/num_kv_heads in
- * {1, 2, 4, 8}; cache dtype equal to the act dtype (f16, bf16) or fp8 e4m3.
- * ------------------------------------------------------------------------- */
-/* ---------------------------------------------------------------------------
  * pkv_paged_decode_attn_noalloc -- the same decode as pkv_paged_decode_attn,
  * for callers that cannot allocate device memory.
  *
@@ -313,6 +225,109 @@ pkv_status pkv_paged_decode_attn_noalloc(const pkv_cache_desc* desc, const void*
                                          int32_t max_seq_len, int32_t num_splits,
                                          float* lse_out, cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * pkv_paged_decode_attn_shared_prefix -- decode for groups of requests that
+ * share a cached prefix, the prefix attended once per group.
+ *
+ * "KV Cache 완전 정리 — PagedAttention vs RadixAttention, SGLang이 빠른 이유",
+ * section "RadixAttention — SGLang의 혁신", and "PagedAttention과
+ * RadixAttention으로 LLM KV 캐시 최적화", section 03: many requests share one
+ * long prefix (a system prompt) whose KV blocks are stored once.  Plain
+ * decode reads those blocks once per request; this call computes the
+ * prefix's attention for all (request, head) rows of a group in one dense
+ * pass on the tensor cores, attends each request's own tokens with the
+ * split-KV decode kernel, and merges the parts with their log-sum-exps,
+ * which equals attention over the whole sequence up to rounding.
+ *
+ * Groups: request b belongs to group g when group_indptr[g] <= b <
+ * group_indptr[g+1]; group_indptr (int32 [num_groups+1], device) rises from 0
+ * to batch.  group_prefix_lens (int32 [num_groups], device): P_g, the tokens
+ * every member of the group holds with the same K/V (0 = none).  Only whole
+ * blocks are shared: with W_g = floor(P_g / block_size) * block_size, tokens
+ * 0 .. W_g-1 of every member are read once for the group, through the block
+ * table of its first member (block_tables[group_indptr[g]]; the other
+ * members' entries for them are not read), and tokens W_g .. seq_lens[b]-1
+ * through the member's own table.  P_g <= seq_lens[b] for every member (else
+ * the device error word reports PKV_DEVERR_BAD_LENGTH).  A request that no
+ * group covers is attended over its whole sequence through its own table and
+ * reported the same way.
+ *
+ * k_new, v_new:  nullable together; as pkv_paged_decode_attn_append (the
+ *                current token, position seq_lens[b]-1, must lie at or after
+ *                W_g).
+ * desc:          an fp8 cache's k_scale / v_scale are applied in both parts
+ *                (scores and outputs), as in pkv_paged_decode_attn.
+ * max_group_size: host bound of the members per group (sizes the prefix pass).
+ * max_prefix_len: host bound of P_g.  The prefix pass cuts each group's W_g
+ *                shared keys into chunks of whole 128-key tiles, enough of
+ *                them (at most 8, at least 256 keys each except the last)
+ *                that even one group gives about one work item per SM; every
+ *                chunk's partial is one more term of the LSE merge.  Keys
+ *                beyond the chunks the hint allows are not attended and set
+ *                PKV_DEVERR_BAD_LENGTH.
+ * max_suffix_len: host bound of seq_lens[b] - P_g (sizes the split plan).
+ * num_splits:    as pkv_paged_decode_attn, for the members' own tokens.
+ * workspace:     pkv_shared_prefix_decode_workspace_bytes() bytes, 256-byte
+ *                aligned (always needed).
+ * q:             16-byte aligned.  Everything else as pkv_paged_decode_attn.
+ * Streams: the prefix pass runs on a side stream the library keeps per device
+ * (highest priority), forked from `stream` by an event at the call and joined
+ * back before the merge, so it overlaps the decode of the members' own
+ * tokens; the call as a whole is ordered on `stream` like any other and can
+ * be captured into a CUDA graph.  Calls on one device from several host
+ * threads are serialised around the fork and join.
+ * Supported: head_dim 64/128, block_size 16/32, f16 or bf16 cache with the
+ * same act dtype or an fp8 e4m3 cache with either, GQA groups
+ * num_q_heads/num_kv_heads of 1 .. 128 (one 128-row tile holds 128 / group
+ * members x group heads), sm_scale > 0.
+ * ------------------------------------------------------------------------- */
+size_t pkv_shared_prefix_decode_workspace_bytes(const pkv_cache_desc* desc, int32_t batch,
+                                                int32_t num_q_heads, int32_t max_prefix_len,
+                                                int32_t max_suffix_len, int32_t num_splits);
+
+pkv_status pkv_paged_decode_attn_shared_prefix(
+    const pkv_cache_desc* desc, void* k_cache, void* v_cache, const void* k_new,
+    const void* v_new, const void* q, void* out, pkv_dtype act_dtype,
+    const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+    int32_t batch, int32_t num_q_heads, float sm_scale, const int32_t* group_indptr,
+    const int32_t* group_prefix_lens, int32_t num_groups, int32_t max_group_size,
+    int32_t max_prefix_len, int32_t max_suffix_len, int32_t num_splits, float* lse_out,
+    void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * pkv_paged_extend_attn -- suffix prefill over a cached prefix.
+ *
+ * "PagedAttention과 RadixAttention으로 LLM KV 캐시 최적화", section 03: when
+ * the longest cached prefix of a request has P tokens, only the remaining
+ * suffix is computed (2,000-token request with 1,900 cached -> 100 prefilled).
+ * Request b owns query rows q_indptr[b] .. q_indptr[b+1]-1; its row i sits at
+ * position P_b + i (P_b = prefix_lens[b]) and attends to keys 0 .. P_b + i:
+ * every cached prefix token plus the suffix causally.  The suffix's own K/V
+ * must already be in the cache at positions P_b .. P_b+S_b-1 (pkv_kv_append
+ * first), so every key is read through the block table.
+ *
+ * q, out:        [q_indptr[batch]][num_q_heads][head_dim] act dtype.
+ * q_indptr:      int32 [batch+1], device, non-decreasing, q_indptr[0] = 0.
+ * prefix_lens:   int32 [batch], device.
+ * sm_scale:      softmax scale, finite and > 0.
+ * max_suffix_len / max_total_len: host-side upper bounds of S_b and P_b+S_b.
+ * total_q_rows:  q_indptr[batch] (host value; sizes the grid).
+ * lse_out:       nullable float [q_indptr[batch]][num_q_heads], natural log.
+ * workspace:     unused (pass NULL, 0): pkv_extend_workspace_bytes() is 0 for
+ *                every cache dtype.  An fp8 cache is read as codes and each
+ *                K/V tile is widened inside the kernel (exactly: e4m3 fits
+ *                f16 and bf16), with k_scale applied to the scores and
+ *                v_scale to the output; no 16-bit copy of the cache is made.
+ * Device-side checks: a request whose rows q_indptr[b] .. q_indptr[b+1]-1
+ * do not lie inside [0, total_q_rows) is not computed (nothing is written for
+ * it), and suffix rows beyond max_suffix_len are not computed; both set
+ * PKV_DEVERR_BAD_LENGTH.  Block ids outside the pool read zeros
+ * (PKV_DEVERR_BAD_BLOCK).
+ * Supported: head_dim 64/128, block_size 16/32, GQA groups
+ * num_q_heads/num_kv_heads of 1 .. 128 (a 128-row tile holds 128 / group
+ * suffix tokens x group heads); cache dtype equal to the act dtype (f16,
+ * bf16) or fp8 e4m3 with either act dtype.
+ * ------------------------------------------------------------------------- */
 size_t pkv_extend_workspace_bytes(const pkv_cache_desc* desc, int32_t batch,
                                   int32_t num_q_heads, int32_t total_q_rows,
                                   int32_t max_total_len);
@@ -343,12 +358,13 @@ pkv_status pkv_paged_extend_attn(const pkv_cache_desc* desc, const void* k_cache
  * Writing the rows from inside the extend kernel was built and measured
  * slower (the extra warp code displaced the softmax loop's instructions).
  *
- * k_new, v_new:  [total_q_rows][num_kv_heads][head_dim], the cache dtype,
+ * k_new, v_new:  [total_q_rows][num_kv_heads][head_dim], the act dtype,
  *                device, 16-byte aligned; row q_indptr[b] + i is suffix token
- *                i of request b.
- * Everything else as pkv_paged_extend_attn.  16-bit caches only
- * (PKV_ERR_UNSUPPORTED for fp8).  A suffix slot whose block id lies outside
- * the pool is not written and is reported in the device error word.
+ *                i of request b.  An fp8 cache stores e4m3(fp32(x) / scale)
+ *                exactly as pkv_kv_append.
+ * Everything else as pkv_paged_extend_attn.  A suffix slot whose block id
+ * lies outside the pool is not written and is reported in the device error
+ * word.
  * ------------------------------------------------------------------------- */
 pkv_status pkv_paged_extend_attn_append(const pkv_cache_desc* desc, void* k_cache, void* v_cache,
                                         const void* k_new, const void* v_new, const void* q,

@@ -104,11 +104,11 @@ def load():
         lib.pkv_get_device_error.restype = ctypes.c_int
         lib.pkv_version.argtypes = []
         lib.pkv_version.restype = I32
-        lib.pkv_shared_prefix_decode_workspace_bytes.argtypes = [D, I32, I32, I32, I32]
+        lib.pkv_shared_prefix_decode_workspace_bytes.argtypes = [D, I32, I32, I32, I32, I32]
         lib.pkv_shared_prefix_decode_workspace_bytes.restype = SZ
         lib.pkv_paged_decode_attn_shared_prefix.argtypes = [D, P, P, P, P, P, P, ctypes.c_int, P,
                                                              I32, P, I32, I32, F, P, P, I32, I32,
-                                                             I32, I32, P, P, SZ, P]
+                                                             I32, I32, I32, P, P, SZ, P]
         lib.pkv_paged_decode_attn_shared_prefix.restype = ctypes.c_int
         lib.pkv_chain_hash.argtypes = [P, P, I32, I32, P, P, I32, P]
         lib.pkv_chain_hash.restype = ctypes.c_int
@@ -333,26 +333,30 @@ def paged_decode_attn_noalloc(k_cache, v_cache, q, out, block_tables, seq_lens, 
     _check(st, "pkv_paged_decode_attn_noalloc")
 
 
-def shared_prefix_decode_workspace_bytes(k_cache, batch, num_q_heads, max_suffix_len,
-                                         num_splits=0) -> int:
+def shared_prefix_decode_workspace_bytes(k_cache, batch, num_q_heads, max_prefix_len,
+                                         max_suffix_len, num_splits=0) -> int:
     lib = load()
     desc = _desc(k_cache, 1.0, 1.0)
     return int(lib.pkv_shared_prefix_decode_workspace_bytes(ctypes.byref(desc), batch, num_q_heads,
-                                                            max_suffix_len, num_splits))
+                                                            max_prefix_len, max_suffix_len,
+                                                            num_splits))
 
 
 def paged_decode_attn_shared_prefix(k_cache, v_cache, q, out, block_tables, seq_lens, sm_scale,
                                     group_indptr, group_prefix_lens, max_group_size,
-                                    max_suffix_len, k_new=None, v_new=None, num_splits=0,
-                                    lse_out=None, workspace=None, stream=None):
+                                    max_prefix_len, max_suffix_len, k_new=None, v_new=None,
+                                    num_splits=0, lse_out=None, workspace=None, stream=None,
+                                    k_scale=1.0, v_scale=1.0):
     """pkv_paged_decode_attn_shared_prefix: requests [group_indptr[g], group_indptr[g+1])
     share their first group_prefix_lens[g] tokens (read through the group's first member's
-    block table), attended once per group; k_new/v_new as paged_decode_attn_append."""
+    block table), attended once per group; max_prefix_len / max_suffix_len bound the groups'
+    prefixes and the members' own tokens; k_new/v_new as paged_decode_attn_append; k_scale /
+    v_scale are an fp8 cache's scales."""
     _need(torch.int32, block_tables=block_tables, seq_lens=seq_lens)
     b, hq = _decode_shapes(k_cache, v_cache, q, out, block_tables, seq_lens, lse_out, k_new,
                            v_new)
     lib = load()
-    desc = _desc(k_cache, 1.0, 1.0)
+    desc = _desc(k_cache, k_scale, v_scale)
     if group_indptr.dim() != 1:
         raise ValueError("group_indptr must be int32 [num_groups + 1]")
     ng = int(group_indptr.shape[0]) - 1
@@ -365,7 +369,8 @@ def paged_decode_attn_shared_prefix(k_cache, v_cache, q, out, block_tables, seq_
         ctypes.byref(desc), _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new), _ptr(q),
         _ptr(out), _dtype_code(q), _ptr(block_tables), int(block_tables.shape[1]), _ptr(seq_lens),
         b, hq, float(sm_scale), _ptr(group_indptr), _ptr(group_prefix_lens), ng,
-        int(max_group_size), int(max_suffix_len), int(num_splits), _ptr(lse_out),
+        int(max_group_size), int(max_prefix_len), int(max_suffix_len), int(num_splits),
+        _ptr(lse_out),
         _ptr(workspace), ws_bytes, _stream(stream))
     _check(st, "pkv_paged_decode_attn_shared_prefix")
 
@@ -399,14 +404,15 @@ def paged_extend_attn(k_cache, v_cache, q, out, q_indptr, prefix_lens, block_tab
 
 def paged_extend_attn_append(k_cache, v_cache, k_new, v_new, q, out, q_indptr, prefix_lens,
                              block_tables, sm_scale, max_suffix_len, max_total_len, lse_out=None,
-                             stream=None):
-    """pkv_paged_extend_attn_append: k_new/v_new [sum S, Hkv, D] (the cache dtype = q's) are written
-    to positions prefix_lens[b] + i and attended in the same call (16-bit caches)."""
+                             stream=None, k_scale=1.0, v_scale=1.0):
+    """pkv_paged_extend_attn_append: k_new/v_new [sum S, Hkv, D] (q's dtype) are written to
+    positions prefix_lens[b] + i (an fp8 cache stores them quantised with k_scale / v_scale) and
+    attended in the same call."""
     _need(torch.int32, q_indptr=q_indptr, prefix_lens=prefix_lens, block_tables=block_tables)
     rows, hq, batch = _extend_shapes(k_cache, v_cache, q, out, q_indptr, prefix_lens,
                                      block_tables, lse_out, k_new, v_new)
     lib = load()
-    desc = _desc(k_cache, 1.0, 1.0)
+    desc = _desc(k_cache, k_scale, v_scale)
     st = lib.pkv_paged_extend_attn_append(ctypes.byref(desc), _ptr(k_cache), _ptr(v_cache),
                                           _ptr(k_new), _ptr(v_new), _ptr(q), _ptr(out),
                                           _dtype_code(q), _ptr(q_indptr), _ptr(prefix_lens),

@@ -1,8 +1,7 @@
 """Build libpkv.so in-tree with nvcc for sm_103a.
 
 Each .cu (and host-only .cpp) under csrc/ is compiled in parallel to an object under _build/, then
-linked (static CUDA runtime) into paged_kv_cache_285_gb300/libpkv.so; radix_trace.cpp becomes a small
-executable linked against it (the prefix index's native throughput, reported by bench.py).
+linked (static CUDA runtime) into paged_kv_cache_285_gb300/libpkv.so.
 """
 from __future__ import annotations
 
@@ -18,9 +17,6 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIB = os.path.join(HERE, "libpkv.so")
-# native replay of a request trace through the prefix index's C ABI (bench.py reports it)
-TRACE_SRC = os.path.join(HERE, "radix_trace.cpp")
-TRACE_BIN = os.path.join(HERE, "radix_trace")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-diag-suppress", "177",
@@ -77,16 +73,6 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         tmp = LIB + f".tmp{os.getpid()}"
         run([cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs])
         os.replace(tmp, LIB)
-    if force or _stale(TRACE_BIN, [TRACE_SRC, LIB]):
-        # an auxiliary benchmark driver: if it does not build, the library still stands
-        # (bench.py then reports it as not built)
-        tmp = TRACE_BIN + f".tmp{os.getpid()}"
-        try:
-            run([cc, "-O3", "-std=c++17", f"-I{INCLUDE}", TRACE_SRC, "-o", tmp, f"-L{HERE}",
-                 "-lpkv", "-Xlinker", "-rpath", "-Xlinker", "$ORIGIN"])
-            os.replace(tmp, TRACE_BIN)
-        except RuntimeError:
-            sys.stderr.write("radix_trace was not built; the library is unaffected\n")
     return LIB
 
 

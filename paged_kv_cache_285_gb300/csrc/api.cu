@@ -132,7 +132,7 @@ pkv_status make_page_map(CUtensorMap* m, const void* base, const pkv_cache_desc*
 }
 
 // Query rows of the extend call as a 3-D map {head_dim, num_q_heads, rows}:
-// one box {64, group, 128 / group} is the 64-dim half of a 128-row tile of
+// one box {64, group, 128 / group} is the 64-dim column block of a row tile of
 // (suffix token, head of the group) rows, 128-byte swizzled.
 pkv_status make_q_map(CUtensorMap* m, const void* q, int head_dim, int num_q_heads,
                       int total_rows, int group) {
@@ -152,19 +152,35 @@ int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// Workspace of an extend call over an fp8 cache: a claim flag per physical
-// block, then 16-bit shadow K and V pools with the cache's geometry.
-struct ExtendFp8Layout {
-  size_t flags = 0, k16 = 0, v16 = 0, total = 0;
-};
-ExtendFp8Layout fp8_layout(const pkv_cache_desc* d) {
-  ExtendFp8Layout l;
-  const size_t pool16 = (size_t)d->num_blocks * d->num_kv_heads * d->block_size * d->head_dim * 2;
-  l.flags = 0;
-  l.k16 = align256((size_t)d->num_blocks * 4);
-  l.v16 = l.k16 + align256(pool16);
-  l.total = l.v16 + align256(pool16);
-  return l;
+// Work decomposition of an extend launch: rows of one (request, kv head) in
+// tiles of `tok` suffix tokens x `group` heads, a work item = a pair of tiles,
+// one persistent CTA per SM.  False if the item count overflows.
+bool plan_extend(ExtendParams& p, int batch, int num_kv_heads, int group, int max_rows_per_request,
+                 int sm_count) {
+  p.group = group;
+  p.tok = 128 / group;
+  p.kchunks = 1;
+  p.kchunk_keys = 0;
+  p.tiles_per_head = ceil_div((int64_t)max_rows_per_request, p.tok);
+  const int64_t pairs = (p.tiles_per_head + 1) / 2;
+  const int64_t items = pairs * num_kv_heads * batch;
+  if (items > INT32_MAX || pairs * num_kv_heads > UINT32_MAX / 2) return false;
+  p.num_items = (int)items;
+  p.div_pairs = make_fastdiv((uint32_t)pairs);
+  p.div_hkv = make_fastdiv((uint32_t)num_kv_heads);
+  p.div_req = make_fastdiv((uint32_t)(pairs * num_kv_heads));
+  p.num_ctas = (int)std::min<int64_t>(items, sm_count > 0 ? sm_count : 1);
+  return true;
+}
+
+// Softmax scale in base 2 with an fp8 cache's k_scale folded in (scores are
+// computed on the codes), and the output scale (v_scale for fp8, else 1).
+float score_scale_log2(const pkv_cache_desc* d, float sm_scale) {
+  const double kscale = d->cache_dtype == PKV_FP8_E4M3 ? (double)d->k_scale : 1.0;
+  return (float)((double)sm_scale * kscale * 1.4426950408889634);
+}
+float output_scale(const pkv_cache_desc* d) {
+  return d->cache_dtype == PKV_FP8_E4M3 ? d->v_scale : 1.0f;
 }
 
 struct DecodePlan {
@@ -307,14 +323,21 @@ size_t pkv_decode_workspace_bytes(const pkv_cache_desc* desc, int32_t batch, int
 }  // extern "C"
 
 // Plan of a shared-prefix decode: the decode split plan over the requests'
-// own tokens, partials for one more slot (the shared prefix's) per (request,
-// head), always merged.
-static DecodePlan plan_cascade(const pkv_cache_desc* d, int batch, int hq, int max_suffix_len,
-                               int forced, int sm_count) {
+// own tokens, plus workspace slots for the shared prefix's partials (one per
+// key chunk, at most kMaxPrefixChunks, chunks of at least kMinPrefixChunk keys)
+// per (request, head), always merged.
+constexpr int kMaxPrefixChunks = 8;
+constexpr int kMinPrefixChunk = 256;
+int prefix_slots_for(int max_prefix_len) {
+  const int by_len = ceil_div(std::max(max_prefix_len, 1), kMinPrefixChunk);
+  return std::min(kMaxPrefixChunks, std::max(1, by_len));
+}
+static DecodePlan plan_cascade(const pkv_cache_desc* d, int batch, int hq, int max_prefix_len,
+                               int max_suffix_len, int forced, int sm_count) {
   // a member's own tokens start at its group's prefix rounded down to whole
   // blocks: up to block_size - 1 more than seq_len - prefix
   DecodePlan pl = plan_decode(d, batch, hq, max_suffix_len + d->block_size - 1, forced, sm_count);
-  const size_t slots = (size_t)pl.splits + 1;
+  const size_t slots = (size_t)pl.splits + prefix_slots_for(max_prefix_len);
   pl.ws_lse_offset = align256((size_t)batch * hq * slots * d->head_dim * sizeof(float));
   pl.ws_span_offset = align256(pl.ws_lse_offset + (size_t)batch * hq * slots * sizeof(float));
   pl.ws_bytes = pl.ws_span_offset + (size_t)batch * 2 * sizeof(int32_t);
@@ -324,15 +347,16 @@ static DecodePlan plan_cascade(const pkv_cache_desc* d, int batch, int hq, int m
 extern "C" {
 
 size_t pkv_shared_prefix_decode_workspace_bytes(const pkv_cache_desc* desc, int32_t batch,
-                                                int32_t num_q_heads, int32_t max_suffix_len,
-                                                int32_t num_splits) {
-  if (check_desc(desc) != PKV_OK || batch <= 0 || num_q_heads <= 0 || max_suffix_len < 0 ||
-      num_splits < 0)
+                                                int32_t num_q_heads, int32_t max_prefix_len,
+                                                int32_t max_suffix_len, int32_t num_splits) {
+  if (check_desc(desc) != PKV_OK || batch <= 0 || num_q_heads <= 0 || max_prefix_len < 0 ||
+      max_suffix_len < 0 || num_splits < 0)
     return 0;
   cudaError_t e;
   DeviceState* ds = device_state(&e);
   const int sms = ds ? ds->sm_count : 0;
-  return plan_cascade(desc, batch, num_q_heads, max_suffix_len, num_splits, sms).ws_bytes;
+  return plan_cascade(desc, batch, num_q_heads, max_prefix_len, max_suffix_len, num_splits, sms)
+      .ws_bytes;
 }
 
 pkv_status pkv_paged_decode_attn_shared_prefix(
@@ -340,14 +364,15 @@ pkv_status pkv_paged_decode_attn_shared_prefix(
     const void* q, void* out, pkv_dtype act_dtype, const int32_t* block_tables,
     int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t batch, int32_t num_q_heads,
     float sm_scale, const int32_t* group_indptr, const int32_t* group_prefix_lens,
-    int32_t num_groups, int32_t max_group_size, int32_t max_suffix_len, int32_t num_splits,
-    float* lse_out, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    int32_t num_groups, int32_t max_group_size, int32_t max_prefix_len, int32_t max_suffix_len,
+    int32_t num_splits, float* lse_out, void* workspace, size_t workspace_bytes,
+    cudaStream_t stream) {
   pkv_status st = check_desc(desc);
   if (st != PKV_OK) return st;
   if ((st = check_act(desc, act_dtype)) != PKV_OK) return st;
   if (batch < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || num_groups < 0 ||
-      max_group_size < 0 || max_suffix_len < 0 || num_splits < 0 || !std::isfinite(sm_scale) ||
-      !(sm_scale > 0.f))
+      max_group_size < 0 || max_prefix_len < 0 || max_suffix_len < 0 || num_splits < 0 ||
+      !std::isfinite(sm_scale) || !(sm_scale > 0.f))
     return PKV_ERR_INVALID_ARG;
   if (num_q_heads % desc->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
   const int group = num_q_heads / desc->num_kv_heads;
@@ -366,8 +391,8 @@ pkv_status pkv_paged_decode_attn_shared_prefix(
   cudaError_t e;
   DeviceState* ds = device_state(&e);
   if (!ds) return PKV_ERR_CUDA;
-  const DecodePlan pl = plan_cascade(desc, batch, num_q_heads, max_suffix_len, num_splits,
-                                     ds->sm_count);
+  const DecodePlan pl = plan_cascade(desc, batch, num_q_heads, max_prefix_len, max_suffix_len,
+                                     num_splits, ds->sm_count);
   if (!workspace || workspace_bytes < pl.ws_bytes || !aligned(workspace, 256))
     return PKV_ERR_WORKSPACE;
   if (pl.splits > 65535) return PKV_ERR_UNSUPPORTED;
@@ -377,8 +402,9 @@ pkv_status pkv_paged_decode_attn_shared_prefix(
   if ((st = make_q_map(&qmap, q, desc->head_dim, num_q_heads, batch, group)) != PKV_OK) return st;
   float* ws_o = reinterpret_cast<float*>(workspace);
   float* ws_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + pl.ws_lse_offset);
-  const int slots = pl.splits + 1;
-  const float scale_log2 = (float)((double)sm_scale * 1.4426950408889634);
+  const int prefix_slots = prefix_slots_for(max_prefix_len);
+  const int slots = pl.splits + prefix_slots;
+  const float scale_log2 = score_scale_log2(desc, sm_scale);
 
   // 1. the shared prefixes, once per group, on the tensor cores -> slot 0
   //    (on the side stream, beside step 2)
@@ -395,22 +421,30 @@ pkv_status pkv_paged_decode_attn_shared_prefix(
   pe.batch = num_groups;
   pe.num_q_heads = num_q_heads;
   pe.num_kv_heads = desc->num_kv_heads;
-  pe.group = group;
   pe.out_32b = 0;
-  pe.group_shift = group == 1 ? 0 : group == 2 ? 1 : group == 4 ? 2 : 3;
   pe.bs_shift = desc->block_size == 16 ? 4 : 5;
   pe.total_rows = batch;
-  pe.tiles_per_head = ceil_div((int64_t)max_group_size * group, 128);
   pe.scale_log2 = scale_log2;
-  pe.out_scale = 1.0f;
-  const int64_t items = (int64_t)((pe.tiles_per_head + 1) / 2) * desc->num_kv_heads * num_groups;
-  if (items > INT32_MAX) return PKV_ERR_UNSUPPORTED;
-  pe.num_items = (int)items;
-  const uint32_t pairs = (uint32_t)((pe.tiles_per_head + 1) / 2);
-  pe.div_pairs = make_fastdiv(pairs);
-  pe.div_hkv = make_fastdiv((uint32_t)desc->num_kv_heads);
-  pe.div_req = make_fastdiv(pairs * (uint32_t)desc->num_kv_heads);
-  pe.num_ctas = (int)std::min<int64_t>(items, ds->sm_count > 0 ? ds->sm_count : 1);
+  pe.out_scale = output_scale(desc);
+  if (!plan_extend(pe, num_groups, desc->num_kv_heads, group, max_group_size, ds->sm_count))
+    return PKV_ERR_UNSUPPORTED;
+  // The prefix's keys in chunks of whole key tiles, so that the pass has about
+  // one work item per SM even for a single group (each chunk's partial is one
+  // more term of the LSE merge); at most prefix_slots chunks.
+  const int key_tiles = std::max(1, ceil_div(max_prefix_len, 128));
+  const int want = std::max(1, ceil_div(ds->sm_count > 0 ? ds->sm_count : 1, pe.num_items));
+  const int chunk_tiles = ceil_div(key_tiles, std::min(std::min(want, prefix_slots), key_tiles));
+  pe.kchunks = ceil_div(key_tiles, chunk_tiles);
+  pe.kchunk_keys = chunk_tiles * 128;
+  {
+    const int64_t items = (int64_t)pe.num_items * pe.kchunks;
+    const uint32_t pairs = (uint32_t)((pe.tiles_per_head + 1) / 2);
+    if (items > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+    pe.num_items = (int)items;
+    pe.div_pairs = make_fastdiv(pairs * (uint32_t)pe.kchunks);
+    pe.div_req = make_fastdiv(pairs * (uint32_t)pe.kchunks * (uint32_t)desc->num_kv_heads);
+    pe.num_ctas = (int)std::min<int64_t>(items, ds->sm_count > 0 ? ds->sm_count : 1);
+  }
   ExtendPartialParams pp{};
   pp.o = ws_o;
   pp.lse = ws_lse;
@@ -453,7 +487,7 @@ pkv_status pkv_paged_decode_attn_shared_prefix(
   p.chunk = pl.chunk;
   p.num_splits = pl.splits;
   p.scale_log2 = scale_log2;
-  p.out_scale = 1.0f;
+  p.out_scale = output_scale(desc);
   DecodeExtraParams ap{};
   ap.k_new = k_new;
   ap.v_new = v_new;
@@ -465,6 +499,9 @@ pkv_status pkv_paged_decode_attn_shared_prefix(
   ap.group_prefix_lens = group_prefix_lens;
   ap.num_groups = num_groups;
   ap.ws_span = reinterpret_cast<int2*>(static_cast<uint8_t*>(workspace) + pl.ws_span_offset);
+  ap.prefix_slots = prefix_slots;
+  ap.prefix_chunk = pe.kchunk_keys;
+  ap.prefix_chunks = pe.kchunks;
   e = launch_decode_cascade(kmap, vmap, p, ap, desc->head_dim, (int)desc->cache_dtype,
                             (int)act_dtype, stream, ds->join);
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
@@ -488,7 +525,6 @@ static pkv_status decode_common(const pkv_cache_desc* desc, const void* k_cache,
     return PKV_ERR_INVALID_ARG;
   if (num_q_heads % desc->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
   const int group = num_q_heads / desc->num_kv_heads;
-  if (group > 8) return PKV_ERR_UNSUPPORTED;
   if (batch == 0) return PKV_OK;
   if (batch > 65535 || desc->num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
   if (!k_cache || !v_cache || !q || !out || !block_tables || !seq_lens)
@@ -526,9 +562,8 @@ static pkv_status decode_common(const pkv_cache_desc* desc, const void* k_cache,
   p.bs_shift = desc->block_size == 16 ? 4 : 5;
   p.chunk = pl.chunk;
   p.num_splits = pl.splits;
-  const double kscale = desc->cache_dtype == PKV_FP8_E4M3 ? (double)desc->k_scale : 1.0;
-  p.scale_log2 = (float)((double)sm_scale * kscale * 1.4426950408889634);
-  p.out_scale = desc->cache_dtype == PKV_FP8_E4M3 ? desc->v_scale : 1.0f;
+  p.scale_log2 = score_scale_log2(desc, sm_scale);
+  p.out_scale = output_scale(desc);
   DecodeExtraParams ap{};
   ap.k_new = k_new;
   ap.v_new = v_new;
@@ -569,10 +604,9 @@ pkv_status pkv_paged_decode_attn_append(const pkv_cache_desc* desc, void* k_cach
 
 size_t pkv_extend_workspace_bytes(const pkv_cache_desc* desc, int32_t batch, int32_t num_q_heads,
                                   int32_t total_q_rows, int32_t max_total_len) {
-  (void)batch; (void)num_q_heads; (void)total_q_rows; (void)max_total_len;
-  if (check_desc(desc) != PKV_OK || desc->cache_dtype != PKV_FP8_E4M3) return 0;
-  const ExtendFp8Layout l = fp8_layout(desc);
-  return l.total;
+  // every dtype, fp8 included, is read straight from the cache: no scratch
+  (void)desc; (void)batch; (void)num_q_heads; (void)total_q_rows; (void)max_total_len;
+  return 0;
 }
 
 }  // extern "C"
@@ -596,12 +630,9 @@ static pkv_status extend_common(const pkv_cache_desc* desc, const void* k_cache,
     return PKV_ERR_INVALID_ARG;
   if (num_q_heads % desc->num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
   const int group = num_q_heads / desc->num_kv_heads;
-  const bool fp8 = desc->cache_dtype == PKV_FP8_E4M3;
-  // an fp8 cache is read through 16-bit shadow pages of the activation dtype
-  pkv_cache_desc desc16 = *desc;
-  if (fp8) desc16.cache_dtype = act_dtype;
-  if (!extend_supported(desc->head_dim, (int)desc16.cache_dtype, (int)act_dtype, group))
+  if (!extend_supported(desc->head_dim, (int)desc->cache_dtype, (int)act_dtype, group))
     return PKV_ERR_UNSUPPORTED;
+  (void)workspace; (void)workspace_bytes;  // no scratch is needed (pkv_extend_workspace_bytes is 0)
   if (batch == 0 || total_q_rows == 0 || max_suffix_len == 0) return PKV_OK;
   if (!k_cache || !v_cache || !q || !out || !block_tables || !q_indptr || !prefix_lens)
     return PKV_ERR_INVALID_ARG;
@@ -610,38 +641,9 @@ static pkv_status extend_common(const pkv_cache_desc* desc, const void* k_cache,
   cudaError_t e;
   DeviceState* ds = device_state(&e);
   if (!ds) return PKV_ERR_CUDA;
-  const void* k_pages = k_cache;
-  const void* v_pages = v_cache;
-  if (fp8) {
-    const ExtendFp8Layout l = fp8_layout(desc);
-    if (!workspace || workspace_bytes < l.total) return PKV_ERR_WORKSPACE;
-    if (!aligned(workspace, 256)) return PKV_ERR_INVALID_ARG;
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    DequantParams dp;
-    dp.k8 = static_cast<const uint8_t*>(k_cache);
-    dp.v8 = static_cast<const uint8_t*>(v_cache);
-    dp.k16 = reinterpret_cast<uint16_t*>(ws + l.k16);
-    dp.v16 = reinterpret_cast<uint16_t*>(ws + l.v16);
-    dp.flags = reinterpret_cast<int32_t*>(ws + l.flags);
-    dp.q_indptr = q_indptr;
-    dp.prefix_lens = prefix_lens;
-    dp.block_tables = block_tables;
-    dp.max_blocks = max_blocks_per_seq;
-    dp.num_blocks = desc->num_blocks;
-    dp.bs_shift = desc->block_size == 16 ? 4 : 5;
-    dp.page_elems = desc->num_kv_heads * desc->block_size * desc->head_dim;
-    if (cudaMemsetAsync(dp.flags, 0, (size_t)desc->num_blocks * 4, stream) != cudaSuccess)
-      return PKV_ERR_CUDA;
-    // every table entry a request can read: the full table width (the kernel
-    // skips entries past each request's prefix + suffix)
-    if (launch_dequant_pages(dp, batch, max_blocks_per_seq, (int)act_dtype, stream) != cudaSuccess)
-      return PKV_ERR_CUDA;
-    k_pages = dp.k16;
-    v_pages = dp.v16;
-  }
   CUtensorMap kmap, vmap, qmap;
-  if ((st = make_page_map(&kmap, k_pages, &desc16)) != PKV_OK) return st;
-  if ((st = make_page_map(&vmap, v_pages, &desc16)) != PKV_OK) return st;
+  if ((st = make_page_map(&kmap, k_cache, desc)) != PKV_OK) return st;
+  if ((st = make_page_map(&vmap, v_cache, desc)) != PKV_OK) return st;
   if ((st = make_q_map(&qmap, q, desc->head_dim, num_q_heads, total_q_rows, group)) != PKV_OK)
     return st;
   ExtendParams p;
@@ -657,24 +659,13 @@ static pkv_status extend_common(const pkv_cache_desc* desc, const void* k_cache,
   p.batch = batch;
   p.num_q_heads = num_q_heads;
   p.num_kv_heads = desc->num_kv_heads;
-  p.group = group;
   p.out_32b = aligned(out, 32) ? 1 : 0;
-  p.group_shift = group == 1 ? 0 : group == 2 ? 1 : group == 4 ? 2 : 3;
   p.bs_shift = desc->block_size == 16 ? 4 : 5;
   p.total_rows = total_q_rows;
-  p.tiles_per_head = ceil_div((int64_t)max_suffix_len * group, 128);
-  const double kscale = desc->cache_dtype == PKV_FP8_E4M3 ? (double)desc->k_scale : 1.0;
-  p.scale_log2 = (float)((double)sm_scale * kscale * 1.4426950408889634);
-  p.out_scale = desc->cache_dtype == PKV_FP8_E4M3 ? desc->v_scale : 1.0f;
-  // a work item is a pair of consecutive 128-row tiles of one (request, kv head)
-  const int64_t items = (int64_t)((p.tiles_per_head + 1) / 2) * desc->num_kv_heads * batch;
-  if (items > INT32_MAX) return PKV_ERR_UNSUPPORTED;
-  p.num_items = (int)items;
-  const uint32_t pairs = (uint32_t)((p.tiles_per_head + 1) / 2);
-  p.div_pairs = make_fastdiv(pairs);
-  p.div_hkv = make_fastdiv((uint32_t)desc->num_kv_heads);
-  p.div_req = make_fastdiv(pairs * (uint32_t)desc->num_kv_heads);
-  p.num_ctas = (int)std::min<int64_t>(items, ds->sm_count > 0 ? ds->sm_count : 1);
+  p.scale_log2 = score_scale_log2(desc, sm_scale);
+  p.out_scale = output_scale(desc);
+  if (!plan_extend(p, batch, desc->num_kv_heads, group, max_suffix_len, ds->sm_count))
+    return PKV_ERR_UNSUPPORTED;
   if (k_new) {
     // the suffix's K/V first (its slots computed from the extend layout), then
     // the extend kernel reads them back; two launches in stream order
@@ -700,7 +691,7 @@ static pkv_status extend_common(const pkv_cache_desc* desc, const void* k_cache,
     e = launch_append(ap, (int)desc->cache_dtype, (int)act_dtype, stream);
     if (e != cudaSuccess) return PKV_ERR_CUDA;
   }
-  e = launch_extend(kmap, vmap, qmap, p, desc->head_dim, (int)desc16.cache_dtype, (int)act_dtype,
+  e = launch_extend(kmap, vmap, qmap, p, desc->head_dim, (int)desc->cache_dtype, (int)act_dtype,
                     stream);
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
@@ -730,7 +721,6 @@ pkv_status pkv_paged_extend_attn_append(const pkv_cache_desc* desc, void* k_cach
                                         int32_t max_suffix_len, int32_t max_total_len,
                                         float* lse_out, cudaStream_t stream) {
   if (!k_new || !v_new) return PKV_ERR_INVALID_ARG;
-  if (check_desc(desc) == PKV_OK && desc->cache_dtype == PKV_FP8_E4M3) return PKV_ERR_UNSUPPORTED;
   if (!aligned(k_new, 16) || !aligned(v_new, 16)) return PKV_ERR_INVALID_ARG;
   return extend_common(desc, k_cache, v_cache, k_new, v_new, q, out, act_dtype, q_indptr,
                        prefix_lens, block_tables, max_blocks_per_seq, batch, num_q_heads,

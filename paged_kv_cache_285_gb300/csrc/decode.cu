@@ -8,9 +8,12 @@
 //
 // Design (memory-bound stream, so every byte is read once and the arithmetic
 // stays far below the HBM roofline):
-//   * grid (split, kv head, request).  A split is a fixed-length run of the
-//     sequence; all Hq/Hkv query heads of one kv head share one CTA, so every
-//     K/V byte is fetched once per step.
+//   * grid (split, kv head x head chunk, request).  A split is a fixed-length
+//     run of the sequence; up to 8 query heads of one kv head share one CTA
+//     (the N = 8 side of the MMA), so with GQA groups of up to 8 every K/V
+//     byte is fetched once per step; larger groups are cut into chunks of 8
+//     heads, one CTA each, which read the same pages (the second read mostly
+//     from L2).
 //   * each warp owns every NW-th 16-token tile of the split and runs its own
 //     NS-deep TMA pipeline: lane 0 issues cp.async.bulk.tensor copies of the
 //     K and V tiles (128-byte swizzled, conflict-free ldmatrix) completing on a
@@ -135,10 +138,14 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
 
   // split is the slowest grid dimension: every request's first chunk runs
   // before any second chunk, so the partial and empty last splits form the tail
-  const int g = blockIdx.x, b = blockIdx.y, split = blockIdx.z;
+  const int b = blockIdx.y, split = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
   const int G = p.group;
+  // kv head g, chunk hc of its query heads: heads hb .. hb + GC - 1
+  const int nhc = (G + 7) >> 3;
+  const int g = (int)blockIdx.x / nhc, hc = (int)blockIdx.x - g * nhc;
+  const int hb = g * G + hc * 8, GC = min(8, G - hc * 8);
   const int bs = 1 << p.bs_shift;
 
   int n = p.seq_lens[b];
@@ -156,7 +163,7 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
     }
     tb = (tb >> p.bs_shift) << p.bs_shift;  // only whole blocks are shared
     // the merge reads the request's span from here instead of searching again
-    if (split == 0 && g == 0 && threadIdx.x == 0) ap.ws_span[b] = make_int2(tb, n);
+    if (split == 0 && blockIdx.x == 0 && threadIdx.x == 0) ap.ws_span[b] = make_int2(tb, n);
   }
   const int t0 = tb + split * p.chunk;
   if (t0 >= n) {
@@ -164,8 +171,8 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       // nothing after the prefix; the current token cannot be appended there
       if (ap.k_new != nullptr && split == 0 && n > 0 && threadIdx.x == 0) set_err(p.err, 3);
     } else if (split == 0) {  // empty sequence: out = 0, lse = -inf
-      for (int idx = threadIdx.x; idx < G * HD; idx += NW * 32) {
-        const int h = g * G + idx / HD;
+      for (int idx = threadIdx.x; idx < GC * HD; idx += NW * 32) {
+        const int h = hb + idx / HD;
         store_act<AT>(p.out, ((int64_t)b * p.num_q_heads + h) * HD + idx % HD, 0.f);
         if (p.lse_out && idx % HD == 0) p.lse_out[(int64_t)b * p.num_q_heads + h] = -INFINITY;
       }
@@ -183,7 +190,9 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
     // loaded (TMA reads the slot after the proxy fence and the barrier
     // below).  Same bytes as the separate append: a 16-bit copy, or
     // e4m3(fp32(x) / scale) with a correctly rounded division and a
-    // saturating round-to-nearest-even convert.
+    // saturating round-to-nearest-even convert.  With a group of more than 8
+    // heads every head chunk's CTA writes the row (the same bytes), before its
+    // own read of it.
     const int pos = n - 1;
     const int blk = p.block_tables[(int64_t)b * p.max_blocks + (pos >> p.bs_shift)];
     constexpr int VPR = HD / 8;  // 16-byte input vectors per row
@@ -233,7 +242,7 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
   constexpr bool MMA_BF16 = C::MMA_BF16;
   uint32_t qf[HD / 16][2];
   {
-    const int h = g * G + gid;
+    const int h = hb + gid;
     const int64_t qbase = ((int64_t)b * p.num_q_heads + h) * HD;
 #pragma unroll
     for (int s = 0; s < HD / 16; ++s) {
@@ -243,7 +252,7 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       } else {
         d0 = 16 * s + 2 * tig; d1 = d0 + 1; d2 = d0 + 8; d3 = d0 + 9;
       }
-      if (gid < G) {
+      if (gid < GC) {
         if constexpr (CT != DT_E4M3) {
           qf[s][0] = *reinterpret_cast<const uint32_t*>(
               reinterpret_cast<const uint16_t*>(p.q) + qbase + d0);
@@ -495,9 +504,10 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
   __syncthreads();
 
   const bool direct = !CASC && (nsplit_b == 1);
-  constexpr int kSlot0 = CASC ? 1 : 0;  // cascade: slot 0 holds the shared prefix
+  // cascade: the shared prefix's chunks hold the first slots
+  const int kSlot0 = CASC ? ap.prefix_slots : 0;
   const int nslots = p.num_splits + kSlot0;
-  for (int idx = threadIdx.x; idx < G * HD; idx += NW * 32) {
+  for (int idx = threadIdx.x; idx < GC * HD; idx += NW * 32) {
     const int jh = idx / HD, d = idx % HD;
     float mstar = -INFINITY;
 #pragma unroll
@@ -511,7 +521,7 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
     }
     const float res = (O / L) * p.out_scale;
     const float lse2 = mstar + log2f(L);
-    const int h = g * G + jh;
+    const int h = hb + jh;
     const int64_t bh = (int64_t)b * p.num_q_heads + h;
     if (direct) {
       store_act<AT>(p.out, bh * HD + d, res);
@@ -525,8 +535,8 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
 
 // Merge the splits of one (request, head) per warp:
 //   lse* = log2 sum_s 2^lse_s,  out = sum_s 2^(lse_s - lse*) o_s.
-// Cascade: slot 0 (the group's shared prefix, when it has one) and slots
-// 1 .. of the request's own tokens.
+// Cascade: the shared prefix's chunks (slots 0 .. npc-1, when the group has a
+// prefix) and the request's own tokens (slots prefix_slots ..).
 template <int HD, int AT, bool CASC>
 __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, const DecodeExtraParams ap) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -547,11 +557,15 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, const 
   }
   const int ns = (n - tb + p.chunk - 1) / p.chunk;
   if (!CASC && ns <= 1) return;  // written directly by the split kernel
-  constexpr int kSlot0 = CASC ? 1 : 0;
+  const int kSlot0 = CASC ? ap.prefix_slots : 0;
   const int nslots = p.num_splits + kSlot0;
-  const int s_lo = (CASC && tb > 0) ? 0 : kSlot0, s_hi = kSlot0 + ns;
+  // partial i of this row: the prefix's chunks first, then the own splits
+  const int npc =
+      (CASC && tb > 0) ? min((tb + ap.prefix_chunk - 1) / ap.prefix_chunk, ap.prefix_chunks) : 0;
+  const int cnt = npc + ns;
+  auto slot = [&](int i) { return i < npc ? i : kSlot0 + (i - npc); };
   constexpr int PER = HD / 32;
-  if (s_lo >= s_hi) {  // no token at all: out = 0, lse = -inf
+  if (cnt <= 0) {  // no token at all: out = 0, lse = -inf
 #pragma unroll
     for (int k = 0; k < PER; ++k) store_act<AT>(p.out, bh * HD + lane * PER + k, 0.f);
     if (p.lse_out && lane == 0) p.lse_out[bh] = -INFINITY;
@@ -565,20 +579,20 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, const 
   float pre[kPre][PER];
 #pragma unroll
   for (int k = 0; k < kPre; ++k) {
-    if (s_lo + k < s_hi) {
+    if (k < cnt) {
 #pragma unroll
       for (int e = 0; e < PER; ++e) pre[k][e] = 0.f;
       if constexpr (PER == 4) {
-        const float4 v = *reinterpret_cast<const float4*>(po + (int64_t)(s_lo + k) * HD);
+        const float4 v = *reinterpret_cast<const float4*>(po + (int64_t)slot(k) * HD);
         pre[k][0] = v.x; pre[k][1] = v.y; pre[k][2] = v.z; pre[k][3] = v.w;
       } else {
-        const float2 v = *reinterpret_cast<const float2*>(po + (int64_t)(s_lo + k) * HD);
+        const float2 v = *reinterpret_cast<const float2*>(po + (int64_t)slot(k) * HD);
         pre[k][0] = v.x; pre[k][1] = v.y;
       }
     }
   }
   float m = -INFINITY;
-  for (int s = s_lo + lane; s < s_hi; s += 32) m = fmaxf(m, lse[s]);
+  for (int i = lane; i < cnt; i += 32) m = fmaxf(m, lse[slot(i)]);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, off));
   float o[PER];
@@ -587,14 +601,15 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, const 
   float L = 0.f;
 #pragma unroll
   for (int k = 0; k < kPre; ++k) {
-    if (s_lo + k < s_hi) {
-      const float w = fast_exp2(lse[s_lo + k] - m);
+    if (k < cnt) {
+      const float w = fast_exp2(lse[slot(k)] - m);
       L += w;
 #pragma unroll
       for (int e = 0; e < PER; ++e) o[e] += w * pre[k][e];
     }
   }
-  for (int s = s_lo + kPre; s < s_hi; ++s) {  // plans with more than kPre splits
+  for (int i = kPre; i < cnt; ++i) {  // rows with more than kPre partials
+    const int s = slot(i);
     const float w = fast_exp2(lse[s] - m);
     L += w;
     if constexpr (PER == 4) {
@@ -635,7 +650,7 @@ cudaError_t launch_decode_t(const CUtensorMap& kmap, const CUtensorMap& vmap,
   auto kern = decode_kernel<HD, CT, AT, NW, NS, CASC>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.num_kv_heads, p.batch, p.num_splits);
+  dim3 grid(p.num_kv_heads * ((p.group + 7) / 8), p.batch, p.num_splits);
   kern<<<grid, NW * 32, C::SMEM, stream>>>(kmap, vmap, p, ap);
   e = cudaGetLastError();
   if (e != cudaSuccess || (!CASC && p.num_splits <= 1)) return e;
@@ -682,26 +697,30 @@ cudaError_t launch_decode_cascade(const CUtensorMap& kmap, const CUtensorMap& vm
                                   const DecodeParams& p, const DecodeExtraParams& ap, int head_dim,
                                   int cache_dt, int act_dt, cudaStream_t stream,
                                   cudaEvent_t merge_after) {
-  if (head_dim != 128 || act_dt != cache_dt) return cudaErrorInvalidValue;
   if (!ap.group_indptr || !ap.group_prefix_lens || ap.num_groups <= 0 || !p.ws_o)
     return cudaErrorInvalidValue;
   // Short runs per CTA (the members' own tokens are typically a few hundred):
-  // small CTAs of two warps with two stages each (~33 KB), so that many fit
-  // on an SM and their fixed costs (setup, first copy, epilogue) overlap.
-  // Shared-prompt layer, 320 tokens per CTA: 50.5 us, against 51.5 (2 warps,
-  // 1 stage), 53.1 (4 warps, 1 stage), 59.6 (4 warps, 3 stages) and 65.5
-  // (8 warps, 1 stage).  Long runs keep the plain decode's configuration.
+  // small CTAs of two warps with two stages each (~33 KB at bf16 d128), so
+  // that many fit on an SM and their fixed costs (setup, first copy,
+  // epilogue) overlap.  Shared-prompt layer, 320 tokens per CTA: 50.5 us,
+  // against 51.5 (2 warps, 1 stage), 53.1 (4 warps, 1 stage), 59.6 (4 warps,
+  // 3 stages) and 65.5 (8 warps, 1 stage).  Long runs keep the plain decode's
+  // configuration.
   const bool short_runs = p.chunk <= 512;
-  if (cache_dt == DT_F16)
-    return short_runs
-               ? launch_decode_t<128, DT_F16, DT_F16, true, 2, 2>(kmap, vmap, p, ap, stream,
-                                                                 merge_after)
-               : launch_decode_t<128, DT_F16, DT_F16, true>(kmap, vmap, p, ap, stream, merge_after);
-  if (cache_dt == DT_BF16)
-    return short_runs
-               ? launch_decode_t<128, DT_BF16, DT_BF16, true, 2, 2>(kmap, vmap, p, ap, stream,
-                                                                   merge_after)
-               : launch_decode_t<128, DT_BF16, DT_BF16, true>(kmap, vmap, p, ap, stream, merge_after);
+#define PKV_CASC(HD, CT, AT)                                                                   \
+  if (head_dim == HD && cache_dt == CT && act_dt == AT)                                        \
+    return short_runs                                                                          \
+               ? launch_decode_t<HD, CT, AT, true, 2, 2>(kmap, vmap, p, ap, stream, merge_after) \
+               : launch_decode_t<HD, CT, AT, true>(kmap, vmap, p, ap, stream, merge_after);
+  PKV_CASC(64, DT_F16, DT_F16)
+  PKV_CASC(64, DT_BF16, DT_BF16)
+  PKV_CASC(64, DT_E4M3, DT_F16)
+  PKV_CASC(64, DT_E4M3, DT_BF16)
+  PKV_CASC(128, DT_F16, DT_F16)
+  PKV_CASC(128, DT_BF16, DT_BF16)
+  PKV_CASC(128, DT_E4M3, DT_F16)
+  PKV_CASC(128, DT_E4M3, DT_BF16)
+#undef PKV_CASC
   return cudaErrorInvalidValue;
 }
 

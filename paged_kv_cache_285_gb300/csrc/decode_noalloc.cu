@@ -26,10 +26,13 @@ static __device__ __align__(256) unsigned char g_decode_scratch[PKV_NOALLOC_SCRA
 
 constexpr int kMaxDevices = 64;
 
+// Per-device cache of the scratch array's device address.  Only a successful
+// lookup is kept: a failed one (for example a sticky error left by earlier
+// unrelated work, or a first call made while a stream is being captured) is
+// retried by the next call instead of failing every later call on that device.
 struct ScratchState {
-  std::once_flag once;
+  std::mutex mu;
   void* ptr = nullptr;
-  cudaError_t err = cudaSuccess;
 };
 ScratchState g_scratch[kMaxDevices];
 
@@ -43,14 +46,14 @@ void* scratch_for_current_device(pkv_status* st) {
     return nullptr;
   }
   ScratchState* s = &g_scratch[dev];
-  std::call_once(s->once, [s]() {
+  std::lock_guard<std::mutex> lock(s->mu);
+  if (!s->ptr) {
     void* p = nullptr;
-    s->err = cudaGetSymbolAddress(&p, g_decode_scratch);
-    s->ptr = (s->err == cudaSuccess) ? p : nullptr;
-  });
-  if (s->err != cudaSuccess || !s->ptr) {
-    *st = PKV_ERR_CUDA;
-    return nullptr;
+    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || !p) {
+      *st = PKV_ERR_CUDA;
+      return nullptr;
+    }
+    s->ptr = p;
   }
   *st = PKV_OK;
   return s->ptr;

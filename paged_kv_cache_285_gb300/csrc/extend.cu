@@ -7,10 +7,10 @@
 // accumulators.
 //
 // Rows: a 128-row tile packs (suffix token, query head) rows of one
-// (request, kv head): with a GQA group of G heads it holds 128/G consecutive
-// suffix tokens x G heads, all sharing the same K/V.  Row r (token i, head j)
-// attends to keys 0 .. prefix + i.  Keys are consumed in tiles of 128 read
-// through the block table.
+// (request, kv head): with a GQA group of G heads it holds tok = 128/G
+// consecutive suffix tokens x G heads (row = token * G + head), all sharing
+// the same K/V.  Row r (token i, head j) attends to keys 0 .. prefix + i.
+// Keys are consumed in tiles of 128 read through the block table.
 //
 // Work item: two consecutive row tiles A and B of one (request, kv head).
 // Both use every K/V tile, and their softmaxes run on separate warps in
@@ -20,19 +20,19 @@
 // is persistent: one CTA per SM walks the items with a fixed stride and every
 // pipeline runs through item boundaries.
 //
-// TMEM (512 columns): S_A, S_B (fp32, 128 columns each) and O_A, O_B.  P of a
-// tile is written as f16 over the first 64 columns of its own S once the
-// softmax has S in registers, and O += P V reads it from there; the next
-// S = Q K^T of that tile is issued after that PV by the same thread (MMAs of
-// one thread execute in issue order).  Shared memory: Q of three row tiles
-// (the A and B tiles of an item and one tile of the next), 2-stage K and V
-// rings.  S = Q K^T reads both operands from shared memory, O += P V reads P
-// from TMEM and V, as loaded ([key][dim]), as an MN-major operand.
+// TMEM (512 columns): S_A, S_B (fp32, 128 columns each) and O_A, O_B (fp32,
+// head_dim columns each).  P of a tile is written as f16 over the first 64
+// columns of its own S once the softmax has S in registers, and O += P V
+// reads it from there; the next S = Q K^T of that tile is issued after that PV
+// by the same thread (MMAs of one thread execute in issue order).  Shared
+// memory: Q of three row tiles (the A and B tiles of an item and one tile of
+// the next), K and V rings.  S = Q K^T reads both operands from shared memory,
+// O += P V reads P from TMEM and V, as loaded ([key][dim]), as an MN-major
+// operand.
 //
 // Warp roles (512 threads):
 //   warp 0        TMA producer of Q tiles and of the K ring (block ids
-//                 prefetched into registers, 16-token x 64-dim boxes,
-//                 128-byte swizzled).
+//                 prefetched into registers, 16-token boxes, swizzled).
 //   warp 1        TMEM owner and MMA issuer: the whole warp runs the loop with
 //                 warp-uniform operands, one elected lane issues.
 //   warp 2        TMA producer of the V ring.
@@ -40,18 +40,30 @@
 //                 B: row max with lazy rescaling (O is rescaled in TMEM only
 //                 when the max grows by more than 2^8), f16 P, and at the end
 //                 of an item O / l and the LSE.
-//   warps 12-15   V converters: bf16 V tiles are turned into f16 in place and
-//                 keys past the sequence end are zeroed (they may hold NaN).
+//   warps 12-15   converters: bf16 V tiles become f16 in place; fp8 (e4m3) K
+//                 tiles are widened to the activation dtype and fp8 V tiles
+//                 to f16 (exactly: an e4m3 value fits both), one key row per
+//                 thread; V keys past the sequence end are zeroed (they may
+//                 hold NaN, and 0 * NaN is NaN).
 // P is f16 (11 significant bits) because bf16 P alone would put the relative
-// L2 error of the output near 1.5e-3; V is therefore converted to f16 (bf16
-// values beyond +-65504 are outside this path's range).
+// L2 error of the output near 1.5e-3; V is therefore f16 (bf16 values beyond
+// +-65504 are outside this path's range).
+//
+// fp8 caches ("KV Cache 완전 정리 — PagedAttention vs RadixAttention, SGLang이
+// 빠른 이유", "FP8 KV 캐시": half the bytes of a 16-bit cache) are read as
+// codes: the TMA copies one byte per element, the converter warps widen each
+// tile in shared memory, and the per-tensor scales are folded into the softmax
+// scale (k_scale) and the output scale (v_scale), so no 16-bit copy of the
+// cache exists anywhere.
 //
 // Prefix pass (PP = true), for decode over a prefix shared by a group of
 // requests: each group is one pseudo-request whose rows are the group
 // members' query vectors (one token each), keys are the group's P shared
 // tokens read through its first member's block table, every row sees all P
-// of them and no other, and each row's result leaves as an fp32 partial
-// (O / l and the base-2 LSE) for an LSE merge with the member's own tokens.
+// of them and no other.  The keys are cut into chunks of kchunk_keys, one work
+// item each (so that a few groups still fill the GPU), and each row's result
+// over a chunk leaves as an fp32 partial (O / l and the base-2 LSE) in the
+// chunk's slot, for an LSE merge with the member's own tokens.
 #include "internal.h"
 #include "ptx.cuh"
 #include "tcgen05.cuh"
@@ -62,40 +74,161 @@ namespace {
 
 constexpr int BM = 128;       // rows per tile
 constexpr int BN = 128;       // keys per tile
-constexpr int HD = 128;       // head dim
 constexpr int NTHREADS = 512;
-constexpr int NCONV = 128;    // V converter threads (warps 12-15)
-constexpr int NST = 2;        // K and V ring depth
+constexpr int NCONV = 128;    // converter threads (warps 12-15), one per key row
 constexpr int NQB = 3;        // Q tile buffers
-constexpr int TILE = BN * HD * 2;   // 32 KB: 128 x 128 16-bit elements
-constexpr int CHUNK = 16384;        // one 64-element column block [128 rows][128 B]
+constexpr int CHUNK = 16384;  // one 64-element column block of a 16-bit tile: [128 rows][128 B]
 
-constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + NQB * TILE;
-constexpr int OFF_V = OFF_K + NST * TILE;
-constexpr int OFF_BAR = OFF_V + NST * TILE;
-enum {
-  B_KFULL = 0, B_VFULL = B_KFULL + NST, B_VCONV = B_VFULL + NST,
-  B_KFREE = B_VCONV + NST,   // [stage] S_B(n) = Q_B K(n)^T done (S_A(n) before it): K stage free
-  B_VFREE = B_KFREE + NST,   // [stage] O_B += P_B V(n) done (O_A's before it): V stage free
-  B_SDONE = B_VFREE + NST,   // [2] S_x(n) = Q_x K(n)^T done
-  B_PFULL = B_SDONE + 2,     // [2] P_x(n) written
-  B_QFULL = B_PFULL + 2,     // [tile x][item parity] Q tile x of the item loaded
-  B_QFREE = B_QFULL + 4,     // [item parity] the item's last S_B = Q_B K^T done
-  B_ODONE = B_QFREE + 2,     // the item's last O_B += P_B V done (O_A's before it)
-  B_OFREE = B_ODONE + 1,     // [2] O_x of the item read out of TMEM
-  NBAR = B_OFREE + 2
+template <int HD, int CT>
+struct ExtCfg {
+  static constexpr bool FP8 = (CT == DT_E4M3);
+  static constexpr int NCH = HD / 64;           // 64-element column blocks per 16-bit row
+  static constexpr int NST = HD == 64 ? 3 : 2;  // K and V ring depth
+  static constexpr int T16 = BM * HD * 2;       // a 16-bit tile (Q, K or V): 16 or 32 KB
+  static constexpr int T8 = BN * HD;            // an fp8 K or V tile as loaded
+  // fp8 tiles are loaded into the first half of their 16-bit slot and widened
+  // in place at d128 (each converter thread owns one key row, and the 16-bit
+  // bytes of that row's dims 0-63 are exactly its fp8 row); at d64 a 16-bit
+  // row covers two fp8 rows, so the fp8 tiles get a staging ring of their own
+  static constexpr bool STAGE8 = FP8 && HD == 64;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + NQB * T16;
+  static constexpr int OFF_V = OFF_K + NST * T16;
+  static constexpr int OFF_K8 = OFF_V + NST * T16;
+  static constexpr int OFF_V8 = OFF_K8 + (STAGE8 ? NST * T8 : 0);
+  static constexpr int OFF_BAR = OFF_V8 + (STAGE8 ? NST * T8 : 0);
+  enum {
+    B_KFULL = 0,              // [stage] K tile loaded
+    B_VFULL = B_KFULL + NST,  // [stage] V tile loaded
+    B_KCONV = B_VFULL + NST,  // [stage] fp8 K tile widened
+    B_VCONV = B_KCONV + NST,  // [stage] V tile converted / tail zeroed
+    B_KFREE = B_VCONV + NST,  // [stage] S_B(n) = Q_B K(n)^T done (S_A(n) before it): K stage free
+    B_VFREE = B_KFREE + NST,  // [stage] O_B += P_B V(n) done (O_A's before it): V stage free
+    B_SDONE = B_VFREE + NST,  // [2] S_x(n) = Q_x K(n)^T done
+    B_PFULL = B_SDONE + 2,    // [2] P_x(n) written
+    B_QFULL = B_PFULL + 2,    // [tile x][item parity] Q tile x of the item loaded
+    B_QFREE = B_QFULL + 4,    // [item parity] the item's last S_B = Q_B K^T done
+    B_ODONE = B_QFREE + 2,    // the item's last O_B += P_B V done (O_A's before it)
+    B_OFREE = B_ODONE + 1,    // [2] O_x of the item read out of TMEM
+    NBAR = B_OFREE + 2
+  };
+  static constexpr int OFF_TMEMSLOT = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_TMEMSLOT + 16 + 1024;
+  static_assert(SMEM <= 232448, "shared memory per CTA");
+  // where the fp8 codes of stage s of the K (isv false) or V ring are loaded
+  __host__ __device__ static constexpr int src8(bool isv, int s) {
+    return STAGE8 ? (isv ? OFF_V8 : OFF_K8) + s * T8 : (isv ? OFF_V : OFF_K) + s * T16;
+  }
 };
-constexpr int OFF_TMEMSLOT = OFF_BAR + NBAR * 8;
-constexpr int SMEM_BYTES = OFF_TMEMSLOT + 16 + 1024;
-static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+
 constexpr uint32_t TMEM_COLS = 512;
-__host__ __device__ constexpr uint32_t tm_s(int x) { return (uint32_t)x * 128u; }         // S_x, then P_x
-__host__ __device__ constexpr uint32_t tm_o(int x) { return 256u + (uint32_t)x * 128u; }  // O_x
+__host__ __device__ constexpr uint32_t tm_s(int x) { return (uint32_t)x * 128u; }  // S_x, then P_x
+template <int HD>
+__host__ __device__ constexpr uint32_t tm_o(int x) { return 256u + (uint32_t)x * HD; }  // O_x
 constexpr float kLn2f = 0.6931471805599453f;
 
 __device__ __forceinline__ void set_err(int32_t* err, int code) {
   if (err) atomicCAS(err, 0, code);
+}
+
+// ---- converters ---------------------------------------------------------------
+// A 16-bit tile is NCH column blocks of [128 key rows][128 B] in the 128-byte
+// swizzle: logical 16-byte unit u of row t sits at unit u ^ (t & 7).  The
+// swizzle only permutes units inside a row, so a unit's key row is its byte
+// offset within its column block / 128.
+
+// A 16-bit V tile in place, 16-byte units spread over the converter threads
+// (thread ct takes units ct, ct + 128, ...: consecutive threads, consecutive
+// units): bf16 -> f16 (CVT), and units of keys at or past kv_end -> zeros
+// (TAIL; key0 is the tile's first key).  Measured faster than one key row per
+// thread on the benchmark's bf16 tiles (896 against 945 us per call).
+template <int HD, bool CVT, bool TAIL>
+__device__ __forceinline__ void conv_tile16(uint8_t* tile, int ct, int key0, int kv_end) {
+  constexpr int PER = BN * HD * 2 / 16 / NCONV;  // 16-byte units per thread
+  uint4* v4 = reinterpret_cast<uint4*>(tile);
+  if constexpr (TAIL) {
+#pragma unroll 4
+    for (int i = 0; i < PER; ++i) {
+      const int uu = ct + i * NCONV;
+      uint4 v = v4[uu];
+      if (key0 + ((uu * 16) % CHUNK) / 128 >= kv_end) {
+        v = make_uint4(0u, 0u, 0u, 0u);
+      } else if (CVT) {
+        v.x = to_f16x2<true>(v.x);
+        v.y = to_f16x2<true>(v.y);
+        v.z = to_f16x2<true>(v.z);
+        v.w = to_f16x2<true>(v.w);
+      }
+      v4[uu] = v;
+    }
+  } else {
+#pragma unroll
+    for (int hh = 0; hh < 4; ++hh) {  // four batches of PER / 4 loads in flight
+      uint4 v[PER / 4];
+#pragma unroll
+      for (int i = 0; i < PER / 4; ++i) v[i] = v4[ct + (hh * (PER / 4) + i) * NCONV];
+#pragma unroll
+      for (int i = 0; i < PER / 4; ++i) {
+        v[i].x = to_f16x2<true>(v[i].x);
+        v[i].y = to_f16x2<true>(v[i].y);
+        v[i].z = to_f16x2<true>(v[i].z);
+        v[i].w = to_f16x2<true>(v[i].w);
+        v4[ct + (hh * (PER / 4) + i) * NCONV] = v[i];
+      }
+    }
+  }
+}
+
+// Two e4m3 codes (low byte first) -> a 16-bit pair of OUT (exact).
+template <int OUT>
+__device__ __forceinline__ uint32_t widen2(uint32_t two) {
+  const uint32_t h = e4m3x2_to_f16x2(two);
+  if constexpr (OUT == DT_BF16) return pack2<true>(lo_f32<false>(h), hi_f32<false>(h));
+  else return h;
+}
+
+// 16 codes -> 16 OUT values in two 16-byte units.
+template <int OUT>
+__device__ __forceinline__ void widen16(const uint4& a, uint4& lo, uint4& hi) {
+  lo = make_uint4(widen2<OUT>(a.x & 0xFFFFu), widen2<OUT>(a.x >> 16), widen2<OUT>(a.y & 0xFFFFu),
+                  widen2<OUT>(a.y >> 16));
+  hi = make_uint4(widen2<OUT>(a.z & 0xFFFFu), widen2<OUT>(a.z >> 16), widen2<OUT>(a.w & 0xFFFFu),
+                  widen2<OUT>(a.w >> 16));
+}
+
+// Fp8 key row t (codes at src) -> 16-bit row t of the tile at dst, or zeros.
+//  d128: src == dst (in place).  The fp8 row is 128 B at t * 128 in the
+//        128-byte swizzle (logical unit u = dims 16u .. 16u+15 at u ^ (t & 7)),
+//        and 16-bit unit w of row t in column block 0 sits at the same place as
+//        fp8 unit w: dims 64-127 go to column block 1 (past the fp8 tile)
+//        first, then fp8 units 3, 2 -> 16-bit units 7 .. 4 and fp8 units 1, 0
+//        -> units 3 .. 0, so every store lands on fp8 units already read.  No
+//        other thread touches the row.
+//  d64:  src is a separate staging tile: 64 B rows at t * 64 in the 64-byte
+//        swizzle (unit u at u ^ ((t >> 1) & 3)).
+template <int HD, int OUT>
+__device__ __forceinline__ void widen_row(const uint8_t* src, uint8_t* dst, int t, bool zero) {
+#pragma unroll
+  for (int pr = HD / 32 - 1; pr >= 0; --pr) {  // fp8 unit pairs (2pr, 2pr+1), highest first
+    uint4 a[2];
+    if (!zero) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int u = 2 * pr + j;
+        const int off = (HD == 128) ? t * 128 + 16 * (u ^ (t & 7)) : t * 64 + 16 * (u ^ ((t >> 1) & 3));
+        a[j] = *reinterpret_cast<const uint4*>(src + off);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int u = 2 * pr + j;  // dims 16u .. 16u+15: block u / 4, 16-bit units 2(u%4), 2(u%4)+1
+      uint8_t* row = dst + (u >> 2) * CHUNK + t * 128;
+      uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+      if (!zero) widen16<OUT>(a[j], lo, hi);
+      *reinterpret_cast<uint4*>(row + 16 * ((2 * (u & 3)) ^ (t & 7))) = lo;
+      *reinterpret_cast<uint4*>(row + 16 * ((2 * (u & 3) + 1) ^ (t & 7))) = hi;
+    }
+  }
 }
 
 // Per-request values an item needs, loaded one item ahead.
@@ -104,7 +237,7 @@ struct ItemRaw {
 };
 
 struct Item {
-  int b, g, i0, ntok[2], P, S, row0, kv_total, k_hi, T;
+  int b, g, i0, ntok[2], P, S, row0, kv_total, k_lo, k_hi, T, slot;
 };
 
 __device__ __forceinline__ ItemRaw load_raw(const ExtendParams& p, int item) {
@@ -119,18 +252,35 @@ __device__ __forceinline__ ItemRaw load_raw(const ExtendParams& p, int item) {
 }
 
 // false: the item has no work (the same answer in every role): tile A holds no
-// suffix rows, or, in the prefix pass, the group shares no prefix
+// suffix rows, the request's rows are not a valid range of the call's rows,
+// or, in the prefix pass, the group shares no prefix or none in this item's
+// key chunk.  Rows beyond the max_suffix_len hint (or max_group_size in the
+// prefix pass), and prefix keys beyond the last chunk, are not computed and
+// are reported as a length error.
 template <bool PP>
 __device__ __forceinline__ bool derive(const ExtendParams& p, int item, const ItemRaw& r, Item& it) {
   const uint32_t rest = p.div_pairs.div((uint32_t)item);
-  const int pair = item - (int)(rest * p.div_pairs.d);
+  int pair = item - (int)(rest * p.div_pairs.d);
+  int kc = 0;  // prefix pass: the item's key chunk
+  if constexpr (PP) {
+    kc = pair % p.kchunks;
+    pair /= p.kchunks;
+  }
   it.b = (int)p.div_hkv.div(rest);
   it.g = (int)(rest - (uint32_t)it.b * p.div_hkv.d);
-  const int TOK = BM >> p.group_shift;
+  const int TOK = p.tok;
   it.row0 = r.r0;
   it.S = r.r1 - r.r0;
+  if constexpr (!PP) {
+    // the output rows written below must lie inside the call's rows
+    if (r.r0 < 0 || it.S < 0 || r.r1 > p.total_rows) {
+      set_err(p.err, 3);
+      return false;
+    }
+  }
   it.i0 = 2 * pair * TOK;  // first token of tile A; tile B follows it
   if (it.i0 >= it.S) return false;
+  if ((pair + 1) * p.kchunks == (int)p.div_pairs.d && it.i0 + 2 * TOK < it.S) set_err(p.err, 3);
   it.ntok[0] = min(TOK, it.S - it.i0);
   it.ntok[1] = max(0, min(TOK, it.S - it.i0 - TOK));
   it.P = r.prefix;
@@ -142,10 +292,15 @@ __device__ __forceinline__ bool derive(const ExtendParams& p, int item, const It
       return false;
     }
     it.P = (it.P >> p.bs_shift) << p.bs_shift;  // only whole blocks are shared
-    if (it.P <= 0) return false;
-    it.kv_total = it.P;
-    it.k_hi = it.P;
+    it.k_lo = kc * p.kchunk_keys;
+    if (it.P <= 0 || it.k_lo >= it.P) return false;
+    if (kc == p.kchunks - 1 && it.k_lo + p.kchunk_keys < it.P) set_err(p.err, 3);
+    it.kv_total = min(it.P, it.k_lo + p.kchunk_keys);  // this chunk's keys end here
+    it.k_hi = it.kv_total;
+    it.slot = kc;
   } else {
+    it.k_lo = 0;
+    it.slot = 0;
     it.kv_total = it.P + it.S;
     it.k_hi = it.P + it.i0 + it.ntok[0] + it.ntok[1];  // keys the pair needs
   }
@@ -153,28 +308,32 @@ __device__ __forceinline__ bool derive(const ExtendParams& p, int item, const It
     set_err(p.err, 3);
     it.kv_total = min(max(it.kv_total, 0), cap);
     it.k_hi = min(max(it.k_hi, 1), max(cap, 1));
+    if (it.k_hi <= it.k_lo) return false;  // every item that runs has a key tile
   }
-  it.T = (it.k_hi + BN - 1) / BN;
+  it.T = (it.k_hi - it.k_lo + BN - 1) / BN;
   return true;
 }
 
-template <int CT, bool PP>
+// HD: head dim (64 or 128); CT: cache dtype (f16, bf16 or e4m3); AT: the
+// activation dtype of q and out (equal to CT for 16-bit caches).
+template <int HD, int CT, int AT, bool PP>
 __global__ void __launch_bounds__(NTHREADS, 1)
 extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
               const __grid_constant__ CUtensorMap qmap, const ExtendParams p,
               const ExtendPartialParams pp) {
+  using C = ExtCfg<HD, CT>;
+  constexpr int NST = C::NST;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_TMEMSLOT);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEMSLOT);
   const uint32_t s_base = smem_u32(smem);
   auto bar = [&](int i) -> uint32_t { return smem_u32(&bars[i]); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.group;
-  const int gs = p.group_shift;  // G = 1 << gs
-  const int TOK = BM >> gs;
+  const int TOK = p.tok;
   const int item0 = blockIdx.x, stride = gridDim.x;
 
   if (threadIdx.x == 0) {
@@ -182,21 +341,22 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
     prefetch_tensormap(&vmap);
     prefetch_tensormap(&qmap);
     for (int i = 0; i < NST; ++i) {
-      mbar_init(bar(B_KFULL + i), 1);
-      mbar_init(bar(B_VFULL + i), 1);
-      mbar_init(bar(B_VCONV + i), NCONV / 32);
-      mbar_init(bar(B_KFREE + i), 1);
-      mbar_init(bar(B_VFREE + i), 1);
+      mbar_init(bar(C::B_KFULL + i), 1);
+      mbar_init(bar(C::B_VFULL + i), 1);
+      mbar_init(bar(C::B_KCONV + i), NCONV / 32);
+      mbar_init(bar(C::B_VCONV + i), NCONV / 32);
+      mbar_init(bar(C::B_KFREE + i), 1);
+      mbar_init(bar(C::B_VFREE + i), 1);
     }
     for (int x = 0; x < 2; ++x) {
-      mbar_init(bar(B_SDONE + x), 1);
-      mbar_init(bar(B_PFULL + x), 4);
-      mbar_init(bar(B_QFULL + 2 * x), 1);
-      mbar_init(bar(B_QFULL + 2 * x + 1), 1);
-      mbar_init(bar(B_QFREE + x), 1);
-      mbar_init(bar(B_OFREE + x), 4);
+      mbar_init(bar(C::B_SDONE + x), 1);
+      mbar_init(bar(C::B_PFULL + x), 4);
+      mbar_init(bar(C::B_QFULL + 2 * x), 1);
+      mbar_init(bar(C::B_QFULL + 2 * x + 1), 1);
+      mbar_init(bar(C::B_QFREE + x), 1);
+      mbar_init(bar(C::B_OFREE + x), 4);
     }
-    mbar_init(bar(B_ODONE), 1);
+    mbar_init(bar(C::B_ODONE), 1);
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -217,9 +377,10 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
     const int x = warp >= 8 ? 1 : 0;
     const int qw = warp & 3;
     const int r = qw * 32 + lane;
+    const int rtok = r / G, rhead = r - rtok * G;  // this row's token in the tile and head in the group
     const uint32_t lane_addr = (uint32_t)(qw * 32) << 16;
     const uint32_t srow = tmem + lane_addr + tm_s(x);
-    const uint32_t orow = tmem + lane_addr + tm_o(x);
+    const uint32_t orow = tmem + lane_addr + tm_o<HD>(x);
     int n = 0, js = 0;
     ItemRaw nxt_raw = load_raw(p, item0);
     for (int item = item0; ok && item < p.num_items; item += stride) {
@@ -228,19 +389,20 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       Item it;
       if (!derive<PP>(p, item, raw, it)) continue;
       const int i0x = it.i0 + x * TOK;  // first token of this tile
-      // a row's last visible key is kdiag + its token (prefix pass: P - 1 for all)
-      const int kdiag = PP ? it.P - 1 : it.P + i0x;
+      // a row's last visible key is kdiag + its token (prefix pass: the chunk's
+      // last key for all)
+      const int kdiag = PP ? it.kv_total - 1 : it.P + i0x;
       float m_run = -INFINITY, l_run = 0.f;
       for (int kt = 0; kt < it.T; ++kt, ++n) {
-        if (!mbar_wait(bar(B_SDONE + x), n & 1)) { ok = false; break; }
+        if (!mbar_wait(bar(C::B_SDONE + x), n & 1)) { ok = false; break; }
         tc_fence_after();
-        const int key0 = kt * BN;
+        const int key0 = it.k_lo + kt * BN;
         if (key0 + BN - 1 > kdiag) {
           // causal mask on a tile that reaches past some row's limit (keys
           // key0 .. key0+nvis are visible): applied in TMEM one 32-column
           // chunk at a time, a short rolled loop that runs on one or two key
           // tiles per item
-          const int nvis = kdiag + (PP ? 0 : (r >> gs)) - key0;
+          const int nvis = kdiag + (PP ? 0 : rtok) - key0;
           const uint32_t ninf = __float_as_uint(-INFINITY);
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
@@ -278,7 +440,7 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
           // rescale O_x in TMEM (its last PV completed before S_x(n) did)
           const float f = mine ? alpha : 1.f;
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < HD / 32; ++c) {
             uint32_t o[32];
             tmem_ld32(orow + c * 32, o);
             tmem_wait_ld();
@@ -314,22 +476,22 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_PFULL + x));
+        if (lane == 0) mbar_arrive(bar(C::B_PFULL + x));
       }
       if (!ok) break;
       // ---- item epilogue: O_x out of TMEM (then it is free for the next
       // item), O / l -> out, LSE
-      if (!mbar_wait(bar(B_ODONE), js & 1)) { ok = false; break; }
+      if (!mbar_wait(bar(C::B_ODONE), js & 1)) { ok = false; break; }
       tc_fence_after();
       const float osc = p.out_scale / l_run;
       if constexpr (PP) {
         // fp32 O / l straight from TMEM, 32 columns at a time, then the LSE
-        const int req = it.row0 + i0x + (r >> gs);  // the group member of this row
-        const bool valid = (r >> gs) < it.ntok[x] && req >= 0 && req < p.total_rows;
-        const int64_t qrow = (int64_t)req * p.num_q_heads + it.g * G + (r & (G - 1));
-        float* dst = pp.o + qrow * pp.o_stride;
+        const int req = it.row0 + i0x + rtok;  // the group member of this row
+        const bool valid = rtok < it.ntok[x] && req >= 0 && req < p.total_rows;
+        const int64_t qrow = (int64_t)req * p.num_q_heads + it.g * G + rhead;
+        float* dst = pp.o + qrow * pp.o_stride + it.slot * HD;
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < HD / 32; ++c) {
           uint32_t o[32];
           tmem_ld32(orow + c * 32, o);
           tmem_wait_ld();
@@ -342,36 +504,36 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_OFREE + x));
-        if (valid) pp.lse[qrow * pp.lse_stride] = m_run + log2f(l_run);
+        if (lane == 0) mbar_arrive(bar(C::B_OFREE + x));
+        if (valid) pp.lse[qrow * pp.lse_stride + it.slot] = m_run + log2f(l_run);
       } else {
         // O / l packed to 16-bit in registers; then O_x is free in TMEM
-        uint32_t w[64];
+        uint32_t w[HD / 2];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < HD / 32; ++c) {
           uint32_t o[32];
           tmem_ld32(orow + c * 32, o);
           tmem_wait_ld();
 #pragma unroll
           for (int q = 0; q < 16; ++q)
-            w[c * 16 + q] = pack2<CT == DT_BF16>(__uint_as_float(o[2 * q]) * osc,
+            w[c * 16 + q] = pack2<AT == DT_BF16>(__uint_as_float(o[2 * q]) * osc,
                                                  __uint_as_float(o[2 * q + 1]) * osc);
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_OFREE + x));
-        if ((r >> gs) < it.ntok[x]) {
-          const int64_t qrow = (int64_t)(it.row0 + i0x + (r >> gs)) * p.num_q_heads + it.g * G + (r & (G - 1));
+        if (lane == 0) mbar_arrive(bar(C::B_OFREE + x));
+        if (rtok < it.ntok[x]) {
+          const int64_t qrow = (int64_t)(it.row0 + i0x + rtok) * p.num_q_heads + it.g * G + rhead;
           uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + qrow * HD;
           if (p.out_32b) {
             // 32-byte stores: half the L1 requests of 16-byte ones for the
             // row-strided output
 #pragma unroll
-            for (int q = 0; q < 8; ++q) st_global_v8(dst + 16 * q, &w[8 * q]);
+            for (int q = 0; q < HD / 16; ++q) st_global_v8(dst + 16 * q, &w[8 * q]);
           } else {
             uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-            for (int q = 0; q < 16; ++q) d4[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+            for (int q = 0; q < HD / 8; ++q) d4[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
           }
           if (p.lse_out) p.lse_out[qrow] = (m_run + log2f(l_run)) * kLn2f;
         }
@@ -389,21 +551,21 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       const CUtensorMap* map = is_k ? &kmap : &vmap;
       // a K stage is free once S_B of its tile is done (S_A was issued before
       // it), a V stage once O_B += P_B V is
-      const int full0 = is_k ? B_KFULL : B_VFULL, free0 = is_k ? B_KFREE : B_VFREE;
-      const uint32_t ring = s_base + (is_k ? OFF_K : OFF_V);
+      const int full0 = is_k ? C::B_KFULL : C::B_VFULL, free0 = is_k ? C::B_KFREE : C::B_VFREE;
       // Q tile x of item j goes to buffer (2j + x) mod 3; the buffer was last
       // used by tile B of item j-2 (x = 0) or tile A of item j-1 (x = 1)
+      const uint32_t qbytes = (uint32_t)(C::NCH * 128 * G * TOK);  // the boxes' bytes
       auto load_q = [&](const Item& it, int jq, int xq) -> bool {
         int good = 1;
         if (lane == 0) {
           const int prev = jq - 2 + xq;  // item whose last S_B frees the buffer
-          if (prev >= 0 && !mbar_wait(bar(B_QFREE + (prev & 1)), (prev >> 1) & 1)) good = 0;
+          if (prev >= 0 && !mbar_wait(bar(C::B_QFREE + (prev & 1)), (prev >> 1) & 1)) good = 0;
           if (good) {
-            const uint32_t dst = s_base + OFF_Q + ((2 * jq + xq) % NQB) * TILE;
-            const uint32_t fb = bar(B_QFULL + 2 * xq + (jq & 1));
-            mbar_arrive_expect_tx(fb, TILE);
+            const uint32_t dst = s_base + C::OFF_Q + ((2 * jq + xq) % NQB) * C::T16;
+            const uint32_t fb = bar(C::B_QFULL + 2 * xq + (jq & 1));
+            mbar_arrive_expect_tx(fb, qbytes);
 #pragma unroll
-            for (int c = 0; c < 2; ++c)
+            for (int c = 0; c < C::NCH; ++c)
               tma_load_3d(dst + c * CHUNK, &qmap, fb, c * 64, it.g * G, it.row0 + it.i0 + xq * TOK);
           }
         }
@@ -420,7 +582,7 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
         // prefix pass: the group's first member's table (row0 = its index)
         const int32_t* bt = p.block_tables + (int64_t)(PP ? it.row0 : it.b) * p.max_blocks;
         auto fetch = [&](int wi) -> int {
-          const int key0 = (wi * 32 + lane) * 16;  // sub-tile = 16 keys
+          const int key0 = it.k_lo + (wi * 32 + lane) * 16;  // sub-tile = 16 keys
           int page = -1;
           if (key0 < it.k_hi) {
             const int blk = bt[key0 >> p.bs_shift];
@@ -442,14 +604,26 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
           for (int q = 0; q < 8; ++q) pg[q] = __shfl_sync(0xFFFFFFFFu, cur, (kt & 3) * 8 + q);
           if (n >= NST && !mbar_wait(bar(free0 + s), (uint32_t)((n / NST - 1) & 1))) { ok = false; break; }
           if (lane == 0) {
-            const uint32_t dst = ring + s * TILE;
-            mbar_arrive_expect_tx(bar(full0 + s), TILE);
+            const uint32_t fb = bar(full0 + s);
+            if constexpr (C::FP8) {
+              // one box of 16 keys x head_dim codes per sub-tile
+              const uint32_t dst = s_base + C::src8(!is_k, s);
+              mbar_arrive_expect_tx(fb, C::T8);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const int rip = (kt * BN + 16 * q) & ((1 << p.bs_shift) - 1);
+              for (int q = 0; q < 8; ++q) {
+                const int rip = (it.k_lo + kt * BN + 16 * q) & ((1 << p.bs_shift) - 1);
+                tma_load_3d(dst + q * 16 * HD, map, fb, 0, rip, pg[q]);
+              }
+            } else {
+              const uint32_t dst = s_base + (is_k ? C::OFF_K : C::OFF_V) + s * C::T16;
+              mbar_arrive_expect_tx(fb, C::T16);
 #pragma unroll
-              for (int c = 0; c < 2; ++c)
-                tma_load_3d(dst + c * CHUNK + q * 2048, map, bar(full0 + s), c * 64, rip, pg[q]);
+              for (int q = 0; q < 8; ++q) {
+                const int rip = (it.k_lo + kt * BN + 16 * q) & ((1 << p.bs_shift) - 1);
+#pragma unroll
+                for (int c = 0; c < C::NCH; ++c)
+                  tma_load_3d(dst + c * CHUNK + q * 2048, map, fb, c * 64, rip, pg[q]);
+              }
             }
           }
           // Q of tile B once tile A of the previous item is done with its buffer
@@ -463,36 +637,38 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       // elected lane issues the MMAs and commits.  Order per key tile n:
       // O_A += P_A(n-1) V(n-1), S_A(n), O_B += P_B(n-1) V(n-1), S_B(n): each
       // S_x(n) overwrites P_x(n-1) after the PV that reads it.
-      constexpr uint32_t qk_fmt = (CT == DT_BF16) ? 1u : 0u;
+      constexpr uint32_t qk_fmt = (AT == DT_BF16) ? 1u : 0u;
       constexpr uint32_t idesc_qk = umma_idesc_f16(qk_fmt, qk_fmt, BM, BN);
       constexpr uint32_t idesc_pv = umma_idesc_f16(0u, 0u, BM, HD) | (1u << 16);
+      // K is ready for the MMA once loaded, or, for fp8 codes, once widened
+      const int kready0 = C::FP8 ? C::B_KCONV : C::B_KFULL;
       // O_x += P_x(u) V(u); `first`: the first key tile of item ju, which
       // overwrites O_x once the previous item's O_x has been read out
       auto issue_pv = [&](int xx, int u, bool first, int ju) -> bool {
-        if (!mbar_wait(bar(B_PFULL + xx), u & 1)) return false;
-        if (xx == 0 && !mbar_wait(bar(B_VCONV + u % NST), (u / NST) & 1)) return false;
-        if (first && ju >= 1 && !mbar_wait(bar(B_OFREE + xx), (ju - 1) & 1)) return false;
+        if (!mbar_wait(bar(C::B_PFULL + xx), u & 1)) return false;
+        if (xx == 0 && !mbar_wait(bar(C::B_VCONV + u % NST), (u / NST) & 1)) return false;
+        if (first && ju >= 1 && !mbar_wait(bar(C::B_OFREE + xx), (ju - 1) & 1)) return false;
         tc_fence_after();
-        const uint64_t vdesc = umma_desc_sw128_mn(s_base + OFF_V + (u % NST) * TILE, CHUNK);
+        const uint64_t vdesc = umma_desc_sw128_mn(s_base + C::OFF_V + (u % NST) * C::T16, CHUNK);
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
-            umma_f16_ts(tmem + tm_o(xx), tmem + tm_s(xx) + kk * 8, vdesc + (uint64_t)(kk * 2048 >> 4),
+            umma_f16_ts(tmem + tm_o<HD>(xx), tmem + tm_s(xx) + kk * 8, vdesc + (uint64_t)(kk * 2048 >> 4),
                         idesc_pv, (!first || kk > 0) ? 1u : 0u);
         }
         __syncwarp();
         return true;
       };
       auto issue_qk = [&](int xx, int nn, int qbuf) {
-        const uint64_t kdesc = umma_desc_sw128(s_base + OFF_K + (nn % NST) * TILE);
-        const uint64_t qdesc = umma_desc_sw128(s_base + OFF_Q + qbuf * TILE);
+        const uint64_t kdesc = umma_desc_sw128(s_base + C::OFF_K + (nn % NST) * C::T16);
+        const uint64_t qdesc = umma_desc_sw128(s_base + C::OFF_Q + qbuf * C::T16);
         if (elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < HD / 16; ++kk) {
             const uint64_t off = (uint64_t)(((kk >> 2) * CHUNK + (kk & 3) * 32) >> 4);
             umma_f16(tmem + tm_s(xx), qdesc + off, kdesc + off, idesc_qk, kk > 0 ? 1u : 0u);
           }
-          umma_commit(bar(B_SDONE + xx));
+          umma_commit(bar(C::B_SDONE + xx));
         }
         __syncwarp();
       };
@@ -512,20 +688,20 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
         const int qa = (2 * j) % NQB, qb = (2 * j + 1) % NQB;
         for (int kt = 0; kt < it.T; ++kt, ++n) {
           if (have_prev && !issue_pv(0, prev_n, prev_first, prev_j)) { ok = false; break; }
-          if (!mbar_wait(bar(B_KFULL + n % NST), (n / NST) & 1)) { ok = false; break; }
-          if (kt == 0 && !mbar_wait(bar(B_QFULL + (j & 1)), (j >> 1) & 1)) { ok = false; break; }
+          if (!mbar_wait(bar(kready0 + n % NST), (n / NST) & 1)) { ok = false; break; }
+          if (kt == 0 && !mbar_wait(bar(C::B_QFULL + (j & 1)), (j >> 1) & 1)) { ok = false; break; }
           tc_fence_after();
           issue_qk(0, n, qa);
           if (have_prev) {
             if (!issue_pv(1, prev_n, prev_first, prev_j)) { ok = false; break; }
-            commit(B_VFREE + prev_n % NST);
-            if (prev_last) commit(B_ODONE);
+            commit(C::B_VFREE + prev_n % NST);
+            if (prev_last) commit(C::B_ODONE);
           }
-          if (kt == 0 && !mbar_wait(bar(B_QFULL + 2 + (j & 1)), (j >> 1) & 1)) { ok = false; break; }
+          if (kt == 0 && !mbar_wait(bar(C::B_QFULL + 2 + (j & 1)), (j >> 1) & 1)) { ok = false; break; }
           tc_fence_after();
           issue_qk(1, n, qb);
-          commit(B_KFREE + n % NST);
-          if (kt == it.T - 1) commit(B_QFREE + (j & 1));
+          commit(C::B_KFREE + n % NST);
+          if (kt == it.T - 1) commit(C::B_QFREE + (j & 1));
           have_prev = true;
           prev_n = n;
           prev_first = (kt == 0);
@@ -537,22 +713,20 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       if (ok && have_prev) {
         ok = issue_pv(0, prev_n, prev_first, prev_j) && issue_pv(1, prev_n, prev_first, prev_j);
         if (ok) {
-          commit(B_VFREE + prev_n % NST);
-          commit(B_ODONE);
+          commit(C::B_VFREE + prev_n % NST);
+          commit(C::B_ODONE);
         }
       }
     }
   } else {
     regs_dec<48>();
     {
-      // ------------------------------------------------------------ V converters (12-15)
-      // In place, per 16-byte unit: bf16 -> f16 (the PV product is f16 x f16),
-      // and keys at or past the sequence end -> 0 (they may hold anything, and
-      // 0 * NaN is NaN).  The swizzle only permutes units inside a 128-byte key
-      // row, so the key of a unit is its byte offset / 128 within its block.
-      const int ct = threadIdx.x - 384;  // 0..127
-      constexpr int PER = TILE / 16 / NCONV;  // 16 units of 16 bytes per thread
-      static_assert(PER * NCONV * 16 == TILE, "converter units");
+      // ------------------------------------------------------------ converters (12-15)
+      // Per key tile: fp8 K rows are widened to the activation dtype (then the
+      // S MMA may read the tile); V becomes f16 (bf16 or fp8 sources) and keys
+      // at or past the sequence end become zeros (then the PV MMA may read the
+      // tile).  fp8 tiles: thread t owns key row t.
+      const int t = threadIdx.x - 384;  // 0..127
       int n = 0;
       ItemRaw nxt_raw = load_raw(p, item0);
       for (int item = item0; ok && item < p.num_items; item += stride) {
@@ -561,45 +735,31 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
         Item it;
         if (!derive<PP>(p, item, raw, it)) continue;
         for (int kt = 0; kt < it.T; ++kt, ++n) {
-          const int vs = n % NST;
-          if (!mbar_wait(bar(B_VFULL + vs), (n / NST) & 1)) { ok = false; break; }
-          const int kbase = kt * BN;
-          uint4* vt = reinterpret_cast<uint4*>(smem + OFF_V + vs * TILE);
-          if (kbase + BN > it.kv_total) {  // tail tile: zero the keys past the end
-#pragma unroll 4
-            for (int i = 0; i < PER; ++i) {
-              const int uu = ct + i * NCONV;
-              uint4 v = vt[uu];
-              if (kbase + ((uu * 16) % CHUNK) / 128 >= it.kv_total) {
-                v = make_uint4(0u, 0u, 0u, 0u);
-              } else if (CT == DT_BF16) {
-                v.x = to_f16x2<true>(v.x);
-                v.y = to_f16x2<true>(v.y);
-                v.z = to_f16x2<true>(v.z);
-                v.w = to_f16x2<true>(v.w);
-              }
-              vt[uu] = v;
-            }
+          const int s = n % NST;
+          const uint32_t ph = (uint32_t)((n / NST) & 1);
+          if constexpr (C::FP8) {
+            if (!mbar_wait(bar(C::B_KFULL + s), ph)) { ok = false; break; }
+            widen_row<HD, AT>(smem + C::src8(false, s), smem + C::OFF_K + s * C::T16, t, false);
             fence_async_smem();
-          } else if (CT == DT_BF16) {
-#pragma unroll
-            for (int hh = 0; hh < 4; ++hh) {  // four batches of 4 loads in flight
-              uint4 v[PER / 4];
-#pragma unroll
-              for (int i = 0; i < PER / 4; ++i) v[i] = vt[ct + (hh * (PER / 4) + i) * NCONV];
-#pragma unroll
-              for (int i = 0; i < PER / 4; ++i) {
-                v[i].x = to_f16x2<true>(v[i].x);
-                v[i].y = to_f16x2<true>(v[i].y);
-                v[i].z = to_f16x2<true>(v[i].z);
-                v[i].w = to_f16x2<true>(v[i].w);
-                vt[ct + (hh * (PER / 4) + i) * NCONV] = v[i];
-              }
-            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::B_KCONV + s));
+          }
+          if (!mbar_wait(bar(C::B_VFULL + s), ph)) { ok = false; break; }
+          const int kbase = it.k_lo + kt * BN;
+          const bool zero = kbase + t >= it.kv_total;
+          uint8_t* vt = smem + C::OFF_V + s * C::T16;
+          if constexpr (C::FP8) {
+            widen_row<HD, DT_F16>(smem + C::src8(true, s), vt, t, zero);
+            fence_async_smem();
+          } else if (kbase + BN > it.kv_total) {  // tail tile: zero the keys past the end
+            conv_tile16<HD, CT == DT_BF16, true>(vt, t, kbase, it.kv_total);
+            fence_async_smem();
+          } else if constexpr (CT == DT_BF16) {
+            conv_tile16<HD, true, false>(vt, t, kbase, it.kv_total);
             fence_async_smem();
           }
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar(B_VCONV + vs));
+          if (lane == 0) mbar_arrive(bar(C::B_VCONV + s));
         }
       }
     }
@@ -617,25 +777,45 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
 }  // namespace
 
 bool extend_supported(int head_dim, int cache_dt, int act_dt, int group) {
-  if (head_dim != HD) return false;
-  if (!(cache_dt == DT_F16 || cache_dt == DT_BF16) || act_dt != cache_dt) return false;
-  return group == 1 || group == 2 || group == 4 || group == 8;
+  if (head_dim != 64 && head_dim != 128) return false;
+  if (!(act_dt == DT_F16 || act_dt == DT_BF16)) return false;
+  if (!(cache_dt == act_dt || cache_dt == DT_E4M3)) return false;
+  return group >= 1 && group <= BM;
 }
 
 namespace {
 
-template <bool PP>
+template <int HD, int CT, int AT, bool PP>
 cudaError_t launch_extend_t(const CUtensorMap& kmap, const CUtensorMap& vmap, const CUtensorMap& qmap,
-                            const ExtendParams& p, const ExtendPartialParams& pp, int head_dim,
-                            int cache_dt, int act_dt, cudaStream_t stream) {
-  if (!extend_supported(head_dim, cache_dt, act_dt, p.group)) return cudaErrorInvalidValue;
-  if (p.num_items <= 0 || p.num_ctas <= 0) return cudaErrorInvalidValue;
-  const dim3 grid(p.num_ctas);
-  auto k = cache_dt == DT_BF16 ? extend_kernel<DT_BF16, PP> : extend_kernel<DT_F16, PP>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+                            const ExtendParams& p, const ExtendPartialParams& pp,
+                            cudaStream_t stream) {
+  auto k = extend_kernel<HD, CT, AT, PP>;
+  constexpr int smem = ExtCfg<HD, CT>::SMEM;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  k<<<grid, NTHREADS, SMEM_BYTES, stream>>>(kmap, vmap, qmap, p, pp);
+  k<<<dim3(p.num_ctas), NTHREADS, smem, stream>>>(kmap, vmap, qmap, p, pp);
   return cudaGetLastError();
+}
+
+template <bool PP>
+cudaError_t launch_extend_any(const CUtensorMap& kmap, const CUtensorMap& vmap, const CUtensorMap& qmap,
+                              const ExtendParams& p, const ExtendPartialParams& pp, int head_dim,
+                              int cache_dt, int act_dt, cudaStream_t stream) {
+  if (!extend_supported(head_dim, cache_dt, act_dt, p.group)) return cudaErrorInvalidValue;
+  if (p.num_items <= 0 || p.num_ctas <= 0 || p.tok != BM / p.group) return cudaErrorInvalidValue;
+#define PKV_EXT(HD, CT, AT)                                    \
+  if (head_dim == HD && cache_dt == CT && act_dt == AT)        \
+    return launch_extend_t<HD, CT, AT, PP>(kmap, vmap, qmap, p, pp, stream);
+  PKV_EXT(128, DT_F16, DT_F16)
+  PKV_EXT(128, DT_BF16, DT_BF16)
+  PKV_EXT(128, DT_E4M3, DT_F16)
+  PKV_EXT(128, DT_E4M3, DT_BF16)
+  PKV_EXT(64, DT_F16, DT_F16)
+  PKV_EXT(64, DT_BF16, DT_BF16)
+  PKV_EXT(64, DT_E4M3, DT_F16)
+  PKV_EXT(64, DT_E4M3, DT_BF16)
+#undef PKV_EXT
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
@@ -643,8 +823,8 @@ cudaError_t launch_extend_t(const CUtensorMap& kmap, const CUtensorMap& vmap, co
 cudaError_t launch_extend(const CUtensorMap& kmap, const CUtensorMap& vmap, const CUtensorMap& qmap,
                           const ExtendParams& p, int head_dim, int cache_dt, int act_dt,
                           cudaStream_t stream) {
-  return launch_extend_t<false>(kmap, vmap, qmap, p, ExtendPartialParams{}, head_dim, cache_dt,
-                                act_dt, stream);
+  return launch_extend_any<false>(kmap, vmap, qmap, p, ExtendPartialParams{}, head_dim, cache_dt,
+                                  act_dt, stream);
 }
 
 cudaError_t launch_extend_prefix_pass(const CUtensorMap& kmap, const CUtensorMap& vmap,
@@ -652,7 +832,7 @@ cudaError_t launch_extend_prefix_pass(const CUtensorMap& kmap, const CUtensorMap
                                       const ExtendPartialParams& pp, int head_dim, int cache_dt,
                                       int act_dt, cudaStream_t stream) {
   if (!pp.o || !pp.lse) return cudaErrorInvalidValue;
-  return launch_extend_t<true>(kmap, vmap, qmap, p, pp, head_dim, cache_dt, act_dt, stream);
+  return launch_extend_any<true>(kmap, vmap, qmap, p, pp, head_dim, cache_dt, act_dt, stream);
 }
 
 }  // namespace pkv

@@ -27,7 +27,7 @@ struct DecodeParams {
   int batch;
   int num_q_heads;
   int num_kv_heads;
-  int group;          // Hq / Hkv (<= 8)
+  int group;          // Hq / Hkv (a CTA takes up to 8 of them)
   int bs_shift;       // log2(block_size)
   int chunk;          // tokens per split, multiple of 16
   int num_splits;     // S of the plan
@@ -56,6 +56,12 @@ struct DecodeExtraParams {
   const int32_t* group_prefix_lens;  // [num_groups]
   int num_groups;
   int2* ws_span;                     // [batch] (first own token, length), for the merge
+  // workspace slots 0 .. prefix_slots-1 hold the shared prefix's partials, one
+  // per chunk of prefix_chunk keys (a prefix of W tokens fills the first
+  // ceil(W / prefix_chunk)); the own tokens' splits follow them
+  int prefix_slots;
+  int prefix_chunk;
+  int prefix_chunks;  // chunks the prefix pass computes (<= prefix_slots)
 };
 
 // Division of unsigned n < 2^31 by a divisor fixed for a launch, as a
@@ -126,15 +132,17 @@ struct ExtendParams {
   int batch;
   int num_q_heads;
   int num_kv_heads;
-  int group;
-  int group_shift;      // log2(group); the group is 1, 2, 4 or 8
+  int group;            // Hq / Hkv, 1 .. 128
+  int tok;              // suffix tokens per 128-row tile: 128 / group (rounded down)
   int bs_shift;
   int total_rows;
-  int tiles_per_head;   // ceil(max_suffix_len * group / 128)
+  int tiles_per_head;   // ceil(max_suffix_len / tok)
   int num_items;        // ceil(tiles_per_head / 2) * num_kv_heads * batch (pairs of tiles)
   int num_ctas;         // persistent grid: min(num_items, SM count)
   int out_32b;          // out is 32-byte aligned: rows are written with 32-byte stores
-  FastDiv div_pairs;    // by ceil(tiles_per_head / 2)
+  int kchunks;          // prefix pass: key chunks per pair of row tiles (1 otherwise)
+  int kchunk_keys;      // prefix pass: keys per chunk, a multiple of 128
+  FastDiv div_pairs;    // by ceil(tiles_per_head / 2) * kchunks
   FastDiv div_hkv;      // by num_kv_heads
   FastDiv div_req;      // by ceil(tiles_per_head / 2) * num_kv_heads (items per request)
   float scale_log2;
@@ -142,9 +150,9 @@ struct ExtendParams {
 };
 
 // Partial output of the extend kernel's prefix pass: row q (request b, head h:
-// q = b * num_q_heads + h) writes O / l to o[q * o_stride .. + head_dim) and
-// the base-2 LSE to lse[q * lse_stride] (o 32-byte aligned, o_stride a
-// multiple of 8).
+// q = b * num_q_heads + h) over key chunk c writes O / l to
+// o[q * o_stride + c * head_dim .. + head_dim) and the base-2 LSE to
+// lse[q * lse_stride + c] (o 32-byte aligned, o_stride a multiple of 8).
 struct ExtendPartialParams {
   float* o;
   float* lse;
@@ -158,8 +166,7 @@ cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap,
                           int cache_dt, int act_dt, cudaStream_t stream);
 // Decode over each request's tokens after its group's shared prefix, partials
 // in slots 1.. of the workspace, then (after `merge_after`, the prefix pass's
-// completion, when not null) the merge with slot 0; head_dim 128, 16-bit
-// caches.
+// completion, when not null) the merge with slot 0.
 cudaError_t launch_decode_cascade(const CUtensorMap& kmap, const CUtensorMap& vmap,
                                   const DecodeParams& p, const DecodeExtraParams& ap, int head_dim,
                                   int cache_dt, int act_dt, cudaStream_t stream,
@@ -178,26 +185,8 @@ struct ChainHashParams {
 };
 cudaError_t launch_chain_hash(const ChainHashParams& p, int batch, cudaStream_t stream);
 
-// fp8 pages read by an extend call -> 16-bit shadow pages (same layout).
-struct DequantParams {
-  const uint8_t* k8;          // fp8 K pool
-  const uint8_t* v8;          // fp8 V pool
-  uint16_t* k16;              // shadow K pool, activation dtype
-  uint16_t* v16;              // shadow V pool
-  int32_t* flags;             // [num_blocks], zero before the launch
-  const int32_t* q_indptr;
-  const int32_t* prefix_lens;
-  const int32_t* block_tables;
-  int max_blocks;
-  int num_blocks;
-  int bs_shift;
-  int page_elems;             // Hkv * block_size * head_dim
-};
-cudaError_t launch_dequant_pages(const DequantParams& p, int batch, int blocks_per_seq, int act_dt,
-                                 cudaStream_t stream);
-
-// kmap/vmap: page maps of the K and V caches; qmap: the query rows, dims
-// {head_dim, num_q_heads, total_rows}, box {64, group, 128 / group}.
+// kmap/vmap: page maps of the K and V caches (16-bit or fp8 codes); qmap: the
+// query rows, dims {head_dim, num_q_heads, total_rows}, box {64, group, tok}.
 cudaError_t launch_extend(const CUtensorMap& kmap, const CUtensorMap& vmap,
                           const CUtensorMap& qmap, const ExtendParams& p, int head_dim,
                           int cache_dt, int act_dt, cudaStream_t stream);

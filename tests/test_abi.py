@@ -66,7 +66,6 @@ def test_decode_argument_errors(lib):
     assert _decode(lib, _desc(num_blocks=0)) == 1
     assert _decode(lib, _desc(), act=0) == 2                # bf16 cache with f16 queries
     assert _decode(lib, _desc(), act=2) == 1                # fp8 is not an act dtype
-    assert _decode(lib, _desc(), hq=2 * 9) == 2             # GQA group of 9 > 8
     assert _decode(lib, _desc(cache_dtype=2, k_scale=0.0)) == 1   # fp8 needs scales > 0
     assert _decode(lib, _desc(), scale=float("nan")) == 1
     assert _decode(lib, _desc(), batch=-1) == 1
@@ -91,6 +90,18 @@ def test_extend_argument_errors(lib):
     r = lib.pkv_paged_extend_attn(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, 1, FAKE, FAKE, FAKE, 4,
                                   1, 3, 0.1, 10, 10, 100, None, None, 0, None)
     assert r == 1                                            # Hq % Hkv != 0
+    ext = lambda desc, hq=4, act=1: lib.pkv_paged_extend_attn(
+        ctypes.byref(desc), FAKE, FAKE, FAKE, FAKE, act, FAKE, FAKE, FAKE, 4, 1, hq, 0.1, 10, 10,
+        100, None, None, 0, None)
+    assert ext(_desc(), hq=2 * 129) == 2                     # GQA group above 128 rows
+    assert ext(_desc(head_dim=96)) == 2                      # unsupported head_dim
+    assert ext(_desc(), act=0) == 2                          # bf16 cache with f16 queries
+    assert ext(_desc(), act=2) == 1                          # fp8 is not an act dtype
+    # no dtype needs scratch: fp8 caches are widened inside the kernel
+    for dt in (0, 1, 2):
+        for hd in (64, 128):
+            assert lib.pkv_extend_workspace_bytes(ctypes.byref(_desc(cache_dtype=dt, head_dim=hd)),
+                                                  4, 8, 400, 2000) == 0
 
 
 def test_decode_workspace_plan(lib):
@@ -116,12 +127,12 @@ class torch_free_cache:
 def _shared(lib, desc, hq=8, act=1, batch=2, groups=1, scale=0.1, ws=None, ws_bytes=0):
     return lib.pkv_paged_decode_attn_shared_prefix(
         ctypes.byref(desc), FAKE, FAKE, None, None, FAKE, FAKE, act, FAKE, 4, FAKE, batch, hq,
-        scale, FAKE, FAKE, groups, 2, 100, 0, None, ws, ws_bytes, None)
+        scale, FAKE, FAKE, groups, 2, 64, 100, 0, None, ws, ws_bytes, None)
 
 
 def test_shared_prefix_decode_argument_errors(lib):
-    assert _shared(lib, _desc(head_dim=64)) == 2              # no prefix pass at d64
-    assert _shared(lib, _desc(cache_dtype=2)) == 2            # fp8 cache
+    assert _shared(lib, _desc(), hq=2 * 129) == 2             # group above one 128-row tile
+    assert _shared(lib, _desc(), act=0) == 2                  # bf16 cache with f16 queries
     assert _shared(lib, _desc(), scale=-0.1) == 1             # the prefix pass needs scale > 0
     assert _shared(lib, _desc(), hq=3) == 1                   # Hq % Hkv != 0
     assert _shared(lib, _desc(), groups=0) == 1               # requests but no group
@@ -130,8 +141,15 @@ def test_shared_prefix_decode_argument_errors(lib):
     # down to whole blocks): 8 tiles -> 4 per split; slots = 2 + the prefix's
     d = _desc()
     # (+ 256-byte alignment, then one int2 span per request)
-    assert lib.pkv_shared_prefix_decode_workspace_bytes(ctypes.byref(d), 2, 8, 100, 2) == \
+    assert lib.pkv_shared_prefix_decode_workspace_bytes(ctypes.byref(d), 2, 8, 100, 100, 2) == \
         2 * 8 * 3 * 128 * 4 + 256 + 2 * 8
+    # a 1,000-token prefix bound: 4 chunks of 256 keys -> 4 prefix slots + 2 own splits
+    assert lib.pkv_shared_prefix_decode_workspace_bytes(ctypes.byref(d), 2, 8, 1000, 100, 2) == \
+        2 * 8 * 6 * 128 * 4 + 512 + 2 * 8
+    # at most 8 prefix chunks, however long the prefix
+    assert lib.pkv_shared_prefix_decode_workspace_bytes(ctypes.byref(d), 2, 8, 100000, 100, 2) == \
+        2 * 8 * 10 * 128 * 4 + 768 + 2 * 8
+    assert lib.pkv_shared_prefix_decode_workspace_bytes(ctypes.byref(d), 2, 8, -1, 100, 2) == 0
 
 
 def test_chain_hash_and_extend_append_argument_errors(lib):
@@ -146,11 +164,11 @@ def test_chain_hash_and_extend_append_argument_errors(lib):
     with pytest.raises(ValueError):  # int64 token ids: refused by the binding
         pkv.chain_hash(torch.zeros(4, dtype=torch.int64), torch.zeros(2, dtype=torch.int32), 16,
                        torch.zeros((1, 1), dtype=torch.int64))
-    d8 = _desc(cache_dtype=2)
     ext = lambda desc, kn=FAKE: lib.pkv_paged_extend_attn_append(
         ctypes.byref(desc), FAKE, FAKE, kn, kn, FAKE, FAKE, 1, FAKE, FAKE, FAKE, 4, 1, 4, 0.1, 10,
         10, 100, None, None)
-    assert ext(d8) == 2                                       # fp8 cache
+    assert ext(_desc(head_dim=96)) == 2                       # unsupported head_dim
+    assert ext(_desc(cache_dtype=2, v_scale=float("inf"))) == 1   # fp8 scales finite and > 0
     assert ext(_desc(), kn=None) == 1                         # the suffix K/V are required
 
 
@@ -191,8 +209,8 @@ def test_binding_refuses_inconsistent_shapes(lib):
                                                   lse_out=torch.zeros((3, 7)))),
         ("k_new", lambda: pkv.paged_decode_attn_append(c, c, kn[:2], kn[:2], q, q, bt, sl, 0.1, 64)),
         ("seq_lens", lambda: pkv.paged_decode_attn_noalloc(c, c, q, q, bt, sl[:2], 0.1, 64)),
-        ("k_new", lambda: pkv.paged_decode_attn_shared_prefix(c, c, q, q, bt, sl, 0.1, gi, gp, 3, 64,
-                                                              k_new=kn[:1], v_new=kn[:1])),
+        ("k_new", lambda: pkv.paged_decode_attn_shared_prefix(c, c, q, q, bt, sl, 0.1, gi, gp, 3, 32,
+                                                              64, k_new=kn[:1], v_new=kn[:1])),
         ("k_new", lambda: pkv.kv_append(c, c, kn, kn, torch.zeros(2, dtype=torch.int64))),
         ("v_new", lambda: pkv.kv_append(c, c, kn, kn.half(), torch.zeros(3, dtype=torch.int64))),
         ("q_indptr", lambda: pkv.paged_extend_attn(c, c, q, q, ip[:3], sl, bt, 0.1, 8, 64)),

@@ -1,8 +1,8 @@
 """GPU parity of pkv_paged_decode_attn against the fp64 oracle.
 
 Small cases span several 16-token tiles, partial last blocks, every supported
-head_dim / block_size / dtype / GQA group, forced split counts and the edge
-cases; the workload-sized cases run in the launch configuration the benchmark
+head_dim / block_size / dtype, GQA groups from 1 to 16 (powers of two and
+others), forced split counts and the edge cases; the workload-sized cases run in the launch configuration the benchmark
 times, compared in full where the oracle is fast enough and on sampled
 (request, head) pairs otherwise."""
 import math
@@ -84,6 +84,11 @@ CONFIGS = [
     ([45, 90, 16], 8, 1, 64, 16, E4M3, F16),
     ([33, 250], 4, 2, 128, 32, E4M3, F16),
     ([40, 7, 500], 4, 4, 64, 16, F16, F16),
+    # GQA groups above 8 (one CTA per 8 heads of a kv head) and not powers of two
+    ([130, 17, 600], 64, 4, 128, 16, BF16, BF16),
+    ([33, 90], 12, 1, 64, 32, F16, F16),
+    ([300, 5], 96, 8, 128, 16, E4M3, BF16),
+    ([77, 200, 1], 6, 2, 128, 16, BF16, BF16),
 ]
 
 

@@ -51,6 +51,9 @@ CASES = [
     ([33, 250, 4096, 65], 32, 8, 128, 32, BF16, BF16),
     ([200, 3, 64, 17], 64, 8, 128, 16, E4M3, BF16),
     ([45, 90, 16, 1], 8, 1, 64, 16, E4M3, F16),
+    # groups above 8: every head chunk's CTA writes the current token's row (the same bytes)
+    ([130, 17, 1, 600], 64, 4, 128, 16, BF16, BF16),
+    ([300, 5, 33], 96, 8, 128, 16, E4M3, BF16),
 ]
 
 

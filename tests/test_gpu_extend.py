@@ -1,8 +1,9 @@
 """GPU parity of pkv_paged_extend_attn (suffix prefill over cached prefix
 blocks) against the fp64 oracle: ragged suffixes spanning several 128-row
-tiles, prefixes that end mid-block, every GQA group the kernel takes, both
-block sizes and 16-bit dtypes; the 1,900 + 100 case of the first page; and the
-256-request shared-prefix workload the benchmark times (sampled rows)."""
+tiles, prefixes that end mid-block, GQA groups from 1 to 32 (powers of two and
+others), head_dim 64 and 128, both block sizes, 16-bit and fp8 caches; the
+1,900 + 100 case of the first page; the 256-request shared-prefix workload the
+benchmark times (sampled rows); and the device-side length checks."""
 import numpy as np
 import pytest
 import torch
@@ -50,28 +51,43 @@ def check(case, out, lse, what, rows=None, fp8=False):
 
 
 CASES = [
-    # (prefix_lens, suffix_lens, hq, hkv, bs, dtype)
-    ([0], [5], 4, 1, 16, F16),
-    ([4], [1], 4, 1, 16, F16),
-    ([1900], [100], 32, 8, 16, BF16),
-    ([0, 13, 30, 200], [37, 19, 130, 1], 8, 2, 16, BF16),
-    ([100, 0], [300, 129], 8, 8, 32, F16),
-    ([17, 250], [64, 33], 16, 2, 16, BF16),
-    ([129, 64, 1], [200, 17, 256], 64, 8, 16, BF16),
-    ([500], [40], 4, 2, 32, BF16),
+    # (prefix_lens, suffix_lens, hq, hkv, bs, dtype, head_dim)
+    ([0], [5], 4, 1, 16, F16, 128),
+    ([4], [1], 4, 1, 16, F16, 128),
+    ([1900], [100], 32, 8, 16, BF16, 128),
+    ([0, 13, 30, 200], [37, 19, 130, 1], 8, 2, 16, BF16, 128),
+    ([100, 0], [300, 129], 8, 8, 32, F16, 128),
+    ([17, 250], [64, 33], 16, 2, 16, BF16, 128),
+    ([129, 64, 1], [200, 17, 256], 64, 8, 16, BF16, 128),
+    ([500], [40], 4, 2, 32, BF16, 128),
     # requests with no suffix rows between others (equal q_indptr entries)
-    ([40, 7, 0, 300, 0], [0, 50, 0, 3, 0], 8, 2, 16, BF16),
+    ([40, 7, 0, 300, 0], [0, 50, 0, 3, 0], 8, 2, 16, BF16, 128),
+    # GQA groups that are not powers of two (3, 6: tiles of 42 / 21 tokens) and above 8
+    ([33, 0, 90], [70, 45, 130], 12, 4, 16, BF16, 128),
+    ([200, 16], [50, 77], 24, 4, 32, F16, 128),
+    ([64, 301], [40, 19], 64, 4, 16, BF16, 128),
+    ([10], [37], 32, 1, 16, F16, 128),
+    # head_dim 64: ragged, mid-block prefixes, groups 1 / 4 / 8, both block sizes
+    ([0], [5], 4, 1, 16, F16, 64),
+    ([4], [1], 4, 1, 16, F16, 64),
+    ([1900], [100], 32, 8, 16, BF16, 64),
+    ([0, 13, 30, 200], [37, 19, 130, 1], 8, 2, 16, BF16, 64),
+    ([100, 0], [300, 129], 8, 8, 32, F16, 64),
+    ([129, 64, 1], [200, 17, 256], 64, 8, 16, BF16, 64),
+    ([37, 60, 16, 1], [20, 3, 64, 9], 4, 1, 16, F16, 64),
+    ([500, 7], [40, 250], 24, 4, 32, BF16, 64),
 ]
 
 
-@pytest.mark.parametrize("cfg", CASES, ids=lambda c: f"P{c[0]}-S{c[1]}-h{c[2]}x{c[3]}-bs{c[4]}-d{c[5]}")
+@pytest.mark.parametrize("cfg", CASES,
+                         ids=lambda c: f"P{c[0]}-S{c[1]}-h{c[2]}x{c[3]}-bs{c[4]}-d{c[5]}-hd{c[6]}")
 def test_extend_small(cfg):
-    P, Sx, hq, hkv, bs, dt = cfg
-    case = W.extend_case(P, Sx, hq, hkv, 128, bs, dt, dt, seed=sum(P) + sum(Sx) + hq, device="cuda")
+    P, Sx, hq, hkv, bs, dt, hd = cfg
+    case = W.extend_case(P, Sx, hq, hkv, hd, bs, dt, dt, seed=sum(P) + sum(Sx) + hq + hd,
+                         device="cuda")
     out, lse = gpu_extend(case)
     check(case, out, lse, str(cfg))
     assert pkv.get_device_error() == 0
-
 
 
 def test_extend_with_no_suffix_rows_is_a_no_op():
@@ -166,40 +182,45 @@ def test_extend_garbage_past_end_is_ignored():
 
 
 FP8_CASES = [
-    # (prefix_lens, suffix_lens, hq, hkv, bs, act dtype)
-    ([0, 13, 30, 200], [37, 19, 130, 1], 8, 2, 16, BF16),
-    ([1900], [100], 32, 8, 16, BF16),
-    ([100, 0], [300, 129], 8, 8, 32, F16),
-    ([129, 64, 1], [200, 17, 256], 64, 8, 16, BF16),
+    # (prefix_lens, suffix_lens, hq, hkv, bs, act dtype, head_dim)
+    ([0, 13, 30, 200], [37, 19, 130, 1], 8, 2, 16, BF16, 128),
+    ([1900], [100], 32, 8, 16, BF16, 128),
+    ([100, 0], [300, 129], 8, 8, 32, F16, 128),
+    ([129, 64, 1], [200, 17, 256], 64, 8, 16, BF16, 128),
+    ([33, 0, 90], [70, 45, 130], 12, 4, 16, F16, 128),
+    ([0, 13, 30, 200], [37, 19, 130, 1], 8, 2, 16, BF16, 64),
+    ([1900], [100], 32, 8, 16, F16, 64),
+    ([100, 0], [300, 129], 8, 8, 32, BF16, 64),
+    ([129, 64, 1], [200, 17, 256], 64, 8, 16, F16, 64),
 ]
 
 
-@pytest.mark.parametrize("cfg", FP8_CASES, ids=lambda c: f"fp8-P{c[0]}-S{c[1]}-h{c[2]}x{c[3]}-bs{c[4]}-a{c[5]}")
+@pytest.mark.parametrize("cfg", FP8_CASES,
+                         ids=lambda c: f"fp8-P{c[0]}-S{c[1]}-h{c[2]}x{c[3]}-bs{c[4]}-a{c[5]}-hd{c[6]}")
 def test_extend_fp8_cache(cfg):
-    # e4m3 pages with per-tensor scales: widened once per page into the
-    # workspace, then the 16-bit path; vs the oracle on the same dequantised
-    # values, fp8 bound
-    P, Sx, hq, hkv, bs, act = cfg
-    case = W.extend_case(P, Sx, hq, hkv, 128, bs, E4M3, act, seed=90 + sum(Sx), device="cuda")
+    # e4m3 pages with per-tensor scales, read as codes and widened inside the
+    # kernel; vs the oracle on the same dequantised values, fp8 bound
+    P, Sx, hq, hkv, bs, act, hd = cfg
+    case = W.extend_case(P, Sx, hq, hkv, hd, bs, E4M3, act, seed=90 + sum(Sx) + hd, device="cuda")
     out, lse = gpu_extend(case)
     check(case, out, lse, "fp8 " + str(cfg), fp8=True)
     assert pkv.get_device_error() == 0
 
 
-def test_extend_fp8_shared_prefix_pages_widened_once():
-    # 64 requests over one shared 1,900-token prefix: the shared pages are
-    # claimed by one CTA each; results match the oracle on sampled rows
+def test_extend_fp8_shared_prefix_many_requests():
+    # 64 requests over one shared 1,900-token prefix in an fp8 pool; sampled rows
     case = W.extend_case([1900] * 64, [100] * 64, 32, 8, 128, 16, E4M3, BF16, seed=95,
                          device="cuda", shared_prefix=1900)
     out, lse = gpu_extend(case)
     rng = np.random.default_rng(5)
-    rows = [(int(r), int(h)) for r, h in zip(rng.integers(0, case.q.shape[0], 96), rng.integers(0, 32, 96))]
+    rows = [(int(r), int(h)) for r, h in zip(rng.integers(0, case.q.shape[0], 256), rng.integers(0, 32, 256))]
     check(case, out, lse, "fp8 shared prefix", rows=rows, fp8=True)
     assert pkv.get_device_error() == 0
 
 
-def test_extend_fp8_garbage_past_end_is_ignored():
-    case = W.extend_case([30], [20], 8, 2, 128, 16, E4M3, BF16, seed=96, device="cuda")
+@pytest.mark.parametrize("hd", [128, 64])
+def test_extend_fp8_garbage_past_end_is_ignored(hd):
+    case = W.extend_case([30], [20], 8, 2, hd, 16, E4M3, BF16, seed=96, device="cuda")
     total = 50
     blk = int(case.block_tables[0, (total - 1) // 16])
     case.k_cache[blk, :, total % 16:] = 0x7F  # e4m3 NaN codes
@@ -208,19 +229,56 @@ def test_extend_fp8_garbage_past_end_is_ignored():
     check(case, out, lse, "fp8 garbage tail", fp8=True)
 
 
-def test_extend_fp8_workspace_checks():
-    case = W.extend_case([16], [8], 8, 2, 128, 16, E4M3, BF16, seed=97, device="cuda")
-    need = pkv.extend_workspace_bytes(case.k_cache, 1, 8, 8, 24, k_scale=case.k_scale, v_scale=case.v_scale)
-    nb, hkv, bs, d = case.k_cache.shape
-    pool16 = nb * hkv * bs * d * 2
-    assert need == -(-nb * 4 // 256) * 256 + 2 * (-(-pool16 // 256) * 256)
-    with pytest.raises(pkv.PkvError):
-        gpu_extend(case, workspace=None)
-    with pytest.raises(pkv.PkvError):
-        gpu_extend(case, workspace=torch.empty(need - 256, dtype=torch.uint8, device="cuda"))
+def test_extend_needs_no_workspace():
+    # every cache dtype is read in place: the workspace size is 0 and none is passed
+    for dt, act in ((F16, F16), (BF16, BF16), (E4M3, BF16)):
+        case = W.extend_case([16], [8], 8, 2, 128, 16, dt, act, seed=97, device="cuda")
+        assert pkv.extend_workspace_bytes(case.k_cache, 1, 8, 8, 24, k_scale=case.k_scale,
+                                          v_scale=case.v_scale) == 0
+        out, lse = gpu_extend(case, workspace=None)
+        check(case, out, lse, f"no workspace {dt}", fp8=(dt == E4M3))
 
 
 def test_extend_unsupported_combinations_raise():
-    case = W.extend_case([4], [4], 4, 1, 64, 16, F16, F16, seed=73, device="cuda")
-    with pytest.raises(pkv.PkvError):
-        gpu_extend(case)  # head_dim 64 is not built for extend
+    case = W.extend_case([4], [4], 4, 1, 128, 16, BF16, BF16, seed=73, device="cuda")
+    with pytest.raises(pkv.PkvError):  # f16 queries over a bf16 cache
+        pkv.paged_extend_attn(case.k_cache, case.v_cache, case.q.half(), case.q.half(),
+                              case.q_indptr, case.prefix_lens, case.block_tables, case.sm_scale,
+                              4, 8)
+
+
+def test_extend_rows_beyond_the_call_are_reported_not_written():
+    # q_indptr[batch] larger than the call's rows: the request is not computed, the length
+    # error is recorded and nothing past `out` is written (guard rows keep their value)
+    case = W.extend_case([20, 30], [10, 12], 8, 2, 128, 16, BF16, BF16, seed=74, device="cuda")
+    rows = case.q.shape[0]
+    big = torch.full((rows + 16, 8, 128), 7.0, dtype=torch.bfloat16, device="cuda")
+    out = big[:rows]
+    bad_indptr = case.q_indptr.clone()
+    bad_indptr[2] = rows + 9
+    pkv.get_device_error()  # clear
+    pkv.paged_extend_attn(case.k_cache, case.v_cache, case.q, out, bad_indptr, case.prefix_lens,
+                          case.block_tables, case.sm_scale, 21, 60)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 3
+    assert bool(torch.all(big[rows:] == 7.0))
+    # request 0 is intact and still computed
+    ref, _, st = oracle.paged_extend(S(case.k_cache), S(case.v_cache), BF16, 1, 1, S(case.q), BF16,
+                                     case.q_indptr.cpu().numpy(), case.prefix_lens.cpu().numpy(),
+                                     case.block_tables.cpu().numpy(), 8, case.sm_scale,
+                                     rows=[(r, h) for r in range(10) for h in range(8)])
+    assert st == 0
+    got = to_f64(out[:10]).reshape(80, 128)
+    assert_attention_close(got, ref, BF16, what="request 0 beside a bad one")
+
+
+def test_extend_suffix_longer_than_hint_is_reported():
+    # max_suffix_len below the real suffix: the rows past the hint's tiles are not computed
+    # and the device error word says so
+    case = W.extend_case([40], [300], 8, 2, 128, 16, BF16, BF16, seed=75, device="cuda")
+    out = torch.zeros_like(case.q)
+    pkv.get_device_error()  # clear
+    pkv.paged_extend_attn(case.k_cache, case.v_cache, case.q, out, case.q_indptr, case.prefix_lens,
+                          case.block_tables, case.sm_scale, 100, 340)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 3

@@ -16,19 +16,21 @@ import torch
 import oracle
 import paged_kv_cache_285_gb300 as pkv
 from paged_kv_cache_285_gb300 import workloads as W
-from tests.pkv_testlib import BF16, F16, assert_attention_close, to_f64
+from tests.pkv_testlib import BF16, E4M3, F16, assert_attention_close, to_f64
 
 pytestmark = pytest.mark.gpu
 S = W.to_numpy_storage
 
 
-def grouped_case(groups, suffixes, hq, hkv, bs, dt, seed):
-    """groups: [(members, P)]; suffixes: one own-token count per request (>= 0)."""
+def grouped_case(groups, suffixes, hq, hkv, bs, dt, seed, hd=128, act=None):
+    """groups: [(members, P)]; suffixes: one own-token count per request (>= 0); dt is the
+    cache dtype, act the query / output dtype (dt unless the cache is fp8)."""
     lens = []
     it = iter(suffixes)
     for size, prefix in groups:
         lens += [prefix + next(it) for _ in range(size)]
-    case = W.decode_case(lens, hq, hkv, 128, bs, dt, dt, seed=seed, device="cuda")
+    case = W.decode_case(lens, hq, hkv, hd, bs, dt, dt if act is None else act, seed=seed,
+                         device="cuda")
     tables = case.block_tables.cpu()
     indptr, plens, start = [0], [], 0
     for size, prefix in groups:
@@ -55,21 +57,24 @@ def run_cascade(case, gi, gp, max_group, max_suffix, splits=0, append=False):
     b = case.q.shape[0]
     out = torch.full_like(case.q, float("nan"))
     lse = torch.full((b, case.num_q_heads), float("nan"), dtype=torch.float32, device="cuda")
+    max_prefix = int(gp.max()) if gp.numel() else 0
     nbytes = pkv.shared_prefix_decode_workspace_bytes(case.k_cache, b, case.num_q_heads,
-                                                      max_suffix, splits)
+                                                      max_prefix, max_suffix, splits)
     ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
     kw = dict(k_new=case.new_k, v_new=case.new_v) if append else {}
     pkv.paged_decode_attn_shared_prefix(case.k_cache, case.v_cache, case.q, out, case.block_tables,
                                         case.seq_lens, case.sm_scale, gi, gp, max_group,
-                                        max_suffix, num_splits=splits, lse_out=lse, workspace=ws,
-                                        **kw)
+                                        max_prefix, max_suffix, num_splits=splits, lse_out=lse,
+                                        workspace=ws,
+                                        k_scale=case.k_scale, v_scale=case.v_scale, **kw)
     torch.cuda.synchronize()
     return out, lse
 
 
 def oracle_ref(case, pools=None, pairs=None):
     k, v = (S(case.k_cache), S(case.v_cache)) if pools is None else pools
-    ref, ref_lse, st = oracle.paged_decode(k, v, case.cache_dtype, 1.0, 1.0, S(case.q),
+    ref, ref_lse, st = oracle.paged_decode(k, v, case.cache_dtype, case.k_scale, case.v_scale,
+                                           S(case.q),
                                            case.act_dtype, case.block_tables.cpu().numpy(),
                                            case.seq_lens.cpu().numpy(), case.num_q_heads,
                                            case.sm_scale, pairs=pairs)
@@ -79,11 +84,12 @@ def oracle_ref(case, pools=None, pairs=None):
 
 def check(case, out, lse, what, pools=None):
     ref, ref_lse = oracle_ref(case, pools)
-    assert_attention_close(to_f64(out), ref, case.act_dtype, what=what)
+    fp8 = case.cache_dtype == E4M3
+    assert_attention_close(to_f64(out), ref, case.act_dtype, fp8=fp8, what=what)
     gl = lse.cpu().double().numpy()
     fin = np.isfinite(ref_lse)
     assert np.all(np.isfinite(gl) == fin), what
-    assert np.max(np.abs(gl[fin] - ref_lse[fin]), initial=0) <= 1e-3, what
+    assert np.max(np.abs(gl[fin] - ref_lse[fin]), initial=0) <= (3e-2 if fp8 else 1e-3), what
 
 
 def rand_suffixes(n, lo, hi, seed):
@@ -101,6 +107,9 @@ CASES = [
     # pipeline variant of the decode)
     ([(12, 200)], (600, 1000), 16, 8, 16, BF16),
     ([(4, 96), (6, 32)], (520, 700), 8, 2, 32, F16),
+    # GQA groups above 8 (the decode takes them in chunks of 8 heads) and not a power of two
+    ([(10, 300), (3, 32)], (1, 200), 64, 4, 16, BF16),
+    ([(7, 128)], (1, 90), 12, 4, 32, F16),
 ]
 
 
@@ -113,6 +122,47 @@ def test_groups_match_oracle(cfg, splits):
                                         hkv, bs, dt, seed=nreq + hq + splits)
     out, lse = run_cascade(case, gi, gp, mg, ms, splits)
     check(case, out, lse, f"{cfg} splits={splits}")
+    assert pkv.get_device_error() == 0
+
+
+MORE_CASES = [
+    # (groups, suffix range, hq, hkv, bs, cache dtype, act dtype, head_dim)
+    ([(64, 500)], (1, 300), 32, 8, 16, BF16, BF16, 64),
+    ([(1, 0), (5, 100), (30, 1000), (3, 37)], (1, 200), 4, 1, 16, F16, F16, 64),
+    ([(12, 200)], (600, 1000), 16, 8, 32, BF16, BF16, 64),
+    ([(64, 500)], (1, 300), 32, 8, 16, E4M3, BF16, 128),
+    ([(1, 0), (5, 100), (30, 1000), (3, 37)], (1, 200), 8, 2, 16, E4M3, F16, 128),
+    ([(40, 256)], (1, 90), 64, 8, 32, E4M3, BF16, 64),
+    ([(12, 200)], (600, 1000), 16, 8, 16, E4M3, F16, 64),
+]
+
+
+@pytest.mark.parametrize("splits", [0, 3])
+@pytest.mark.parametrize("cfg", MORE_CASES,
+                         ids=lambda c: f"g{len(c[0])}-h{c[2]}x{c[3]}-bs{c[4]}-c{c[5]}a{c[6]}-hd{c[7]}")
+def test_groups_match_oracle_d64_and_fp8(cfg, splits):
+    groups, (lo, hi), hq, hkv, bs, dt, act, hd = cfg
+    nreq = sum(s for s, _ in groups)
+    case, gi, gp, mg, ms = grouped_case(groups, rand_suffixes(nreq, lo, hi, nreq + splits + hd), hq,
+                                        hkv, bs, dt, seed=nreq + hq + splits + hd, hd=hd, act=act)
+    out, lse = run_cascade(case, gi, gp, mg, ms, splits)
+    check(case, out, lse, f"{cfg} splits={splits}")
+    assert pkv.get_device_error() == 0
+
+
+@pytest.mark.parametrize("dt,act,hd", [(E4M3, BF16, 128), (E4M3, F16, 64), (BF16, BF16, 64)])
+def test_fused_append_d64_and_fp8(dt, act, hd):
+    groups = [(20, 320), (6, 40)]
+    suf = rand_suffixes(26, 1, 120, 6)
+    case, gi, gp, mg, ms = grouped_case(groups, suf, 32, 8, 16, dt, seed=22, hd=hd, act=act)
+    k0, v0 = S(case.k_cache), S(case.v_cache)
+    out, lse = run_cascade(case, gi, gp, mg, ms, append=True)
+    kr, vr, st = oracle.kv_append(k0, v0, case.cache_dtype, case.k_scale, case.v_scale,
+                                  S(case.new_k), S(case.new_v), case.act_dtype,
+                                  case.slot_last.cpu().numpy())
+    assert st == 0
+    assert np.array_equal(kr, S(case.k_cache)) and np.array_equal(vr, S(case.v_cache))
+    check(case, out, lse, "fused append", pools=(kr, vr))
     assert pkv.get_device_error() == 0
 
 
@@ -185,25 +235,26 @@ def test_prefix_longer_than_a_member_is_reported():
 
 
 def test_unsupported_and_bad_arguments_are_refused_on_the_host():
-    c64 = W.decode_case([40, 50], 4, 1, 64, 16, F16, F16, seed=1, device="cuda")
     gi = torch.tensor([0, 2], dtype=torch.int32, device="cuda")
     gp = torch.tensor([32], dtype=torch.int32, device="cuda")
     ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
-    with pytest.raises(pkv.PkvError) as e:  # head_dim 64 has no prefix pass
-        pkv.paged_decode_attn_shared_prefix(c64.k_cache, c64.v_cache, c64.q, torch.empty_like(c64.q),
-                                            c64.block_tables, c64.seq_lens, c64.sm_scale, gi, gp,
-                                            2, 20, workspace=ws)
+    cbig = W.decode_case([40, 50], 2 * 129, 2, 64, 16, F16, F16, seed=1, device="cuda")
+    with pytest.raises(pkv.PkvError) as e:  # a group of 129 heads does not fit one row tile
+        pkv.paged_decode_attn_shared_prefix(cbig.k_cache, cbig.v_cache, cbig.q,
+                                            torch.empty_like(cbig.q), cbig.block_tables,
+                                            cbig.seq_lens, cbig.sm_scale, gi, gp, 2, 32, 20,
+                                            workspace=ws)
     assert e.value.status == 2
     c = W.decode_case([40, 50], 8, 2, 128, 16, BF16, BF16, seed=2, device="cuda")
     small = torch.empty(64, dtype=torch.uint8, device="cuda")
     with pytest.raises(pkv.PkvError) as e:
         pkv.paged_decode_attn_shared_prefix(c.k_cache, c.v_cache, c.q, torch.empty_like(c.q),
-                                            c.block_tables, c.seq_lens, c.sm_scale, gi, gp, 2, 20,
-                                            workspace=small)
+                                            c.block_tables, c.seq_lens, c.sm_scale, gi, gp, 2, 32,
+                                            20, workspace=small)
     assert e.value.status == 3
     with pytest.raises(pkv.PkvError) as e:  # a negative softmax scale
         pkv.paged_decode_attn_shared_prefix(c.k_cache, c.v_cache, c.q, torch.empty_like(c.q),
-                                            c.block_tables, c.seq_lens, -0.1, gi, gp, 2, 20,
+                                            c.block_tables, c.seq_lens, -0.1, gi, gp, 2, 32, 20,
                                             workspace=ws)
     assert e.value.status == 1
 

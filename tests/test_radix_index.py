@@ -229,14 +229,18 @@ def test_random_workload_with_eviction_keeps_the_pool_consistent():
 
 
 def test_native_trace_driver():
-    # the C++ replay that bench.py reports: builds with the library, runs the whole trace
-    # through the C ABI without an error, refuses no request, and reuses the shared prompts
+    # the C++ replay that bench.py reports (bench_native/radix_trace.cpp, built by the bench
+    # against the library): runs the whole trace through the C ABI without an error, refuses
+    # no request, and reuses the shared prompts
     import json
     import subprocess
 
+    import bench
     from paged_kv_cache_285_gb300 import build as pkv_build
     pkv_build.build()
-    r = subprocess.run([pkv_build.TRACE_BIN, "3000"], capture_output=True, text=True, timeout=120)
+    exe = bench._build_radix_trace()
+    assert exe is not None
+    r = subprocess.run([exe, "3000"], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stderr
     d = json.loads(r.stdout)
     assert d["requests"] == 3000 and d["refused"] == 0

@@ -79,7 +79,7 @@ def test_noalloc_rejects_plans_beyond_the_scratch():
     fn = _lib()
     case = W.decode_case([40, 50], 8, 2, 128, 16, BF16, BF16, seed=91, device="cuda")
     out = torch.empty_like(case.q)
-    # 2 requests x 8 heads x 8,000 splits x 129 floats = 33 MB of partials > 16 MiB
+    # 2 requests x 8 heads x 8,000 splits x 129 floats x 4 bytes = 66 MB of partials > 16 MiB
     big = 128_000
     assert pkv.decode_workspace_bytes(case.k_cache, 2, 8, big, 8000) > SCRATCH_BYTES
     assert _noalloc(fn, case, case.q, out, None, big, 8000) == 3      # PKV_ERR_WORKSPACE
