@@ -358,6 +358,8 @@ def run_decode_bench(args, world, rank, local):
     # step (q, the new token's K/V, seq_lens, block tables) go host->device
     # from pinned memory and the output comes back device->host
     res["e2e"] = e2e_decode(case, pkv, max_len, ws, out, stream, K, world)
+    if args.no_side:
+        return res
     if args.extend and rank == 0 and world == 1:
         res["extend"] = run_extend_bench(args, dev, bf16, bf16_sus, peak_src)
     if rank == 0 and world == 1:
@@ -973,6 +975,21 @@ def run_reference(args, world, rank):
             "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_only(args, local):
+    import paged_kv_cache_285_gb300 as pkv
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pkv.load()
+    hbm, bf16, bf16_sus, peak_src = peaks()
+    fns = {"extend": lambda: run_extend_bench(args, dev, bf16, bf16_sus, peak_src),
+           "shared_prefix_decode": lambda: run_shared_prefix_bench(dev, hbm, peak_src),
+           "append_fill": lambda: run_append_fill_bench(dev, hbm, peak_src),
+           "more_decode_configs": lambda: run_more_decode_configs_bench(dev, hbm, peak_src),
+           "chain_hash": lambda: run_chain_hash_bench(dev, hbm, peak_src),
+           "prefix_index": run_prefix_index_bench}
+    return {"only": args.only, args.only: fns[args.only]()}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -983,11 +1000,20 @@ def main(argv=None):
                     choices=["llama3_8b_layer", "fp8_70b_layer", "shared_prefix_decode", "tiny"])
     ap.add_argument("--no-extend", dest="extend", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-side", action="store_true",
+                    help="the decode step only: no extend, no side benchmarks (profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--only", default=None,
+                    choices=["extend", "shared_prefix_decode", "append_fill", "more_decode_configs",
+                             "chain_hash", "prefix_index"],
+                    help="run one side benchmark alone (for profiling on a small device footprint); "
+                         "prints that object only, not the benchmark line")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)
     world, rank, local = dist_setup(args.gpus)
-    if args.impl == "reference":
+    if args.only is not None:
+        res = run_only(args, local)
+    elif args.impl == "reference":
         res = run_reference(args, world, rank)
     else:
         res = run_decode_bench(args, world, rank, local)

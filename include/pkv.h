@@ -258,13 +258,13 @@ pkv_status pkv_paged_decode_attn_noalloc(const pkv_cache_desc* desc, const void*
  * desc:          an fp8 cache's k_scale / v_scale are applied in both parts
  *                (scores and outputs), as in pkv_paged_decode_attn.
  * max_group_size: host bound of the members per group (sizes the prefix pass).
- * max_prefix_len: host bound of P_g.  The prefix pass cuts each group's W_g
- *                shared keys into chunks of whole 128-key tiles, enough of
- *                them (at most 8, at least 256 keys each except the last)
- *                that even one group gives about one work item per SM; every
- *                chunk's partial is one more term of the LSE merge.  Keys
- *                beyond the chunks the hint allows are not attended and set
- *                PKV_DEVERR_BAD_LENGTH.
+ * max_prefix_len: host bound of P_g.  When the groups give few work items,
+ *                the prefix pass cuts each group's W_g shared keys into chunks
+ *                of whole 128-key tiles (at most 8, at least 256 keys each
+ *                except the last), so that the pass fills about a quarter of
+ *                the SMs beside the own-token decode; every chunk's partial is
+ *                one more term of the LSE merge.  Keys beyond the chunks the
+ *                hint allows are not attended and set PKV_DEVERR_BAD_LENGTH.
  * max_suffix_len: host bound of seq_lens[b] - P_g (sizes the split plan).
  * num_splits:    as pkv_paged_decode_attn, for the members' own tokens.
  * workspace:     pkv_shared_prefix_decode_workspace_bytes() bytes, 256-byte

@@ -406,8 +406,9 @@ pkv_status pkv_paged_decode_attn_shared_prefix(
   const int slots = pl.splits + prefix_slots;
   const float scale_log2 = score_scale_log2(desc, sm_scale);
 
-  // 1. the shared prefixes, once per group, on the tensor cores -> slot 0
-  //    (on the side stream, beside step 2)
+  // 1. the shared prefixes, once per group, on the tensor cores -> one
+  //    partial per key chunk in the first prefix_slots slots (on the side
+  //    stream, beside step 2)
   ExtendParams pe;
   pe.q_indptr = group_indptr;
   pe.prefix_lens = group_prefix_lens;
@@ -428,11 +429,15 @@ pkv_status pkv_paged_decode_attn_shared_prefix(
   pe.out_scale = output_scale(desc);
   if (!plan_extend(pe, num_groups, desc->num_kv_heads, group, max_group_size, ds->sm_count))
     return PKV_ERR_UNSUPPORTED;
-  // The prefix's keys in chunks of whole key tiles, so that the pass has about
-  // one work item per SM even for a single group (each chunk's partial is one
-  // more term of the LSE merge); at most prefix_slots chunks.
+  // The prefix's keys in chunks of whole key tiles when the groups give few
+  // work items: the pass runs beside the own-token decode and should take
+  // about a quarter of the SMs (measured on the shared-prompt layer: 32 items
+  // of 8 key tiles beside the decode, 55 us per call; 128 items of 2 tiles run
+  // before it, 75 us).  Each chunk's partial is one more term of the LSE
+  // merge; at most prefix_slots chunks.
   const int key_tiles = std::max(1, ceil_div(max_prefix_len, 128));
-  const int want = std::max(1, ceil_div(ds->sm_count > 0 ? ds->sm_count : 1, pe.num_items));
+  const int quarter = std::max(1, (ds->sm_count > 0 ? ds->sm_count : 4) / 4);
+  const int want = std::max(1, quarter / pe.num_items);
   const int chunk_tiles = ceil_div(key_tiles, std::min(std::min(want, prefix_slots), key_tiles));
   pe.kchunks = ceil_div(key_tiles, chunk_tiles);
   pe.kchunk_keys = chunk_tiles * 128;
@@ -466,8 +471,9 @@ pkv_status pkv_paged_decode_attn_shared_prefix(
     return PKV_ERR_CUDA;
   }
 
-  // 2. each request's own tokens (current token appended first) -> slots 1..,
-  //    then, once the prefix pass has joined, the merge of all slots
+  // 2. each request's own tokens (current token appended first) -> the slots
+  //    after the prefix's, then, once the prefix pass has joined, the merge
+  //    of all of them
   DecodeParams p;
   p.block_tables = block_tables;
   p.seq_lens = seq_lens;
@@ -495,6 +501,8 @@ pkv_status pkv_paged_decode_attn_shared_prefix(
   ap.v_cache = v_cache;
   ap.k_scale = desc->k_scale;
   ap.v_scale = desc->v_scale;
+  ap.k_rcp = (float)(1.0 / (double)desc->k_scale);
+  ap.v_rcp = (float)(1.0 / (double)desc->v_scale);
   ap.group_indptr = group_indptr;
   ap.group_prefix_lens = group_prefix_lens;
   ap.num_groups = num_groups;
@@ -571,6 +579,8 @@ static pkv_status decode_common(const pkv_cache_desc* desc, const void* k_cache,
   ap.v_cache = const_cast<void*>(v_cache);
   ap.k_scale = desc->k_scale;
   ap.v_scale = desc->v_scale;
+  ap.k_rcp = (float)(1.0 / (double)desc->k_scale);
+  ap.v_rcp = (float)(1.0 / (double)desc->v_scale);
   e = launch_decode(kmap, vmap, p, ap, desc->head_dim, (int)desc->cache_dtype, (int)act_dtype,
                     stream);
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;

@@ -124,8 +124,8 @@ __device__ __forceinline__ int group_prefix_len(const DecodeExtraParams& ap, int
   return __ldg(ap.group_prefix_lens + lo);
 }
 
-// CASC: a cascade launch (tokens from the group's shared prefix on, partials
-// in workspace slots 1.., always merged).
+// CASC: a cascade launch (tokens from the group's shared prefix on; partials
+// in the workspace slots after the prefix's chunks, always merged).
 template <int HD, int CT, int AT, int NW, int NS, bool CASC>
 __global__ void __launch_bounds__(NW * 32)
 decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
@@ -189,7 +189,7 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
     // rows of kv head g go to their slot before any tile of this CTA is
     // loaded (TMA reads the slot after the proxy fence and the barrier
     // below).  Same bytes as the separate append: a 16-bit copy, or
-    // e4m3(fp32(x) / scale) with a correctly rounded division and a
+    // e4m3(fp32(x) / scale) from the correctly rounded quotient and a
     // saturating round-to-nearest-even convert.  With a group of more than 8
     // heads every head chunk's CTA writes the row (the same bytes), before its
     // own read of it.
@@ -210,6 +210,7 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
         *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(cache) + dst) = x;
       } else {
         const float sc = isv ? ap.v_scale : ap.k_scale;
+        const float rc = isv ? ap.v_rcp : ap.k_rcp;
         const uint32_t w[4] = {x.x, x.y, x.z, x.w};
         uint32_t o[2];
 #pragma unroll
@@ -218,8 +219,8 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
 #pragma unroll
           for (int q2 = 0; q2 < 2; ++q2) {
             const uint32_t ww = w[2 * h2 + q2];
-            const float a0 = __fdiv_rn(to_f32_bits<AT>(ww & 0xFFFFu), sc);
-            const float a1 = __fdiv_rn(to_f32_bits<AT>(ww >> 16), sc);
+            const float a0 = quot_for_e4m3(to_f32_bits<AT>(ww & 0xFFFFu), sc, rc);
+            const float a1 = quot_for_e4m3(to_f32_bits<AT>(ww >> 16), sc, rc);
             ob |= f32x2_to_e4m3x2(a0, a1) << (16 * q2);
           }
           o[h2] = ob;
@@ -536,7 +537,7 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
 // Merge the splits of one (request, head) per warp:
 //   lse* = log2 sum_s 2^lse_s,  out = sum_s 2^(lse_s - lse*) o_s.
 // Cascade: the shared prefix's chunks (slots 0 .. npc-1, when the group has a
-// prefix) and the request's own tokens (slots prefix_slots ..).
+// prefix) and the request's own splits (slots prefix_slots ..).
 template <int HD, int AT, bool CASC>
 __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, const DecodeExtraParams ap) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

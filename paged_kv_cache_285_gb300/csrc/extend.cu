@@ -41,10 +41,11 @@
 //                 when the max grows by more than 2^8), f16 P, and at the end
 //                 of an item O / l and the LSE.
 //   warps 12-15   converters: bf16 V tiles become f16 in place; fp8 (e4m3) K
-//                 tiles are widened to the activation dtype and fp8 V tiles
-//                 to f16 (exactly: an e4m3 value fits both), one key row per
-//                 thread; V keys past the sequence end are zeroed (they may
-//                 hold NaN, and 0 * NaN is NaN).
+//                 and V tiles are widened to f16 (exactly), one key row per
+//                 thread, and with bf16 queries each Q tile is converted to
+//                 f16 once per item, so S = Q K^T runs in f16; V keys past the
+//                 sequence end are zeroed (they may hold NaN, and 0 * NaN is
+//                 NaN).
 // P is f16 (11 significant bits) because bf16 P alone would put the relative
 // L2 error of the output near 1.5e-3; V is therefore f16 (bf16 values beyond
 // +-65504 are outside this path's range).
@@ -54,7 +55,9 @@
 // codes: the TMA copies one byte per element, the converter warps widen each
 // tile in shared memory, and the per-tensor scales are folded into the softmax
 // scale (k_scale) and the output scale (v_scale), so no 16-bit copy of the
-// cache exists anywhere.
+// cache exists anywhere.  bf16 queries over an fp8 cache are taken as f16
+// (exact within the f16 range; query values beyond +-65504 are outside this
+// path's range, like bf16 V values).
 //
 // Prefix pass (PP = true), for decode over a prefix shared by a group of
 // requests: each group is one pseudo-request whose rows are the group
@@ -79,9 +82,14 @@ constexpr int NCONV = 128;    // converter threads (warps 12-15), one per key ro
 constexpr int NQB = 3;        // Q tile buffers
 constexpr int CHUNK = 16384;  // one 64-element column block of a 16-bit tile: [128 rows][128 B]
 
-template <int HD, int CT>
+template <int HD, int CT, int AT>
 struct ExtCfg {
   static constexpr bool FP8 = (CT == DT_E4M3);
+  // S = Q K^T runs in f16 for fp8 caches: K codes widen to f16 with one
+  // convert per pair, and bf16 queries (QCVT) are converted to f16 once per
+  // item instead of K to bf16 at every key tile
+  static constexpr bool QCVT = FP8 && (AT == DT_BF16);
+  static constexpr bool QK_BF16 = !FP8 && (AT == DT_BF16);
   static constexpr int NCH = HD / 64;           // 64-element column blocks per 16-bit row
   static constexpr int NST = HD == 64 ? 3 : 2;  // K and V ring depth
   static constexpr int T16 = BM * HD * 2;       // a 16-bit tile (Q, K or V): 16 or 32 KB
@@ -107,7 +115,8 @@ struct ExtCfg {
     B_SDONE = B_VFREE + NST,  // [2] S_x(n) = Q_x K(n)^T done
     B_PFULL = B_SDONE + 2,    // [2] P_x(n) written
     B_QFULL = B_PFULL + 2,    // [tile x][item parity] Q tile x of the item loaded
-    B_QFREE = B_QFULL + 4,    // [item parity] the item's last S_B = Q_B K^T done
+    B_QCONV = B_QFULL + 4,    // [tile x][item parity] Q tile x converted to f16 (fp8 cache, bf16 q)
+    B_QFREE = B_QCONV + 4,    // [item parity] the item's last S_B = Q_B K^T done
     B_ODONE = B_QFREE + 2,    // the item's last O_B += P_B V done (O_A's before it)
     B_OFREE = B_ODONE + 1,    // [2] O_x of the item read out of TMEM
     NBAR = B_OFREE + 2
@@ -206,27 +215,29 @@ __device__ __forceinline__ void widen16(const uint4& a, uint4& lo, uint4& hi) {
 //        other thread touches the row.
 //  d64:  src is a separate staging tile: 64 B rows at t * 64 in the 64-byte
 //        swizzle (unit u at u ^ ((t >> 1) & 3)).
+// A swizzled offset row + 16 (u ^ c) is (row | 16 c) ^ 16 u: one xor with a
+// constant per unit.
 template <int HD, int OUT>
 __device__ __forceinline__ void widen_row(const uint8_t* src, uint8_t* dst, int t, bool zero) {
+  const uint32_t sbase = (HD == 128) ? ((uint32_t)t * 128u) | (((uint32_t)t & 7u) << 4)
+                                     : ((uint32_t)t * 64u) | ((((uint32_t)t >> 1) & 3u) << 4);
+  const uint32_t dbase = ((uint32_t)t * 128u) | (((uint32_t)t & 7u) << 4);
 #pragma unroll
   for (int pr = HD / 32 - 1; pr >= 0; --pr) {  // fp8 unit pairs (2pr, 2pr+1), highest first
     uint4 a[2];
     if (!zero) {
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int u = 2 * pr + j;
-        const int off = (HD == 128) ? t * 128 + 16 * (u ^ (t & 7)) : t * 64 + 16 * (u ^ ((t >> 1) & 3));
-        a[j] = *reinterpret_cast<const uint4*>(src + off);
-      }
+      for (int j = 0; j < 2; ++j)
+        a[j] = *reinterpret_cast<const uint4*>(src + (sbase ^ (uint32_t)((2 * pr + j) << 4)));
     }
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       const int u = 2 * pr + j;  // dims 16u .. 16u+15: block u / 4, 16-bit units 2(u%4), 2(u%4)+1
-      uint8_t* row = dst + (u >> 2) * CHUNK + t * 128;
+      uint8_t* blk = dst + (u >> 2) * CHUNK;
       uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
       if (!zero) widen16<OUT>(a[j], lo, hi);
-      *reinterpret_cast<uint4*>(row + 16 * ((2 * (u & 3)) ^ (t & 7))) = lo;
-      *reinterpret_cast<uint4*>(row + 16 * ((2 * (u & 3) + 1) ^ (t & 7))) = hi;
+      *reinterpret_cast<uint4*>(blk + (dbase ^ (uint32_t)((2 * (u & 3)) << 4))) = lo;
+      *reinterpret_cast<uint4*>(blk + (dbase ^ (uint32_t)((2 * (u & 3) + 1) << 4))) = hi;
     }
   }
 }
@@ -321,7 +332,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
               const __grid_constant__ CUtensorMap qmap, const ExtendParams p,
               const ExtendPartialParams pp) {
-  using C = ExtCfg<HD, CT>;
+  using C = ExtCfg<HD, CT, AT>;
   constexpr int NST = C::NST;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -353,6 +364,8 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       mbar_init(bar(C::B_PFULL + x), 4);
       mbar_init(bar(C::B_QFULL + 2 * x), 1);
       mbar_init(bar(C::B_QFULL + 2 * x + 1), 1);
+      mbar_init(bar(C::B_QCONV + 2 * x), NCONV / 32);
+      mbar_init(bar(C::B_QCONV + 2 * x + 1), NCONV / 32);
       mbar_init(bar(C::B_QFREE + x), 1);
       mbar_init(bar(C::B_OFREE + x), 4);
     }
@@ -368,9 +381,12 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
 
   // registers: launched with 128 per thread (512 x 128); the two softmax
   // warpgroups (warps 4-7 and 8-11) raise their budget to 184, the producer /
-  // MMA warpgroup (0-3) lowers its to 96 and the converters (12-15) to 48:
-  // 2 x 184 + 96 + 48 = 4 x 128.
-  static_assert(2 * 184 + 96 + 48 == 4 * 128, "register split must equal the launch budget");
+  // MMA warpgroup (0-3) lowers its to 96 and the converters (12-15) to 48
+  // (fp8 caches, whose converters widen K and V: 88 and 56); the shares add up
+  // to the launch budget, 4 x 128.
+  constexpr int kRegsProd = C::FP8 ? 88 : 96, kRegsConv = C::FP8 ? 56 : 48;
+  static_assert(2 * 184 + kRegsProd + kRegsConv == 4 * 128,
+                "register split must equal the launch budget");
   if (warp >= 4 && warp < 12) {
     regs_inc<184>();
     // ------------------------------------------------------------ softmax of tile x
@@ -541,7 +557,7 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       ++js;
     }
   } else if (warp < 4) {
-    regs_dec<96>();
+    regs_dec<kRegsProd>();
     if (warp == 0 || warp == 2) {
       // ------------------------------------------------------------ producers
       // warp 0: Q tiles and the K ring; warp 2: the V ring.  Block ids: lane l
@@ -637,11 +653,13 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       // elected lane issues the MMAs and commits.  Order per key tile n:
       // O_A += P_A(n-1) V(n-1), S_A(n), O_B += P_B(n-1) V(n-1), S_B(n): each
       // S_x(n) overwrites P_x(n-1) after the PV that reads it.
-      constexpr uint32_t qk_fmt = (AT == DT_BF16) ? 1u : 0u;
+      constexpr uint32_t qk_fmt = C::QK_BF16 ? 1u : 0u;
       constexpr uint32_t idesc_qk = umma_idesc_f16(qk_fmt, qk_fmt, BM, BN);
       constexpr uint32_t idesc_pv = umma_idesc_f16(0u, 0u, BM, HD) | (1u << 16);
-      // K is ready for the MMA once loaded, or, for fp8 codes, once widened
+      // K is ready for the MMA once loaded, or, for fp8 codes, once widened;
+      // Q once loaded, or once converted to f16
       const int kready0 = C::FP8 ? C::B_KCONV : C::B_KFULL;
+      const int qready0 = C::QCVT ? C::B_QCONV : C::B_QFULL;
       // O_x += P_x(u) V(u); `first`: the first key tile of item ju, which
       // overwrites O_x once the previous item's O_x has been read out
       auto issue_pv = [&](int xx, int u, bool first, int ju) -> bool {
@@ -689,7 +707,7 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
         for (int kt = 0; kt < it.T; ++kt, ++n) {
           if (have_prev && !issue_pv(0, prev_n, prev_first, prev_j)) { ok = false; break; }
           if (!mbar_wait(bar(kready0 + n % NST), (n / NST) & 1)) { ok = false; break; }
-          if (kt == 0 && !mbar_wait(bar(C::B_QFULL + (j & 1)), (j >> 1) & 1)) { ok = false; break; }
+          if (kt == 0 && !mbar_wait(bar(qready0 + (j & 1)), (j >> 1) & 1)) { ok = false; break; }
           tc_fence_after();
           issue_qk(0, n, qa);
           if (have_prev) {
@@ -697,7 +715,7 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
             commit(C::B_VFREE + prev_n % NST);
             if (prev_last) commit(C::B_ODONE);
           }
-          if (kt == 0 && !mbar_wait(bar(C::B_QFULL + 2 + (j & 1)), (j >> 1) & 1)) { ok = false; break; }
+          if (kt == 0 && !mbar_wait(bar(qready0 + 2 + (j & 1)), (j >> 1) & 1)) { ok = false; break; }
           tc_fence_after();
           issue_qk(1, n, qb);
           commit(C::B_KFREE + n % NST);
@@ -719,7 +737,7 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       }
     }
   } else {
-    regs_dec<48>();
+    regs_dec<kRegsConv>();
     {
       // ------------------------------------------------------------ converters (12-15)
       // Per key tile: fp8 K rows are widened to the activation dtype (then the
@@ -727,7 +745,16 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       // at or past the sequence end become zeros (then the PV MMA may read the
       // tile).  fp8 tiles: thread t owns key row t.
       const int t = threadIdx.x - 384;  // 0..127
-      int n = 0;
+      int n = 0, j = 0;
+      // bf16 Q tile x of item j -> f16 in place (fp8 caches: S runs in f16)
+      auto conv_q = [&](int xq) -> bool {
+        if (!mbar_wait(bar(C::B_QFULL + 2 * xq + (j & 1)), (j >> 1) & 1)) return false;
+        conv_tile16<HD, true, false>(smem + C::OFF_Q + ((2 * j + xq) % NQB) * C::T16, t, 0, 0);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::B_QCONV + 2 * xq + (j & 1)));
+        return true;
+      };
       ItemRaw nxt_raw = load_raw(p, item0);
       for (int item = item0; ok && item < p.num_items; item += stride) {
         const ItemRaw raw = nxt_raw;
@@ -737,12 +764,20 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
         for (int kt = 0; kt < it.T; ++kt, ++n) {
           const int s = n % NST;
           const uint32_t ph = (uint32_t)((n / NST) & 1);
+          // order of the first key tile: Q_A, K, Q_B, V (the MMA's order of use;
+          // the producer loads Q_B after the first K tile)
+          if constexpr (C::QCVT) {
+            if (kt == 0 && !conv_q(0)) { ok = false; break; }
+          }
           if constexpr (C::FP8) {
             if (!mbar_wait(bar(C::B_KFULL + s), ph)) { ok = false; break; }
-            widen_row<HD, AT>(smem + C::src8(false, s), smem + C::OFF_K + s * C::T16, t, false);
+            widen_row<HD, DT_F16>(smem + C::src8(false, s), smem + C::OFF_K + s * C::T16, t, false);
             fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::B_KCONV + s));
+          }
+          if constexpr (C::QCVT) {
+            if (kt == 0 && !conv_q(1)) { ok = false; break; }
           }
           if (!mbar_wait(bar(C::B_VFULL + s), ph)) { ok = false; break; }
           const int kbase = it.k_lo + kt * BN;
@@ -761,6 +796,7 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(C::B_VCONV + s));
         }
+        ++j;
       }
     }
   }
@@ -790,7 +826,7 @@ cudaError_t launch_extend_t(const CUtensorMap& kmap, const CUtensorMap& vmap, co
                             const ExtendParams& p, const ExtendPartialParams& pp,
                             cudaStream_t stream) {
   auto k = extend_kernel<HD, CT, AT, PP>;
-  constexpr int smem = ExtCfg<HD, CT>::SMEM;
+  constexpr int smem = ExtCfg<HD, CT, AT>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   k<<<dim3(p.num_ctas), NTHREADS, smem, stream>>>(kmap, vmap, qmap, p, pp);

@@ -50,8 +50,10 @@ struct DecodeExtraParams {
   const void* v_new;
   void* k_cache;
   void* v_cache;
-  float k_scale;      // fp8 store scales
+  float k_scale;      // fp8 store scales and their fp32 reciprocals
   float v_scale;
+  float k_rcp;
+  float v_rcp;
   const int32_t* group_indptr;       // [num_groups + 1]
   const int32_t* group_prefix_lens;  // [num_groups]
   int num_groups;
@@ -106,6 +108,8 @@ struct AppendParams {
   int num_blocks;
   float k_scale;
   float v_scale;
+  float k_rcp;         // RN(1 / k_scale), RN(1 / v_scale)
+  float v_rcp;
   // slots == null: token t is suffix row t of an extend call (request b with
   // q_indptr[b] <= t < q_indptr[b+1]) at position prefix_lens[b] + t - q_indptr[b]
   const int32_t* q_indptr;
@@ -165,8 +169,9 @@ cudaError_t launch_decode(const CUtensorMap& kmap, const CUtensorMap& vmap,
                           const DecodeParams& p, const DecodeExtraParams& ap, int head_dim,
                           int cache_dt, int act_dt, cudaStream_t stream);
 // Decode over each request's tokens after its group's shared prefix, partials
-// in slots 1.. of the workspace, then (after `merge_after`, the prefix pass's
-// completion, when not null) the merge with slot 0.
+// in the workspace slots after the prefix's, then (after `merge_after`, the
+// prefix pass's completion, when not null) the merge with the prefix's
+// partials (slots 0 .. prefix_slots-1).
 cudaError_t launch_decode_cascade(const CUtensorMap& kmap, const CUtensorMap& vmap,
                                   const DecodeParams& p, const DecodeExtraParams& ap, int head_dim,
                                   int cache_dt, int act_dt, cudaStream_t stream,

@@ -5,11 +5,12 @@
 // the token's slot (physical block, offset) -- "PagedAttention과
 // RadixAttention으로 LLM KV 캐시 최적화", section 02.
 //
-// One thread moves 16 bytes of one (token, kv head) row for K and for V, so a
-// warp covers two 256-byte rows with fully coalesced 16-byte loads and stores.
-// 16-bit caches copy the bits; fp8 caches store e4m3(fp32(x) / scale) with a
-// correctly rounded fp32 division and a saturating round-to-nearest-even
-// convert (cvt.rn.satfinite).  Slots whose block lies outside the pool are
+// One thread moves 8 elements of one (token, kv head) row for K and for V (16
+// for the fp8 store), with coalesced 16-byte loads and stores.
+// 16-bit caches copy the bits; fp8 caches store e4m3(fp32(x) / scale) -- the
+// correctly rounded fp32 quotient (a multiply by the reciprocal, with the
+// division only where the two could round differently) and a saturating
+// round-to-nearest-even convert (cvt.rn.satfinite).  Slots whose block lies outside the pool are
 // skipped and reported in the error word; negative slots are skipped silently.
 #include "internal.h"
 #include "ptx.cuh"
@@ -24,9 +25,16 @@ __device__ __forceinline__ float act_to_f32(uint16_t bits) {
   else return __half2float(__ushort_as_half(bits));
 }
 
+// Elements of a row one thread moves: 8 (one 16-byte input vector) for a
+// 16-bit copy; 16 for the fp8 store (two input vectors per tensor in flight
+// and one 16-byte store of codes).
+template <int CT>
+__host__ __device__ constexpr int append_ept() { return CT == DT_E4M3 ? 16 : 8; }
+
 template <int CT, int AT, int HD>
 __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
-  constexpr int VPR = HD / 8;  // 16-byte input vectors per row (a power of two)
+  constexpr int EPT = append_ept<CT>();
+  constexpr int VPR = HD / EPT;  // threads per row (a power of two)
   const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t total = p.num_tokens * p.num_kv_heads * VPR;
   if (idx >= total) return;
@@ -68,44 +76,49 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
     if (v == 0 && p.err) atomicCAS(p.err, 0, 2);
     return;
   }
-  const int64_t src = idx * 8;  // row * HD + v * 8
-  const int64_t dst = (((blk * p.num_kv_heads + g) << p.bs_shift) + off) * HD + v * 8;
-  const uint4 kx = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.k_new) + src));
-  const uint4 vx = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.v_new) + src));
+  const int64_t src = idx * EPT;  // row * HD + v * EPT
+  const int64_t dst = (((blk * p.num_kv_heads + g) << p.bs_shift) + off) * HD + v * EPT;
+  const uint4* ksrc = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.k_new) + src);
+  const uint4* vsrc = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.v_new) + src);
   if constexpr (CT != DT_E4M3) {
+    const uint4 kx = __ldg(ksrc), vx = __ldg(vsrc);
     *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.k_cache) + dst) = kx;
     *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.v_cache) + dst) = vx;
   } else {
-    const uint32_t kw[4] = {kx.x, kx.y, kx.z, kx.w};
-    const uint32_t vw[4] = {vx.x, vx.y, vx.z, vx.w};
-    uint32_t ko[2], vo[2];
+    const uint4 kx0 = __ldg(ksrc), kx1 = __ldg(ksrc + 1);
+    const uint4 vx0 = __ldg(vsrc), vx1 = __ldg(vsrc + 1);
+    const uint32_t kw[8] = {kx0.x, kx0.y, kx0.z, kx0.w, kx1.x, kx1.y, kx1.z, kx1.w};
+    const uint32_t vw[8] = {vx0.x, vx0.y, vx0.z, vx0.w, vx1.x, vx1.y, vx1.z, vx1.w};
+    uint32_t ko[4], vo[4];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < 4; ++h) {
       uint32_t kb = 0, vb = 0;
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         const uint32_t wk = kw[2 * h + q], wv = vw[2 * h + q];
-        const float k0 = __fdiv_rn(act_to_f32<AT>((uint16_t)(wk & 0xFFFFu)), p.k_scale);
-        const float k1 = __fdiv_rn(act_to_f32<AT>((uint16_t)(wk >> 16)), p.k_scale);
-        const float v0 = __fdiv_rn(act_to_f32<AT>((uint16_t)(wv & 0xFFFFu)), p.v_scale);
-        const float v1 = __fdiv_rn(act_to_f32<AT>((uint16_t)(wv >> 16)), p.v_scale);
+        const float k0 = quot_for_e4m3(act_to_f32<AT>((uint16_t)(wk & 0xFFFFu)), p.k_scale, p.k_rcp);
+        const float k1 = quot_for_e4m3(act_to_f32<AT>((uint16_t)(wk >> 16)), p.k_scale, p.k_rcp);
+        const float v0 = quot_for_e4m3(act_to_f32<AT>((uint16_t)(wv & 0xFFFFu)), p.v_scale, p.v_rcp);
+        const float v1 = quot_for_e4m3(act_to_f32<AT>((uint16_t)(wv >> 16)), p.v_scale, p.v_rcp);
         kb |= f32x2_to_e4m3x2(k0, k1) << (16 * q);
         vb |= f32x2_to_e4m3x2(v0, v1) << (16 * q);
       }
       ko[h] = kb;
       vo[h] = vb;
     }
-    *reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(p.k_cache) + dst) = make_uint2(ko[0], ko[1]);
-    *reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(p.v_cache) + dst) = make_uint2(vo[0], vo[1]);
+    *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.k_cache) + dst) = make_uint4(ko[0], ko[1], ko[2], ko[3]);
+    *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.v_cache) + dst) = make_uint4(vo[0], vo[1], vo[2], vo[3]);
   }
 }
 
 template <int CT, int AT>
 cudaError_t launch_append_t(const AppendParams& in, cudaStream_t stream) {
-  const int64_t total = in.num_tokens * in.num_kv_heads * (in.head_dim / 8);
+  const int64_t total = in.num_tokens * in.num_kv_heads * (in.head_dim / append_ept<CT>());
   if (total == 0) return cudaSuccess;
   AppendParams p = in;
   p.bs_shift = p.block_size == 16 ? 4 : 5;
+  p.k_rcp = (float)(1.0 / (double)p.k_scale);
+  p.v_rcp = (float)(1.0 / (double)p.v_scale);
   p.rows_fit32 = p.num_tokens * p.num_kv_heads < ((int64_t)1 << 31) ? 1 : 0;
   p.div_hkv = make_fastdiv((uint32_t)p.num_kv_heads);
   const unsigned blocks = (unsigned)((total + 255) / 256);

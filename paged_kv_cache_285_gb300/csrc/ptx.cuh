@@ -226,6 +226,24 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// The fp32 quotient x / s as far as its e4m3 code goes.  The code stored for a
+// value is e4m3(RN_fp32(x / s)) (round to nearest even, saturating).  With
+// rcp = RN(1/s), q = RN(x * rcp) is within 2.5 fp32 ulps of RN(x / s)
+// (rcp carries one rounding, the product another), and e4m3 keeps 3 of fp32's
+// 23 mantissa bits, so both round to the same code unless q lies within a few
+// ulps of an e4m3 rounding midpoint (its low 20 mantissa bits near 0x80000;
+// checked with a margin of 8 ulps) or in the e4m3 subnormal range (|q| < 2^-6,
+// where the midpoints sit at other bits).  Those rare values take the
+// correctly rounded division.  NaN and infinities give the same code either way.
+__device__ __forceinline__ float quot_for_e4m3(float x, float s, float rcp) {
+  const float q = __fmul_rn(x, rcp);
+  const uint32_t b = __float_as_uint(q);
+  const uint32_t ex = (b >> 23) & 0xFFu;
+  const uint32_t d = (b & 0xFFFFFu) - 0x80000u + 8u;  // within 8 ulps of the midpoint: d <= 16
+  if (ex < 121u || d <= 16u) return __fdiv_rn(x, s);
+  return q;
+}
+
 // fp32 -> e4m3 pair (low input -> low byte), round to nearest even, saturating.
 __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
   uint32_t r;

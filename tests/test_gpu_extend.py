@@ -120,11 +120,16 @@ def test_extend_matches_full_prefill_rows():
 
 
 def test_shared_prefix_extend_workload_sampled():
+    # the benchmark's launch: 256 requests x 100 suffix rows over a shared 1,900-token prefix;
+    # 2,048 (row, head) outputs: for 8 requests spread over the batch, every head (so every kv
+    # head) of the first and last token of each 32-token row tile (both tiles of both pairs,
+    # the 4-token tail tile included) against the oracle
     case = W.shared_prefix_extend(device="cuda")
     out, lse = gpu_extend(case)
-    rng = np.random.default_rng(3)
-    rows = [(int(r), int(h)) for r, h in zip(rng.integers(0, case.q.shape[0], 96),
-                                              rng.integers(0, 32, 96))]
+    reqs = [0, 37, 64, 101, 128, 170, 211, 255]
+    toks = [0, 31, 32, 63, 64, 95, 96, 99]
+    rows = [(r * 100 + i, h) for r in reqs for i in toks for h in range(32)]
+    assert len(rows) == 2048
     check(case, out, lse, "shared-prefix extend", rows=rows)
     assert pkv.get_device_error() == 0
 

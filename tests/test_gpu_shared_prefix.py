@@ -234,6 +234,30 @@ def test_prefix_longer_than_a_member_is_reported():
     assert pkv.get_device_error() == 3
 
 
+def test_prefix_beyond_the_hint_is_reported():
+    # max_prefix_len 256 (one 256-key chunk) under a 600-token prefix: the keys past the
+    # chunk are not attended and the device error word says so
+    case, gi, gp, mg, ms = grouped_case([(4, 600)], [30, 30, 30, 30], 8, 2, 16, BF16, seed=42)
+    b = case.q.shape[0]
+    ws = torch.empty(pkv.shared_prefix_decode_workspace_bytes(case.k_cache, b, 8, 256, ms, 0),
+                     dtype=torch.uint8, device="cuda")
+    pkv.get_device_error()  # clear
+    pkv.paged_decode_attn_shared_prefix(case.k_cache, case.v_cache, case.q, torch.empty_like(case.q),
+                                        case.block_tables, case.seq_lens, case.sm_scale, gi, gp, mg,
+                                        256, ms, workspace=ws)
+    torch.cuda.synchronize()
+    assert pkv.get_device_error() == 3
+
+
+def test_long_shared_prefix_in_chunks():
+    # one group of 3 members over a 5,000-token prefix: few work items, so the prefix pass
+    # cuts the keys into chunks (one more partial each in the merge)
+    case, gi, gp, mg, ms = grouped_case([(3, 5000)], [40, 7, 130], 8, 2, 16, BF16, seed=43)
+    out, lse = run_cascade(case, gi, gp, mg, ms)
+    check(case, out, lse, "5,000-token prefix in chunks")
+    assert pkv.get_device_error() == 0
+
+
 def test_unsupported_and_bad_arguments_are_refused_on_the_host():
     gi = torch.tensor([0, 2], dtype=torch.int32, device="cuda")
     gp = torch.tensor([32], dtype=torch.int32, device="cuda")
