@@ -67,6 +67,9 @@ CASES = [
     ([200, 16], [50, 77], 24, 4, 32, F16, 128),
     ([64, 301], [40, 19], 64, 4, 16, BF16, 128),
     ([10], [37], 32, 1, 16, F16, 128),
+    # the largest groups a 128-row tile takes: 2 tokens x 64 heads, 1 token x 128 heads
+    ([40, 3], [9, 5], 128, 2, 16, BF16, 128),
+    ([17, 0], [6, 3], 128, 1, 32, F16, 64),
     # head_dim 64: ragged, mid-block prefixes, groups 1 / 4 / 8, both block sizes
     ([0], [5], 4, 1, 16, F16, 64),
     ([4], [1], 4, 1, 16, F16, 64),
