@@ -522,11 +522,41 @@ def _time_extend_case(case, P, Sfx, n, flush, with_append):
     return t
 
 
+def _time_extend_shared(case, groups, shared, max_group_rows, max_total, n, flush):
+    """Device times (ms) of paged_extend_attn_shared_prefix on `case` with the given groups,
+    L2 flushed before each call."""
+    import paged_kv_cache_285_gb300 as pkv
+    out = torch.empty_like(case.q)
+    gi = torch.tensor(groups, dtype=torch.int32, device=case.q.device)
+    gs = torch.tensor(shared, dtype=torch.int32, device=case.q.device)
+
+    def call():
+        pkv.paged_extend_attn_shared_prefix(case.k_cache, case.v_cache, case.q, out, case.q_indptr,
+                                            case.prefix_lens, case.block_tables, gi, gs,
+                                            case.sm_scale, max_group_rows, max_total,
+                                            k_scale=case.k_scale, v_scale=case.v_scale)
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ts = []
+    for _ in range(n):
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return ts
+
+
 def run_extend_bench(args, dev, bf16, bf16_sus, peak_src):
     """paged_extend_attn on 256 requests x 100 suffix tokens over a shared 1,900-token
     prefix (useful causal flops only); the step with the suffix's kv_append as a
     separate launch and as paged_extend_attn_append.  The same workload is also timed with
-    an fp8 e4m3 cache (bf16 queries) and at head_dim 64."""
+    an fp8 e4m3 cache (bf16 queries), at head_dim 64, and through
+    paged_extend_attn_shared_prefix (the 256 requests as one group)."""
     import paged_kv_cache_285_gb300 as pkv
     from paged_kv_cache_285_gb300 import workloads as W
     try:
@@ -598,6 +628,29 @@ def run_extend_bench(args, dev, bf16, bf16_sus, peak_src):
                                                                   v_scale=c.v_scale),
                     "cache_bytes": 2 * c.k_cache.numel() * c.k_cache.element_size()}
         del c
+    # the same rows through the shared-prefix call: one group, the 1,900-token prompt shared
+    # (118 whole blocks), the 256 x 100 rows packed into tiles without per-request padding
+    shared = {}
+    for key, cdt, hd in (("bf16", W.BF16, 128), ("fp8", W.E4M3, 128), ("d64", W.BF16, 64)):
+        try:
+            c = W.extend_case([P] * B, [Sfx] * B, hq, 8, hd, 16, cdt, W.BF16, seed=3,
+                              device="cuda", shared_prefix=P)
+            ts = _time_extend_shared(c, [0, B], [P], B * Sfx, P + Sfx, n, flush)
+        except pkv.PkvError as e:
+            shared[key] = {"status": "failed", "error": str(e)}
+            continue
+        te, tm = sum(ts) / n, _median(ts)
+        fl = extend_useful_flops([P] * B, [Sfx] * B, hq, hd)
+        tfx = fl / (te * 1e-3) / 1e12
+        shared[key] = {"cache_dtype": W.DTYPE_NAME[cdt], "act_dtype": "bf16", "head_dim": hd,
+                       "ms_per_call": round(te, 5), "ms_per_call_median": round(tm, 5),
+                       "useful_flops_per_call": fl, "tflops": round(tfx, 1),
+                       "frac": round(tfx / bf16, 4),
+                       "frac_of_nominal": round(tfx / NOMINAL_BF16_TFLOPS, 4)}
+        del c
+    res["extend_shared_prefix"] = {
+        "call": "paged_extend_attn_shared_prefix, groups [0, 256], shared 1,900 tokens",
+        "peak_source": f"{peak_src} (bf16_tflops burst)", **shared}
     return res
 
 

@@ -343,6 +343,48 @@ pkv_status pkv_paged_extend_attn(const pkv_cache_desc* desc, const void* k_cache
                                  cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * pkv_paged_extend_attn_shared_prefix -- suffix prefill for groups of
+ * requests that share a cached prefix.
+ *
+ * "PagedAttention과 RadixAttention으로 LLM KV 캐시 최적화", sections 02-03:
+ * requests that share a prompt prefix point their block tables at the same
+ * physical blocks, and only each request's suffix is computed.  The result is
+ * that of pkv_paged_extend_attn on the same arguments (every row i of request
+ * b attends to keys 0 .. P_b + i through b's block table); the call differs in
+ * how the work is laid out.  The suffix rows of a group's requests are packed
+ * back to back into 128-row tiles (no tile is padded at a request's end), and
+ * each tile pair reads the group's shared blocks once for all of its rows,
+ * then each of its requests' remaining keys (its unshared prefix tail and its
+ * suffix) with the other requests' rows masked.
+ *
+ * group_indptr:      int32 [num_groups+1], device: group g is requests
+ *                    group_indptr[g] .. group_indptr[g+1]-1 (consecutive in
+ *                    q_indptr order); the groups partition 0 .. batch-1.
+ * group_shared_lens: int32 [num_groups], device: W_g, the tokens whose blocks
+ *                    every member of group g shares (the same physical block
+ *                    ids in the first W_g / block_size entries of their
+ *                    tables), rounded down to whole blocks by the kernel.
+ *                    Every member with rows must have prefix_lens[b] >= W_g.
+ *                    W_g = 0 is allowed (rows are still packed).
+ * max_group_rows:    host-side upper bound of the suffix rows of a group
+ *                    (q_indptr[group_indptr[g+1]] - q_indptr[group_indptr[g]]);
+ *                    it sizes the grid.
+ * Everything else as pkv_paged_extend_attn (no workspace).
+ * Device-side checks: a group whose request range or rows are not valid, rows
+ * beyond max_group_rows, and a request whose prefix is shorter than W_g or
+ * whose keys do not fit its block table are not computed (nothing is written
+ * for the rows of the tile pairs concerned) and set PKV_DEVERR_BAD_LENGTH.
+ * Supported: as pkv_paged_extend_attn.
+ * ------------------------------------------------------------------------- */
+pkv_status pkv_paged_extend_attn_shared_prefix(
+    const pkv_cache_desc* desc, const void* k_cache, const void* v_cache, const void* q, void* out,
+    pkv_dtype act_dtype, const int32_t* q_indptr, const int32_t* prefix_lens,
+    const int32_t* block_tables, int32_t max_blocks_per_seq, int32_t batch, int32_t num_q_heads,
+    float sm_scale, int32_t total_q_rows, const int32_t* group_indptr,
+    const int32_t* group_shared_lens, int32_t num_groups, int32_t max_group_rows,
+    int32_t max_total_len, float* lse_out, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------
  * pkv_paged_extend_attn_append -- suffix prefill with the suffix's K/V written
  * into the cache by the same call.
  *

@@ -98,6 +98,10 @@ def load():
         lib.pkv_paged_extend_attn_append.argtypes = [D, P, P, P, P, P, P, ctypes.c_int, P, P, P, I32,
                                                      I32, I32, F, I32, I32, I32, P, P]
         lib.pkv_paged_extend_attn_append.restype = ctypes.c_int
+        lib.pkv_paged_extend_attn_shared_prefix.argtypes = [D, P, P, P, P, ctypes.c_int, P, P, P,
+                                                            I32, I32, I32, F, I32, P, P, I32, I32,
+                                                            I32, P, P]
+        lib.pkv_paged_extend_attn_shared_prefix.restype = ctypes.c_int
         lib.pkv_status_string.argtypes = [ctypes.c_int]
         lib.pkv_status_string.restype = ctypes.c_char_p
         lib.pkv_get_device_error.argtypes = [ctypes.POINTER(I32), I32, P]
@@ -400,6 +404,33 @@ def paged_extend_attn(k_cache, v_cache, q, out, q_indptr, prefix_lens, block_tab
                                    int(max_total_len), _ptr(lse_out), _ptr(workspace), ws_bytes,
                                    _stream(stream))
     _check(st, "pkv_paged_extend_attn")
+
+
+def paged_extend_attn_shared_prefix(k_cache, v_cache, q, out, q_indptr, prefix_lens, block_tables,
+                                    group_indptr, group_shared_lens, sm_scale, max_group_rows,
+                                    max_total_len, k_scale=1.0, v_scale=1.0, lse_out=None,
+                                    stream=None):
+    """pkv_paged_extend_attn_shared_prefix: as paged_extend_attn, for groups of requests
+    (group_indptr int32 [G+1], consecutive requests) sharing the blocks of their first
+    group_shared_lens[g] tokens (int32 [G]); the groups' rows are packed into shared tiles."""
+    _need(torch.int32, q_indptr=q_indptr, prefix_lens=prefix_lens, block_tables=block_tables,
+          group_indptr=group_indptr, group_shared_lens=group_shared_lens)
+    rows, hq, batch = _extend_shapes(k_cache, v_cache, q, out, q_indptr, prefix_lens,
+                                     block_tables, lse_out)
+    ng = int(group_indptr.shape[0]) - 1
+    if group_indptr.dim() != 1 or ng < 0 or tuple(group_shared_lens.shape) != (ng,):
+        raise ValueError("group_indptr must be [G+1] and group_shared_lens [G]")
+    for name, t in (("group_indptr", group_indptr), ("group_shared_lens", group_shared_lens)):
+        if t.device != q.device:
+            raise ValueError(f"{name} must be on {q.device}")
+    lib = load()
+    desc = _desc(k_cache, k_scale, v_scale)
+    st = lib.pkv_paged_extend_attn_shared_prefix(
+        ctypes.byref(desc), _ptr(k_cache), _ptr(v_cache), _ptr(q), _ptr(out), _dtype_code(q),
+        _ptr(q_indptr), _ptr(prefix_lens), _ptr(block_tables), int(block_tables.shape[1]), batch,
+        hq, float(sm_scale), rows, _ptr(group_indptr), _ptr(group_shared_lens), ng,
+        int(max_group_rows), int(max_total_len), _ptr(lse_out), _stream(stream))
+    _check(st, "pkv_paged_extend_attn_shared_prefix")
 
 
 def paged_extend_attn_append(k_cache, v_cache, k_new, v_new, q, out, q_indptr, prefix_lens,

@@ -409,7 +409,7 @@ pkv_status pkv_paged_decode_attn_shared_prefix(
   // 1. the shared prefixes, once per group, on the tensor cores -> one
   //    partial per key chunk in the first prefix_slots slots (on the side
   //    stream, beside step 2)
-  ExtendParams pe;
+  ExtendParams pe{};
   pe.q_indptr = group_indptr;
   pe.prefix_lens = group_prefix_lens;
   pe.block_tables = block_tables;
@@ -621,8 +621,17 @@ size_t pkv_extend_workspace_bytes(const pkv_cache_desc* desc, int32_t batch, int
 
 }  // extern "C"
 
+// Shared-prefix extend: the groups (null group_indptr: plain extend).
+struct ExtendGroups {
+  const int32_t* group_indptr;
+  const int32_t* group_shared;
+  int32_t num_groups;
+  int32_t max_group_rows;
+};
+
 // Extend, optionally with the suffix's K/V (k_new/v_new, [rows][Hkv][D] in
-// the cache dtype) written into the cache by the extend kernel.
+// the act dtype) written into the cache before the extend kernel runs, or
+// (groups) with the rows of each group's requests packed into shared tiles.
 static pkv_status extend_common(const pkv_cache_desc* desc, const void* k_cache,
                                 const void* v_cache, const void* k_new, const void* v_new,
                                 const void* q, void* out, pkv_dtype act_dtype,
@@ -631,7 +640,8 @@ static pkv_status extend_common(const pkv_cache_desc* desc, const void* k_cache,
                                 int32_t batch, int32_t num_q_heads, float sm_scale,
                                 int32_t total_q_rows, int32_t max_suffix_len,
                                 int32_t max_total_len, float* lse_out, void* workspace,
-                                size_t workspace_bytes, cudaStream_t stream) {
+                                size_t workspace_bytes, cudaStream_t stream,
+                                const ExtendGroups* groups = nullptr) {
   pkv_status st = check_desc(desc);
   if (st != PKV_OK) return st;
   if ((st = check_act(desc, act_dtype)) != PKV_OK) return st;
@@ -643,23 +653,35 @@ static pkv_status extend_common(const pkv_cache_desc* desc, const void* k_cache,
   if (!extend_supported(desc->head_dim, (int)desc->cache_dtype, (int)act_dtype, group))
     return PKV_ERR_UNSUPPORTED;
   (void)workspace; (void)workspace_bytes;  // no scratch is needed (pkv_extend_workspace_bytes is 0)
-  if (batch == 0 || total_q_rows == 0 || max_suffix_len == 0) return PKV_OK;
+  if (groups) {
+    if (groups->num_groups < 0 || groups->max_group_rows < 0 || groups->num_groups > batch)
+      return PKV_ERR_INVALID_ARG;
+    if (batch > 0 && groups->num_groups == 0) return PKV_ERR_INVALID_ARG;
+  }
+  const int32_t rows_hint = groups ? groups->max_group_rows : max_suffix_len;
+  if (batch == 0 || total_q_rows == 0 || rows_hint == 0) return PKV_OK;
   if (!k_cache || !v_cache || !q || !out || !block_tables || !q_indptr || !prefix_lens)
     return PKV_ERR_INVALID_ARG;
+  if (groups && (!groups->group_indptr || !groups->group_shared)) return PKV_ERR_INVALID_ARG;
   if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q, 16) || !aligned(out, 16))
     return PKV_ERR_INVALID_ARG;
   cudaError_t e;
   DeviceState* ds = device_state(&e);
   if (!ds) return PKV_ERR_CUDA;
-  CUtensorMap kmap, vmap, qmap;
+  CUtensorMap kmap, vmap, qmap, omap;
   if ((st = make_page_map(&kmap, k_cache, desc)) != PKV_OK) return st;
   if ((st = make_page_map(&vmap, v_cache, desc)) != PKV_OK) return st;
   if ((st = make_q_map(&qmap, q, desc->head_dim, num_q_heads, total_q_rows, group)) != PKV_OK)
     return st;
-  ExtendParams p;
+  // the output has q's shape and layout: the same map over out
+  if ((st = make_q_map(&omap, out, desc->head_dim, num_q_heads, total_q_rows, group)) != PKV_OK)
+    return st;
+  ExtendParams p{};
   p.q_indptr = q_indptr;
   p.prefix_lens = prefix_lens;
   p.block_tables = block_tables;
+  p.group_indptr = groups ? groups->group_indptr : nullptr;
+  p.group_shared = groups ? groups->group_shared : nullptr;
   p.q = q;
   p.out = out;
   p.lse_out = lse_out;
@@ -670,12 +692,20 @@ static pkv_status extend_common(const pkv_cache_desc* desc, const void* k_cache,
   p.num_q_heads = num_q_heads;
   p.num_kv_heads = desc->num_kv_heads;
   p.out_32b = aligned(out, 32) ? 1 : 0;
+  p.out_tma = 1;
   p.bs_shift = desc->block_size == 16 ? 4 : 5;
   p.total_rows = total_q_rows;
   p.scale_log2 = score_scale_log2(desc, sm_scale);
   p.out_scale = output_scale(desc);
-  if (!plan_extend(p, batch, desc->num_kv_heads, group, max_suffix_len, ds->sm_count))
+  // work items per (request or group, kv head): pairs of row tiles
+  if (!plan_extend(p, groups ? groups->num_groups : batch, desc->num_kv_heads, group, rows_hint,
+                   ds->sm_count))
     return PKV_ERR_UNSUPPORTED;
+  if (groups) {
+    e = launch_extend_shared(kmap, vmap, qmap, omap, p, desc->head_dim, (int)desc->cache_dtype,
+                             (int)act_dtype, stream);
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  }
   if (k_new) {
     // the suffix's K/V first (its slots computed from the extend layout), then
     // the extend kernel reads them back; two launches in stream order
@@ -701,8 +731,8 @@ static pkv_status extend_common(const pkv_cache_desc* desc, const void* k_cache,
     e = launch_append(ap, (int)desc->cache_dtype, (int)act_dtype, stream);
     if (e != cudaSuccess) return PKV_ERR_CUDA;
   }
-  e = launch_extend(kmap, vmap, qmap, p, desc->head_dim, (int)desc->cache_dtype, (int)act_dtype,
-                    stream);
+  e = launch_extend(kmap, vmap, qmap, omap, p, desc->head_dim, (int)desc->cache_dtype,
+                    (int)act_dtype, stream);
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
@@ -720,6 +750,20 @@ pkv_status pkv_paged_extend_attn(const pkv_cache_desc* desc, const void* k_cache
                        prefix_lens, block_tables, max_blocks_per_seq, batch, num_q_heads,
                        sm_scale, total_q_rows, max_suffix_len, max_total_len, lse_out, workspace,
                        workspace_bytes, stream);
+}
+
+pkv_status pkv_paged_extend_attn_shared_prefix(
+    const pkv_cache_desc* desc, const void* k_cache, const void* v_cache, const void* q, void* out,
+    pkv_dtype act_dtype, const int32_t* q_indptr, const int32_t* prefix_lens,
+    const int32_t* block_tables, int32_t max_blocks_per_seq, int32_t batch, int32_t num_q_heads,
+    float sm_scale, int32_t total_q_rows, const int32_t* group_indptr,
+    const int32_t* group_shared_lens, int32_t num_groups, int32_t max_group_rows,
+    int32_t max_total_len, float* lse_out, cudaStream_t stream) {
+  const ExtendGroups groups{group_indptr, group_shared_lens, num_groups, max_group_rows};
+  return extend_common(desc, k_cache, v_cache, nullptr, nullptr, q, out, act_dtype, q_indptr,
+                       prefix_lens, block_tables, max_blocks_per_seq, batch, num_q_heads,
+                       sm_scale, total_q_rows, max_group_rows, max_total_len, lse_out, nullptr, 0,
+                       stream, &groups);
 }
 
 pkv_status pkv_paged_extend_attn_append(const pkv_cache_desc* desc, void* k_cache, void* v_cache,

@@ -119,7 +119,9 @@ struct ExtCfg {
     B_QFREE = B_QCONV + 4,    // [item parity] the item's last S_B = Q_B K^T done
     B_ODONE = B_QFREE + 2,    // the item's last O_B += P_B V done (O_A's before it)
     B_OFREE = B_ODONE + 1,    // [2] O_x of the item read out of TMEM
-    NBAR = B_OFREE + 2
+    B_EST = B_OFREE + 2,      // [2] tile x's output rows staged in shared memory (4 warps)
+    B_EFREE = B_EST + 2,      // [2] tile x done with the staging buffer (its store has read it)
+    NBAR = B_EFREE + 2
   };
   static constexpr int OFF_TMEMSLOT = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_TMEMSLOT + 16 + 1024;
@@ -128,6 +130,11 @@ struct ExtCfg {
   __host__ __device__ static constexpr int src8(bool isv, int s) {
     return STAGE8 ? (isv ? OFF_V8 : OFF_K8) + s * T8 : (isv ? OFF_V : OFF_K) + s * T16;
   }
+  // whole output tiles leave through shared memory and TMA stores issued by
+  // warp 3; not with fp8 codes at d128, whose kernel (in-place widening and Q
+  // conversion) already fills the instruction cache: the extra code raised
+  // its "no instruction" stalls from 0.81 to 1.31 per issue and cost 8 %
+  static constexpr bool OUT_TMA = !(FP8 && HD == 128);
 };
 
 constexpr uint32_t TMEM_COLS = 512;
@@ -151,6 +158,29 @@ __device__ __forceinline__ void set_err(int32_t* err, int code) {
 // units): bf16 -> f16 (CVT), and units of keys at or past kv_end -> zeros
 // (TAIL; key0 is the tile's first key).  Measured faster than one key row per
 // thread on the benchmark's bf16 tiles (896 against 945 us per call).
+// A bf16 Q tile to f16 in place, once per item: a rolled loop (four units in
+// flight per pass), so that this cold code takes little instruction cache
+// beside the key-tile loops.
+template <int HD>
+__device__ __forceinline__ void conv_q_tile(uint8_t* tile, int ct) {
+  constexpr int PER = BM * HD * 2 / 16 / NCONV;  // 16-byte units per thread
+  uint4* v4 = reinterpret_cast<uint4*>(tile);
+#pragma unroll 1
+  for (int hh = 0; hh < PER; hh += 4) {
+    uint4 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = v4[ct + (hh + i) * NCONV];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[i].x = to_f16x2<true>(v[i].x);
+      v[i].y = to_f16x2<true>(v[i].y);
+      v[i].z = to_f16x2<true>(v[i].z);
+      v[i].w = to_f16x2<true>(v[i].w);
+      v4[ct + (hh + i) * NCONV] = v[i];
+    }
+  }
+}
+
 template <int HD, bool CVT, bool TAIL>
 __device__ __forceinline__ void conv_tile16(uint8_t* tile, int ct, int key0, int kv_end) {
   constexpr int PER = BN * HD * 2 / 16 / NCONV;  // 16-byte units per thread
@@ -242,24 +272,132 @@ __device__ __forceinline__ void widen_row(const uint8_t* src, uint8_t* dst, int 
   }
 }
 
-// Per-request values an item needs, loaded one item ahead.
+// Per-request values an item needs, loaded one item ahead.  Shared-prefix
+// extend (SX): per-group values (rows r0 .. r1-1 of requests ga .. gb-1,
+// `prefix` = the group's shared prefix length).
 struct ItemRaw {
-  int r0, r1, prefix;
+  int r0, r1, prefix, ga, gb;
 };
 
+// Tsh, r_lo, r_hi (SX): the shared prefix's key tiles, and the requests that
+// hold the item's first and last rows.
 struct Item {
-  int b, g, i0, ntok[2], P, S, row0, kv_total, k_lo, k_hi, T, slot;
+  int b, g, i0, ntok[2], P, S, row0, kv_total, k_lo, k_hi, T, slot, Tsh, r_lo, r_hi;
 };
 
+template <bool SX>
 __device__ __forceinline__ ItemRaw load_raw(const ExtendParams& p, int item) {
-  ItemRaw r{0, 0, 0};
+  ItemRaw r{0, 0, 0, 0, 0};
   if (item < p.num_items) {
     const int b = (int)p.div_req.div((uint32_t)item);
-    r.r0 = __ldg(p.q_indptr + b);
-    r.r1 = __ldg(p.q_indptr + b + 1);
-    r.prefix = __ldg(p.prefix_lens + b);
+    if constexpr (SX) {
+      r.ga = __ldg(p.group_indptr + b);
+      r.gb = __ldg(p.group_indptr + b + 1);
+      if (r.ga >= 0 && r.ga <= r.gb && r.gb <= p.batch) {
+        r.r0 = __ldg(p.q_indptr + r.ga);
+        r.r1 = __ldg(p.q_indptr + r.gb);
+      } else {
+        r.r0 = 0;
+        r.r1 = -1;  // rejected by derive()
+      }
+      r.prefix = __ldg(p.group_shared + b);
+    } else {
+      r.r0 = __ldg(p.q_indptr + b);
+      r.r1 = __ldg(p.q_indptr + b + 1);
+      r.prefix = __ldg(p.prefix_lens + b);
+    }
   }
   return r;
+}
+
+// A run of key tiles that the same rows may see through the same block
+// table: the whole key range of a plain or prefix-pass item, or (SX) the
+// group's shared prefix (req = -1, every row) or request req's own keys.
+struct Seg {
+  int req, k_lo, k_hi, kv_total, tiles;
+};
+
+// SX: request r's keys past the group's shared prefix (it.P) up to its last
+// row in the item; none if it has no rows.
+__device__ __forceinline__ Seg own_seg(const ExtendParams& p, const Item& it, int r) {
+  Seg sg;
+  sg.req = r;
+  const int qs = __ldg(p.q_indptr + r), qe = __ldg(p.q_indptr + r + 1);
+  const int pr = __ldg(p.prefix_lens + r);
+  const int last = min(qe, it.row0 + it.i0 + it.ntok[0] + it.ntok[1]) - qs;  // r's rows in the item
+  sg.k_lo = it.P;
+  sg.k_hi = pr + last;
+  sg.kv_total = pr + (qe - qs);
+  sg.tiles = (qe > qs && sg.k_hi > sg.k_lo) ? (sg.k_hi - sg.k_lo + BN - 1) / BN : 0;
+  return sg;
+}
+
+// The request of rows lo .. hi-1 (q_indptr order) that holds row t: the last
+// one starting at or before t, so empty requests are passed over.
+__device__ __forceinline__ int find_req(const int32_t* q_indptr, int lo, int hi, int t) {
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(q_indptr + mid) <= t) lo = mid;
+    else hi = mid;
+  }
+  return lo;
+}
+
+// find_req by the whole warp (t the same in every lane): each round reads 32
+// entries spread over the span at once and keeps the stretch between the last
+// one at or before t and the next, so 256 requests take two rounds of one
+// load each instead of eight dependent loads.
+__device__ __forceinline__ int find_req_warp(const int32_t* q_indptr, int lo, int hi, int t) {
+  const int lane = threadIdx.x & 31;
+  while (hi - lo > 1) {
+    const int step = (hi - lo + 31) >> 5;
+    const int idx = lo + lane * step;
+    const int v = idx < hi ? __ldg(q_indptr + idx) : INT_MAX;
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, v <= t);
+    const int k = m ? 31 - __clz(m) : 0;
+    lo += k * step;
+    hi = min(hi, lo + step);
+  }
+  return lo;
+}
+
+// The key tiles of an item walked in order, segment by segment; every role
+// walks them the same way.
+struct SegIter {
+  Seg sg;
+  int st;  // tile within the segment
+  int rr;  // SX: the next request whose own keys follow
+};
+
+template <bool SX>
+__device__ __forceinline__ void seg_next_nonempty(const ExtendParams& p, const Item& it, SegIter& si) {
+  if constexpr (SX) {
+    while (si.st >= si.sg.tiles && si.rr <= it.r_hi) {
+      si.sg = own_seg(p, it, si.rr++);
+      si.st = 0;
+    }
+  }
+}
+
+template <bool SX>
+__device__ __forceinline__ void seg_begin(const ExtendParams& p, const Item& it, SegIter& si) {
+  if constexpr (!SX) return;  // a plain or prefix-pass item is one run: tile kt at k_lo + kt * BN
+  si.sg.req = -1;
+  si.sg.k_lo = it.k_lo;
+  si.sg.k_hi = it.k_hi;
+  si.sg.kv_total = it.kv_total;
+  si.sg.tiles = SX ? it.Tsh : it.T;
+  si.st = 0;
+  si.rr = it.r_lo;
+  seg_next_nonempty<SX>(p, it, si);
+}
+
+template <bool SX>
+__device__ __forceinline__ void seg_advance(const ExtendParams& p, const Item& it, SegIter& si) {
+  if constexpr (SX) {
+    ++si.st;
+    seg_next_nonempty<SX>(p, it, si);
+  }
 }
 
 // false: the item has no work (the same answer in every role): tile A holds no
@@ -267,8 +405,12 @@ __device__ __forceinline__ ItemRaw load_raw(const ExtendParams& p, int item) {
 // or, in the prefix pass, the group shares no prefix or none in this item's
 // key chunk.  Rows beyond the max_suffix_len hint (or max_group_size in the
 // prefix pass), and prefix keys beyond the last chunk, are not computed and
-// are reported as a length error.
-template <bool PP>
+// are reported as a length error.  SX: the item is a pair of tiles of the
+// group's rows (requests packed back to back); a group whose request range or
+// rows are not valid, or a request in the item whose prefix is shorter than
+// the group's shared prefix or whose keys do not fit its block table, is not
+// computed and is reported as a length error.
+template <bool PP, bool SX>
 __device__ __forceinline__ bool derive(const ExtendParams& p, int item, const ItemRaw& r, Item& it) {
   const uint32_t rest = p.div_pairs.div((uint32_t)item);
   int pair = item - (int)(rest * p.div_pairs.d);
@@ -289,6 +431,9 @@ __device__ __forceinline__ bool derive(const ExtendParams& p, int item, const It
       return false;
     }
   }
+  it.Tsh = 0;
+  it.r_lo = 0;
+  it.r_hi = -1;
   it.i0 = 2 * pair * TOK;  // first token of tile A; tile B follows it
   if (it.i0 >= it.S) return false;
   if ((pair + 1) * p.kchunks == (int)p.div_pairs.d && it.i0 + 2 * TOK < it.S) set_err(p.err, 3);
@@ -296,6 +441,33 @@ __device__ __forceinline__ bool derive(const ExtendParams& p, int item, const It
   it.ntok[1] = max(0, min(TOK, it.S - it.i0 - TOK));
   it.P = r.prefix;
   const int cap = p.max_blocks << p.bs_shift;
+  if constexpr (SX) {
+    it.P = (max(it.P, 0) >> p.bs_shift) << p.bs_shift;  // only whole blocks are shared
+    if (it.P > cap) {
+      set_err(p.err, 3);
+      return false;
+    }
+    it.slot = 0;
+    it.k_lo = 0;
+    it.k_hi = it.P;
+    it.kv_total = it.P;
+    it.Tsh = (it.P + BN - 1) / BN;
+    const int t_first = it.row0 + it.i0, t_last = t_first + it.ntok[0] + it.ntok[1] - 1;
+    it.r_lo = find_req_warp(p.q_indptr, r.ga, r.gb, t_first);
+    it.r_hi = find_req_warp(p.q_indptr, it.r_lo, r.gb, t_last);
+    int T = it.Tsh;
+    for (int rq = it.r_lo; rq <= it.r_hi; ++rq) {
+      const Seg sg = own_seg(p, it, rq);
+      const int pr = __ldg(p.prefix_lens + rq);
+      if (sg.kv_total > pr && (pr < it.P || sg.kv_total > cap)) {  // a request with rows
+        set_err(p.err, 3);
+        return false;
+      }
+      T += sg.tiles;
+    }
+    it.T = T;
+    return T > 0;
+  }
   if constexpr (PP) {
     // the group's first member supplies the block table and must exist
     if (it.row0 < 0 || it.row0 >= p.total_rows) {
@@ -326,12 +498,13 @@ __device__ __forceinline__ bool derive(const ExtendParams& p, int item, const It
 }
 
 // HD: head dim (64 or 128); CT: cache dtype (f16, bf16 or e4m3); AT: the
-// activation dtype of q and out (equal to CT for 16-bit caches).
-template <int HD, int CT, int AT, bool PP>
+// activation dtype of q and out (equal to CT for 16-bit caches); PP: the
+// prefix pass; SX: shared-prefix extend.
+template <int HD, int CT, int AT, bool PP, bool SX>
 __global__ void __launch_bounds__(NTHREADS, 1)
 extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-              const __grid_constant__ CUtensorMap qmap, const ExtendParams p,
-              const ExtendPartialParams pp) {
+              const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
+              const ExtendParams p, const ExtendPartialParams pp) {
   using C = ExtCfg<HD, CT, AT>;
   constexpr int NST = C::NST;
   extern __shared__ uint8_t smem_raw[];
@@ -368,6 +541,8 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       mbar_init(bar(C::B_QCONV + 2 * x + 1), NCONV / 32);
       mbar_init(bar(C::B_QFREE + x), 1);
       mbar_init(bar(C::B_OFREE + x), 4);
+      mbar_init(bar(C::B_EST + x), 4);
+      mbar_init(bar(C::B_EFREE + x), 1);
     }
     mbar_init(bar(C::B_ODONE), 1);
     fence_mbar_init();
@@ -398,27 +573,50 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
     const uint32_t srow = tmem + lane_addr + tm_s(x);
     const uint32_t orow = tmem + lane_addr + tm_o<HD>(x);
     int n = 0, js = 0;
-    ItemRaw nxt_raw = load_raw(p, item0);
+    ItemRaw nxt_raw = load_raw<SX>(p, item0);
     for (int item = item0; ok && item < p.num_items; item += stride) {
       const ItemRaw raw = nxt_raw;
-      nxt_raw = load_raw(p, item + stride);
+      nxt_raw = load_raw<SX>(p, item + stride);
       Item it;
-      if (!derive<PP>(p, item, raw, it)) continue;
+      if (!derive<PP, SX>(p, item, raw, it)) continue;
       const int i0x = it.i0 + x * TOK;  // first token of this tile
       // a row's last visible key is kdiag + its token (prefix pass: the chunk's
       // last key for all)
       const int kdiag = PP ? it.kv_total - 1 : it.P + i0x;
+      // SX: this row's request and its last visible key (rows past the
+      // group's end see nothing)
+      int row_req = -2, row_lim = -1;
+      if constexpr (SX) {
+        if (rtok < it.ntok[x]) {
+          const int tg = it.row0 + i0x + rtok;
+          row_req = find_req(p.q_indptr, it.r_lo, it.r_hi + 1, tg);
+          row_lim = __ldg(p.prefix_lens + row_req) + (tg - __ldg(p.q_indptr + row_req));
+        }
+      }
+      SegIter si;
+      seg_begin<SX>(p, it, si);
       float m_run = -INFINITY, l_run = 0.f;
-      for (int kt = 0; kt < it.T; ++kt, ++n) {
+      for (int kt = 0; kt < it.T; ++kt, ++n, seg_advance<SX>(p, it, si)) {
         if (!mbar_wait(bar(C::B_SDONE + x), n & 1)) { ok = false; break; }
         tc_fence_after();
-        const int key0 = it.k_lo + kt * BN;
-        if (key0 + BN - 1 > kdiag) {
-          // causal mask on a tile that reaches past some row's limit (keys
-          // key0 .. key0+nvis are visible): applied in TMEM one 32-column
-          // chunk at a time, a short rolled loop that runs on one or two key
-          // tiles per item
-          const int nvis = kdiag + (PP ? 0 : rtok) - key0;
+        const int key0 = SX ? si.sg.k_lo + si.st * BN : it.k_lo + kt * BN;
+        // keys key0 .. key0 + nvis of the tile are visible to this row
+        int nvis;
+        bool masked;
+        if constexpr (SX) {
+          // the shared prefix: keys before its end, up to the row's limit;
+          // a request's own keys: only that request's rows, causally
+          const int lim = si.sg.req < 0 ? min(it.P - 1, row_lim) : (row_req == si.sg.req ? row_lim : -1);
+          nvis = lim - key0;
+          masked = __any_sync(0xFFFFFFFFu, nvis < BN - 1);
+        } else {
+          nvis = kdiag + (PP ? 0 : rtok) - key0;
+          masked = key0 + BN - 1 > kdiag;
+        }
+        if (masked) {
+          // causal mask on a tile that reaches past some row's limit:
+          // applied in TMEM one 32-column chunk at a time, a short rolled loop
+          // that runs on one or two key tiles per item
           const uint32_t ninf = __float_as_uint(-INFINITY);
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
@@ -450,7 +648,10 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
                                fmaxf(mx[6], mx[7])) * p.scale_log2;
         float m_new = m_run;
         if (mt > m_run + 8.f) m_new = mt;
-        const float alpha = fast_exp2(m_run - m_new);
+        // SX: a row that has seen no key yet keeps m = -inf and takes 0 as
+        // the exponent's base, so its masked scores give exact zeros
+        const float m_base = (SX && m_new == -INFINITY) ? 0.f : m_new;
+        const float alpha = fast_exp2(m_run - m_base);
         const bool mine = (m_new != m_run);
         if (kt >= 1 && __any_sync(0xFFFFFFFFu, mine)) {
           // rescale O_x in TMEM (its last PV completed before S_x(n) did)
@@ -472,7 +673,7 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
 #pragma unroll
         for (int a = 0; a < 4; ++a) sm[a] = make_float2(0.f, 0.f);
         const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
-        const float2 nm2 = make_float2(-m_new, -m_new);
+        const float2 nm2 = make_float2(-m_base, -m_base);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pk[16];
@@ -499,6 +700,11 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       // item), O / l -> out, LSE
       if (!mbar_wait(bar(C::B_ODONE), js & 1)) { ok = false; break; }
       tc_fence_after();
+      // a whole tile of 16-bit output rows leaves through shared memory and
+      // TMA stores (a tile with fewer rows, whose box would reach the next
+      // request's rows, and the prefix pass's fp32 partials are stored by
+      // each thread)
+      const bool staged = C::OUT_TMA && !PP && p.out_tma && it.ntok[x] == TOK;
       const float osc = p.out_scale / l_run;
       if constexpr (PP) {
         // fp32 O / l straight from TMEM, 32 columns at a time, then the LSE
@@ -538,7 +744,27 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(C::B_OFREE + x));
-        if (rtok < it.ntok[x]) {
+        if (staged) {
+          // the rows go to shared memory in the layout of a Q tile (128-byte
+          // rows, 128-byte swizzle, one block per 64 dims) and leave in TMA
+          // stores: 128 coalesced boxes instead of 32 row-strided cache lines
+          // per warp store, issued by warp 3.  Tile B writes after tile A's
+          // store has read the buffer.
+          if (x == 1 && !mbar_wait(bar(C::B_EFREE), js & 1)) { ok = false; break; }
+          uint8_t* stg = smem + C::OFF_Q + ((2 * js + 1) % NQB) * C::T16;
+#pragma unroll
+          for (int c = 0; c < HD / 64; ++c)
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              *reinterpret_cast<uint4*>(stg + c * CHUNK + r * 128 + ((u ^ (r & 7)) << 4)) =
+                  make_uint4(w[c * 32 + 4 * u], w[c * 32 + 4 * u + 1], w[c * 32 + 4 * u + 2],
+                             w[c * 32 + 4 * u + 3]);
+          fence_async_smem();
+          if (p.lse_out && rtok < it.ntok[x]) {
+            const int64_t qrow = (int64_t)(it.row0 + i0x + rtok) * p.num_q_heads + it.g * G + rhead;
+            p.lse_out[qrow] = (m_run + log2f(l_run)) * kLn2f;
+          }
+        } else if (rtok < it.ntok[x]) {
           const int64_t qrow = (int64_t)(it.row0 + i0x + rtok) * p.num_q_heads + it.g * G + rhead;
           uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + qrow * HD;
           if (p.out_32b) {
@@ -553,6 +779,12 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
           }
           if (p.lse_out) p.lse_out[qrow] = (m_run + log2f(l_run)) * kLn2f;
         }
+      }
+      // the tile's rows are staged (or it has none to stage): warp 3 takes
+      // over.  Every warp arrives once per item, so that the phase counts items.
+      if constexpr (C::OUT_TMA) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::B_EST + x));
       }
       ++js;
     }
@@ -576,6 +808,9 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
         if (lane == 0) {
           const int prev = jq - 2 + xq;  // item whose last S_B frees the buffer
           if (prev >= 0 && !mbar_wait(bar(C::B_QFREE + (prev & 1)), (prev >> 1) & 1)) good = 0;
+          // tile A's buffer is where item j-2 staged its output
+          if (C::OUT_TMA && good && xq == 0 && jq >= 2 && !mbar_wait(bar(C::B_EFREE + 1), (jq - 2) & 1))
+            good = 0;
           if (good) {
             const uint32_t dst = s_base + C::OFF_Q + ((2 * jq + xq) % NQB) * C::T16;
             const uint32_t fb = bar(C::B_QFULL + 2 * xq + (jq & 1));
@@ -588,36 +823,51 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
         return __shfl_sync(0xFFFFFFFFu, good, 0) != 0;
       };
       int n = 0, j = 0;
-      ItemRaw nxt_raw = load_raw(p, item0);
+      ItemRaw nxt_raw = load_raw<SX>(p, item0);
       for (int item = item0; ok && item < p.num_items; item += stride) {
         const ItemRaw raw = nxt_raw;
-        nxt_raw = load_raw(p, item + stride);
+        nxt_raw = load_raw<SX>(p, item + stride);
         Item it;
-        if (!derive<PP>(p, item, raw, it)) continue;
+        if (!derive<PP, SX>(p, item, raw, it)) continue;
         if (is_k && !load_q(it, j, 0)) { ok = false; break; }
-        // prefix pass: the group's first member's table (row0 = its index)
-        const int32_t* bt = p.block_tables + (int64_t)(PP ? it.row0 : it.b) * p.max_blocks;
+        SegIter si;
+        seg_begin<SX>(p, it, si);
+        const int32_t* bt = p.block_tables;
+        int sk_lo = 0, sk_hi = 0;  // the segment's keys
         auto fetch = [&](int wi) -> int {
-          const int key0 = it.k_lo + (wi * 32 + lane) * 16;  // sub-tile = 16 keys
+          const int key0 = sk_lo + (wi * 32 + lane) * 16;  // sub-tile = 16 keys
           int page = -1;
-          if (key0 < it.k_hi) {
+          if (key0 < sk_hi) {
             const int blk = bt[key0 >> p.bs_shift];
             if (blk < 0 || blk >= p.num_blocks) set_err(p.err, 1);  // TMA zero-fills page -1
             else page = blk * p.num_kv_heads + it.g;
           }
           return page;
         };
-        int win = 0, cur = fetch(0), nxt = fetch(1);
-        for (int kt = 0; kt < it.T; ++kt, ++n) {
+        int win = 0, cur = -1, nxt = -1;
+        for (int kt = 0; kt < it.T; ++kt, ++n, seg_advance<SX>(p, it, si)) {
           const int s = n % NST;
-          if ((kt >> 2) > win) {  // 4 tiles x 8 sub-tiles per window
+          const int st = SX ? si.st : kt;  // tile within the segment
+          if (st == 0) {
+            // a segment's table: the prefix pass reads the group's first
+            // member's (row0 = its index); a shared prefix (SX) is read
+            // through the table of the item's first request, whose blocks
+            // for it are the group's
+            const int breq = SX ? (si.sg.req < 0 ? it.r_lo : si.sg.req) : (PP ? it.row0 : it.b);
+            bt = p.block_tables + (int64_t)breq * p.max_blocks;
+            sk_lo = SX ? si.sg.k_lo : it.k_lo;
+            sk_hi = SX ? si.sg.k_hi : it.k_hi;
+            win = 0;
+            cur = fetch(0);
+            nxt = fetch(1);
+          } else if ((st >> 2) > win) {  // 4 tiles x 8 sub-tiles per window
             cur = nxt;
             ++win;
             nxt = fetch(win + 1);
           }
           int pg[8];
 #pragma unroll
-          for (int q = 0; q < 8; ++q) pg[q] = __shfl_sync(0xFFFFFFFFu, cur, (kt & 3) * 8 + q);
+          for (int q = 0; q < 8; ++q) pg[q] = __shfl_sync(0xFFFFFFFFu, cur, (st & 3) * 8 + q);
           if (n >= NST && !mbar_wait(bar(free0 + s), (uint32_t)((n / NST - 1) & 1))) { ok = false; break; }
           if (lane == 0) {
             const uint32_t fb = bar(full0 + s);
@@ -627,7 +877,7 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
               mbar_arrive_expect_tx(fb, C::T8);
 #pragma unroll
               for (int q = 0; q < 8; ++q) {
-                const int rip = (it.k_lo + kt * BN + 16 * q) & ((1 << p.bs_shift) - 1);
+                const int rip = (sk_lo + st * BN + 16 * q) & ((1 << p.bs_shift) - 1);
                 tma_load_3d(dst + q * 16 * HD, map, fb, 0, rip, pg[q]);
               }
             } else {
@@ -635,7 +885,7 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
               mbar_arrive_expect_tx(fb, C::T16);
 #pragma unroll
               for (int q = 0; q < 8; ++q) {
-                const int rip = (it.k_lo + kt * BN + 16 * q) & ((1 << p.bs_shift) - 1);
+                const int rip = (sk_lo + st * BN + 16 * q) & ((1 << p.bs_shift) - 1);
 #pragma unroll
                 for (int c = 0; c < C::NCH; ++c)
                   tma_load_3d(dst + c * CHUNK + q * 2048, map, fb, c * 64, rip, pg[q]);
@@ -646,6 +896,45 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
           if (is_k && kt == min(1, it.T - 1) && !load_q(it, j, 1)) { ok = false; break; }
         }
         ++j;
+      }
+    } else if (warp == 3) {
+      if constexpr (C::OUT_TMA) {
+      // ------------------------------------------------------------ output stores
+      // Per item and tile: once the softmax warps have staged a whole tile of
+      // 16-bit output rows in tile B's Q buffer, TMA-store it, wait until the
+      // stores have read the buffer and release it (tile A first; tile B
+      // stages only after tile A's store has read, and the Q load of tile A
+      // two items on waits for tile B's release).  Waiting here keeps the
+      // softmax warps off the TMA engine's queue.
+      int js = 0;
+      ItemRaw nxt_raw = load_raw<SX>(p, item0);
+      for (int item = item0; ok && item < p.num_items; item += stride) {
+        const ItemRaw raw = nxt_raw;
+        nxt_raw = load_raw<SX>(p, item + stride);
+        Item it;
+        if (!derive<PP, SX>(p, item, raw, it)) continue;
+        const uint32_t stg = s_base + C::OFF_Q + ((2 * js + 1) % NQB) * C::T16;
+#pragma unroll 1
+        for (int x = 0; x < 2 && ok; ++x) {
+          const bool staged = !PP && p.out_tma && it.ntok[x] == TOK;
+          // every item, staged or not: this warp stays in step with the barrier
+          if (!mbar_wait(bar(C::B_EST + x), js & 1)) { ok = false; break; }
+          if (staged) {
+            if (lane == 0) {
+#pragma unroll
+              for (int c = 0; c < C::NCH; ++c)
+                tma_store_3d(&omap, stg + c * CHUNK, c * 64, it.g * G, it.row0 + it.i0 + x * TOK);
+              bulk_commit();
+              bulk_wait_read_all();
+            }
+            __syncwarp();
+          }
+          if (lane == 0) mbar_arrive(bar(C::B_EFREE + x));
+        }
+        ++js;
+      }
+      // the stores complete before the CTA exits
+      if (lane == 0) bulk_wait_all();
       }
     } else if (warp == 1) {
       // ------------------------------------------------------------ MMA issuer
@@ -697,12 +986,12 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       int n = 0, j = 0;
       bool have_prev = false, prev_first = false, prev_last = false;
       int prev_n = 0, prev_j = 0;
-      ItemRaw nxt_raw = load_raw(p, item0);
+      ItemRaw nxt_raw = load_raw<SX>(p, item0);
       for (int item = item0; ok && item < p.num_items; item += stride) {
         const ItemRaw raw = nxt_raw;
-        nxt_raw = load_raw(p, item + stride);
+        nxt_raw = load_raw<SX>(p, item + stride);
         Item it;
-        if (!derive<PP>(p, item, raw, it)) continue;
+        if (!derive<PP, SX>(p, item, raw, it)) continue;
         const int qa = (2 * j) % NQB, qb = (2 * j + 1) % NQB;
         for (int kt = 0; kt < it.T; ++kt, ++n) {
           if (have_prev && !issue_pv(0, prev_n, prev_first, prev_j)) { ok = false; break; }
@@ -749,19 +1038,21 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       // bf16 Q tile x of item j -> f16 in place (fp8 caches: S runs in f16)
       auto conv_q = [&](int xq) -> bool {
         if (!mbar_wait(bar(C::B_QFULL + 2 * xq + (j & 1)), (j >> 1) & 1)) return false;
-        conv_tile16<HD, true, false>(smem + C::OFF_Q + ((2 * j + xq) % NQB) * C::T16, t, 0, 0);
+        conv_q_tile<HD>(smem + C::OFF_Q + ((2 * j + xq) % NQB) * C::T16, t);
         fence_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(C::B_QCONV + 2 * xq + (j & 1)));
         return true;
       };
-      ItemRaw nxt_raw = load_raw(p, item0);
+      ItemRaw nxt_raw = load_raw<SX>(p, item0);
       for (int item = item0; ok && item < p.num_items; item += stride) {
         const ItemRaw raw = nxt_raw;
-        nxt_raw = load_raw(p, item + stride);
+        nxt_raw = load_raw<SX>(p, item + stride);
         Item it;
-        if (!derive<PP>(p, item, raw, it)) continue;
-        for (int kt = 0; kt < it.T; ++kt, ++n) {
+        if (!derive<PP, SX>(p, item, raw, it)) continue;
+        SegIter si;
+        seg_begin<SX>(p, it, si);
+        for (int kt = 0; kt < it.T; ++kt, ++n, seg_advance<SX>(p, it, si)) {
           const int s = n % NST;
           const uint32_t ph = (uint32_t)((n / NST) & 1);
           // order of the first key tile: Q_A, K, Q_B, V (the MMA's order of use;
@@ -780,17 +1071,21 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
             if (kt == 0 && !conv_q(1)) { ok = false; break; }
           }
           if (!mbar_wait(bar(C::B_VFULL + s), ph)) { ok = false; break; }
-          const int kbase = it.k_lo + kt * BN;
-          const bool zero = kbase + t >= it.kv_total;
+          // keys at or past the segment's end are zeroed (a shared prefix's
+          // last tile reaches into one member's own keys, which no row of the
+          // segment sees)
+          const int kbase = SX ? si.sg.k_lo + si.st * BN : it.k_lo + kt * BN;
+          const int kv_end = SX ? si.sg.kv_total : it.kv_total;
+          const bool zero = kbase + t >= kv_end;
           uint8_t* vt = smem + C::OFF_V + s * C::T16;
           if constexpr (C::FP8) {
             widen_row<HD, DT_F16>(smem + C::src8(true, s), vt, t, zero);
             fence_async_smem();
-          } else if (kbase + BN > it.kv_total) {  // tail tile: zero the keys past the end
-            conv_tile16<HD, CT == DT_BF16, true>(vt, t, kbase, it.kv_total);
+          } else if (kbase + BN > kv_end) {  // tail tile: zero the keys past the end
+            conv_tile16<HD, CT == DT_BF16, true>(vt, t, kbase, kv_end);
             fence_async_smem();
           } else if constexpr (CT == DT_BF16) {
-            conv_tile16<HD, true, false>(vt, t, kbase, it.kv_total);
+            conv_tile16<HD, true, false>(vt, t, kbase, kv_end);
             fence_async_smem();
           }
           __syncwarp();
@@ -821,27 +1116,28 @@ bool extend_supported(int head_dim, int cache_dt, int act_dt, int group) {
 
 namespace {
 
-template <int HD, int CT, int AT, bool PP>
+template <int HD, int CT, int AT, bool PP, bool SX>
 cudaError_t launch_extend_t(const CUtensorMap& kmap, const CUtensorMap& vmap, const CUtensorMap& qmap,
-                            const ExtendParams& p, const ExtendPartialParams& pp,
-                            cudaStream_t stream) {
-  auto k = extend_kernel<HD, CT, AT, PP>;
+                            const CUtensorMap& omap, const ExtendParams& p,
+                            const ExtendPartialParams& pp, cudaStream_t stream) {
+  auto k = extend_kernel<HD, CT, AT, PP, SX>;
   constexpr int smem = ExtCfg<HD, CT, AT>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  k<<<dim3(p.num_ctas), NTHREADS, smem, stream>>>(kmap, vmap, qmap, p, pp);
+  k<<<dim3(p.num_ctas), NTHREADS, smem, stream>>>(kmap, vmap, qmap, omap, p, pp);
   return cudaGetLastError();
 }
 
-template <bool PP>
+template <bool PP, bool SX>
 cudaError_t launch_extend_any(const CUtensorMap& kmap, const CUtensorMap& vmap, const CUtensorMap& qmap,
-                              const ExtendParams& p, const ExtendPartialParams& pp, int head_dim,
-                              int cache_dt, int act_dt, cudaStream_t stream) {
+                              const CUtensorMap& omap, const ExtendParams& p,
+                              const ExtendPartialParams& pp, int head_dim, int cache_dt, int act_dt,
+                              cudaStream_t stream) {
   if (!extend_supported(head_dim, cache_dt, act_dt, p.group)) return cudaErrorInvalidValue;
   if (p.num_items <= 0 || p.num_ctas <= 0 || p.tok != BM / p.group) return cudaErrorInvalidValue;
 #define PKV_EXT(HD, CT, AT)                                    \
   if (head_dim == HD && cache_dt == CT && act_dt == AT)        \
-    return launch_extend_t<HD, CT, AT, PP>(kmap, vmap, qmap, p, pp, stream);
+    return launch_extend_t<HD, CT, AT, PP, SX>(kmap, vmap, qmap, omap, p, pp, stream);
   PKV_EXT(128, DT_F16, DT_F16)
   PKV_EXT(128, DT_BF16, DT_BF16)
   PKV_EXT(128, DT_E4M3, DT_F16)
@@ -857,18 +1153,29 @@ cudaError_t launch_extend_any(const CUtensorMap& kmap, const CUtensorMap& vmap, 
 }  // namespace
 
 cudaError_t launch_extend(const CUtensorMap& kmap, const CUtensorMap& vmap, const CUtensorMap& qmap,
-                          const ExtendParams& p, int head_dim, int cache_dt, int act_dt,
-                          cudaStream_t stream) {
-  return launch_extend_any<false>(kmap, vmap, qmap, p, ExtendPartialParams{}, head_dim, cache_dt,
-                                  act_dt, stream);
+                          const CUtensorMap& omap, const ExtendParams& p, int head_dim,
+                          int cache_dt, int act_dt, cudaStream_t stream) {
+  return launch_extend_any<false, false>(kmap, vmap, qmap, omap, p, ExtendPartialParams{},
+                                         head_dim, cache_dt, act_dt, stream);
+}
+
+cudaError_t launch_extend_shared(const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                 const CUtensorMap& qmap, const CUtensorMap& omap,
+                                 const ExtendParams& p, int head_dim, int cache_dt, int act_dt,
+                                 cudaStream_t stream) {
+  if (!p.group_indptr || !p.group_shared) return cudaErrorInvalidValue;
+  return launch_extend_any<false, true>(kmap, vmap, qmap, omap, p, ExtendPartialParams{},
+                                        head_dim, cache_dt, act_dt, stream);
 }
 
 cudaError_t launch_extend_prefix_pass(const CUtensorMap& kmap, const CUtensorMap& vmap,
                                       const CUtensorMap& qmap, const ExtendParams& p,
                                       const ExtendPartialParams& pp, int head_dim, int cache_dt,
                                       int act_dt, cudaStream_t stream) {
-  if (!pp.o || !pp.lse) return cudaErrorInvalidValue;
-  return launch_extend_any<true>(kmap, vmap, qmap, p, pp, head_dim, cache_dt, act_dt, stream);
+  if (!pp.o || !pp.lse || p.out_tma) return cudaErrorInvalidValue;
+  // the partials are stored by each thread: the output map is not read
+  return launch_extend_any<true, false>(kmap, vmap, qmap, qmap, p, pp, head_dim, cache_dt, act_dt,
+                                        stream);
 }
 
 }  // namespace pkv

@@ -127,6 +127,11 @@ struct ExtendParams {
   const int32_t* q_indptr;
   const int32_t* prefix_lens;
   const int32_t* block_tables;
+  // shared-prefix extend: requests group_indptr[g] .. group_indptr[g+1]-1
+  // form group g and share their first group_shared[g] tokens' blocks
+  // (null otherwise)
+  const int32_t* group_indptr;
+  const int32_t* group_shared;
   const void* q;
   void* out;
   float* lse_out;
@@ -144,6 +149,7 @@ struct ExtendParams {
   int num_items;        // ceil(tiles_per_head / 2) * num_kv_heads * batch (pairs of tiles)
   int num_ctas;         // persistent grid: min(num_items, SM count)
   int out_32b;          // out is 32-byte aligned: rows are written with 32-byte stores
+  int out_tma;          // whole row tiles of out are stored by TMA (through the output map)
   int kchunks;          // prefix pass: key chunks per pair of row tiles (1 otherwise)
   int kchunk_keys;      // prefix pass: keys per chunk, a multiple of 128
   FastDiv div_pairs;    // by ceil(tiles_per_head / 2) * kchunks
@@ -192,15 +198,24 @@ cudaError_t launch_chain_hash(const ChainHashParams& p, int batch, cudaStream_t 
 
 // kmap/vmap: page maps of the K and V caches (16-bit or fp8 codes); qmap: the
 // query rows, dims {head_dim, num_q_heads, total_rows}, box {64, group, tok}.
+// omap: the output rows, the same dims and box as qmap (whole 16-bit row
+// tiles are stored through it when p.out_tma is set).
 cudaError_t launch_extend(const CUtensorMap& kmap, const CUtensorMap& vmap,
-                          const CUtensorMap& qmap, const ExtendParams& p, int head_dim,
-                          int cache_dt, int act_dt, cudaStream_t stream);
+                          const CUtensorMap& qmap, const CUtensorMap& omap, const ExtendParams& p,
+                          int head_dim, int cache_dt, int act_dt, cudaStream_t stream);
 // The prefix pass: ExtendParams over groups (q_indptr = group offsets into
 // the batch, prefix_lens = the groups' shared prefix lengths); see extend.cu.
 cudaError_t launch_extend_prefix_pass(const CUtensorMap& kmap, const CUtensorMap& vmap,
                                       const CUtensorMap& qmap, const ExtendParams& p,
                                       const ExtendPartialParams& pp, int head_dim, int cache_dt,
                                       int act_dt, cudaStream_t stream);
+// Shared-prefix extend: the rows of each group's requests packed into
+// 128-row tiles; every row attends to the group's shared prefix and to its
+// own request's remaining keys in one online softmax.
+cudaError_t launch_extend_shared(const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                 const CUtensorMap& qmap, const CUtensorMap& omap,
+                                 const ExtendParams& p, int head_dim, int cache_dt, int act_dt,
+                                 cudaStream_t stream);
 bool extend_supported(int head_dim, int cache_dt, int act_dt, int group);
 
 }  // namespace pkv

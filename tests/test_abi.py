@@ -172,6 +172,24 @@ def test_chain_hash_and_extend_append_argument_errors(lib):
     assert ext(_desc(), kn=None) == 1                         # the suffix K/V are required
 
 
+def test_shared_prefix_extend_argument_errors(lib):
+    # every case is refused (or empty) before anything is enqueued
+    call = lambda batch=2, groups=1, rows=10, gi=FAKE, gs=FAKE, hq=8, scale=0.1, desc=None: \
+        lib.pkv_paged_extend_attn_shared_prefix(
+            ctypes.byref(desc or _desc()), FAKE, FAKE, FAKE, FAKE, 1, FAKE, FAKE, FAKE, 4, batch,
+            hq, scale, 20, gi, gs, groups, rows, 100, None, None)
+    assert call(groups=0) == 1                                # requests but no group
+    assert call(groups=3) == 1                                # more groups than requests
+    assert call(groups=-1) == 1
+    assert call(rows=-1) == 1                                 # negative row bound
+    assert call(gi=None) == 1 and call(gs=None) == 1          # the groups are required
+    assert call(hq=3) == 1                                    # Hq % Hkv != 0
+    assert call(scale=float("nan")) == 1
+    assert call(desc=_desc(head_dim=96)) == 2                 # unsupported head_dim
+    assert call(batch=0, groups=0) == 0                       # empty batch: nothing to do
+    assert call(rows=0) == 0                                  # no rows in any group
+
+
 def test_binding_refuses_wrong_index_dtypes():
     import torch
     c = torch.zeros((4, 2, 16, 128), dtype=torch.bfloat16)
