@@ -707,21 +707,25 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       const bool staged = C::OUT_TMA && !PP && p.out_tma && it.ntok[x] == TOK;
       const float osc = p.out_scale / l_run;
       if constexpr (PP) {
-        // fp32 O / l straight from TMEM, 32 columns at a time, then the LSE
+        // fp32 O / l straight from TMEM (the whole row before one wait), then
+        // the LSE
         const int req = it.row0 + i0x + rtok;  // the group member of this row
         const bool valid = rtok < it.ntok[x] && req >= 0 && req < p.total_rows;
         const int64_t qrow = (int64_t)req * p.num_q_heads + it.g * G + rhead;
         float* dst = pp.o + qrow * pp.o_stride + it.slot * HD;
-#pragma unroll 1
-        for (int c = 0; c < HD / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(orow + c * 32, o);
+        {
+          uint32_t o[HD / 32][32];
+#pragma unroll
+          for (int c = 0; c < HD / 32; ++c) tmem_ld32(orow + c * 32, o[c]);
           tmem_wait_ld();
           if (valid) {
 #pragma unroll
-            for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * osc);
+            for (int c = 0; c < HD / 32; ++c) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) st_global_v8(dst + c * 32 + 8 * q, &o[8 * q]);
+              for (int q = 0; q < 32; ++q) o[c][q] = __float_as_uint(__uint_as_float(o[c][q]) * osc);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) st_global_v8(dst + c * 32 + 8 * q, &o[c][8 * q]);
+            }
           }
         }
         tc_fence_before();
@@ -729,17 +733,21 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
         if (lane == 0) mbar_arrive(bar(C::B_OFREE + x));
         if (valid) pp.lse[qrow * pp.lse_stride + it.slot] = m_run + log2f(l_run);
       } else {
-        // O / l packed to 16-bit in registers; then O_x is free in TMEM
+        // O / l packed to 16-bit in registers; then O_x is free in TMEM.  The
+        // whole row is loaded before one wait (the score registers are free
+        // by now): one TMEM round trip instead of one per 32 columns
         uint32_t w[HD / 2];
+        {
+          uint32_t o[HD / 32][32];
 #pragma unroll
-        for (int c = 0; c < HD / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(orow + c * 32, o);
+          for (int c = 0; c < HD / 32; ++c) tmem_ld32(orow + c * 32, o[c]);
           tmem_wait_ld();
 #pragma unroll
-          for (int q = 0; q < 16; ++q)
-            w[c * 16 + q] = pack2<AT == DT_BF16>(__uint_as_float(o[2 * q]) * osc,
-                                                 __uint_as_float(o[2 * q + 1]) * osc);
+          for (int c = 0; c < HD / 32; ++c)
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+              w[c * 16 + q] = pack2<AT == DT_BF16>(__uint_as_float(o[c][2 * q]) * osc,
+                                                   __uint_as_float(o[c][2 * q + 1]) * osc);
         }
         tc_fence_before();
         __syncwarp();
