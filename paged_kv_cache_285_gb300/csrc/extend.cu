@@ -130,12 +130,15 @@ struct ExtCfg {
   __host__ __device__ static constexpr int src8(bool isv, int s) {
     return STAGE8 ? (isv ? OFF_V8 : OFF_K8) + s * T8 : (isv ? OFF_V : OFF_K) + s * T16;
   }
-  // whole output tiles leave through shared memory and TMA stores issued by
-  // warp 3; not with fp8 codes at d128, whose kernel (in-place widening and Q
-  // conversion) already fills the instruction cache: the extra code raised
-  // its "no instruction" stalls from 0.81 to 1.31 per issue and cost 8 %
-  static constexpr bool OUT_TMA = !(FP8 && HD == 128);
 };
+
+// Whole output tiles leave through shared memory and TMA stores issued by warp
+// 3, except in the shared-prefix kernel over fp8 codes at d128, whose segment
+// walk, in-place widening and Q conversion already fill the instruction cache
+// (with the stores: 904-910 against 879-881 us; the plain fp8 d128 kernel
+// gains, 855 against 877).
+template <int HD, int CT, bool SX>
+__host__ __device__ constexpr bool out_tma_for() { return !(CT == DT_E4M3 && HD == 128 && SX); }
 
 constexpr uint32_t TMEM_COLS = 512;
 __host__ __device__ constexpr uint32_t tm_s(int x) { return (uint32_t)x * 128u; }  // S_x, then P_x
@@ -714,7 +717,7 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       // TMA stores (a tile with fewer rows, whose box would reach the next
       // request's rows, and the prefix pass's fp32 partials are stored by
       // each thread)
-      const bool staged = C::OUT_TMA && !PP && p.out_tma && it.ntok[x] == TOK;
+      const bool staged = out_tma_for<HD, CT, SX>() && !PP && p.out_tma && it.ntok[x] == TOK;
       const float osc = p.out_scale / l_run;
       if constexpr (PP) {
         // fp32 O / l straight from TMEM (the whole row before one wait), then
@@ -800,7 +803,7 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       }
       // the tile's rows are staged (or it has none to stage): warp 3 takes
       // over.  Every warp arrives once per item, so that the phase counts items.
-      if constexpr (C::OUT_TMA) {
+      if constexpr (out_tma_for<HD, CT, SX>()) {
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(C::B_EST + x));
       }
@@ -827,7 +830,8 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
           const int prev = jq - 2 + xq;  // item whose last S_B frees the buffer
           if (prev >= 0 && !mbar_wait(bar(C::B_QFREE + (prev & 1)), (prev >> 1) & 1)) good = 0;
           // tile A's buffer is where item j-2 staged its output
-          if (C::OUT_TMA && good && xq == 0 && jq >= 2 && !mbar_wait(bar(C::B_EFREE + 1), (jq - 2) & 1))
+          if (out_tma_for<HD, CT, SX>() && good && xq == 0 && jq >= 2 &&
+              !mbar_wait(bar(C::B_EFREE + 1), (jq - 2) & 1))
             good = 0;
           if (good) {
             const uint32_t dst = s_base + C::OFF_Q + ((2 * jq + xq) % NQB) * C::T16;
@@ -916,7 +920,7 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
         ++j;
       }
     } else if (warp == 3) {
-      if constexpr (C::OUT_TMA) {
+      if constexpr (out_tma_for<HD, CT, SX>()) {
       // ------------------------------------------------------------ output stores
       // Per item and tile: once the softmax warps have staged a whole tile of
       // 16-bit output rows in tile B's Q buffer, TMA-store it, wait until the
@@ -1012,19 +1016,42 @@ extend_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
         if (!derive<PP, SX>(p, item, raw, it)) continue;
         const int qa = (2 * j) % NQB, qb = (2 * j + 1) % NQB;
         for (int kt = 0; kt < it.T; ++kt, ++n) {
-          if (have_prev && !issue_pv(0, prev_n, prev_first, prev_j)) { ok = false; break; }
-          if (!mbar_wait(bar(kready0 + n % NST), (n / NST) & 1)) { ok = false; break; }
-          if (kt == 0 && !mbar_wait(bar(qready0 + (j & 1)), (j >> 1) & 1)) { ok = false; break; }
-          tc_fence_after();
-          issue_qk(0, n, qa);
-          if (have_prev) {
-            if (!issue_pv(1, prev_n, prev_first, prev_j)) { ok = false; break; }
-            commit(C::B_VFREE + prev_n % NST);
-            if (prev_last) commit(C::B_ODONE);
+          if constexpr (C::FP8 && HD == 128) {
+            // the same order as a rolled loop over the two tiles: half the
+            // issue code, which the fp8 d128 kernel (in-place widening, Q
+            // conversion) needs more than the unrolled form's shorter path
+            // (878 against 942 us; bf16 would take 827 against 785, fp8 d64
+            // 693 against 679)
+#pragma unroll 1
+            for (int xx = 0; xx < 2; ++xx) {
+              if (have_prev) {
+                if (!issue_pv(xx, prev_n, prev_first, prev_j)) { ok = false; break; }
+                if (xx == 1) {
+                  commit(C::B_VFREE + prev_n % NST);
+                  if (prev_last) commit(C::B_ODONE);
+                }
+              }
+              if (xx == 0 && !mbar_wait(bar(kready0 + n % NST), (n / NST) & 1)) { ok = false; break; }
+              if (kt == 0 && !mbar_wait(bar(qready0 + 2 * xx + (j & 1)), (j >> 1) & 1)) { ok = false; break; }
+              tc_fence_after();
+              issue_qk(xx, n, xx ? qb : qa);
+            }
+            if (!ok) break;
+          } else {
+            if (have_prev && !issue_pv(0, prev_n, prev_first, prev_j)) { ok = false; break; }
+            if (!mbar_wait(bar(kready0 + n % NST), (n / NST) & 1)) { ok = false; break; }
+            if (kt == 0 && !mbar_wait(bar(qready0 + (j & 1)), (j >> 1) & 1)) { ok = false; break; }
+            tc_fence_after();
+            issue_qk(0, n, qa);
+            if (have_prev) {
+              if (!issue_pv(1, prev_n, prev_first, prev_j)) { ok = false; break; }
+              commit(C::B_VFREE + prev_n % NST);
+              if (prev_last) commit(C::B_ODONE);
+            }
+            if (kt == 0 && !mbar_wait(bar(qready0 + 2 + (j & 1)), (j >> 1) & 1)) { ok = false; break; }
+            tc_fence_after();
+            issue_qk(1, n, qb);
           }
-          if (kt == 0 && !mbar_wait(bar(qready0 + 2 + (j & 1)), (j >> 1) & 1)) { ok = false; break; }
-          tc_fence_after();
-          issue_qk(1, n, qb);
           commit(C::B_KFREE + n % NST);
           if (kt == it.T - 1) commit(C::B_QFREE + (j & 1));
           have_prev = true;
