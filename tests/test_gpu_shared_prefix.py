@@ -293,3 +293,52 @@ def test_request_outside_every_group_is_reported():
     out, lse = run_cascade(case, gi, gp, mg, max(ms, 124))
     check(case, out, lse, "uncovered requests")
     assert pkv.get_device_error() == 3
+
+
+def test_merge_is_bit_identical_across_calls():
+    # the prefix pass runs beside the own-token decode, in whatever order the
+    # GPU schedules them; the merge takes the parts in a fixed slot order, so the
+    # output and LSE bits do not depend on it
+    case, gi, gp, mg, ms = grouped_case([(64, 500), (9, 1000)], rand_suffixes(73, 0, 300, 7),
+                                        32, 8, 16, BF16, seed=51)
+    runs = [run_cascade(case, gi, gp, mg, ms, splits=sp) for sp in (0, 0, 0, 2, 2)]
+    for out, lse in runs[1:3]:
+        assert torch.equal(out, runs[0][0]) and torch.equal(lse, runs[0][1])
+    assert torch.equal(runs[4][0], runs[3][0]) and torch.equal(runs[4][1], runs[3][1])
+    check(case, runs[0][0], runs[0][1], "repeated calls")
+    check(case, runs[3][0], runs[3][1], "repeated calls, 2 splits")
+    assert pkv.get_device_error() == 0
+
+
+def test_workspace_with_stale_contents():
+    # the workspace needs no initial contents: one holding any bytes (here all
+    # ones, then the previous call's state) gives the same result as a fresh one
+    case, gi, gp, mg, ms = grouped_case([(20, 320), (6, 40)], rand_suffixes(26, 1, 120, 8),
+                                        32, 8, 16, F16, seed=52)
+    b = case.q.shape[0]
+    nbytes = pkv.shared_prefix_decode_workspace_bytes(case.k_cache, b, case.num_q_heads, 320, ms, 0)
+    ws = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(2):
+        out = torch.full_like(case.q, float("nan"))
+        pkv.paged_decode_attn_shared_prefix(case.k_cache, case.v_cache, case.q, out,
+                                            case.block_tables, case.seq_lens, case.sm_scale, gi, gp,
+                                            mg, 320, ms, workspace=ws)
+        torch.cuda.synchronize()
+        outs.append(out)
+    fresh, _ = run_cascade(case, gi, gp, mg, ms)
+    assert torch.equal(outs[0], fresh) and torch.equal(outs[1], fresh)
+    assert pkv.get_device_error() == 0
+
+
+def test_empty_requests_get_zero_output():
+    # a request with no token at all (no prefix, seq_len 0) has no partial to
+    # merge: out = 0, lse = -inf
+    case, gi, gp, mg, ms = grouped_case([(3, 0), (2, 64)], [0, 17, 0, 5, 9], 8, 2, 16, BF16,
+                                        seed=53)
+    out, lse = run_cascade(case, gi, gp, mg, ms)
+    for r in (0, 2):
+        assert torch.count_nonzero(out[r]) == 0
+        assert torch.all(torch.isneginf(lse[r]))
+    check(case, out, lse, "empty requests")
+    assert pkv.get_device_error() == 0
