@@ -544,12 +544,37 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, const 
   const int64_t bh = (int64_t)blockIdx.x * 4 + warp;
   if (bh >= (int64_t)p.batch * p.num_q_heads) return;
   const int b = (int)(bh / p.num_q_heads);
+  constexpr int PER = HD / 32;
   int n, tb = 0;
   if constexpr (CASC) {
+    // The usual row has one prefix chunk (slot 0) and one own split (slot
+    // prefix_slots): both are loaded beside the request's span, so that such
+    // a row waits on one round trip instead of two.
+    const int ns0 = p.num_splits + ap.prefix_slots;
+    const float* o0 = p.ws_o + bh * ns0 * HD + lane * PER;
+    const float* o1 = o0 + (int64_t)ap.prefix_slots * HD;
+    float a0[PER], a1[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) {
+      a0[e] = o0[e];
+      a1[e] = o1[e];
+    }
+    const float l0 = p.ws_lse[bh * ns0], l1 = p.ws_lse[bh * ns0 + ap.prefix_slots];
     // (first own token, clamped length) as the split kernel settled them
     const int2 span = ap.ws_span[b];
     tb = span.x;
     n = span.y;
+    const bool one_chunk = tb > 0 && (tb <= ap.prefix_chunk || ap.prefix_chunks == 1);
+    if (one_chunk && n > tb && n - tb <= p.chunk) {
+      const float m = fmaxf(l0, l1);
+      const float w0 = fast_exp2(l0 - m), w1 = fast_exp2(l1 - m);
+      const float inv = 1.f / (w0 + w1);
+#pragma unroll
+      for (int e = 0; e < PER; ++e)
+        store_act<AT>(p.out, bh * HD + lane * PER + e, (w0 * a0[e] + w1 * a1[e]) * inv);
+      if (p.lse_out && lane == 0) p.lse_out[bh] = (m + log2f(w0 + w1)) * kLn2;
+      return;
+    }
   } else {
     const int bs = 1 << p.bs_shift;
     n = p.seq_lens[b];
@@ -565,7 +590,6 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p, const 
       (CASC && tb > 0) ? min((tb + ap.prefix_chunk - 1) / ap.prefix_chunk, ap.prefix_chunks) : 0;
   const int cnt = npc + ns;
   auto slot = [&](int i) { return i < npc ? i : kSlot0 + (i - npc); };
-  constexpr int PER = HD / 32;
   if (cnt <= 0) {  // no token at all: out = 0, lse = -inf
 #pragma unroll
     for (int k = 0; k < PER; ++k) store_act<AT>(p.out, bh * HD + lane * PER + k, 0.f);
