@@ -139,6 +139,14 @@ pkv_status pkv_kv_append(const pkv_cache_desc* desc, void* k_cache, void* v_cach
  * workspace:     device scratch of pkv_decode_workspace_bytes() bytes (may be
  *                NULL when that is 0).  Concurrent calls need separate
  *                workspaces.
+ * Host memory:   q, out, block_tables, seq_lens, lse_out (and k_new / v_new
+ *                of pkv_paged_decode_attn_append) are read and written with
+ *                plain loads and stores, so they may also be pinned host
+ *                memory that the GPU addresses directly (zero-copy over a
+ *                coherent host link, as on Grace-Blackwell): the bytes then
+ *                cross the link inside the kernels.  The caches and the
+ *                workspace must be device memory (the caches are read by
+ *                TMA).
  * Supported: head_dim 64/128, block_size 16/32, any GQA group
  * num_q_heads/num_kv_heads.  One CTA takes up to 8 query heads of a kv head:
  * a group of more than 8 is split into chunks of 8 heads whose CTAs each read

@@ -104,3 +104,58 @@ def test_fused_append_rejects_half_inputs():
         pkv.paged_decode_attn_append(case.k_cache, case.v_cache, case.new_k, None, case.q,
                                      torch.empty_like(case.q), case.block_tables, case.seq_lens,
                                      case.sm_scale, 20)
+
+
+class _Mapped:
+    """Device-addressable view of a pinned host tensor (the GPU reads and writes
+    it directly over the host link)."""
+
+    def __init__(self, t):
+        self.__cuda_array_interface__ = {"shape": tuple(t.shape), "typestr": _typestr(t.dtype),
+                                         "data": (t.data_ptr(), False), "version": 3}
+
+
+def _typestr(dt):
+    return {torch.int32: "<i4", torch.float32: "<f4", torch.float16: "<f2",
+            torch.int16: "<i2"}[dt]
+
+
+def _on_host(t):
+    """A pinned host copy of t and a CUDA tensor addressing the same host bytes
+    (16-bit floats travel as int16: only their bits matter)."""
+    bits = t.view(torch.int16) if t.element_size() == 2 and t.is_floating_point() else t
+    h = bits.cpu().pin_memory()
+    d = torch.as_tensor(_Mapped(h), device="cuda")
+    assert d.data_ptr() == h.data_ptr()
+    return h, (d.view(t.dtype) if d.dtype != t.dtype else d)
+
+
+@pytest.mark.parametrize("cfg", [CASES[0], CASES[3]], ids=["bf16", "fp8"])
+def test_zero_copy_host_buffers_give_the_same_bits(cfg):
+    # q, the new K/V, block tables, seq_lens, out and lse_out in pinned host
+    # memory, read and written by the kernels over the host link: the same bits
+    # as the same call on device buffers (caches and workspace stay on device)
+    lens, hq, hkv, d, bs, dt, act = cfg
+    dev = W.decode_case(lens, hq, hkv, d, bs, dt, act, seed=77, device="cuda")
+    host = W.decode_case(lens, hq, hkv, d, bs, dt, act, seed=77, device="cuda")
+    ref_out, ref_lse = _run(dev, True, 0)
+    n_max = int(host.seq_lens.max())
+    b = host.q.shape[0]
+    args = {}
+    keep = []
+    for name in ("q", "new_k", "new_v", "block_tables", "seq_lens"):
+        h, view = _on_host(getattr(host, name))
+        keep.append(h)
+        args[name] = view
+    out_h, out_v = _on_host(torch.full_like(host.q, float("nan")))
+    lse_h, lse_v = _on_host(torch.full((b, hq), float("nan"), dtype=torch.float32, device="cuda"))
+    pkv.paged_decode_attn_append(host.k_cache, host.v_cache, args["new_k"], args["new_v"],
+                                 args["q"], out_v, args["block_tables"], args["seq_lens"],
+                                 host.sm_scale, n_max, k_scale=host.k_scale, v_scale=host.v_scale,
+                                 lse_out=lse_v, workspace=_ws(host, n_max, 0))
+    torch.cuda.synchronize()
+    assert torch.equal(out_h.view(torch.int16), ref_out.view(torch.int16).cpu())
+    assert torch.equal(lse_h, ref_lse.cpu())
+    assert np.array_equal(S(host.k_cache), S(dev.k_cache))
+    assert np.array_equal(S(host.v_cache), S(dev.v_cache))
+    assert pkv.get_device_error() == 0
