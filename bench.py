@@ -569,9 +569,9 @@ def _time_extend_case(case, P, Sfx, n, flush, with_append):
     return t
 
 
-def _time_extend_shared(case, groups, shared, max_group_rows, max_total, n, flush):
-    """Device times (ms) of paged_extend_attn_shared_prefix on `case` with the given groups,
-    L2 flushed before each call."""
+def _time_extend_shared(case, groups, shared, max_group_rows, max_total, n, flush, ws=None):
+    """Device times (ms) of paged_extend_attn_shared_prefix on `case` with the given groups
+    (and the optional workspace `ws`), L2 flushed before each call."""
     import paged_kv_cache_285_gb300 as pkv
     out = torch.empty_like(case.q)
     gi = torch.tensor(groups, dtype=torch.int32, device=case.q.device)
@@ -581,7 +581,8 @@ def _time_extend_shared(case, groups, shared, max_group_rows, max_total, n, flus
         pkv.paged_extend_attn_shared_prefix(case.k_cache, case.v_cache, case.q, out, case.q_indptr,
                                             case.prefix_lens, case.block_tables, gi, gs,
                                             case.sm_scale, max_group_rows, max_total,
-                                            k_scale=case.k_scale, v_scale=case.v_scale)
+                                            k_scale=case.k_scale, v_scale=case.v_scale,
+                                            workspace=ws)
     for _ in range(3):
         call()
     torch.cuda.synchronize()
@@ -694,6 +695,19 @@ def run_extend_bench(args, dev, bf16, bf16_sus, peak_src):
                        "useful_flops_per_call": fl, "tflops": round(tfx, 1),
                        "frac": round(tfx / bf16, 4),
                        "frac_of_nominal": round(tfx / NOMINAL_BF16_TFLOPS, 4)}
+        # with the optional workspace: a bf16 cache's V pages widened to f16 once per
+        # call (the widening pass is inside the timed call), then read by the kernel
+        wsb = pkv.extend_shared_prefix_workspace_bytes(c.k_cache, c.k_scale, c.v_scale)
+        if wsb:
+            ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+            tw = _time_extend_shared(c, [0, B], [P], B * Sfx, P + Sfx, n, flush, ws=ws)
+            tw_mean = sum(tw) / n
+            tfw = fl / (tw_mean * 1e-3) / 1e12
+            shared[key]["with_workspace"] = {
+                "ms_per_call": round(tw_mean, 5), "ms_per_call_median": round(_median(tw), 5),
+                "tflops": round(tfw, 1), "frac": round(tfw / bf16, 4),
+                "frac_of_nominal": round(tfw / NOMINAL_BF16_TFLOPS, 4), "workspace_bytes": wsb}
+            del ws
         del c
     res["extend_shared_prefix"] = {
         "call": "paged_extend_attn_shared_prefix, groups [0, 256], shared 1,900 tokens",

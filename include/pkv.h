@@ -377,7 +377,20 @@ pkv_status pkv_paged_extend_attn(const pkv_cache_desc* desc, const void* k_cache
  * max_group_rows:    host-side upper bound of the suffix rows of a group
  *                    (q_indptr[group_indptr[g+1]] - q_indptr[group_indptr[g]]);
  *                    it sizes the grid.
- * Everything else as pkv_paged_extend_attn (no workspace).
+ * workspace:         NULL, or pkv_extend_shared_prefix_workspace_bytes()
+ *                    bytes of device memory, 256-byte aligned (any contents;
+ *                    the size is 0 unless the cache is bf16).  With a bf16
+ *                    cache the kernel feeds V to the tensor cores as f16 (P is
+ *                    f16), which it otherwise converts tile by tile in shared
+ *                    memory; with a workspace, the call first widens the V
+ *                    pages it reads (each group's shared blocks once, every
+ *                    request's own blocks) into an f16 copy of the V pool
+ *                    there, and the kernel reads V from it.  The same
+ *                    rounding either way: the results are bit-identical.  A
+ *                    workspace smaller than the size, or misaligned, gives
+ *                    PKV_ERR_WORKSPACE.  Calls that run at the same time
+ *                    need workspaces of their own.
+ * Everything else as pkv_paged_extend_attn.
  * Device-side checks: a group whose request range or rows are not valid, rows
  * beyond max_group_rows, and a request whose prefix is shorter than W_g or
  * whose keys do not fit its block table are not computed (nothing is written
@@ -390,7 +403,12 @@ pkv_status pkv_paged_extend_attn_shared_prefix(
     const int32_t* block_tables, int32_t max_blocks_per_seq, int32_t batch, int32_t num_q_heads,
     float sm_scale, int32_t total_q_rows, const int32_t* group_indptr,
     const int32_t* group_shared_lens, int32_t num_groups, int32_t max_group_rows,
-    int32_t max_total_len, float* lse_out, cudaStream_t stream);
+    int32_t max_total_len, float* lse_out, void* workspace, size_t workspace_bytes,
+    cudaStream_t stream);
+/* Bytes of the optional workspace of pkv_paged_extend_attn_shared_prefix: the
+ * size of the V pool in 16-bit elements for a bf16 cache, 0 for other caches
+ * (and for an invalid desc). */
+size_t pkv_extend_shared_prefix_workspace_bytes(const pkv_cache_desc* desc);
 
 /* ---------------------------------------------------------------------------
  * pkv_paged_extend_attn_append -- suffix prefill with the suffix's K/V written

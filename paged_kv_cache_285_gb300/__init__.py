@@ -32,7 +32,8 @@ __all__ = ["F16", "BF16", "FP8_E4M3", "PkvError", "CacheDesc", "lib_path", "load
            "extend_workspace_bytes", "get_device_error", "status_string", "version",
            "paged_decode_attn_append", "RadixIndex", "NO_SPACE", "chain_hash",
            "paged_decode_attn_shared_prefix", "shared_prefix_decode_workspace_bytes",
-           "paged_extend_attn_append"]
+           "paged_extend_attn_append", "paged_extend_attn_shared_prefix",
+           "extend_shared_prefix_workspace_bytes"]
 
 F16, BF16, FP8_E4M3 = 0, 1, 2
 NO_SPACE = 5  # PKV_ERR_NO_SPACE
@@ -100,8 +101,10 @@ def load():
         lib.pkv_paged_extend_attn_append.restype = ctypes.c_int
         lib.pkv_paged_extend_attn_shared_prefix.argtypes = [D, P, P, P, P, ctypes.c_int, P, P, P,
                                                             I32, I32, I32, F, I32, P, P, I32, I32,
-                                                            I32, P, P]
+                                                            I32, P, P, SZ, P]
         lib.pkv_paged_extend_attn_shared_prefix.restype = ctypes.c_int
+        lib.pkv_extend_shared_prefix_workspace_bytes.argtypes = [D]
+        lib.pkv_extend_shared_prefix_workspace_bytes.restype = SZ
         lib.pkv_status_string.argtypes = [ctypes.c_int]
         lib.pkv_status_string.restype = ctypes.c_char_p
         lib.pkv_get_device_error.argtypes = [ctypes.POINTER(I32), I32, P]
@@ -406,13 +409,23 @@ def paged_extend_attn(k_cache, v_cache, q, out, q_indptr, prefix_lens, block_tab
     _check(st, "pkv_paged_extend_attn")
 
 
+def extend_shared_prefix_workspace_bytes(k_cache, k_scale=1.0, v_scale=1.0) -> int:
+    """pkv_extend_shared_prefix_workspace_bytes: the optional workspace of
+    paged_extend_attn_shared_prefix (an f16 copy of a bf16 cache's V pool; 0 otherwise)."""
+    lib = load()
+    desc = _desc(k_cache, k_scale, v_scale)
+    return int(lib.pkv_extend_shared_prefix_workspace_bytes(ctypes.byref(desc)))
+
+
 def paged_extend_attn_shared_prefix(k_cache, v_cache, q, out, q_indptr, prefix_lens, block_tables,
                                     group_indptr, group_shared_lens, sm_scale, max_group_rows,
                                     max_total_len, k_scale=1.0, v_scale=1.0, lse_out=None,
-                                    stream=None):
+                                    workspace=None, stream=None):
     """pkv_paged_extend_attn_shared_prefix: as paged_extend_attn, for groups of requests
     (group_indptr int32 [G+1], consecutive requests) sharing the blocks of their first
-    group_shared_lens[g] tokens (int32 [G]); the groups' rows are packed into shared tiles."""
+    group_shared_lens[g] tokens (int32 [G]); the groups' rows are packed into shared tiles.
+    workspace: None, or a uint8 device tensor of extend_shared_prefix_workspace_bytes() bytes
+    (a bf16 cache's V pages are then widened to f16 once per call instead of per tile)."""
     _need(torch.int32, q_indptr=q_indptr, prefix_lens=prefix_lens, block_tables=block_tables,
           group_indptr=group_indptr, group_shared_lens=group_shared_lens)
     rows, hq, batch = _extend_shapes(k_cache, v_cache, q, out, q_indptr, prefix_lens,
@@ -425,11 +438,13 @@ def paged_extend_attn_shared_prefix(k_cache, v_cache, q, out, q_indptr, prefix_l
             raise ValueError(f"{name} must be on {q.device}")
     lib = load()
     desc = _desc(k_cache, k_scale, v_scale)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     st = lib.pkv_paged_extend_attn_shared_prefix(
         ctypes.byref(desc), _ptr(k_cache), _ptr(v_cache), _ptr(q), _ptr(out), _dtype_code(q),
         _ptr(q_indptr), _ptr(prefix_lens), _ptr(block_tables), int(block_tables.shape[1]), batch,
         hq, float(sm_scale), rows, _ptr(group_indptr), _ptr(group_shared_lens), ng,
-        int(max_group_rows), int(max_total_len), _ptr(lse_out), _stream(stream))
+        int(max_group_rows), int(max_total_len), _ptr(lse_out), _ptr(workspace), ws_bytes,
+        _stream(stream))
     _check(st, "pkv_paged_extend_attn_shared_prefix")
 
 

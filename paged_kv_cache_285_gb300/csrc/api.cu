@@ -632,6 +632,14 @@ struct ExtendGroups {
 // Extend, optionally with the suffix's K/V (k_new/v_new, [rows][Hkv][D] in
 // the act dtype) written into the cache before the extend kernel runs, or
 // (groups) with the rows of each group's requests packed into shared tiles.
+// Workspace the shared-prefix extend can use over a bf16 cache: an f16 copy of
+// the V pool (the same block ids), into which the call widens the V pages it
+// reads, so that the kernel takes V as f16 instead of converting every tile.
+static size_t shared_prefix_v16_bytes(const pkv_cache_desc* d) {
+  if (d->cache_dtype != PKV_BF16) return 0;
+  return align256((size_t)d->num_blocks * d->num_kv_heads * d->block_size * d->head_dim * 2);
+}
+
 static pkv_status extend_common(const pkv_cache_desc* desc, const void* k_cache,
                                 const void* v_cache, const void* k_new, const void* v_new,
                                 const void* q, void* out, pkv_dtype act_dtype,
@@ -652,7 +660,11 @@ static pkv_status extend_common(const pkv_cache_desc* desc, const void* k_cache,
   const int group = num_q_heads / desc->num_kv_heads;
   if (!extend_supported(desc->head_dim, (int)desc->cache_dtype, (int)act_dtype, group))
     return PKV_ERR_UNSUPPORTED;
-  (void)workspace; (void)workspace_bytes;  // no scratch is needed (pkv_extend_workspace_bytes is 0)
+  // plain extend needs no scratch (pkv_extend_workspace_bytes is 0); the
+  // shared-prefix call may take one to widen a bf16 cache's V pages first
+  const size_t v16_bytes = groups ? shared_prefix_v16_bytes(desc) : 0;
+  const bool widen = groups && workspace != nullptr && v16_bytes > 0;
+  if (widen && (workspace_bytes < v16_bytes || !aligned(workspace, 256))) return PKV_ERR_WORKSPACE;
   if (groups) {
     if (groups->num_groups < 0 || groups->max_group_rows < 0 || groups->num_groups > batch)
       return PKV_ERR_INVALID_ARG;
@@ -702,8 +714,20 @@ static pkv_status extend_common(const pkv_cache_desc* desc, const void* k_cache,
                    ds->sm_count))
     return PKV_ERR_UNSUPPORTED;
   if (groups) {
-    e = launch_extend_shared(kmap, vmap, qmap, omap, p, desc->head_dim, (int)desc->cache_dtype,
-                             (int)act_dtype, stream);
+    int cache_dt = (int)desc->cache_dtype;
+    if (widen) {
+      // the V pages the call reads, widened to f16 in the workspace (same
+      // block ids), then read by the kernel through a map over that pool
+      pkv_cache_desc d16 = *desc;
+      d16.cache_dtype = PKV_F16;
+      if ((st = make_page_map(&vmap, workspace, &d16)) != PKV_OK) return st;
+      e = launch_widen_v(v_cache, workspace, p, groups->num_groups, desc->head_dim,
+                         desc->block_size, max_total_len, stream);
+      if (e != cudaSuccess) return PKV_ERR_CUDA;
+      cache_dt = DT_BF16_V16;
+    }
+    e = launch_extend_shared(kmap, vmap, qmap, omap, p, desc->head_dim, cache_dt, (int)act_dtype,
+                             stream);
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
   }
   if (k_new) {
@@ -752,18 +776,24 @@ pkv_status pkv_paged_extend_attn(const pkv_cache_desc* desc, const void* k_cache
                        workspace_bytes, stream);
 }
 
+size_t pkv_extend_shared_prefix_workspace_bytes(const pkv_cache_desc* desc) {
+  if (check_desc(desc) != PKV_OK) return 0;
+  return shared_prefix_v16_bytes(desc);
+}
+
 pkv_status pkv_paged_extend_attn_shared_prefix(
     const pkv_cache_desc* desc, const void* k_cache, const void* v_cache, const void* q, void* out,
     pkv_dtype act_dtype, const int32_t* q_indptr, const int32_t* prefix_lens,
     const int32_t* block_tables, int32_t max_blocks_per_seq, int32_t batch, int32_t num_q_heads,
     float sm_scale, int32_t total_q_rows, const int32_t* group_indptr,
     const int32_t* group_shared_lens, int32_t num_groups, int32_t max_group_rows,
-    int32_t max_total_len, float* lse_out, cudaStream_t stream) {
+    int32_t max_total_len, float* lse_out, void* workspace, size_t workspace_bytes,
+    cudaStream_t stream) {
   const ExtendGroups groups{group_indptr, group_shared_lens, num_groups, max_group_rows};
   return extend_common(desc, k_cache, v_cache, nullptr, nullptr, q, out, act_dtype, q_indptr,
                        prefix_lens, block_tables, max_blocks_per_seq, batch, num_q_heads,
-                       sm_scale, total_q_rows, max_group_rows, max_total_len, lse_out, nullptr, 0,
-                       stream, &groups);
+                       sm_scale, total_q_rows, max_group_rows, max_total_len, lse_out, workspace,
+                       workspace_bytes, stream, &groups);
 }
 
 pkv_status pkv_paged_extend_attn_append(const pkv_cache_desc* desc, void* k_cache, void* v_cache,

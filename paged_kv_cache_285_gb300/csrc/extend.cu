@@ -1178,11 +1178,17 @@ cudaError_t launch_extend_any(const CUtensorMap& kmap, const CUtensorMap& vmap, 
                               const CUtensorMap& omap, const ExtendParams& p,
                               const ExtendPartialParams& pp, int head_dim, int cache_dt, int act_dt,
                               cudaStream_t stream) {
-  if (!extend_supported(head_dim, cache_dt, act_dt, p.group)) return cudaErrorInvalidValue;
+  // a bf16 cache with its V pages widened beforehand is a bf16 cache here
+  const int checked_dt = cache_dt == DT_BF16_V16 ? DT_BF16 : cache_dt;
+  if (!extend_supported(head_dim, checked_dt, act_dt, p.group)) return cudaErrorInvalidValue;
   if (p.num_items <= 0 || p.num_ctas <= 0 || p.tok != BM / p.group) return cudaErrorInvalidValue;
 #define PKV_EXT(HD, CT, AT)                                    \
   if (head_dim == HD && cache_dt == CT && act_dt == AT)        \
     return launch_extend_t<HD, CT, AT, PP, SX>(kmap, vmap, qmap, omap, p, pp, stream);
+  if constexpr (SX && !PP) {
+    PKV_EXT(128, DT_BF16_V16, DT_BF16)
+    PKV_EXT(64, DT_BF16_V16, DT_BF16)
+  }
   PKV_EXT(128, DT_F16, DT_F16)
   PKV_EXT(128, DT_BF16, DT_BF16)
   PKV_EXT(128, DT_E4M3, DT_F16)
@@ -1195,7 +1201,77 @@ cudaError_t launch_extend_any(const CUtensorMap& kmap, const CUtensorMap& vmap, 
   return cudaErrorInvalidValue;
 }
 
+// V pages of a shared-prefix extend widened from bf16 to f16 into a shadow
+// pool with the cache's block ids, so that the extend kernel reads V as f16
+// and its converter warps only zero the keys past a segment's end.  Request r
+// (the k-th member of its group of n) widens its own blocks, from the group's
+// shared prefix to its last key, and every n-th of the group's shared blocks
+// from the k-th on (read through the group's first member's table), so a long
+// shared prefix is spread over the members.  CTA (x, r) takes every
+// gridDim.x-th block of r's list from the x-th; each thread moves 8 16-byte
+// vectors of a block in one round trip.  The same conversion as the converter
+// warps' (round to nearest, +-inf beyond the f16 range), so either path gives
+// the same bits.
+__global__ void __launch_bounds__(256) widen_v_kernel(const uint4* __restrict__ v,
+                                                      uint4* __restrict__ v16, const ExtendParams p,
+                                                      int num_groups, int block_vec) {
+  const int r = blockIdx.y;
+  if (r < __ldg(p.group_indptr) || r >= __ldg(p.group_indptr + num_groups)) return;
+  int lo = 0, hi = num_groups;  // r's group: the last g with group_indptr[g] <= r
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(p.group_indptr + mid) <= r) lo = mid;
+    else hi = mid;
+  }
+  const int first = __ldg(p.group_indptr + lo);
+  const int members = __ldg(p.group_indptr + lo + 1) - first, k = r - first;
+  const int total = __ldg(p.prefix_lens + r) + (__ldg(p.q_indptr + r + 1) - __ldg(p.q_indptr + r));
+  const int nb = min(p.max_blocks, (max(total, 0) + (1 << p.bs_shift) - 1) >> p.bs_shift);
+  const int ws = min(max(__ldg(p.group_shared + lo), 0) >> p.bs_shift, p.max_blocks);
+  const int n_own = max(nb - ws, 0);
+  const int n_shared = ws > k ? (ws - k + members - 1) / members : 0;
+  for (int t = blockIdx.x; t < n_own + n_shared; t += gridDim.x) {
+    const int row = t < n_own ? r : first;
+    const int i = t < n_own ? ws + t : k + (t - n_own) * members;
+    const int blk = __ldg(p.block_tables + (int64_t)row * p.max_blocks + i);
+    if (blk < 0 || blk >= p.num_blocks) continue;
+    const uint4* src = v + (int64_t)blk * block_vec;
+    uint4* dst = v16 + (int64_t)blk * block_vec;
+    for (int u0 = threadIdx.x; u0 < block_vec; u0 += 8 * 256) {
+      uint4 x[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if (u0 + e * 256 < block_vec) x[e] = __ldg(src + u0 + e * 256);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if (u0 + e * 256 < block_vec) {
+          x[e].x = to_f16x2<true>(x[e].x);
+          x[e].y = to_f16x2<true>(x[e].y);
+          x[e].z = to_f16x2<true>(x[e].z);
+          x[e].w = to_f16x2<true>(x[e].w);
+          dst[u0 + e * 256] = x[e];
+        }
+      }
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_widen_v(const void* v_cache, void* v16, const ExtendParams& p, int num_groups,
+                           int head_dim, int block_size, int max_total_len, cudaStream_t stream) {
+  if (!v_cache || !v16 || !p.group_indptr || !p.group_shared || num_groups <= 0 || p.batch <= 0)
+    return cudaErrorInvalidValue;
+  const int block_vec = p.num_kv_heads * block_size * head_dim * 2 / 16;
+  // a request's list is at most its own blocks plus its share of the shared
+  // ones, both bounded by its table; about 16 blocks per CTA at the hint's length
+  const int max_nb = std::min(p.max_blocks, (std::max(max_total_len, 1) + block_size - 1) / block_size);
+  dim3 grid((unsigned)std::max(1, std::min(8, (max_nb + 15) / 16)), (unsigned)p.batch);
+  if (grid.y > 65535) return cudaErrorInvalidValue;
+  widen_v_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(v_cache),
+                                           static_cast<uint4*>(v16), p, num_groups, block_vec);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_extend(const CUtensorMap& kmap, const CUtensorMap& vmap, const CUtensorMap& qmap,
                           const CUtensorMap& omap, const ExtendParams& p, int head_dim,

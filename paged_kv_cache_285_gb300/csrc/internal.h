@@ -9,7 +9,14 @@
 
 namespace pkv {
 
-enum : int { DT_F16 = 0, DT_BF16 = 1, DT_E4M3 = 2 };
+enum : int {
+  DT_F16 = 0,
+  DT_BF16 = 1,
+  DT_E4M3 = 2,
+  // shared-prefix extend over a bf16 cache whose V pages were widened to f16
+  // beforehand (widen_v_kernel): K read as bf16, V from the f16 shadow pool
+  DT_BF16_V16 = 3
+};
 
 constexpr int kSubTokens = 16;  // tokens per staged K/V tile (one MMA row block)
 
@@ -217,5 +224,12 @@ cudaError_t launch_extend_shared(const CUtensorMap& kmap, const CUtensorMap& vma
                                  const ExtendParams& p, int head_dim, int cache_dt, int act_dt,
                                  cudaStream_t stream);
 bool extend_supported(int head_dim, int cache_dt, int act_dt, int group);
+// The V pages a shared-prefix extend reads (each group's shared blocks through
+// its first member's table, every request's own blocks through its own),
+// widened from bf16 to f16 into `v16`, a pool of the cache's shape and block
+// ids.  p: the call's ExtendParams (tables, lengths, groups).  Pages that are
+// out of the pool are skipped (the extend kernel reports them).
+cudaError_t launch_widen_v(const void* v_cache, void* v16, const ExtendParams& p, int num_groups,
+                           int head_dim, int block_size, int max_total_len, cudaStream_t stream);
 
 }  // namespace pkv

@@ -174,10 +174,10 @@ def test_chain_hash_and_extend_append_argument_errors(lib):
 
 def test_shared_prefix_extend_argument_errors(lib):
     # every case is refused (or empty) before anything is enqueued
-    call = lambda batch=2, groups=1, rows=10, gi=FAKE, gs=FAKE, hq=8, scale=0.1, desc=None: \
-        lib.pkv_paged_extend_attn_shared_prefix(
+    call = lambda batch=2, groups=1, rows=10, gi=FAKE, gs=FAKE, hq=8, scale=0.1, desc=None, \
+        ws=None, ws_bytes=0: lib.pkv_paged_extend_attn_shared_prefix(
             ctypes.byref(desc or _desc()), FAKE, FAKE, FAKE, FAKE, 1, FAKE, FAKE, FAKE, 4, batch,
-            hq, scale, 20, gi, gs, groups, rows, 100, None, None)
+            hq, scale, 20, gi, gs, groups, rows, 100, None, ws, ws_bytes, None)
     assert call(groups=0) == 1                                # requests but no group
     assert call(groups=3) == 1                                # more groups than requests
     assert call(groups=-1) == 1
@@ -188,6 +188,16 @@ def test_shared_prefix_extend_argument_errors(lib):
     assert call(desc=_desc(head_dim=96)) == 2                 # unsupported head_dim
     assert call(batch=0, groups=0) == 0                       # empty batch: nothing to do
     assert call(rows=0) == 0                                  # no rows in any group
+    # the optional workspace of a bf16 cache: an f16 copy of the V pool, 256-byte aligned
+    need = lib.pkv_extend_shared_prefix_workspace_bytes(ctypes.byref(_desc()))
+    assert need == 8 * 2 * 16 * 128 * 2
+    assert call(ws=FAKE, ws_bytes=need - 1) == 3              # too small
+    assert call(ws=ctypes.c_void_p(0x10010), ws_bytes=need) == 3  # misaligned
+    # other caches take no workspace (a given one is not used)
+    assert lib.pkv_extend_shared_prefix_workspace_bytes(ctypes.byref(_desc(cache_dtype=0))) == 0
+    assert lib.pkv_extend_shared_prefix_workspace_bytes(ctypes.byref(_desc(cache_dtype=2))) == 0
+    assert call(desc=_desc(cache_dtype=2), ws=FAKE, ws_bytes=1, batch=0, groups=0) == 0
+    assert lib.pkv_extend_shared_prefix_workspace_bytes(ctypes.byref(_desc(head_dim=96))) == 0
 
 
 def test_binding_refuses_wrong_index_dtypes():

@@ -33,8 +33,14 @@ def grouped_extend_case(P, Sx, groups, shared, hq, hkv, hd, bs, cdt, adt, seed):
     return case
 
 
-def run_shared(case, groups, shared, max_group_rows=None, lse=True):
+def run_shared(case, groups, shared, max_group_rows=None, lse=True, workspace=False):
+    """workspace: give the call its optional workspace (bf16 caches widen their V
+    pages into it first), filled with 0xFF bytes (NaN halves) beforehand."""
     rows, hq, _ = case.q.shape
+    ws = None
+    if workspace:
+        nbytes = pkv.extend_shared_prefix_workspace_bytes(case.k_cache, case.k_scale, case.v_scale)
+        ws = torch.full((max(nbytes, 256),), 0xFF, dtype=torch.uint8, device="cuda")
     out = torch.full_like(case.q, float("nan"))
     lse_t = torch.full((rows, hq), float("nan"), dtype=torch.float32, device="cuda") if lse else None
     qi = case.q_indptr.cpu()
@@ -46,7 +52,7 @@ def run_shared(case, groups, shared, max_group_rows=None, lse=True):
         case.k_cache, case.v_cache, case.q, out, case.q_indptr, case.prefix_lens,
         case.block_tables, gi.to("cuda"), torch.tensor(shared, dtype=torch.int32, device="cuda"),
         case.sm_scale, max_group_rows, int(tot.max()), k_scale=case.k_scale, v_scale=case.v_scale,
-        lse_out=lse_t)
+        lse_out=lse_t, workspace=ws)
     torch.cuda.synchronize()
     return out, lse_t
 
@@ -96,6 +102,36 @@ def test_shared_prefix_extend_matches_oracle(cfg):
                                seed=sum(P) + sum(Sx) + hq + hd)
     out, lse = run_shared(case, groups, shared)
     check(case, out, lse, str(cfg), fp8=(cdt == E4M3))
+    assert pkv.get_device_error() == 0
+
+
+@pytest.mark.parametrize("cfg", CASES, ids=lambda c: f"P{c[0][:3]}-g{c[2]}-W{c[3]}-h{c[4]}x{c[5]}-"
+                                                     f"bs{c[6]}-{c[7]}{c[8]}-hd{c[9]}")
+def test_workspace_gives_the_same_bits(cfg):
+    # a bf16 cache's V pages widened to f16 once per call (into the workspace) and
+    # read from there, against the per-tile conversion in shared memory: the same
+    # rounding, so the same output and LSE bits; other caches take no workspace
+    P, Sx, groups, shared, hq, hkv, bs, cdt, adt, hd = cfg
+    case = grouped_extend_case(P, Sx, groups, shared, hq, hkv, hd, bs, cdt, adt,
+                               seed=sum(P) + sum(Sx) + hq + hd + 1)
+    nbytes = pkv.extend_shared_prefix_workspace_bytes(case.k_cache, case.k_scale, case.v_scale)
+    v = case.v_cache
+    assert nbytes == ((v.numel() * 2 + 255) // 256 * 256 if cdt == BF16 else 0)
+    out_a, lse_a = run_shared(case, groups, shared)
+    out_b, lse_b = run_shared(case, groups, shared, workspace=True)
+    assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
+    assert torch.equal(lse_a.view(torch.int32), lse_b.view(torch.int32))
+    assert pkv.get_device_error() == 0
+
+
+def test_workspace_on_the_benchmark_workload():
+    # 256 requests over one shared 1,900-token prefix: every output bit the same
+    # with the V pages widened once per call
+    case = W.shared_prefix_extend(device="cuda")
+    out_a, lse_a = run_shared(case, [0, 256], [1900])
+    out_b, lse_b = run_shared(case, [0, 256], [1900], workspace=True)
+    assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
+    assert torch.equal(lse_a.view(torch.int32), lse_b.view(torch.int32))
     assert pkv.get_device_error() == 0
 
 
