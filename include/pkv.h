@@ -379,17 +379,19 @@ pkv_status pkv_paged_extend_attn(const pkv_cache_desc* desc, const void* k_cache
  *                    it sizes the grid.
  * workspace:         NULL, or pkv_extend_shared_prefix_workspace_bytes()
  *                    bytes of device memory, 256-byte aligned (any contents;
- *                    the size is 0 unless the cache is bf16).  With a bf16
- *                    cache the kernel feeds V to the tensor cores as f16 (P is
- *                    f16), which it otherwise converts tile by tile in shared
- *                    memory; with a workspace, the call first widens the V
- *                    pages it reads (each group's shared blocks once, every
- *                    request's own blocks) into an f16 copy of the V pool
- *                    there, and the kernel reads V from it.  The same
- *                    rounding either way: the results are bit-identical.  A
- *                    workspace smaller than the size, or misaligned, gives
- *                    PKV_ERR_WORKSPACE.  Calls that run at the same time
- *                    need workspaces of their own.
+ *                    the size is 0 for an f16 cache).  The tensor cores take
+ *                    P as f16, so a bf16 cache's V tiles, and an fp8 cache's K
+ *                    and V tiles, are otherwise converted to f16 tile by tile
+ *                    in shared memory.  With a workspace, the call first
+ *                    widens the pages it reads (each group's shared blocks
+ *                    once, every request's own blocks) into f16 copies of
+ *                    those pools there -- V for bf16, K and V for fp8 (twice
+ *                    an fp8 cache's size: memory traded for speed) -- and the
+ *                    kernel reads them from it.  The same conversions either
+ *                    way: the results are bit-identical.  A workspace smaller
+ *                    than the size, or misaligned, gives PKV_ERR_WORKSPACE.
+ *                    Calls that run at the same time need workspaces of their
+ *                    own.
  * Everything else as pkv_paged_extend_attn.
  * Device-side checks: a group whose request range or rows are not valid, rows
  * beyond max_group_rows, and a request whose prefix is shorter than W_g or
@@ -406,8 +408,8 @@ pkv_status pkv_paged_extend_attn_shared_prefix(
     int32_t max_total_len, float* lse_out, void* workspace, size_t workspace_bytes,
     cudaStream_t stream);
 /* Bytes of the optional workspace of pkv_paged_extend_attn_shared_prefix: the
- * size of the V pool in 16-bit elements for a bf16 cache, 0 for other caches
- * (and for an invalid desc). */
+ * V pool in 16-bit elements for a bf16 cache, the K and V pools in 16-bit
+ * elements for an fp8 cache, 0 for an f16 cache (and for an invalid desc). */
 size_t pkv_extend_shared_prefix_workspace_bytes(const pkv_cache_desc* desc);
 
 /* ---------------------------------------------------------------------------

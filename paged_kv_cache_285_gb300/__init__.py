@@ -411,7 +411,8 @@ def paged_extend_attn(k_cache, v_cache, q, out, q_indptr, prefix_lens, block_tab
 
 def extend_shared_prefix_workspace_bytes(k_cache, k_scale=1.0, v_scale=1.0) -> int:
     """pkv_extend_shared_prefix_workspace_bytes: the optional workspace of
-    paged_extend_attn_shared_prefix (an f16 copy of a bf16 cache's V pool; 0 otherwise)."""
+    paged_extend_attn_shared_prefix (f16 copies of a bf16 cache's V pool or of an fp8
+    cache's K and V pools; 0 for an f16 cache)."""
     lib = load()
     desc = _desc(k_cache, k_scale, v_scale)
     return int(lib.pkv_extend_shared_prefix_workspace_bytes(ctypes.byref(desc)))
@@ -425,7 +426,8 @@ def paged_extend_attn_shared_prefix(k_cache, v_cache, q, out, q_indptr, prefix_l
     (group_indptr int32 [G+1], consecutive requests) sharing the blocks of their first
     group_shared_lens[g] tokens (int32 [G]); the groups' rows are packed into shared tiles.
     workspace: None, or a uint8 device tensor of extend_shared_prefix_workspace_bytes() bytes
-    (a bf16 cache's V pages are then widened to f16 once per call instead of per tile)."""
+    (the pages of a bf16 or fp8 cache are then widened to f16 once per call instead of per
+    tile)."""
     _need(torch.int32, q_indptr=q_indptr, prefix_lens=prefix_lens, block_tables=block_tables,
           group_indptr=group_indptr, group_shared_lens=group_shared_lens)
     rows, hq, batch = _extend_shapes(k_cache, v_cache, q, out, q_indptr, prefix_lens,

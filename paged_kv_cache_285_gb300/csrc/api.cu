@@ -632,12 +632,17 @@ struct ExtendGroups {
 // Extend, optionally with the suffix's K/V (k_new/v_new, [rows][Hkv][D] in
 // the act dtype) written into the cache before the extend kernel runs, or
 // (groups) with the rows of each group's requests packed into shared tiles.
-// Workspace the shared-prefix extend can use over a bf16 cache: an f16 copy of
-// the V pool (the same block ids), into which the call widens the V pages it
-// reads, so that the kernel takes V as f16 instead of converting every tile.
-static size_t shared_prefix_v16_bytes(const pkv_cache_desc* d) {
-  if (d->cache_dtype != PKV_BF16) return 0;
+// Workspace the shared-prefix extend can use: f16 copies of the pools (the same
+// block ids) into which the call widens the pages it reads, so that the kernel
+// takes them as f16 instead of converting every tile -- the V pool of a bf16
+// cache, the K and V pools of an fp8 cache (K first); none for an f16 cache.
+static size_t shared_prefix_pool16_bytes(const pkv_cache_desc* d) {
   return align256((size_t)d->num_blocks * d->num_kv_heads * d->block_size * d->head_dim * 2);
+}
+static size_t shared_prefix_widen_bytes(const pkv_cache_desc* d) {
+  if (d->cache_dtype == PKV_BF16) return shared_prefix_pool16_bytes(d);
+  if (d->cache_dtype == PKV_FP8_E4M3) return 2 * shared_prefix_pool16_bytes(d);
+  return 0;
 }
 
 static pkv_status extend_common(const pkv_cache_desc* desc, const void* k_cache,
@@ -662,9 +667,9 @@ static pkv_status extend_common(const pkv_cache_desc* desc, const void* k_cache,
     return PKV_ERR_UNSUPPORTED;
   // plain extend needs no scratch (pkv_extend_workspace_bytes is 0); the
   // shared-prefix call may take one to widen a bf16 cache's V pages first
-  const size_t v16_bytes = groups ? shared_prefix_v16_bytes(desc) : 0;
-  const bool widen = groups && workspace != nullptr && v16_bytes > 0;
-  if (widen && (workspace_bytes < v16_bytes || !aligned(workspace, 256))) return PKV_ERR_WORKSPACE;
+  const size_t widen_bytes = groups ? shared_prefix_widen_bytes(desc) : 0;
+  const bool widen = groups && workspace != nullptr && widen_bytes > 0;
+  if (widen && (workspace_bytes < widen_bytes || !aligned(workspace, 256))) return PKV_ERR_WORKSPACE;
   if (groups) {
     if (groups->num_groups < 0 || groups->max_group_rows < 0 || groups->num_groups > batch)
       return PKV_ERR_INVALID_ARG;
@@ -716,15 +721,20 @@ static pkv_status extend_common(const pkv_cache_desc* desc, const void* k_cache,
   if (groups) {
     int cache_dt = (int)desc->cache_dtype;
     if (widen) {
-      // the V pages the call reads, widened to f16 in the workspace (same
-      // block ids), then read by the kernel through a map over that pool
+      // the pages the call reads, widened to f16 in the workspace (same block
+      // ids), then read by the kernel through maps over those pools; the
+      // scales of an fp8 cache stay folded into p's softmax and output scales
       pkv_cache_desc d16 = *desc;
       d16.cache_dtype = PKV_F16;
-      if ((st = make_page_map(&vmap, workspace, &d16)) != PKV_OK) return st;
-      e = launch_widen_v(v_cache, workspace, p, groups->num_groups, desc->head_dim,
-                         desc->block_size, max_total_len, stream);
+      const bool fp8 = desc->cache_dtype == PKV_FP8_E4M3;
+      void* k16 = fp8 ? workspace : nullptr;
+      void* v16 = static_cast<uint8_t*>(workspace) + (fp8 ? shared_prefix_pool16_bytes(desc) : 0);
+      if (fp8 && (st = make_page_map(&kmap, k16, &d16)) != PKV_OK) return st;
+      if ((st = make_page_map(&vmap, v16, &d16)) != PKV_OK) return st;
+      e = launch_widen(fp8 ? DT_E4M3 : DT_BF16, k_cache, v_cache, k16, v16, p,
+                       groups->num_groups, desc->head_dim, desc->block_size, max_total_len, stream);
       if (e != cudaSuccess) return PKV_ERR_CUDA;
-      cache_dt = DT_BF16_V16;
+      cache_dt = fp8 ? DT_E4M3_W16 : DT_BF16_V16;
     }
     e = launch_extend_shared(kmap, vmap, qmap, omap, p, desc->head_dim, cache_dt, (int)act_dtype,
                              stream);
@@ -778,7 +788,7 @@ pkv_status pkv_paged_extend_attn(const pkv_cache_desc* desc, const void* k_cache
 
 size_t pkv_extend_shared_prefix_workspace_bytes(const pkv_cache_desc* desc) {
   if (check_desc(desc) != PKV_OK) return 0;
-  return shared_prefix_v16_bytes(desc);
+  return shared_prefix_widen_bytes(desc);
 }
 
 pkv_status pkv_paged_extend_attn_shared_prefix(

@@ -88,8 +88,8 @@ struct ExtCfg {
   // S = Q K^T runs in f16 for fp8 caches: K codes widen to f16 with one
   // convert per pair, and bf16 queries (QCVT) are converted to f16 once per
   // item instead of K to bf16 at every key tile
-  static constexpr bool QCVT = FP8 && (AT == DT_BF16);
-  static constexpr bool QK_BF16 = !FP8 && (AT == DT_BF16);
+  static constexpr bool QCVT = (FP8 || CT == DT_E4M3_W16) && (AT == DT_BF16);
+  static constexpr bool QK_BF16 = !FP8 && CT != DT_E4M3_W16 && (AT == DT_BF16);
   static constexpr int NCH = HD / 64;           // 64-element column blocks per 16-bit row
   static constexpr int NST = HD == 64 ? 3 : 2;  // K and V ring depth
   static constexpr int T16 = BM * HD * 2;       // a 16-bit tile (Q, K or V): 16 or 32 KB
@@ -1178,8 +1178,9 @@ cudaError_t launch_extend_any(const CUtensorMap& kmap, const CUtensorMap& vmap, 
                               const CUtensorMap& omap, const ExtendParams& p,
                               const ExtendPartialParams& pp, int head_dim, int cache_dt, int act_dt,
                               cudaStream_t stream) {
-  // a bf16 cache with its V pages widened beforehand is a bf16 cache here
-  const int checked_dt = cache_dt == DT_BF16_V16 ? DT_BF16 : cache_dt;
+  // caches whose pages were widened beforehand are checked as what they hold
+  const int checked_dt =
+      cache_dt == DT_BF16_V16 ? DT_BF16 : (cache_dt == DT_E4M3_W16 ? DT_E4M3 : cache_dt);
   if (!extend_supported(head_dim, checked_dt, act_dt, p.group)) return cudaErrorInvalidValue;
   if (p.num_items <= 0 || p.num_ctas <= 0 || p.tok != BM / p.group) return cudaErrorInvalidValue;
 #define PKV_EXT(HD, CT, AT)                                    \
@@ -1188,6 +1189,10 @@ cudaError_t launch_extend_any(const CUtensorMap& kmap, const CUtensorMap& vmap, 
   if constexpr (SX && !PP) {
     PKV_EXT(128, DT_BF16_V16, DT_BF16)
     PKV_EXT(64, DT_BF16_V16, DT_BF16)
+    PKV_EXT(128, DT_E4M3_W16, DT_F16)
+    PKV_EXT(128, DT_E4M3_W16, DT_BF16)
+    PKV_EXT(64, DT_E4M3_W16, DT_F16)
+    PKV_EXT(64, DT_E4M3_W16, DT_BF16)
   }
   PKV_EXT(128, DT_F16, DT_F16)
   PKV_EXT(128, DT_BF16, DT_BF16)
@@ -1201,20 +1206,53 @@ cudaError_t launch_extend_any(const CUtensorMap& kmap, const CUtensorMap& vmap, 
   return cudaErrorInvalidValue;
 }
 
-// V pages of a shared-prefix extend widened from bf16 to f16 into a shadow
-// pool with the cache's block ids, so that the extend kernel reads V as f16
-// and its converter warps only zero the keys past a segment's end.  Request r
-// (the k-th member of its group of n) widens its own blocks, from the group's
-// shared prefix to its last key, and every n-th of the group's shared blocks
-// from the k-th on (read through the group's first member's table), so a long
-// shared prefix is spread over the members.  CTA (x, r) takes every
-// gridDim.x-th block of r's list from the x-th; each thread moves 8 16-byte
-// vectors of a block in one round trip.  The same conversion as the converter
-// warps' (round to nearest, +-inf beyond the f16 range), so either path gives
-// the same bits.
-__global__ void __launch_bounds__(256) widen_v_kernel(const uint4* __restrict__ v,
-                                                      uint4* __restrict__ v16, const ExtendParams p,
-                                                      int num_groups, int block_vec) {
+// Pages of a shared-prefix extend widened to f16 into shadow pools with the
+// cache's block ids, so that the extend kernel reads them as f16 and its
+// converter warps only zero the keys past a segment's end: a bf16 cache's V
+// pages (SRC = DT_BF16), or an fp8 cache's K and V pages (SRC = DT_E4M3).
+// Request r (the k-th member of its group of n) widens its own blocks, from
+// the group's shared prefix to its last key, and every n-th of the group's
+// shared blocks from the k-th on (read through the group's first member's
+// table), so a long shared prefix is spread over the members.  CTA (x, r)
+// takes every gridDim.x-th block of r's list from the x-th.  The same
+// conversions as the converter warps' (bf16: round to nearest, +-inf beyond
+// the f16 range; e4m3: exact), so either path gives the same bits.
+template <int SRC>
+__device__ __forceinline__ void widen_block(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                            int in_vec) {
+  // in_vec 16-byte input vectors: bf16 -> one f16 vector each, e4m3 -> two
+  for (int u0 = threadIdx.x; u0 < in_vec; u0 += 8 * 256) {
+    uint4 x[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      if (u0 + e * 256 < in_vec) x[e] = __ldg(src + u0 + e * 256);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int u = u0 + e * 256;
+      if (u < in_vec) {
+        if constexpr (SRC == DT_BF16) {
+          x[e].x = to_f16x2<true>(x[e].x);
+          x[e].y = to_f16x2<true>(x[e].y);
+          x[e].z = to_f16x2<true>(x[e].z);
+          x[e].w = to_f16x2<true>(x[e].w);
+          dst[u] = x[e];
+        } else {
+          uint4 lo, hi;
+          widen16<DT_F16>(x[e], lo, hi);
+          dst[2 * u] = lo;
+          dst[2 * u + 1] = hi;
+        }
+      }
+    }
+  }
+}
+
+template <int SRC>
+__global__ void __launch_bounds__(256) widen_kernel(const uint4* __restrict__ k,
+                                                    const uint4* __restrict__ v,
+                                                    uint4* __restrict__ k16, uint4* __restrict__ v16,
+                                                    const ExtendParams p, int num_groups,
+                                                    int in_vec) {
   const int r = blockIdx.y;
   if (r < __ldg(p.group_indptr) || r >= __ldg(p.group_indptr + num_groups)) return;
   int lo = 0, hi = num_groups;  // r's group: the last g with group_indptr[g] <= r
@@ -1224,52 +1262,47 @@ __global__ void __launch_bounds__(256) widen_v_kernel(const uint4* __restrict__ 
     else hi = mid;
   }
   const int first = __ldg(p.group_indptr + lo);
-  const int members = __ldg(p.group_indptr + lo + 1) - first, k = r - first;
+  const int members = __ldg(p.group_indptr + lo + 1) - first, kk = r - first;
   const int total = __ldg(p.prefix_lens + r) + (__ldg(p.q_indptr + r + 1) - __ldg(p.q_indptr + r));
   const int nb = min(p.max_blocks, (max(total, 0) + (1 << p.bs_shift) - 1) >> p.bs_shift);
   const int ws = min(max(__ldg(p.group_shared + lo), 0) >> p.bs_shift, p.max_blocks);
   const int n_own = max(nb - ws, 0);
-  const int n_shared = ws > k ? (ws - k + members - 1) / members : 0;
+  const int n_shared = ws > kk ? (ws - kk + members - 1) / members : 0;
+  const int out_vec = SRC == DT_BF16 ? in_vec : 2 * in_vec;
   for (int t = blockIdx.x; t < n_own + n_shared; t += gridDim.x) {
     const int row = t < n_own ? r : first;
-    const int i = t < n_own ? ws + t : k + (t - n_own) * members;
+    const int i = t < n_own ? ws + t : kk + (t - n_own) * members;
     const int blk = __ldg(p.block_tables + (int64_t)row * p.max_blocks + i);
     if (blk < 0 || blk >= p.num_blocks) continue;
-    const uint4* src = v + (int64_t)blk * block_vec;
-    uint4* dst = v16 + (int64_t)blk * block_vec;
-    for (int u0 = threadIdx.x; u0 < block_vec; u0 += 8 * 256) {
-      uint4 x[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e)
-        if (u0 + e * 256 < block_vec) x[e] = __ldg(src + u0 + e * 256);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        if (u0 + e * 256 < block_vec) {
-          x[e].x = to_f16x2<true>(x[e].x);
-          x[e].y = to_f16x2<true>(x[e].y);
-          x[e].z = to_f16x2<true>(x[e].z);
-          x[e].w = to_f16x2<true>(x[e].w);
-          dst[u0 + e * 256] = x[e];
-        }
-      }
-    }
+    if constexpr (SRC == DT_E4M3)
+      widen_block<SRC>(k + (int64_t)blk * in_vec, k16 + (int64_t)blk * out_vec, in_vec);
+    widen_block<SRC>(v + (int64_t)blk * in_vec, v16 + (int64_t)blk * out_vec, in_vec);
   }
 }
 
 }  // namespace
 
-cudaError_t launch_widen_v(const void* v_cache, void* v16, const ExtendParams& p, int num_groups,
-                           int head_dim, int block_size, int max_total_len, cudaStream_t stream) {
+cudaError_t launch_widen(int cache_dt, const void* k_cache, const void* v_cache, void* k16,
+                         void* v16, const ExtendParams& p, int num_groups, int head_dim,
+                         int block_size, int max_total_len, cudaStream_t stream) {
   if (!v_cache || !v16 || !p.group_indptr || !p.group_shared || num_groups <= 0 || p.batch <= 0)
     return cudaErrorInvalidValue;
-  const int block_vec = p.num_kv_heads * block_size * head_dim * 2 / 16;
+  if (cache_dt != DT_BF16 && (cache_dt != DT_E4M3 || !k_cache || !k16)) return cudaErrorInvalidValue;
+  const int elem = cache_dt == DT_BF16 ? 2 : 1;
+  const int in_vec = p.num_kv_heads * block_size * head_dim * elem / 16;
   // a request's list is at most its own blocks plus its share of the shared
   // ones, both bounded by its table; about 16 blocks per CTA at the hint's length
   const int max_nb = std::min(p.max_blocks, (std::max(max_total_len, 1) + block_size - 1) / block_size);
   dim3 grid((unsigned)std::max(1, std::min(8, (max_nb + 15) / 16)), (unsigned)p.batch);
   if (grid.y > 65535) return cudaErrorInvalidValue;
-  widen_v_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(v_cache),
-                                           static_cast<uint4*>(v16), p, num_groups, block_vec);
+  const uint4* k = static_cast<const uint4*>(k_cache);
+  const uint4* v = static_cast<const uint4*>(v_cache);
+  if (cache_dt == DT_BF16)
+    widen_kernel<DT_BF16><<<grid, 256, 0, stream>>>(k, v, static_cast<uint4*>(k16),
+                                                    static_cast<uint4*>(v16), p, num_groups, in_vec);
+  else
+    widen_kernel<DT_E4M3><<<grid, 256, 0, stream>>>(k, v, static_cast<uint4*>(k16),
+                                                    static_cast<uint4*>(v16), p, num_groups, in_vec);
   return cudaGetLastError();
 }
 

@@ -193,10 +193,11 @@ def test_shared_prefix_extend_argument_errors(lib):
     assert need == 8 * 2 * 16 * 128 * 2
     assert call(ws=FAKE, ws_bytes=need - 1) == 3              # too small
     assert call(ws=ctypes.c_void_p(0x10010), ws_bytes=need) == 3  # misaligned
-    # other caches take no workspace (a given one is not used)
+    # an fp8 cache: f16 copies of its K and V pools; an f16 cache takes none
+    assert lib.pkv_extend_shared_prefix_workspace_bytes(ctypes.byref(_desc(cache_dtype=2))) == \
+        2 * 8 * 2 * 16 * 128 * 2
+    assert call(desc=_desc(cache_dtype=2), ws=FAKE, ws_bytes=need) == 3  # too small for K and V
     assert lib.pkv_extend_shared_prefix_workspace_bytes(ctypes.byref(_desc(cache_dtype=0))) == 0
-    assert lib.pkv_extend_shared_prefix_workspace_bytes(ctypes.byref(_desc(cache_dtype=2))) == 0
-    assert call(desc=_desc(cache_dtype=2), ws=FAKE, ws_bytes=1, batch=0, groups=0) == 0
     assert lib.pkv_extend_shared_prefix_workspace_bytes(ctypes.byref(_desc(head_dim=96))) == 0
 
 

@@ -108,15 +108,16 @@ def test_shared_prefix_extend_matches_oracle(cfg):
 @pytest.mark.parametrize("cfg", CASES, ids=lambda c: f"P{c[0][:3]}-g{c[2]}-W{c[3]}-h{c[4]}x{c[5]}-"
                                                      f"bs{c[6]}-{c[7]}{c[8]}-hd{c[9]}")
 def test_workspace_gives_the_same_bits(cfg):
-    # a bf16 cache's V pages widened to f16 once per call (into the workspace) and
-    # read from there, against the per-tile conversion in shared memory: the same
-    # rounding, so the same output and LSE bits; other caches take no workspace
+    # a bf16 cache's V pages (an fp8 cache's K and V pages) widened to f16 once per
+    # call into the workspace and read from there, against the per-tile conversion
+    # in shared memory: the same rounding, so the same output and LSE bits; an f16
+    # cache takes no workspace
     P, Sx, groups, shared, hq, hkv, bs, cdt, adt, hd = cfg
     case = grouped_extend_case(P, Sx, groups, shared, hq, hkv, hd, bs, cdt, adt,
                                seed=sum(P) + sum(Sx) + hq + hd + 1)
     nbytes = pkv.extend_shared_prefix_workspace_bytes(case.k_cache, case.k_scale, case.v_scale)
-    v = case.v_cache
-    assert nbytes == ((v.numel() * 2 + 255) // 256 * 256 if cdt == BF16 else 0)
+    pool16 = (case.v_cache.numel() * 2 + 255) // 256 * 256  # elements x 2 bytes
+    assert nbytes == {BF16: pool16, E4M3: 2 * pool16}.get(cdt, 0)
     out_a, lse_a = run_shared(case, groups, shared)
     out_b, lse_b = run_shared(case, groups, shared, workspace=True)
     assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
