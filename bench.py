@@ -74,8 +74,9 @@ def src_hash(*rel):
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(name, sources):
-    """DRAM bytes per launch from a committed ncu summary, if the kernel source is unchanged."""
+def profiled_traffic(name, sources, key="dram_bytes_per_launch"):
+    """DRAM bytes per launch (the summary's `key` line) from a committed ncu summary, if the
+    kernel source is unchanged."""
     path = os.path.join(ROOT, "profiles", name)
     try:
         kv = {}
@@ -86,7 +87,7 @@ def profiled_traffic(name, sources):
                     kv[k.strip()] = v.strip().strip("`")
         if kv.get("source_sha256_16") != src_hash(*sources):
             return None
-        return float(kv["dram_bytes_per_launch"])
+        return float(kv[key])
     except Exception:
         return None
 
@@ -712,6 +713,22 @@ def run_extend_bench(args, dev, bf16, bf16_sus, peak_src):
     res["extend_shared_prefix"] = {
         "call": "paged_extend_attn_shared_prefix, groups [0, 256], shared 1,900 tokens",
         "peak_source": f"{peak_src} (bf16_tflops burst)", **shared}
+    # the same workload and useful flops through the call made for it (rows packed
+    # across the requests that share the prefix), with its workspace
+    ww = shared.get("bf16", {}).get("with_workspace")
+    if ww:
+        res["roofline_shared_prefix_call"] = {
+            "kernel": "paged_extend_attn_shared_prefix (one group; workspace: V pages widened to "
+                      "f16 once per call, the widening pass inside the timed call)",
+            "bound": "tensor", "achieved": ww["tflops"], "peak": bf16, "unit": "TFLOP/s",
+            "frac": ww["frac"], "peak_source": f"{peak_src} (bf16_tflops burst)",
+            "frac_of_nominal": ww["frac_of_nominal"], "nominal_peak": NOMINAL_BF16_TFLOPS,
+            "traffic": profiled_traffic(
+                "extend_kernel_shared_prefix_extend.md",
+                ["paged_kv_cache_285_gb300/csrc/extend.cu", "paged_kv_cache_285_gb300/csrc/ptx.cuh",
+                 "paged_kv_cache_285_gb300/csrc/tcgen05.cuh",
+                 "paged_kv_cache_285_gb300/csrc/internal.h#ExtendParams,ExtendPartialParams,FastDiv"],
+                key="dram_bytes_per_launch_shared_prefix_workspace")}
     return res
 
 
