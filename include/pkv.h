@@ -390,6 +390,7 @@ pkv_status pkv_paged_extend_attn(const pkv_cache_desc* desc, const void* k_cache
  *                    kernel reads them from it.  The same conversions either
  *                    way: the results are bit-identical.  A workspace smaller
  *                    than the size, or misaligned, gives PKV_ERR_WORKSPACE.
+ *                    Batches of more than 65,535 requests do not use it.
  *                    Calls that run at the same time need workspaces of their
  *                    own.
  * Everything else as pkv_paged_extend_attn.

@@ -668,7 +668,9 @@ static pkv_status extend_common(const pkv_cache_desc* desc, const void* k_cache,
   // plain extend needs no scratch (pkv_extend_workspace_bytes is 0); the
   // shared-prefix call may take one to widen a bf16 cache's V pages first
   const size_t widen_bytes = groups ? shared_prefix_widen_bytes(desc) : 0;
-  const bool widen = groups && workspace != nullptr && widen_bytes > 0;
+  // (the widening pass takes one CTA row per request: larger batches keep the
+  // per-tile conversion)
+  const bool widen = groups && workspace != nullptr && widen_bytes > 0 && batch <= 65535;
   if (widen && (workspace_bytes < widen_bytes || !aligned(workspace, 256))) return PKV_ERR_WORKSPACE;
   if (groups) {
     if (groups->num_groups < 0 || groups->max_group_rows < 0 || groups->num_groups > batch)
