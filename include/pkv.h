@@ -560,7 +560,8 @@ const char* pkv_status_string(pkv_status status);
  * Synchronises `stream`.  Returns PKV_OK and writes the word to *word. */
 pkv_status pkv_get_device_error(int32_t* word, int32_t clear, cudaStream_t stream);
 
-/* Library version, major*10000 + minor*100 + patch. */
+/* Library version, major*10000 + minor*100 + patch.  2.0.0: the shared-prefix
+ * extend takes a workspace (two arguments before the stream). */
 int32_t pkv_version(void);
 
 #ifdef __cplusplus

@@ -259,7 +259,7 @@ const char* pkv_status_string(pkv_status s) {
   }
 }
 
-int32_t pkv_version(void) { return 10000; }
+int32_t pkv_version(void) { return 20000; }
 
 pkv_status pkv_get_device_error(int32_t* word, int32_t clear, cudaStream_t stream) {
   if (!word) return PKV_ERR_INVALID_ARG;

@@ -41,7 +41,7 @@ def test_status_strings_and_version(lib):
     assert pkv.status_string(0) == "PKV_OK"
     assert pkv.status_string(3) == "PKV_ERR_WORKSPACE"
     assert pkv.status_string(99) == "PKV_ERR_UNKNOWN"
-    assert pkv.version() == 10000
+    assert pkv.version() == 20000
 
 
 def _desc(**kw):
