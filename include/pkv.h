@@ -385,10 +385,14 @@ pkv_status pkv_paged_extend_attn(const pkv_cache_desc* desc, const void* k_cache
  *                    in shared memory.  With a workspace, the call first
  *                    widens the pages it reads (each group's shared blocks
  *                    once, every request's own blocks) into f16 copies of
- *                    those pools there -- V for bf16, K and V for fp8 (twice
- *                    an fp8 cache's size: memory traded for speed) -- and the
- *                    kernel reads them from it.  The same conversions either
- *                    way: the results are bit-identical.  A workspace smaller
+ *                    those pools there -- V for bf16 (as f16), K and V for fp8
+ *                    (K in the queries' type, V as f16: twice an fp8 cache's
+ *                    size, memory traded for speed) -- and the kernel reads
+ *                    them from it.  The same conversions either way, so the
+ *                    results are bit-identical, except for an fp8 cache under
+ *                    bf16 queries: the per-tile path rounds the queries to f16
+ *                    for S = Q K^T, this one keeps them bf16 (K widened to
+ *                    bf16 exactly), no less accurate.  A workspace smaller
  *                    than the size, or misaligned, gives PKV_ERR_WORKSPACE.
  *                    Batches of more than 65,535 requests do not use it.
  *                    Calls that run at the same time need workspaces of their

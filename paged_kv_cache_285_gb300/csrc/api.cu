@@ -723,9 +723,10 @@ static pkv_status extend_common(const pkv_cache_desc* desc, const void* k_cache,
   if (groups) {
     int cache_dt = (int)desc->cache_dtype;
     if (widen) {
-      // the pages the call reads, widened to f16 in the workspace (same block
-      // ids), then read by the kernel through maps over those pools; the
-      // scales of an fp8 cache stay folded into p's softmax and output scales
+      // the pages the call reads, widened in the workspace (same block ids),
+      // then read by the kernel through maps over those pools: V as f16, an
+      // fp8 cache's K in the queries' type; the scales of an fp8 cache stay
+      // folded into p's softmax and output scales
       pkv_cache_desc d16 = *desc;
       d16.cache_dtype = PKV_F16;
       const bool fp8 = desc->cache_dtype == PKV_FP8_E4M3;
@@ -733,10 +734,12 @@ static pkv_status extend_common(const pkv_cache_desc* desc, const void* k_cache,
       void* v16 = static_cast<uint8_t*>(workspace) + (fp8 ? shared_prefix_pool16_bytes(desc) : 0);
       if (fp8 && (st = make_page_map(&kmap, k16, &d16)) != PKV_OK) return st;
       if ((st = make_page_map(&vmap, v16, &d16)) != PKV_OK) return st;
-      e = launch_widen(fp8 ? DT_E4M3 : DT_BF16, k_cache, v_cache, k16, v16, p,
+      e = launch_widen(fp8 ? DT_E4M3 : DT_BF16, (int)act_dtype, k_cache, v_cache, k16, v16, p,
                        groups->num_groups, desc->head_dim, desc->block_size, max_total_len, stream);
       if (e != cudaSuccess) return PKV_ERR_CUDA;
-      cache_dt = fp8 ? DT_E4M3_W16 : DT_BF16_V16;
+      // K bf16 (cache or widened) with f16 V; an fp8 cache under f16 queries
+      // is then an f16 cache
+      cache_dt = act_dtype == PKV_BF16 ? DT_BF16_V16 : DT_F16;
     }
     e = launch_extend_shared(kmap, vmap, qmap, omap, p, desc->head_dim, cache_dt, (int)act_dtype,
                              stream);

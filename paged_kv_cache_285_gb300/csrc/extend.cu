@@ -88,8 +88,8 @@ struct ExtCfg {
   // S = Q K^T runs in f16 for fp8 caches: K codes widen to f16 with one
   // convert per pair, and bf16 queries (QCVT) are converted to f16 once per
   // item instead of K to bf16 at every key tile
-  static constexpr bool QCVT = (FP8 || CT == DT_E4M3_W16) && (AT == DT_BF16);
-  static constexpr bool QK_BF16 = !FP8 && CT != DT_E4M3_W16 && (AT == DT_BF16);
+  static constexpr bool QCVT = FP8 && (AT == DT_BF16);
+  static constexpr bool QK_BF16 = !FP8 && (AT == DT_BF16);
   static constexpr int NCH = HD / 64;           // 64-element column blocks per 16-bit row
   static constexpr int NST = HD == 64 ? 3 : 2;  // K and V ring depth
   static constexpr int T16 = BM * HD * 2;       // a 16-bit tile (Q, K or V): 16 or 32 KB
@@ -1178,9 +1178,8 @@ cudaError_t launch_extend_any(const CUtensorMap& kmap, const CUtensorMap& vmap, 
                               const CUtensorMap& omap, const ExtendParams& p,
                               const ExtendPartialParams& pp, int head_dim, int cache_dt, int act_dt,
                               cudaStream_t stream) {
-  // caches whose pages were widened beforehand are checked as what they hold
-  const int checked_dt =
-      cache_dt == DT_BF16_V16 ? DT_BF16 : (cache_dt == DT_E4M3_W16 ? DT_E4M3 : cache_dt);
+  // K bf16 with V widened to f16 beforehand is checked as a bf16 cache
+  const int checked_dt = cache_dt == DT_BF16_V16 ? DT_BF16 : cache_dt;
   if (!extend_supported(head_dim, checked_dt, act_dt, p.group)) return cudaErrorInvalidValue;
   if (p.num_items <= 0 || p.num_ctas <= 0 || p.tok != BM / p.group) return cudaErrorInvalidValue;
 #define PKV_EXT(HD, CT, AT)                                    \
@@ -1189,10 +1188,6 @@ cudaError_t launch_extend_any(const CUtensorMap& kmap, const CUtensorMap& vmap, 
   if constexpr (SX && !PP) {
     PKV_EXT(128, DT_BF16_V16, DT_BF16)
     PKV_EXT(64, DT_BF16_V16, DT_BF16)
-    PKV_EXT(128, DT_E4M3_W16, DT_F16)
-    PKV_EXT(128, DT_E4M3_W16, DT_BF16)
-    PKV_EXT(64, DT_E4M3_W16, DT_F16)
-    PKV_EXT(64, DT_E4M3_W16, DT_BF16)
   }
   PKV_EXT(128, DT_F16, DT_F16)
   PKV_EXT(128, DT_BF16, DT_BF16)
@@ -1206,18 +1201,19 @@ cudaError_t launch_extend_any(const CUtensorMap& kmap, const CUtensorMap& vmap, 
   return cudaErrorInvalidValue;
 }
 
-// Pages of a shared-prefix extend widened to f16 into shadow pools with the
-// cache's block ids, so that the extend kernel reads them as f16 and its
-// converter warps only zero the keys past a segment's end: a bf16 cache's V
-// pages (SRC = DT_BF16), or an fp8 cache's K and V pages (SRC = DT_E4M3).
+// Pages of a shared-prefix extend widened into 16-bit shadow pools with the
+// cache's block ids, so that the extend kernel reads them without converting
+// and its converter warps only zero the keys past a segment's end: a bf16
+// cache's V pages to f16 (SRC = DT_BF16), or an fp8 cache's K pages to KOUT
+// (the queries' type, so that S = Q K^T needs no query conversion) and V
+// pages to f16 (SRC = DT_E4M3; every e4m3 value is exact in both).
 // Request r (the k-th member of its group of n) widens its own blocks, from
 // the group's shared prefix to its last key, and every n-th of the group's
 // shared blocks from the k-th on (read through the group's first member's
 // table), so a long shared prefix is spread over the members.  CTA (x, r)
-// takes every gridDim.x-th block of r's list from the x-th.  The same
-// conversions as the converter warps' (bf16: round to nearest, +-inf beyond
-// the f16 range; e4m3: exact), so either path gives the same bits.
-template <int SRC>
+// takes every gridDim.x-th block of r's list from the x-th.  bf16 -> f16
+// rounds to nearest (+-inf beyond the f16 range) as the converter warps do.
+template <int SRC, int OUT>
 __device__ __forceinline__ void widen_block(const uint4* __restrict__ src, uint4* __restrict__ dst,
                                             int in_vec) {
   // in_vec 16-byte input vectors: bf16 -> one f16 vector each, e4m3 -> two
@@ -1238,7 +1234,7 @@ __device__ __forceinline__ void widen_block(const uint4* __restrict__ src, uint4
           dst[u] = x[e];
         } else {
           uint4 lo, hi;
-          widen16<DT_F16>(x[e], lo, hi);
+          widen16<OUT>(x[e], lo, hi);
           dst[2 * u] = lo;
           dst[2 * u + 1] = hi;
         }
@@ -1247,7 +1243,7 @@ __device__ __forceinline__ void widen_block(const uint4* __restrict__ src, uint4
   }
 }
 
-template <int SRC>
+template <int SRC, int KOUT>
 __global__ void __launch_bounds__(256) widen_kernel(const uint4* __restrict__ k,
                                                     const uint4* __restrict__ v,
                                                     uint4* __restrict__ k16, uint4* __restrict__ v16,
@@ -1275,15 +1271,15 @@ __global__ void __launch_bounds__(256) widen_kernel(const uint4* __restrict__ k,
     const int blk = __ldg(p.block_tables + (int64_t)row * p.max_blocks + i);
     if (blk < 0 || blk >= p.num_blocks) continue;
     if constexpr (SRC == DT_E4M3)
-      widen_block<SRC>(k + (int64_t)blk * in_vec, k16 + (int64_t)blk * out_vec, in_vec);
-    widen_block<SRC>(v + (int64_t)blk * in_vec, v16 + (int64_t)blk * out_vec, in_vec);
+      widen_block<SRC, KOUT>(k + (int64_t)blk * in_vec, k16 + (int64_t)blk * out_vec, in_vec);
+    widen_block<SRC, DT_F16>(v + (int64_t)blk * in_vec, v16 + (int64_t)blk * out_vec, in_vec);
   }
 }
 
 }  // namespace
 
-cudaError_t launch_widen(int cache_dt, const void* k_cache, const void* v_cache, void* k16,
-                         void* v16, const ExtendParams& p, int num_groups, int head_dim,
+cudaError_t launch_widen(int cache_dt, int act_dt, const void* k_cache, const void* v_cache,
+                         void* k16, void* v16, const ExtendParams& p, int num_groups, int head_dim,
                          int block_size, int max_total_len, cudaStream_t stream) {
   if (!v_cache || !v16 || !p.group_indptr || !p.group_shared || num_groups <= 0 || p.batch <= 0)
     return cudaErrorInvalidValue;
@@ -1297,12 +1293,14 @@ cudaError_t launch_widen(int cache_dt, const void* k_cache, const void* v_cache,
   if (grid.y > 65535) return cudaErrorInvalidValue;
   const uint4* k = static_cast<const uint4*>(k_cache);
   const uint4* v = static_cast<const uint4*>(v_cache);
+  uint4* k16v = static_cast<uint4*>(k16);
+  uint4* v16v = static_cast<uint4*>(v16);
   if (cache_dt == DT_BF16)
-    widen_kernel<DT_BF16><<<grid, 256, 0, stream>>>(k, v, static_cast<uint4*>(k16),
-                                                    static_cast<uint4*>(v16), p, num_groups, in_vec);
+    widen_kernel<DT_BF16, DT_F16><<<grid, 256, 0, stream>>>(k, v, k16v, v16v, p, num_groups, in_vec);
+  else if (act_dt == DT_BF16)
+    widen_kernel<DT_E4M3, DT_BF16><<<grid, 256, 0, stream>>>(k, v, k16v, v16v, p, num_groups, in_vec);
   else
-    widen_kernel<DT_E4M3><<<grid, 256, 0, stream>>>(k, v, static_cast<uint4*>(k16),
-                                                    static_cast<uint4*>(v16), p, num_groups, in_vec);
+    widen_kernel<DT_E4M3, DT_F16><<<grid, 256, 0, stream>>>(k, v, k16v, v16v, p, num_groups, in_vec);
   return cudaGetLastError();
 }
 

@@ -13,13 +13,10 @@ enum : int {
   DT_F16 = 0,
   DT_BF16 = 1,
   DT_E4M3 = 2,
-  // shared-prefix extend over a bf16 cache whose V pages were widened to f16
-  // beforehand (widen_kernel): K read as bf16, V from the f16 shadow pool
-  DT_BF16_V16 = 3,
-  // shared-prefix extend over an fp8 cache whose K and V pages were widened to
-  // f16 beforehand: both read from the f16 shadow pools (the values are the
-  // codes, exactly; the scales stay folded into the softmax and output scales)
-  DT_E4M3_W16 = 4
+  // shared-prefix extend with K read as bf16 and V pages widened to f16
+  // beforehand (widen_kernel): a bf16 cache's K with its V shadow pool, or an
+  // fp8 cache's K and V shadow pools (bf16 queries)
+  DT_BF16_V16 = 3
 };
 
 constexpr int kSubTokens = 16;  // tokens per staged K/V tile (one MMA row block)
@@ -230,13 +227,13 @@ cudaError_t launch_extend_shared(const CUtensorMap& kmap, const CUtensorMap& vma
 bool extend_supported(int head_dim, int cache_dt, int act_dt, int group);
 // The pages a shared-prefix extend reads (each group's shared blocks through
 // its first member's table, every request's own blocks through its own),
-// widened to f16 into pools of the cache's shape and block ids: a bf16
-// cache's V pages into v16 (k16 unused), an fp8 cache's K and V pages into k16
-// and v16 (the codes' values, exactly).  p: the call's ExtendParams (tables,
-// lengths, groups).  Pages out of the pool are skipped (the extend kernel
-// reports them).
-cudaError_t launch_widen(int cache_dt, const void* k_cache, const void* v_cache, void* k16,
-                         void* v16, const ExtendParams& p, int num_groups, int head_dim,
+// widened into 16-bit pools of the cache's shape and block ids: a bf16 cache's
+// V pages into v16 as f16 (k16 unused); an fp8 cache's K pages into k16 in the
+// queries' type act_dt and its V pages into v16 as f16 (the codes' values,
+// exactly).  p: the call's ExtendParams (tables, lengths, groups).  Pages out
+// of the pool are skipped (the extend kernel reports them).
+cudaError_t launch_widen(int cache_dt, int act_dt, const void* k_cache, const void* v_cache,
+                         void* k16, void* v16, const ExtendParams& p, int num_groups, int head_dim,
                          int block_size, int max_total_len, cudaStream_t stream);
 
 }  // namespace pkv

@@ -108,10 +108,13 @@ def test_shared_prefix_extend_matches_oracle(cfg):
 @pytest.mark.parametrize("cfg", CASES, ids=lambda c: f"P{c[0][:3]}-g{c[2]}-W{c[3]}-h{c[4]}x{c[5]}-"
                                                      f"bs{c[6]}-{c[7]}{c[8]}-hd{c[9]}")
 def test_workspace_gives_the_same_bits(cfg):
-    # a bf16 cache's V pages (an fp8 cache's K and V pages) widened to f16 once per
-    # call into the workspace and read from there, against the per-tile conversion
-    # in shared memory: the same rounding, so the same output and LSE bits; an f16
-    # cache takes no workspace
+    # a bf16 cache's V pages (an fp8 cache's K and V pages) widened once per call
+    # into the workspace and read from there, against the per-tile conversion in
+    # shared memory: the same conversions, so the same output and LSE bits -- except
+    # for an fp8 cache under bf16 queries, whose K is widened to bf16 so that the
+    # queries need no rounding to f16 (as the per-tile path does): checked against
+    # the oracle and within rounding of the per-tile path; an f16 cache takes no
+    # workspace
     P, Sx, groups, shared, hq, hkv, bs, cdt, adt, hd = cfg
     case = grouped_extend_case(P, Sx, groups, shared, hq, hkv, hd, bs, cdt, adt,
                                seed=sum(P) + sum(Sx) + hq + hd + 1)
@@ -120,8 +123,13 @@ def test_workspace_gives_the_same_bits(cfg):
     assert nbytes == {BF16: pool16, E4M3: 2 * pool16}.get(cdt, 0)
     out_a, lse_a = run_shared(case, groups, shared)
     out_b, lse_b = run_shared(case, groups, shared, workspace=True)
-    assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
-    assert torch.equal(lse_a.view(torch.int32), lse_b.view(torch.int32))
+    if cdt == E4M3 and adt == BF16:
+        check(case, out_b, lse_b, str(cfg) + " with workspace", fp8=True)
+        assert np.max(np.abs(to_f64(out_a) - to_f64(out_b))) <= 1.6e-2  # two bf16 ulps at 1
+        assert torch.allclose(lse_a, lse_b, atol=1e-3, rtol=0)
+    else:
+        assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
+        assert torch.equal(lse_a.view(torch.int32), lse_b.view(torch.int32))
     assert pkv.get_device_error() == 0
 
 
