@@ -517,10 +517,11 @@ def _median(xs):
     return ys[n // 2] if n % 2 else 0.5 * (ys[n // 2 - 1] + ys[n // 2])
 
 
-def _time_extend_case(case, P, Sfx, n, flush, with_append):
+def _time_extend_case(case, P, Sfx, n, flush, with_append, ws=None):
     """Mean and median device time of paged_extend_attn on `case` (L2 flushed before each
-    call); with_append: also the step with the suffix's kv_append before it and the one-call
-    paged_extend_attn_append.  Returns a dict of lists of ms."""
+    call; `ws` its optional widening workspace); with_append: also the step with the
+    suffix's kv_append before it and the one-call paged_extend_attn_append.  Returns a dict
+    of lists of ms."""
     import paged_kv_cache_285_gb300 as pkv
     out = torch.empty_like(case.q)
     sc = dict(k_scale=case.k_scale, v_scale=case.v_scale)
@@ -532,7 +533,7 @@ def _time_extend_case(case, P, Sfx, n, flush, with_append):
     def extend():
         pkv.paged_extend_attn(case.k_cache, case.v_cache, case.q, out, case.q_indptr,
                               case.prefix_lens, case.block_tables, case.sm_scale, Sfx, P + Sfx,
-                              **sc)
+                              workspace=ws, **sc)
 
     def fused():
         pkv.paged_extend_attn_append(case.k_cache, case.v_cache, case.suffix_k, case.suffix_v,
@@ -600,6 +601,24 @@ def _time_extend_shared(case, groups, shared, max_group_rows, max_total, n, flus
     return ts
 
 
+def _extend_with_workspace(case, P, Sfx, n, flush, flops, bf16):
+    """paged_extend_attn with its optional widening workspace (each block read widened to
+    16 bits once per call; the widening pass inside the timed call), or None where the
+    cache dtype needs none."""
+    import paged_kv_cache_285_gb300 as pkv
+    wsb = pkv.extend_widen_workspace_bytes(case.k_cache, case.k_scale, case.v_scale)
+    if not wsb:
+        return None
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    tw = _time_extend_case(case, P, Sfx, n, flush, False, ws=ws)["extend"]
+    del ws
+    tw_mean = sum(tw) / n
+    tfw = flops / (tw_mean * 1e-3) / 1e12
+    return {"ms_per_call": round(tw_mean, 5), "ms_per_call_median": round(_median(tw), 5),
+            "tflops": round(tfw, 1), "frac": round(tfw / bf16, 4),
+            "frac_of_nominal": round(tfw / NOMINAL_BF16_TFLOPS, 4), "workspace_bytes": wsb}
+
+
 def run_extend_bench(args, dev, bf16, bf16_sus, peak_src):
     """paged_extend_attn on 256 requests x 100 suffix tokens over a shared 1,900-token
     prefix (useful causal flops only); the step with the suffix's kv_append as a
@@ -654,6 +673,16 @@ def run_extend_bench(args, dev, bf16, bf16_sus, peak_src):
                              "paged_kv_cache_285_gb300/csrc/tcgen05.cuh",
                              "paged_kv_cache_285_gb300/csrc/internal.h"
                              "#ExtendParams,ExtendPartialParams,FastDiv"])}}
+    ww = _extend_with_workspace(case, P, Sfx, n, flush, flops, bf16)
+    if ww:
+        # the widened kernel's DRAM bytes per launch (the widening pass not included)
+        ww["traffic"] = profiled_traffic(
+            "extend_kernel_shared_prefix_extend.md",
+            ["paged_kv_cache_285_gb300/csrc/extend.cu", "paged_kv_cache_285_gb300/csrc/ptx.cuh",
+             "paged_kv_cache_285_gb300/csrc/tcgen05.cuh",
+             "paged_kv_cache_285_gb300/csrc/internal.h#ExtendParams,ExtendPartialParams,FastDiv"],
+            key="dram_bytes_per_launch_workspace")
+        res["with_workspace"] = ww
     del case
     # the same workload over an fp8 cache (codes widened inside the kernel) and at d64
     for key, cdt, hd in (("extend_fp8", W.E4M3, 128), ("extend_d64", W.BF16, 64)):
@@ -676,6 +705,9 @@ def run_extend_bench(args, dev, bf16, bf16_sus, peak_src):
                                                                   k_scale=c.k_scale,
                                                                   v_scale=c.v_scale),
                     "cache_bytes": 2 * c.k_cache.numel() * c.k_cache.element_size()}
+        ww = _extend_with_workspace(c, P, Sfx, n, flush, fl, bf16)
+        if ww:
+            res[key]["with_workspace"] = ww
         del c
     # the same rows through the shared-prefix call: one group, the 1,900-token prompt shared
     # (118 whole blocks), the 256 x 100 rows packed into tiles without per-request padding

@@ -321,11 +321,25 @@ pkv_status pkv_paged_decode_attn_shared_prefix(
  * max_suffix_len / max_total_len: host-side upper bounds of S_b and P_b+S_b.
  * total_q_rows:  q_indptr[batch] (host value; sizes the grid).
  * lse_out:       nullable float [q_indptr[batch]][num_q_heads], natural log.
- * workspace:     unused (pass NULL, 0): pkv_extend_workspace_bytes() is 0 for
- *                every cache dtype.  An fp8 cache is read as codes and each
- *                K/V tile is widened inside the kernel (exactly: e4m3 fits
- *                f16 and bf16), with k_scale applied to the scores and
- *                v_scale to the output; no 16-bit copy of the cache is made.
+ * workspace:     optional: pkv_extend_workspace_bytes() is 0 for every cache
+ *                dtype, and NULL, 0 is always accepted.  An fp8 cache is then
+ *                read as codes and each K/V tile is widened inside the kernel
+ *                (exactly: e4m3 fits f16 and bf16), with k_scale applied to
+ *                the scores and v_scale to the output; the tensor cores take
+ *                P as f16, so a bf16 cache's V tiles are converted to f16 the
+ *                same way.  Given pkv_extend_widen_workspace_bytes() bytes or
+ *                more, 256-byte aligned (any contents), the call first widens
+ *                each cache block its requests read once (a block shared by
+ *                several requests included) into 16-bit copies of the pools
+ *                there -- V as f16 for bf16, and for fp8 also K in the
+ *                queries' type -- and the kernel reads those.  The same
+ *                conversions either way, so the results are bit-identical,
+ *                except for an fp8 cache under bf16 queries: the per-tile
+ *                path rounds the queries to f16 for S = Q K^T, this one keeps
+ *                them bf16 (K widened to bf16 exactly), no less accurate.  A
+ *                smaller or misaligned workspace, an f16 cache, and batches
+ *                of more than 65,535 requests take the per-tile path.  Calls
+ *                that run at the same time need workspaces of their own.
  * Device-side checks: a request whose rows q_indptr[b] .. q_indptr[b+1]-1
  * do not lie inside [0, total_q_rows) is not computed (nothing is written for
  * it), and suffix rows beyond max_suffix_len are not computed; both set
@@ -339,6 +353,11 @@ pkv_status pkv_paged_decode_attn_shared_prefix(
 size_t pkv_extend_workspace_bytes(const pkv_cache_desc* desc, int32_t batch,
                                   int32_t num_q_heads, int32_t total_q_rows,
                                   int32_t max_total_len);
+/* Bytes of the optional widening workspace of pkv_paged_extend_attn: the V
+ * pool in 16-bit elements for a bf16 cache (the K and V pools for an fp8
+ * cache), then int32 claims (a counter, and a flag and a list entry per block),
+ * each part 256-byte aligned; 0 for an f16 cache (and for an invalid desc). */
+size_t pkv_extend_widen_workspace_bytes(const pkv_cache_desc* desc);
 
 pkv_status pkv_paged_extend_attn(const pkv_cache_desc* desc, const void* k_cache,
                                  const void* v_cache, const void* q, void* out,
@@ -565,7 +584,9 @@ const char* pkv_status_string(pkv_status status);
 pkv_status pkv_get_device_error(int32_t* word, int32_t clear, cudaStream_t stream);
 
 /* Library version, major*10000 + minor*100 + patch.  2.0.0: the shared-prefix
- * extend takes a workspace (two arguments before the stream). */
+ * extend takes a workspace (two arguments before the stream).  2.1.0:
+ * pkv_extend_widen_workspace_bytes; the plain extend uses a workspace of that
+ * size (its signature unchanged). */
 int32_t pkv_version(void);
 
 #ifdef __cplusplus

@@ -33,7 +33,7 @@ __all__ = ["F16", "BF16", "FP8_E4M3", "PkvError", "CacheDesc", "lib_path", "load
            "paged_decode_attn_append", "RadixIndex", "NO_SPACE", "chain_hash",
            "paged_decode_attn_shared_prefix", "shared_prefix_decode_workspace_bytes",
            "paged_extend_attn_append", "paged_extend_attn_shared_prefix",
-           "extend_shared_prefix_workspace_bytes"]
+           "extend_shared_prefix_workspace_bytes", "extend_widen_workspace_bytes"]
 
 F16, BF16, FP8_E4M3 = 0, 1, 2
 NO_SPACE = 5  # PKV_ERR_NO_SPACE
@@ -105,6 +105,8 @@ def load():
         lib.pkv_paged_extend_attn_shared_prefix.restype = ctypes.c_int
         lib.pkv_extend_shared_prefix_workspace_bytes.argtypes = [D]
         lib.pkv_extend_shared_prefix_workspace_bytes.restype = SZ
+        lib.pkv_extend_widen_workspace_bytes.argtypes = [D]
+        lib.pkv_extend_widen_workspace_bytes.restype = SZ
         lib.pkv_status_string.argtypes = [ctypes.c_int]
         lib.pkv_status_string.restype = ctypes.c_char_p
         lib.pkv_get_device_error.argtypes = [ctypes.POINTER(I32), I32, P]
@@ -393,7 +395,9 @@ def extend_workspace_bytes(k_cache, batch, num_q_heads, total_q_rows, max_total_
 def paged_extend_attn(k_cache, v_cache, q, out, q_indptr, prefix_lens, block_tables, sm_scale,
                       max_suffix_len, max_total_len, k_scale=1.0, v_scale=1.0, lse_out=None,
                       workspace=None, stream=None):
-    """pkv_paged_extend_attn: q/out [sum S, Hq, D]; q_indptr int32 [B+1]; prefix_lens int32 [B]."""
+    """pkv_paged_extend_attn: q/out [sum S, Hq, D]; q_indptr int32 [B+1]; prefix_lens int32 [B];
+    workspace: None, or a uint8 device tensor of extend_widen_workspace_bytes() bytes or more
+    (the pages read are then widened to 16 bits once per block; smaller ones are not used)."""
     _need(torch.int32, q_indptr=q_indptr, prefix_lens=prefix_lens, block_tables=block_tables)
     rows, hq, batch = _extend_shapes(k_cache, v_cache, q, out, q_indptr, prefix_lens,
                                      block_tables, lse_out)
@@ -407,6 +411,15 @@ def paged_extend_attn(k_cache, v_cache, q, out, q_indptr, prefix_lens, block_tab
                                    int(max_total_len), _ptr(lse_out), _ptr(workspace), ws_bytes,
                                    _stream(stream))
     _check(st, "pkv_paged_extend_attn")
+
+
+def extend_widen_workspace_bytes(k_cache, k_scale=1.0, v_scale=1.0) -> int:
+    """pkv_extend_widen_workspace_bytes: the optional widening workspace of paged_extend_attn
+    (16-bit copies of a bf16 cache's V pool or of an fp8 cache's K and V pools, and the
+    per-block claims; 0 for an f16 cache)."""
+    lib = load()
+    desc = _desc(k_cache, k_scale, v_scale)
+    return int(lib.pkv_extend_widen_workspace_bytes(ctypes.byref(desc)))
 
 
 def extend_shared_prefix_workspace_bytes(k_cache, k_scale=1.0, v_scale=1.0) -> int:

@@ -259,7 +259,7 @@ const char* pkv_status_string(pkv_status s) {
   }
 }
 
-int32_t pkv_version(void) { return 20000; }
+int32_t pkv_version(void) { return 20100; }
 
 pkv_status pkv_get_device_error(int32_t* word, int32_t clear, cudaStream_t stream) {
   if (!word) return PKV_ERR_INVALID_ARG;
@@ -644,6 +644,13 @@ static size_t shared_prefix_widen_bytes(const pkv_cache_desc* d) {
   if (d->cache_dtype == PKV_FP8_E4M3) return 2 * shared_prefix_pool16_bytes(d);
   return 0;
 }
+// The plain extend's optional workspace: the same pools, then a counter, a
+// claim flag per block and a list of the blocks claimed (requests may share
+// blocks without the call knowing it).
+static size_t plain_widen_bytes(const pkv_cache_desc* d) {
+  const size_t pools = shared_prefix_widen_bytes(d);
+  return pools ? pools + align256((1 + 2 * (size_t)d->num_blocks) * sizeof(int32_t)) : 0;
+}
 
 static pkv_status extend_common(const pkv_cache_desc* desc, const void* k_cache,
                                 const void* v_cache, const void* k_new, const void* v_new,
@@ -665,8 +672,13 @@ static pkv_status extend_common(const pkv_cache_desc* desc, const void* k_cache,
   const int group = num_q_heads / desc->num_kv_heads;
   if (!extend_supported(desc->head_dim, (int)desc->cache_dtype, (int)act_dtype, group))
     return PKV_ERR_UNSUPPORTED;
-  // plain extend needs no scratch (pkv_extend_workspace_bytes is 0); the
-  // shared-prefix call may take one to widen a bf16 cache's V pages first
+  // no call needs scratch; either may take one to widen the pages it reads
+  // once instead of per tile (a plain call whose workspace is smaller than
+  // that, such as the 0 bytes of pkv_extend_workspace_bytes, does without)
+  const size_t plain_bytes = groups ? 0 : plain_widen_bytes(desc);
+  const bool widen_plain = !groups && workspace != nullptr && plain_bytes > 0 &&
+                           workspace_bytes >= plain_bytes && aligned(workspace, 256) &&
+                           batch <= 65535;
   const size_t widen_bytes = groups ? shared_prefix_widen_bytes(desc) : 0;
   // (the widening pass takes one CTA row per request: larger batches keep the
   // per-tile conversion)
@@ -770,8 +782,26 @@ static pkv_status extend_common(const pkv_cache_desc* desc, const void* k_cache,
     e = launch_append(ap, (int)desc->cache_dtype, (int)act_dtype, stream);
     if (e != cudaSuccess) return PKV_ERR_CUDA;
   }
-  e = launch_extend(kmap, vmap, qmap, omap, p, desc->head_dim, (int)desc->cache_dtype,
-                    (int)act_dtype, stream);
+  int cache_dt = (int)desc->cache_dtype;
+  if (widen_plain) {
+    // the pages the call reads, each block widened once (claimed in the
+    // workspace) into 16-bit pools read through maps over them
+    pkv_cache_desc d16 = *desc;
+    d16.cache_dtype = PKV_F16;
+    const bool fp8 = desc->cache_dtype == PKV_FP8_E4M3;
+    uint8_t* base = static_cast<uint8_t*>(workspace);
+    void* k16 = fp8 ? base : nullptr;
+    void* v16 = base + (fp8 ? shared_prefix_pool16_bytes(desc) : 0);
+    int32_t* claims = reinterpret_cast<int32_t*>(base + shared_prefix_widen_bytes(desc));
+    if (fp8 && (st = make_page_map(&kmap, k16, &d16)) != PKV_OK) return st;
+    if ((st = make_page_map(&vmap, v16, &d16)) != PKV_OK) return st;
+    e = launch_widen_claim(fp8 ? DT_E4M3 : DT_BF16, (int)act_dtype, k_cache, v_cache, k16, v16,
+                           claims, p, desc->head_dim, desc->block_size, max_total_len,
+                           ds->sm_count, stream);
+    if (e != cudaSuccess) return PKV_ERR_CUDA;
+    cache_dt = act_dtype == PKV_BF16 ? DT_BF16_V16 : DT_F16;
+  }
+  e = launch_extend(kmap, vmap, qmap, omap, p, desc->head_dim, cache_dt, (int)act_dtype, stream);
   return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
@@ -789,6 +819,11 @@ pkv_status pkv_paged_extend_attn(const pkv_cache_desc* desc, const void* k_cache
                        prefix_lens, block_tables, max_blocks_per_seq, batch, num_q_heads,
                        sm_scale, total_q_rows, max_suffix_len, max_total_len, lse_out, workspace,
                        workspace_bytes, stream);
+}
+
+size_t pkv_extend_widen_workspace_bytes(const pkv_cache_desc* desc) {
+  if (check_desc(desc) != PKV_OK) return 0;
+  return plain_widen_bytes(desc);
 }
 
 size_t pkv_extend_shared_prefix_workspace_bytes(const pkv_cache_desc* desc) {

@@ -1185,7 +1185,7 @@ cudaError_t launch_extend_any(const CUtensorMap& kmap, const CUtensorMap& vmap, 
 #define PKV_EXT(HD, CT, AT)                                    \
   if (head_dim == HD && cache_dt == CT && act_dt == AT)        \
     return launch_extend_t<HD, CT, AT, PP, SX>(kmap, vmap, qmap, omap, p, pp, stream);
-  if constexpr (SX && !PP) {
+  if constexpr (!PP) {
     PKV_EXT(128, DT_BF16_V16, DT_BF16)
     PKV_EXT(64, DT_BF16_V16, DT_BF16)
   }
@@ -1276,7 +1276,84 @@ __global__ void __launch_bounds__(256) widen_kernel(const uint4* __restrict__ k,
   }
 }
 
+// Plain extend: the pages each request reads (blocks 0 .. ceil((P + S) /
+// block_size) - 1 of its table), widened once per block although requests
+// may share blocks.  claims = [count][flag per block][list]: the claim pass
+// gives thread (x, r, t) block 256 x + t of request r; the first request to
+// set a block's flag (zeroed before the pass) appends it to the list.  The
+// widening pass then spreads the list over a grid of persistent CTAs, so that
+// the blocks of a shared prefix, which the requests that start first win, do
+// not queue up in those requests' CTAs.
+__global__ void __launch_bounds__(256) claim_kernel(int* claims, const ExtendParams p) {
+  const int r = blockIdx.y;
+  const int total = __ldg(p.prefix_lens + r) + (__ldg(p.q_indptr + r + 1) - __ldg(p.q_indptr + r));
+  const int nb = min(p.max_blocks, (max(total, 0) + (1 << p.bs_shift) - 1) >> p.bs_shift);
+  const int i = blockIdx.x * 256 + threadIdx.x;
+  int blk = -1;
+  if (i < nb) blk = __ldg(p.block_tables + (int64_t)r * p.max_blocks + i);
+  const bool won = blk >= 0 && blk < p.num_blocks && atomicCAS(claims + 1 + blk, 0, 1) == 0;
+  // one list slot reservation per warp
+  const unsigned m = __ballot_sync(0xffffffffu, won);
+  if (m == 0) return;
+  const int lane = threadIdx.x & 31, leader = __ffs(m) - 1;
+  int base = 0;
+  if (lane == leader) base = atomicAdd(claims, __popc(m));
+  base = __shfl_sync(0xffffffffu, base, leader);
+  if (won) claims[1 + p.num_blocks + base + __popc(m & ((1u << lane) - 1))] = blk;
+}
+
+template <int SRC, int KOUT>
+__global__ void __launch_bounds__(256) widen_list_kernel(const uint4* __restrict__ k,
+                                                         const uint4* __restrict__ v,
+                                                         uint4* __restrict__ k16,
+                                                         uint4* __restrict__ v16,
+                                                         const int* __restrict__ claims,
+                                                         int num_blocks, int in_vec) {
+  const int n = min(claims[0], num_blocks);
+  const int* list = claims + 1 + num_blocks;
+  const int out_vec = SRC == DT_BF16 ? in_vec : 2 * in_vec;
+  for (int j = blockIdx.x; j < n; j += gridDim.x) {
+    const int blk = list[j];
+    if constexpr (SRC == DT_E4M3)
+      widen_block<SRC, KOUT>(k + (int64_t)blk * in_vec, k16 + (int64_t)blk * out_vec, in_vec);
+    widen_block<SRC, DT_F16>(v + (int64_t)blk * in_vec, v16 + (int64_t)blk * out_vec, in_vec);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_widen_claim(int cache_dt, int act_dt, const void* k_cache,
+                               const void* v_cache, void* k16, void* v16, int* claims,
+                               const ExtendParams& p, int head_dim, int block_size,
+                               int max_total_len, int sm_count, cudaStream_t stream) {
+  if (!v_cache || !v16 || !claims || p.batch <= 0 || p.num_blocks <= 0 || sm_count <= 0)
+    return cudaErrorInvalidValue;
+  if (cache_dt != DT_BF16 && (cache_dt != DT_E4M3 || !k_cache || !k16)) return cudaErrorInvalidValue;
+  const int elem = cache_dt == DT_BF16 ? 2 : 1;
+  const int in_vec = p.num_kv_heads * block_size * head_dim * elem / 16;
+  const int max_nb = std::min(p.max_blocks, (std::max(max_total_len, 1) + block_size - 1) / block_size);
+  dim3 grid((unsigned)((max_nb + 255) / 256), (unsigned)p.batch);
+  if (grid.y > 65535) return cudaErrorInvalidValue;
+  cudaError_t e = cudaMemsetAsync(claims, 0, (size_t)(1 + p.num_blocks) * sizeof(int), stream);
+  if (e != cudaSuccess) return e;
+  claim_kernel<<<grid, 256, 0, stream>>>(claims, p);
+  // 8 CTAs of 256 threads fill an SM
+  const int ctas = std::min(8 * sm_count, p.num_blocks);
+  const uint4* k = static_cast<const uint4*>(k_cache);
+  const uint4* v = static_cast<const uint4*>(v_cache);
+  uint4* k16v = static_cast<uint4*>(k16);
+  uint4* v16v = static_cast<uint4*>(v16);
+  if (cache_dt == DT_BF16)
+    widen_list_kernel<DT_BF16, DT_F16><<<ctas, 256, 0, stream>>>(k, v, k16v, v16v, claims,
+                                                                   p.num_blocks, in_vec);
+  else if (act_dt == DT_BF16)
+    widen_list_kernel<DT_E4M3, DT_BF16><<<ctas, 256, 0, stream>>>(k, v, k16v, v16v, claims,
+                                                                    p.num_blocks, in_vec);
+  else
+    widen_list_kernel<DT_E4M3, DT_F16><<<ctas, 256, 0, stream>>>(k, v, k16v, v16v, claims,
+                                                                   p.num_blocks, in_vec);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_widen(int cache_dt, int act_dt, const void* k_cache, const void* v_cache,
                          void* k16, void* v16, const ExtendParams& p, int num_groups, int head_dim,

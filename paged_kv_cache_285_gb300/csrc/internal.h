@@ -13,9 +13,9 @@ enum : int {
   DT_F16 = 0,
   DT_BF16 = 1,
   DT_E4M3 = 2,
-  // shared-prefix extend with K read as bf16 and V pages widened to f16
-  // beforehand (widen_kernel): a bf16 cache's K with its V shadow pool, or an
-  // fp8 cache's K and V shadow pools (bf16 queries)
+  // extend with K read as bf16 and V pages widened to f16 beforehand (a
+  // widening pass): a bf16 cache's K with its V shadow pool, or an fp8 cache's
+  // K and V shadow pools (bf16 queries)
   DT_BF16_V16 = 3
 };
 
@@ -235,5 +235,14 @@ bool extend_supported(int head_dim, int cache_dt, int act_dt, int group);
 cudaError_t launch_widen(int cache_dt, int act_dt, const void* k_cache, const void* v_cache,
                          void* k16, void* v16, const ExtendParams& p, int num_groups, int head_dim,
                          int block_size, int max_total_len, cudaStream_t stream);
+// The same for a plain extend (no groups): every request's pages, each block
+// widened once although requests may share it.  claims: int32 scratch of
+// 1 + 2 * p.num_blocks entries (any contents; a counter and a flag per block
+// are zeroed first on `stream`, then a list of the blocks claimed is built and
+// widened by a grid of 8 * sm_count CTAs at most).
+cudaError_t launch_widen_claim(int cache_dt, int act_dt, const void* k_cache,
+                               const void* v_cache, void* k16, void* v16, int* claims,
+                               const ExtendParams& p, int head_dim, int block_size,
+                               int max_total_len, int sm_count, cudaStream_t stream);
 
 }  // namespace pkv

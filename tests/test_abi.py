@@ -41,7 +41,7 @@ def test_status_strings_and_version(lib):
     assert pkv.status_string(0) == "PKV_OK"
     assert pkv.status_string(3) == "PKV_ERR_WORKSPACE"
     assert pkv.status_string(99) == "PKV_ERR_UNKNOWN"
-    assert pkv.version() == 20000
+    assert pkv.version() == 20100
 
 
 def _desc(**kw):
@@ -199,6 +199,22 @@ def test_shared_prefix_extend_argument_errors(lib):
     assert call(desc=_desc(cache_dtype=2), ws=FAKE, ws_bytes=need) == 3  # too small for K and V
     assert lib.pkv_extend_shared_prefix_workspace_bytes(ctypes.byref(_desc(cache_dtype=0))) == 0
     assert lib.pkv_extend_shared_prefix_workspace_bytes(ctypes.byref(_desc(head_dim=96))) == 0
+
+
+def test_plain_extend_widen_workspace_size(lib):
+    # the pools of the shared-prefix workspace, then int32 claims (a counter, a
+    # flag and a list entry per block) rounded up to 256 bytes; 0 where nothing
+    # is widened
+    pool = 8 * 2 * 16 * 128 * 2
+    assert lib.pkv_extend_widen_workspace_bytes(ctypes.byref(_desc())) == pool + 256
+    assert lib.pkv_extend_widen_workspace_bytes(ctypes.byref(_desc(num_blocks=100))) == \
+        100 * 2 * 16 * 128 * 2 + 1024
+    assert lib.pkv_extend_widen_workspace_bytes(ctypes.byref(_desc(cache_dtype=2))) == \
+        2 * pool + 256
+    assert lib.pkv_extend_widen_workspace_bytes(ctypes.byref(_desc(cache_dtype=0))) == 0
+    assert lib.pkv_extend_widen_workspace_bytes(ctypes.byref(_desc(head_dim=96))) == 0
+    # pkv_extend_workspace_bytes still asks for nothing: the widening is optional
+    assert lib.pkv_extend_workspace_bytes(ctypes.byref(_desc(cache_dtype=2)), 2, 4, 10, 100) == 0
 
 
 def test_binding_refuses_wrong_index_dtypes():
