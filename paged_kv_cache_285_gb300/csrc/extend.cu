@@ -1279,27 +1279,31 @@ __global__ void __launch_bounds__(256) widen_kernel(const uint4* __restrict__ k,
 // Plain extend: the pages each request reads (blocks 0 .. ceil((P + S) /
 // block_size) - 1 of its table), widened once per block although requests
 // may share blocks.  claims = [count][flag per block][list]: the claim pass
-// gives thread (x, r, t) block 256 x + t of request r; the first request to
-// set a block's flag (zeroed before the pass) appends it to the list.  The
-// widening pass then spreads the list over a grid of persistent CTAs, so that
-// the blocks of a shared prefix, which the requests that start first win, do
-// not queue up in those requests' CTAs.
+// gives thread (x, r, t) blocks 256 x + t, 256 (x + gridDim.x) + t, ... of
+// request r; the first request to set a block's flag (zeroed before the pass)
+// appends it to the list.  The widening pass then spreads the list over a
+// grid of persistent CTAs, so that the blocks of a shared prefix, which the
+// requests that start first win, do not queue up in those requests' CTAs.
 __global__ void __launch_bounds__(256) claim_kernel(int* claims, const ExtendParams p) {
   const int r = blockIdx.y;
   const int total = __ldg(p.prefix_lens + r) + (__ldg(p.q_indptr + r + 1) - __ldg(p.q_indptr + r));
   const int nb = min(p.max_blocks, (max(total, 0) + (1 << p.bs_shift) - 1) >> p.bs_shift);
-  const int i = blockIdx.x * 256 + threadIdx.x;
-  int blk = -1;
-  if (i < nb) blk = __ldg(p.block_tables + (int64_t)r * p.max_blocks + i);
-  const bool won = blk >= 0 && blk < p.num_blocks && atomicCAS(claims + 1 + blk, 0, 1) == 0;
-  // one list slot reservation per warp
-  const unsigned m = __ballot_sync(0xffffffffu, won);
-  if (m == 0) return;
-  const int lane = threadIdx.x & 31, leader = __ffs(m) - 1;
-  int base = 0;
-  if (lane == leader) base = atomicAdd(claims, __popc(m));
-  base = __shfl_sync(0xffffffffu, base, leader);
-  if (won) claims[1 + p.num_blocks + base + __popc(m & ((1u << lane) - 1))] = blk;
+  // the grid is sized from the call's length hint; a request past it loops
+  for (int base = blockIdx.x * 256; base < nb; base += gridDim.x * 256) {
+    const int i = base + threadIdx.x;
+    int blk = -1;
+    if (i < nb) blk = __ldg(p.block_tables + (int64_t)r * p.max_blocks + i);
+    const bool won = blk >= 0 && blk < p.num_blocks && atomicCAS(claims + 1 + blk, 0, 1) == 0;
+    // one list slot reservation per warp
+    const unsigned m = __ballot_sync(0xffffffffu, won);
+    if (m != 0) {
+      const int lane = threadIdx.x & 31, leader = __ffs(m) - 1;
+      int slot = 0;
+      if (lane == leader) slot = atomicAdd(claims, __popc(m));
+      slot = __shfl_sync(0xffffffffu, slot, leader);
+      if (won) claims[1 + p.num_blocks + slot + __popc(m & ((1u << lane) - 1))] = blk;
+    }
+  }
 }
 
 template <int SRC, int KOUT>

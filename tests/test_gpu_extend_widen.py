@@ -147,3 +147,24 @@ def test_widened_extend_on_the_benchmark_workload():
     case = W.shared_prefix_extend(device="cuda")
     same_bits(run(case), run(case, garbage_workspace(case)))
     assert pkv.get_device_error() == 0
+
+
+def test_request_longer_than_the_length_hint_is_widened_whole():
+    # the kernels read every key through the table whatever max_total_len says;
+    # the widening passes, whose grids that hint sizes, cover every block too
+    # (a 5,000-token request is 313 blocks; the hint's grid claims 256 at once)
+    case = W.extend_case([4950, 20], [50, 30], 8, 2, 128, 16, E4M3, BF16, seed=360, device="cuda")
+    suf = (case.q_indptr[1:] - case.q_indptr[:-1]).cpu()
+    outs = []
+    for ws in (None, garbage_workspace(case)):
+        out = torch.full_like(case.q, float("nan"))
+        lse = torch.full(case.q.shape[:2], float("nan"), dtype=torch.float32, device="cuda")
+        pkv.paged_extend_attn(case.k_cache, case.v_cache, case.q, out, case.q_indptr,
+                              case.prefix_lens, case.block_tables, case.sm_scale, int(suf.max()),
+                              100, k_scale=case.k_scale, v_scale=case.v_scale, lse_out=lse,
+                              workspace=ws)
+        torch.cuda.synchronize()
+        outs.append((out, lse))
+    for out, lse in outs:
+        check(case, out, lse, "length hint below the request", fp8=True)
+    assert pkv.get_device_error() == 0
